@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the batched speculative-decoding verifier on one GB300.
+
+Workload (one "step" = one verification call over the whole batch): N=512
+requests, gamma=7 drafts each, V=151936, fp32 probability rows with the
+fused workload's sparse support (50 largest logits at T=0.8), production-mode
+randomness (Philox inside the kernel; the offset advances every step).  Inputs
+are synthetic (workloads.py) and resident in HBM before timing.  The rows one
+step touches (~0.6 GB) exceed the 126 MB L2 several times over, so no flush is
+inserted.
+
+Prints one JSON line: verified draft tokens/s for the whole job, the roofline
+of the verifier kernel against the measured HBM copy bandwidth, an end-to-end
+figure through the C ABI with host buffers, the CPU oracle as a reported
+baseline, and the SM clocks sampled during the timed region.
+
+  python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--gpus N]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "verified draft tokens/s at N=512,gamma=7,V=151936; achieved HBM GB/s vs ~8 TB/s"
+UNIT = "verified draft tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = "fused_probs"
+KERNEL_SOURCES = ["sv_probs.cu", "sv_device.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cluster", type=int, default=0, help="CTAs per request (0 = automatic)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--requests", type=int, default=0, help="override the batch size (profiling runs only)")
+    return ap.parse_args()
+
+
+def measured_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s earlier GB300 copy measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        h.update((ROOT / "speculative_decoding_token_rejection_gb300" / "csrc" / n).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = ROOT / "profiles" / "verify_probs_fused_probs.traffic.json"
+    if not p.exists():
+        return None, None
+    d = json.loads(p.read_text())
+    if d.get("kernel_source_sha") != kernel_source_hash():
+        return None, d.get("kernel_source_sha")
+    return d.get("dram_bytes_per_launch"), d.get("kernel_source_sha")
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        import torch
+        sel = str(self.dev)
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:
+            inside = [s for _, s in self.samples]
+            window = "whole run (timed region shorter than the 200 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for s in inside for k in range(4) if len(s) > 5 + k and "Active" in s[5 + k]
+                          and "Not" not in s[5 + k]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max((num(s[3]) or 0.0) for s in inside)}
+
+
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(nacc, gammas, V, G):
+    """Minimal bytes one call must move per request (probability entry,
+    production mode): draft ids, the gathered p(y)/q(y) at examined positions,
+    one streamed row pair (rejection) or one row (bonus), the temperature, the
+    output row and num_accepted, num_computed_tokens read+write and the slot
+    entries set to -1."""
+    import numpy as np
+    A = nacc.astype(np.int64)
+    g = gammas.astype(np.int64)
+    gathered = np.minimum(A + 1, g)
+    row = np.where(A < g, 8 * V, 4 * V)
+    per = 4 * g + 8 * gathered + row + 4 + 4 * (G + 1) + 4 + 8 + 8 * (g - A)
+    return int(per.sum())
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, world)
+    return run_ours(args, world, rank, local_rank)
+
+
+def run_ours(args, world, rank, local_rank):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_token_rejection_gb300 as sv
+    import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    from speculative_decoding_token_rejection_gb300 import _build
+    if rank == 0:
+        _build.build()
+    barrier()
+
+    # weak scaling: every rank verifies its own batch of 512 requests
+    w = workloads.make(WORKLOAD, seed=3 + 1000 * rank, test_mode=False, N=args.requests or None)
+    N, G, V, T = w["N"], w["gamma"], w["V"], w["T"]
+    gammas = workloads.gammas_of(w)
+    t = workloads.as_torch(w, dev)
+    ver = sv.Verifier(N, G, V, device=local_rank, cluster_ctas=args.cluster)
+    lib = sv.load_library()
+    out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
+    K, W = args.steps, args.warmup
+    nacc_hist = torch.empty((K + W, N), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ncomp = t["num_computed_tokens"].clone()
+    slots = t["slot_mapping"].clone()
+    a = sv.build_args(entry="probs", draft_ids=t["draft_ids"], target=t["target"], draft=t["draft"],
+                      temperature=t["temperature"], out_tokens=out, num_accepted=nacc_hist[0],
+                      num_computed_tokens=ncomp, slot_mapping=slots, status=status, seed=20240601,
+                      rng_request_base=rank * N)
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    handle = ctypes.c_void_p(ver.handle)
+    run = lib.spec_verify_run
+    nacc_base = nacc_hist.data_ptr()
+    nacc_stride = N * 4
+
+    def step(k):
+        a.offset = k
+        a.num_accepted = nacc_base + k * nacc_stride
+        rc = run(handle, ctypes.byref(a), sptr)
+        if rc != 0:
+            raise RuntimeError(lib.spec_verify_last_error().decode())
+
+    for k in range(W):
+        step(k)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.5)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev[0].record(stream)
+    for k in range(K):
+        step(W + k)
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    clocks.stop()
+    total_ms = ev[0].elapsed_time(ev[K])
+    per_launch = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / K
+    value = world * T * K / (total_ms / 1e3)
+
+    nacc_np = nacc_hist[W:].cpu().numpy()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    alg = [algorithmic_bytes(nacc_np[k], gammas, V, G) for k in range(K)]
+    alg_mean = float(np.mean(alg))
+    launch_ms = float(np.mean(per_launch))
+    achieved = alg_mean / (launch_ms / 1e3) / 1e9
+    peak, peak_src = measured_peak()
+    full_bytes = (T + N) * V * 4 + T * V * 4
+    traffic, traffic_sha = stored_traffic()
+    acc = nacc_np.astype(np.int64)
+    e2e = None if args.no_e2e else run_e2e(args, w, t, ver, sv, dev, world, dist)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: N={N} gamma={G} V={V} fp32 probability rows (50-entry support, "
+                               "T=0.8), production Philox, offset advancing per step",
+                   "entry": "probs", "l2": "no flush: rows touched per step ~0.6 GB >> 126 MB L2",
+                   "cluster_ctas": args.cluster or "auto"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": alg_mean, "launch_ms": launch_ms,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "full_tensor_bytes": full_bytes,
+                     "full_tensor_frac": full_bytes / (launch_ms / 1e3) / 1e9 / peak,
+                     "kernel_source_sha": kernel_source_hash(), "traffic_source_sha": traffic_sha},
+        "acceptance": {"rate": float(acc.sum() / (gammas.sum() * K)),
+                       "mean_accepted": float(acc.mean()),
+                       "committed_tokens_per_s": world * float((acc + 1).sum()) / K / (total_ms / 1e3) * 1.0,
+                       "A_hist": np.bincount(acc.reshape(-1), minlength=G + 1).tolist()},
+        "gpu_launches": K,
+        "clocks": clocks.summary(t0, t1),
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, t, ver, sv, dev, world, dist):
+    """Same metric through the public API with pinned host buffers: every step
+    copies the inputs host->device, verifies, and reads the results back."""
+    import torch
+    import workloads
+    h = workloads.as_torch({k: w[k] for k in ("draft_ids", "target", "draft", "temperature",
+                                               "num_computed_tokens", "slot_mapping")}, "cpu", pin=True)
+    N, G, T = w["N"], w["gamma"], w["T"]
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((N,), dtype=torch.int32, device=dev)
+    h_out = torch.empty((N, G + 1), dtype=torch.int32, pin_memory=True)
+    h_nacc = torch.empty((N,), dtype=torch.int32, pin_memory=True)
+    h_ncomp = torch.empty_like(h["num_computed_tokens"], pin_memory=True)
+    h_slots = torch.empty_like(h["slot_mapping"], pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in (h_out, h_nacc, h_ncomp, h_slots))
+
+    def one(k):
+        for key, v in h.items():
+            d_in[key].copy_(v, non_blocking=True)
+        sv.spec_verify_run(ver.handle, entry="probs", draft_ids=d_in["draft_ids"], target=d_in["target"],
+                           draft=d_in["draft"], temperature=d_in["temperature"], out_tokens=out,
+                           num_accepted=nacc, num_computed_tokens=d_in["num_computed_tokens"],
+                           slot_mapping=d_in["slot_mapping"], seed=7, offset=k)
+        h_out.copy_(out, non_blocking=True)
+        h_nacc.copy_(nacc, non_blocking=True)
+        h_ncomp.copy_(d_in["num_computed_tokens"], non_blocking=True)
+        h_slots.copy_(d_in["slot_mapping"], non_blocking=True)
+
+    one(0)
+    torch.cuda.synchronize()
+    steps = max(1, args.e2e_steps)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(steps):
+        one(k + 1)
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    if dist:
+        tt = torch.tensor([el], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el = float(tt.item())
+    return {"value": world * T * steps / el, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": el / steps * 1e3}
+
+
+def cpu_baseline(w, seconds):
+    """The CPU oracle, as it stands, on a bounded sample of the same batch."""
+    import oracle
+    oracle.build()
+    N = w["N"]
+    gam = w["gamma"]
+    t0 = time.perf_counter()
+    reqs = 0
+    passes = 0
+    while True:
+        oracle.verify(w, production=True, seed=1, offset=passes, with_diag=False)
+        passes += 1
+        reqs += N
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": reqs * gam / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{passes} full passes over the N={N} batch (production Philox), {el:.1f} s, one thread"}
+
+
+def run_reference(args, world):
+    """The oracle timed as the reference arm: each step verifies a bounded slice
+    of the same batch on the host, sized so the whole run stays within
+    --reference-seconds."""
+    import oracle
+    import workloads
+    oracle.build()
+    w = workloads.make(WORKLOAD, seed=3, test_mode=False)
+    N, G = w["N"], w["gamma"]
+    t0 = time.perf_counter()
+    oracle.verify(w, production=True, seed=1, offset=0, with_diag=False, req_range=(0, 8))
+    per_req = max((time.perf_counter() - t0) / 8, 1e-6)
+    K, W = args.steps, args.warmup
+    budget = args.reference_seconds / max(1, K + W)
+    n = int(min(N, max(1, budget / per_req)))
+    for k in range(W):
+        s0 = (k * n) % N
+        oracle.verify(w, production=True, seed=1, offset=k, with_diag=False, req_range=(s0, min(N, s0 + n)))
+    done = 0
+    t0 = time.perf_counter()
+    for k in range(K):
+        s0 = ((W + k) * n) % N
+        s1 = min(N, s0 + n)
+        oracle.verify(w, production=True, seed=1, offset=W + k, with_diag=False, req_range=(s0, s1))
+        done += (s1 - s0) * G
+    el = time.perf_counter() - t0
+    value = done / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: N={N} gamma={G} V={w['V']} fp32 probability rows, production "
+                                   "Philox", "entry": "probs"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
+                             "sample": f"{n} requests of the N={N} batch per step, one thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

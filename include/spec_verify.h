@@ -1,0 +1,168 @@
+/*
+ * spec_verify.h -- C ABI of the batched speculative-decoding verifier
+ * (rejection sampler) for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (page titles and sections of the sources it follows):
+ *  - "Speculative Decoding: propose, verify, accept", section 02: per request
+ *    draft ids [gamma], draft distributions q [gamma, V] and target
+ *    distributions p [gamma+1, V]; section 04: draft y is accepted iff
+ *    u < min(1, p(y)/q(y)), evaluated here as fl32(u * q(y)) < p(y); the first
+ *    rejection is replaced by a draw from max(0, p - q) renormalised;
+ *    section 06: keep the accepted prefix, stop at the first rejection, draw a
+ *    bonus token from p[gamma] when every draft is accepted; section 03:
+ *    temperature 0 compares the draft with the target argmax.
+ *  - "vLLM source walk-through (10): speculative decoding", section
+ *    "SpecDecodeMetadata": flattened drafts with cu_num_draft_tokens (inclusive
+ *    prefix sums) and max_spec_len; section "Rejection sampling: the two
+ *    branches of RejectionSampler": identical temperature/top-k/top-p on the
+ *    target and draft sides, output [batch, max_spec_len + 1] filled with
+ *    PLACEHOLDER_TOKEN_ID = -1; section "Random kernel": categorical draws by
+ *    an exponential race (argmax of weight / exponential draw); section
+ *    "Scheduler and KV": rejected draft KV slots become PADDING_SLOT_ID = -1.
+ *  - "How speculative decoding interacts with the KV cache", section 3.1:
+ *    num_computed_tokens -= gamma - A when it is > 0.
+ *
+ * Memory and execution model: every pointer in spec_verify_args is a DEVICE
+ * pointer on the handle's device, owned by the caller (the library allocates
+ * nothing per call).  spec_verify_run only validates on the host and enqueues
+ * kernels on the caller's stream; it never synchronises.  Errors visible on
+ * the host are returned before anything is enqueued.  Errors in the data are
+ * reported through the optional device word `status` (bitwise OR of
+ * SV_DATA_* bits; the caller zeroes it) and never trap: a request with invalid
+ * data emits nothing (its output row stays -1, num_accepted 0, KV bookkeeping
+ * untouched).  One handle may be used from one host thread at a time; calls on
+ * different streams must not share output buffers.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_VERIFY_ABI_VERSION 1u
+#define SV_PLACEHOLDER_TOKEN_ID (-1)
+#define SV_PADDING_SLOT_ID (-1)
+#define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
+
+/* Host-visible result codes. */
+typedef enum sv_status {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1, /* a null, negative, out-of-range or inconsistent argument */
+  SV_ERR_UNSUPPORTED = 2, /* a combination this build does not implement (e.g. probs + bf16) */
+  SV_ERR_CUDA = 3,        /* a CUDA runtime call failed; see spec_verify_last_error() */
+  SV_ERR_CAPACITY = 4     /* the call exceeds the limits the handle was created with */
+} sv_status;
+
+/* Input kinds. */
+enum sv_entry {
+  SV_ENTRY_PROBS = 0, /* target/draft rows are fp32 probabilities, already transformed */
+  SV_ENTRY_LOGITS = 1 /* target/draft rows are logits; temperature/top-k/top-p applied here */
+};
+enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 };
+
+/* Device status bits (bitwise OR into *status). */
+enum sv_data_status {
+  SV_DATA_BAD_CU = 1,             /* cu_num_draft_tokens not a valid range for this request */
+  SV_DATA_BAD_DRAFT_ID = 2,       /* draft id outside [0, V) at an examined position */
+  SV_DATA_BAD_EXPONENTIAL = 4,    /* test-mode E <= 0 or NaN where a key needed it (key taken as 0) */
+  SV_DATA_EMPTY_DISTRIBUTION = 8, /* a draw found no positive key; token 0 emitted */
+  SV_DATA_BAD_VALUES = 16,        /* NaN (greedy) or NaN/+inf/no finite logit (random logits) in a read row */
+  SV_DATA_BAD_PARAM = 32,         /* temperature < 0/NaN/inf, or top_p <= 0/NaN */
+  SV_DATA_MISSING_DRAFT = 64      /* draft == NULL but a random request needs draft rows */
+};
+
+typedef struct spec_verify_ctx *spec_verify_t;
+
+/* Limits fixed at creation. */
+typedef struct spec_verify_config {
+  int32_t max_num_reqs; /* largest num_reqs of any call (>= 1) */
+  int32_t max_spec_len; /* largest max_spec_len of any call (0 .. SV_MAX_SPEC_LEN) */
+  int32_t vocab_size;   /* largest vocab_size of any call (>= 1) */
+  int32_t device;       /* CUDA device ordinal the handle's calls run on */
+  int32_t cluster_ctas; /* CTAs cooperating on one request: 0 = automatic, else 1, 2, 4, 8 or 16 */
+  uint32_t flags;       /* reserved, must be 0 */
+} spec_verify_config;
+
+/* One verification call.  N = num_reqs, G = max_spec_len, V = vocab_size,
+ * T = num_draft_tokens_total.  Request i owns draft rows [s_i, s_i + gamma_i)
+ * and target rows [s_i + i, s_i + i + gamma_i] (its last target row is the
+ * bonus row), where s_i = cu[i-1] (0 for i = 0) and gamma_i = cu[i] - s_i. */
+typedef struct spec_verify_args {
+  int32_t num_reqs;     /* N >= 0 (N = 0 is a no-op) */
+  int32_t max_spec_len; /* G: output row length is G + 1; every gamma_i <= G */
+  int32_t vocab_size;   /* V >= 1 */
+  int32_t entry;        /* SV_ENTRY_PROBS or SV_ENTRY_LOGITS */
+  int32_t dtype;        /* SV_F32 (both entries) or SV_BF16 (logits entry only) */
+  int32_t reserved0;    /* must be 0 */
+  int64_t num_draft_tokens_total; /* T = cu[N-1]; must equal N*G when cu == NULL */
+
+  const int32_t *draft_ids;           /* [T] draft token ids, request-major */
+  const int32_t *cu_num_draft_tokens; /* [N] inclusive prefix sums, or NULL: every gamma_i = G */
+  const void *target;                 /* [T+N rows, target_row_stride] p rows or target logits */
+  int64_t target_row_stride;          /* elements between target rows (>= V) */
+  const void *draft;                  /* [T rows, draft_row_stride] q rows or draft logits; may be NULL
+                                         when no random request has drafts */
+  int64_t draft_row_stride;           /* elements between draft rows (>= V) */
+
+  const float *temperature; /* [N]; 0 selects the greedy path; NULL = 1 for every request */
+  const int32_t *top_k;     /* [N] or NULL; <= 0 or >= V disables (logits entry only) */
+  const float *top_p;       /* [N] or NULL; >= 1 disables; must be > 0 (logits entry only) */
+
+  /* Randomness.  Test mode: both pointers set; u [T] in [0, 1) and E [N rows,
+   * exponentials_row_stride] > 0 are read as given.  Production mode: both
+   * NULL; u and E come from Philox4x32-10 (Salmon et al., SC'11) with key
+   * (seed) and counters (j/4, 2r+1, offset) for u_j and (x/4, 2r, offset) for
+   * E(x), r = rng_request_base + i; u = (w >> 8) 2^-24, E = -ln((2(w >> 9)+1) 2^-24). */
+  const float *uniforms;
+  const float *exponentials;
+  int64_t exponentials_row_stride;
+  uint64_t seed;
+  uint64_t offset;
+  uint32_t rng_request_base;
+  uint32_t reserved1; /* must be 0 */
+
+  /* Outputs. */
+  int32_t *out_tokens;          /* [N, G+1] committed tokens, -1 after the last one */
+  int32_t *num_accepted;        /* [N] accepted draft count A */
+  int32_t *num_computed_tokens; /* [N] in/out or NULL: -= gamma_i - A when > 0 */
+  int64_t *slot_mapping;        /* [T+N] in/out or NULL: verify tokens j in (A, gamma_i] -> -1 */
+  float *dbg_py;                /* [T] or NULL: p_j(y_j) at examined positions j <= min(A, gamma_i - 1) */
+  float *dbg_qy;                /* [T] or NULL: q_j(y_j) at the same positions */
+  int32_t *status;              /* [1] or NULL: SV_DATA_* bits OR-ed in */
+} spec_verify_args;
+
+/* Create a handle.  Queries the device and sets kernel attributes on it
+ * (temporarily making `device` current).  *out is set only on SV_OK. */
+sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *out);
+
+/* Enqueue one verification on `stream` (a cudaStream_t, NULL = legacy default
+ * stream of the current device, which must be the handle's device). */
+sv_status spec_verify_run(spec_verify_t handle, const spec_verify_args *args, void *stream);
+
+/* Release a handle (no device memory is held).  NULL is accepted. */
+sv_status spec_verify_destroy(spec_verify_t handle);
+
+/* Host-only validation of `args` against `config`: the checks spec_verify_run
+ * performs before enqueueing anything.  Touches no device and no pointer target. */
+sv_status spec_verify_check_args(const spec_verify_config *config, const spec_verify_args *args);
+
+/* Static name of a status code. */
+const char *spec_verify_status_string(sv_status status);
+
+/* Message of the last error raised on the calling thread ("" if none). */
+const char *spec_verify_last_error(void);
+
+/* ABI self-description, for bindings that mirror the structs. */
+uint32_t spec_verify_abi_version(void);
+size_t spec_verify_sizeof_config(void);
+size_t spec_verify_sizeof_args(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

@@ -1,0 +1,273 @@
+"""Python binding of the GB300 speculative-decoding verifier (rejection sampler).
+
+A thin ctypes layer over ``libspec_verify.so`` (declared in
+``include/spec_verify.h``): it checks tensor devices, dtypes and strides,
+passes raw device pointers and the current CUDA stream, and returns.  Every
+step of the verification runs in the library's CUDA kernels; there is no
+Python or CPU fallback -- if the library is missing the import of this module
+still works but every call raises ``NativeLibraryMissing``.
+
+Functions keep the C names: ``spec_verify_create``, ``spec_verify_run``,
+``spec_verify_destroy``, ``spec_verify_check_args``,
+``spec_verify_status_string``; ``Verifier`` bundles them with output
+allocation for convenience.
+"""
+from __future__ import annotations
+
+import ctypes
+import pathlib
+from dataclasses import dataclass
+from typing import Optional
+
+_PKG = pathlib.Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libspec_verify.so"
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_CAPACITY = range(5)
+SV_ENTRY_PROBS, SV_ENTRY_LOGITS = 0, 1
+SV_F32, SV_BF16 = 0, 1
+SV_MAX_SPEC_LEN = 256
+DATA_STATUS_BITS = {
+    "BAD_CU": 1, "BAD_DRAFT_ID": 2, "BAD_EXPONENTIAL": 4, "EMPTY_DISTRIBUTION": 8,
+    "BAD_VALUES": 16, "BAD_PARAM": 32, "MISSING_DRAFT": 64,
+}
+
+_P = ctypes.c_void_p
+
+
+class SpecVerifyConfig(ctypes.Structure):
+    _fields_ = [("max_num_reqs", ctypes.c_int32), ("max_spec_len", ctypes.c_int32),
+                ("vocab_size", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("cluster_ctas", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class SpecVerifyArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_reqs", ctypes.c_int32), ("max_spec_len", ctypes.c_int32), ("vocab_size", ctypes.c_int32),
+        ("entry", ctypes.c_int32), ("dtype", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("num_draft_tokens_total", ctypes.c_int64),
+        ("draft_ids", _P), ("cu_num_draft_tokens", _P),
+        ("target", _P), ("target_row_stride", ctypes.c_int64),
+        ("draft", _P), ("draft_row_stride", ctypes.c_int64),
+        ("temperature", _P), ("top_k", _P), ("top_p", _P),
+        ("uniforms", _P), ("exponentials", _P), ("exponentials_row_stride", ctypes.c_int64),
+        ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+        ("rng_request_base", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
+        ("out_tokens", _P), ("num_accepted", _P), ("num_computed_tokens", _P), ("slot_mapping", _P),
+        ("dbg_py", _P), ("dbg_qy", _P), ("status", _P),
+    ]
+
+
+class NativeLibraryMissing(RuntimeError):
+    pass
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{spec_verify_status_string(code)}: {msg}")
+        self.code = code
+
+
+_LIB = None
+EXPORTED = ("spec_verify_create", "spec_verify_run", "spec_verify_destroy", "spec_verify_check_args",
+            "spec_verify_status_string", "spec_verify_last_error", "spec_verify_abi_version",
+            "spec_verify_sizeof_config", "spec_verify_sizeof_args")
+
+
+def load_library(path: Optional[str] = None):
+    """Load libspec_verify.so (once) and bind its prototypes."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = pathlib.Path(path) if path else LIB_PATH
+    if not p.exists():
+        raise NativeLibraryMissing(f"{p} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(str(p))
+    lib.spec_verify_create.argtypes = [ctypes.POINTER(SpecVerifyConfig), ctypes.POINTER(ctypes.c_void_p)]
+    lib.spec_verify_create.restype = ctypes.c_int
+    lib.spec_verify_run.argtypes = [ctypes.c_void_p, ctypes.POINTER(SpecVerifyArgs), ctypes.c_void_p]
+    lib.spec_verify_run.restype = ctypes.c_int
+    lib.spec_verify_destroy.argtypes = [ctypes.c_void_p]
+    lib.spec_verify_destroy.restype = ctypes.c_int
+    lib.spec_verify_check_args.argtypes = [ctypes.POINTER(SpecVerifyConfig), ctypes.POINTER(SpecVerifyArgs)]
+    lib.spec_verify_check_args.restype = ctypes.c_int
+    lib.spec_verify_status_string.argtypes = [ctypes.c_int]
+    lib.spec_verify_status_string.restype = ctypes.c_char_p
+    lib.spec_verify_last_error.argtypes = []
+    lib.spec_verify_last_error.restype = ctypes.c_char_p
+    lib.spec_verify_abi_version.restype = ctypes.c_uint32
+    lib.spec_verify_sizeof_config.restype = ctypes.c_size_t
+    lib.spec_verify_sizeof_args.restype = ctypes.c_size_t
+    if lib.spec_verify_sizeof_config() != ctypes.sizeof(SpecVerifyConfig) or \
+            lib.spec_verify_sizeof_args() != ctypes.sizeof(SpecVerifyArgs):
+        raise RuntimeError("spec_verify struct layout differs from the binding")
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def spec_verify_status_string(code: int) -> str:
+    return load_library().spec_verify_status_string(int(code)).decode()
+
+
+def _check(code: int):
+    if code != SV_OK:
+        raise SpecVerifyError(code, load_library().spec_verify_last_error().decode())
+
+
+def make_config(max_num_reqs: int, max_spec_len: int, vocab_size: int, device: int = 0,
+                cluster_ctas: int = 0) -> SpecVerifyConfig:
+    return SpecVerifyConfig(int(max_num_reqs), int(max_spec_len), int(vocab_size), int(device),
+                            int(cluster_ctas), 0)
+
+
+def spec_verify_create(max_num_reqs: int, max_spec_len: int, vocab_size: int, device: int = 0,
+                       cluster_ctas: int = 0) -> int:
+    cfg = make_config(max_num_reqs, max_spec_len, vocab_size, device, cluster_ctas)
+    h = ctypes.c_void_p()
+    _check(load_library().spec_verify_create(ctypes.byref(cfg), ctypes.byref(h)))
+    return h.value
+
+
+def spec_verify_destroy(handle: int) -> None:
+    _check(load_library().spec_verify_destroy(ctypes.c_void_p(handle)))
+
+
+# ----------------------------------------------------------------------------
+# argument marshalling
+# ----------------------------------------------------------------------------
+def _ptr(t, dtype, name, device, numel=None, ndim=None, contiguous=True):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _rows(t, name, device, V, nrows, dtypes):
+    """A [rows, >=V] tensor whose rows are unit-stride; returns (ptr, row_stride)."""
+    if t is None:
+        return None, 0
+    if t.dim() != 2 or t.shape[1] != V or t.shape[0] != nrows:
+        raise ValueError(f"{name} must have shape [{nrows}, {V}], got {tuple(t.shape)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} dtype {t.dtype} not in {dtypes}")
+    if t.stride(1) != 1 or (nrows > 1 and t.stride(0) < V):
+        raise ValueError(f"{name} rows must be unit-stride and non-overlapping")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t.data_ptr(), (t.stride(0) if nrows > 1 else V)
+
+
+def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft=None, cu_num_draft_tokens=None,
+               temperature=None, top_k=None, top_p=None, uniforms=None, exponentials=None, seed: int = 0,
+               offset: int = 0, rng_request_base: int = 0, num_computed_tokens=None, slot_mapping=None,
+               dbg_py=None, dbg_qy=None, status=None, device=None) -> SpecVerifyArgs:
+    """Validate tensors and fill a SpecVerifyArgs (no device work)."""
+    import torch
+    if entry not in ("probs", "logits"):
+        raise ValueError("entry must be 'probs' or 'logits'")
+    device = target.device if device is None else torch.device(device)
+    N = out_tokens.shape[0]
+    G = out_tokens.shape[1] - 1
+    V = target.shape[-1]
+    T = draft_ids.numel()
+    if target.dtype == torch.bfloat16:
+        dt = SV_BF16
+    elif target.dtype == torch.float32:
+        dt = SV_F32
+    else:
+        raise TypeError("target must be float32 or bfloat16")
+    dts = (target.dtype,)
+    a = SpecVerifyArgs()
+    a.num_reqs, a.max_spec_len, a.vocab_size = N, G, V
+    a.entry = SV_ENTRY_PROBS if entry == "probs" else SV_ENTRY_LOGITS
+    a.dtype = dt
+    a.num_draft_tokens_total = T
+    a.draft_ids = _ptr(draft_ids, torch.int32, "draft_ids", device)
+    a.cu_num_draft_tokens = _ptr(cu_num_draft_tokens, torch.int32, "cu_num_draft_tokens", device, numel=N)
+    a.target, a.target_row_stride = _rows(target, "target", device, V, T + N, dts)
+    a.draft, a.draft_row_stride = _rows(draft, "draft", device, V, T, dts)
+    a.temperature = _ptr(temperature, torch.float32, "temperature", device, numel=N)
+    a.top_k = _ptr(top_k, torch.int32, "top_k", device, numel=N)
+    a.top_p = _ptr(top_p, torch.float32, "top_p", device, numel=N)
+    a.uniforms = _ptr(uniforms, torch.float32, "uniforms", device, numel=T)
+    if exponentials is not None:
+        a.exponentials, a.exponentials_row_stride = _rows(exponentials, "exponentials", device, V, N,
+                                                          (torch.float32,))
+    a.seed, a.offset, a.rng_request_base = int(seed), int(offset), int(rng_request_base)
+    a.out_tokens = _ptr(out_tokens, torch.int32, "out_tokens", device, ndim=2)
+    a.num_accepted = _ptr(num_accepted, torch.int32, "num_accepted", device, numel=N)
+    a.num_computed_tokens = _ptr(num_computed_tokens, torch.int32, "num_computed_tokens", device, numel=N)
+    a.slot_mapping = _ptr(slot_mapping, torch.int64, "slot_mapping", device, numel=T + N)
+    a.dbg_py = _ptr(dbg_py, torch.float32, "dbg_py", device, numel=T)
+    a.dbg_qy = _ptr(dbg_qy, torch.float32, "dbg_qy", device, numel=T)
+    a.status = _ptr(status, torch.int32, "status", device, numel=1)
+    return a
+
+
+def spec_verify_run(handle: int, stream=None, **kw) -> None:
+    """Enqueue one verification on ``stream`` (default: torch's current stream).
+    Keyword arguments are those of ``build_args``."""
+    import torch
+    a = build_args(**kw)
+    if stream is None:
+        stream = torch.cuda.current_stream(kw["target"].device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(load_library().spec_verify_run(ctypes.c_void_p(handle), ctypes.byref(a), ctypes.c_void_p(s)))
+
+
+def spec_verify_check_args(config: SpecVerifyConfig, args: SpecVerifyArgs) -> int:
+    """Host-only validation; returns the sv_status code."""
+    return int(load_library().spec_verify_check_args(ctypes.byref(config), ctypes.byref(args)))
+
+
+@dataclass
+class VerifyResult:
+    out_tokens: "object"
+    num_accepted: "object"
+    status: "object"
+
+
+class Verifier:
+    """A handle plus output allocation.  ``verify`` returns device tensors."""
+
+    def __init__(self, max_num_reqs: int, max_spec_len: int, vocab_size: int, device: int = 0,
+                 cluster_ctas: int = 0):
+        self.device = device
+        self.handle = spec_verify_create(max_num_reqs, max_spec_len, vocab_size, device, cluster_ctas)
+
+    def close(self):
+        if self.handle:
+            spec_verify_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def verify(self, *, entry: str, draft_ids, target, max_spec_len: int, num_reqs: int, stream=None,
+               out_tokens=None, num_accepted=None, status=None, **kw) -> VerifyResult:
+        import torch
+        dev = target.device
+        if out_tokens is None:
+            out_tokens = torch.empty((num_reqs, max_spec_len + 1), dtype=torch.int32, device=dev)
+        if num_accepted is None:
+            num_accepted = torch.empty((num_reqs,), dtype=torch.int32, device=dev)
+        if status is None:
+            status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        spec_verify_run(self.handle, stream=stream, entry=entry, draft_ids=draft_ids, target=target,
+                        out_tokens=out_tokens, num_accepted=num_accepted, status=status, **kw)
+        return VerifyResult(out_tokens, num_accepted, status)

@@ -1,0 +1,210 @@
+// sv_api.cu -- the C ABI declared in include/spec_verify.h: handle lifetime,
+// host-side validation and kernel dispatch.  No allocation, no host sync.
+#include <climits>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <new>
+
+#include "sv_internal.h"
+
+namespace sv {
+
+namespace {
+thread_local char g_last_error[512] = "";
+
+sv_status fail(sv_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+void set_last_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+}
+
+int choose_cluster(const spec_verify_ctx *ctx, int N, int V) {
+  if (ctx->cfg.cluster_ctas > 0) return ctx->cfg.cluster_ctas;
+  // Enough CTAs for several resident waves, but chunks of at least 4096
+  // elements so the per-CTA scan and reduction stay a small share of the work.
+  const long long target = 8LL * ctx->num_sms;
+  int c = 1;
+  while (c < ctx->max_cluster && static_cast<long long>(N) * c < target && V / (2 * c) >= 4096) c *= 2;
+  return c;
+}
+
+}  // namespace sv
+
+using sv::fail;
+
+extern "C" {
+
+const char *spec_verify_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "SV_OK";
+    case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG";
+    case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA";
+    case SV_ERR_CAPACITY: return "SV_ERR_CAPACITY";
+  }
+  return "SV_UNKNOWN_STATUS";
+}
+
+const char *spec_verify_last_error(void) { return sv::g_last_error; }
+
+uint32_t spec_verify_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
+size_t spec_verify_sizeof_config(void) { return sizeof(spec_verify_config); }
+size_t spec_verify_sizeof_args(void) { return sizeof(spec_verify_args); }
+
+static sv_status check_config(const spec_verify_config *c) {
+  if (!c) return fail(SV_ERR_INVALID_ARG, "config is NULL");
+  if (c->max_num_reqs < 1) return fail(SV_ERR_INVALID_ARG, "max_num_reqs must be >= 1");
+  if (c->max_spec_len < 0 || c->max_spec_len > SV_MAX_SPEC_LEN)
+    return fail(SV_ERR_INVALID_ARG, "max_spec_len must be in [0, %d]", SV_MAX_SPEC_LEN);
+  if (c->vocab_size < 1) return fail(SV_ERR_INVALID_ARG, "vocab_size must be >= 1");
+  if (c->device < 0) return fail(SV_ERR_INVALID_ARG, "device must be >= 0");
+  const int cc = c->cluster_ctas;
+  if (!(cc == 0 || cc == 1 || cc == 2 || cc == 4 || cc == 8 || cc == 16))
+    return fail(SV_ERR_INVALID_ARG, "cluster_ctas must be 0, 1, 2, 4, 8 or 16");
+  if (c->flags != 0) return fail(SV_ERR_INVALID_ARG, "flags must be 0");
+  if (static_cast<long long>(c->max_num_reqs) * (cc ? cc : 16) > INT_MAX)
+    return fail(SV_ERR_INVALID_ARG, "max_num_reqs too large for one grid");
+  return SV_OK;
+}
+
+sv_status spec_verify_check_args(const spec_verify_config *c, const spec_verify_args *a) {
+  sv_status st = check_config(c);
+  if (st != SV_OK) return st;
+  if (!a) return fail(SV_ERR_INVALID_ARG, "args is NULL");
+  if (a->num_reqs < 0) return fail(SV_ERR_INVALID_ARG, "num_reqs < 0");
+  if (a->max_spec_len < 0) return fail(SV_ERR_INVALID_ARG, "max_spec_len < 0");
+  if (a->vocab_size < 1) return fail(SV_ERR_INVALID_ARG, "vocab_size < 1");
+  if (a->num_reqs > c->max_num_reqs) return fail(SV_ERR_CAPACITY, "num_reqs %d > handle max %d", a->num_reqs,
+                                                 c->max_num_reqs);
+  if (a->max_spec_len > c->max_spec_len)
+    return fail(SV_ERR_CAPACITY, "max_spec_len %d > handle max %d", a->max_spec_len, c->max_spec_len);
+  if (a->vocab_size > c->vocab_size)
+    return fail(SV_ERR_CAPACITY, "vocab_size %d > handle max %d", a->vocab_size, c->vocab_size);
+  if (a->entry != SV_ENTRY_PROBS && a->entry != SV_ENTRY_LOGITS) return fail(SV_ERR_INVALID_ARG, "bad entry");
+  if (a->dtype != SV_F32 && a->dtype != SV_BF16) return fail(SV_ERR_INVALID_ARG, "bad dtype");
+  if (a->entry == SV_ENTRY_PROBS && a->dtype != SV_F32)
+    return fail(SV_ERR_UNSUPPORTED, "the probability entry takes fp32 rows");
+  if (a->entry == SV_ENTRY_LOGITS) return fail(SV_ERR_UNSUPPORTED, "the logits entry is not built in this library");
+  if (a->reserved0 != 0 || a->reserved1 != 0) return fail(SV_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (a->num_draft_tokens_total < 0) return fail(SV_ERR_INVALID_ARG, "num_draft_tokens_total < 0");
+  if (!a->cu_num_draft_tokens &&
+      a->num_draft_tokens_total != static_cast<int64_t>(a->num_reqs) * a->max_spec_len)
+    return fail(SV_ERR_INVALID_ARG, "without cu_num_draft_tokens, T must be num_reqs * max_spec_len");
+  if (a->num_reqs == 0) return SV_OK;
+  if (a->num_draft_tokens_total > static_cast<int64_t>(a->num_reqs) * a->max_spec_len)
+    return fail(SV_ERR_INVALID_ARG, "T exceeds num_reqs * max_spec_len");
+  if (a->num_draft_tokens_total > 0 && !a->draft_ids) return fail(SV_ERR_INVALID_ARG, "draft_ids is NULL");
+  if (!a->target) return fail(SV_ERR_INVALID_ARG, "target is NULL");
+  if (a->target_row_stride < a->vocab_size) return fail(SV_ERR_INVALID_ARG, "target_row_stride < vocab_size");
+  if (a->draft && a->draft_row_stride < a->vocab_size)
+    return fail(SV_ERR_INVALID_ARG, "draft_row_stride < vocab_size");
+  if ((a->uniforms == nullptr) != (a->exponentials == nullptr))
+    return fail(SV_ERR_INVALID_ARG, "uniforms and exponentials must be given together (test mode) or not at all");
+  if (a->exponentials && a->exponentials_row_stride < a->vocab_size)
+    return fail(SV_ERR_INVALID_ARG, "exponentials_row_stride < vocab_size");
+  if (!a->out_tokens || !a->num_accepted) return fail(SV_ERR_INVALID_ARG, "out_tokens / num_accepted is NULL");
+  return SV_OK;
+}
+
+sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *out) {
+  if (!out) return fail(SV_ERR_INVALID_ARG, "out is NULL");
+  sv_status st = check_config(config);
+  if (st != SV_OK) return st;
+  int old = 0;
+  cudaError_t e = cudaGetDevice(&old);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if ((e = cudaSetDevice(config->device)) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "cudaSetDevice(%d): %s", config->device, cudaGetErrorString(e));
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, config->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, config->device);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, config->device);
+  sv_status result = SV_OK;
+  int max_cluster = 16;
+  if (e != cudaSuccess) {
+    result = fail(SV_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  } else if (major != 10 || minor != 3) {
+    result = fail(SV_ERR_UNSUPPORTED, "built for sm_103a only; device %d is sm_%d%d", config->device, major, minor);
+  } else {
+    if (sv::enable_probs_kernels(16) != cudaSuccess) {
+      cudaGetLastError();
+      max_cluster = 8;
+      if ((e = sv::enable_probs_kernels(8)) != cudaSuccess)
+        result = fail(SV_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(e));
+    }
+    if (config->cluster_ctas > max_cluster)
+      result = fail(SV_ERR_UNSUPPORTED, "cluster_ctas %d > %d on this device", config->cluster_ctas, max_cluster);
+  }
+  cudaSetDevice(old);
+  if (result != SV_OK) return result;
+  spec_verify_ctx *h = new (std::nothrow) spec_verify_ctx;
+  if (!h) return fail(SV_ERR_INVALID_ARG, "out of host memory");
+  h->cfg = *config;
+  h->num_sms = sms;
+  h->max_cluster = max_cluster;
+  *out = h;
+  return SV_OK;
+}
+
+sv_status spec_verify_destroy(spec_verify_t h) {
+  delete h;
+  return SV_OK;
+}
+
+sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stream) {
+  if (!h) return fail(SV_ERR_INVALID_ARG, "handle is NULL");
+  sv_status st = spec_verify_check_args(&h->cfg, a);
+  if (st != SV_OK) return st;
+  if (a->num_reqs == 0) return SV_OK;
+  sv::VerifyParams p{};
+  p.N = a->num_reqs;
+  p.G = a->max_spec_len;
+  p.V = a->vocab_size;
+  p.T = a->num_draft_tokens_total;
+  p.ids = a->draft_ids;
+  p.cu = a->cu_num_draft_tokens;
+  p.target = a->target;
+  p.target_stride = a->target_row_stride;
+  p.draft = a->draft;
+  p.draft_stride = a->draft_row_stride;
+  p.temperature = a->temperature;
+  p.top_k = a->top_k;
+  p.top_p = a->top_p;
+  p.uniforms = a->uniforms;
+  p.exponentials = a->exponentials;
+  p.exp_stride = a->exponentials_row_stride;
+  p.seed_lo = static_cast<uint32_t>(a->seed);
+  p.seed_hi = static_cast<uint32_t>(a->seed >> 32);
+  p.off_lo = static_cast<uint32_t>(a->offset);
+  p.off_hi = static_cast<uint32_t>(a->offset >> 32);
+  p.req_base = a->rng_request_base;
+  p.out = a->out_tokens;
+  p.nacc = a->num_accepted;
+  p.ncomp = a->num_computed_tokens;
+  p.slots = a->slot_mapping;
+  p.dbg_py = a->dbg_py;
+  p.dbg_qy = a->dbg_qy;
+  p.status = a->status;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int cluster = sv::choose_cluster(h, p.N, p.V);
+  const bool vec = sv::aligned16(a->target) && (a->target_row_stride % 4 == 0) &&
+                   (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % 4 == 0));
+  const cudaError_t e = sv::launch_probs(p, cluster, vec, s);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "verifier launch: %s", cudaGetErrorString(e));
+  return SV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// sv_internal.h -- host-side plumbing between the C ABI and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+
+struct spec_verify_ctx {
+  spec_verify_config cfg;
+  int num_sms;
+  int max_cluster;  // largest cluster size the kernels were enabled for (8 or 16)
+};
+
+namespace sv {
+
+// Everything a verifier kernel needs, flattened (device pointers, sizes).
+struct VerifyParams {
+  int32_t N, G, V;
+  int64_t T;
+  const int32_t *ids;
+  const int32_t *cu;
+  const void *target;
+  int64_t target_stride;
+  const void *draft;
+  int64_t draft_stride;
+  const float *temperature;
+  const int32_t *top_k;
+  const float *top_p;
+  const float *uniforms;
+  const float *exponentials;
+  int64_t exp_stride;
+  uint32_t seed_lo, seed_hi, off_lo, off_hi;
+  uint32_t req_base;
+  int32_t *out;
+  int32_t *nacc;
+  int32_t *ncomp;
+  int64_t *slots;
+  float *dbg_py;
+  float *dbg_qy;
+  int32_t *status;
+};
+
+// Picks the CTAs-per-request for a call (power of two, <= ctx->max_cluster).
+int choose_cluster(const spec_verify_ctx *ctx, int N, int V);
+
+cudaError_t enable_probs_kernels(int max_cluster);
+cudaError_t launch_probs(const VerifyParams &p, int cluster, bool vec, cudaStream_t stream);
+
+void set_last_error(const char *fmt, ...);
+
+}  // namespace sv

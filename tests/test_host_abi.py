@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI: the library builds, loads without a GPU,
+exports every function include/spec_verify.h declares, its structs match the
+binding, and spec_verify_check_args rejects bad calls before any launch."""
+import ctypes
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import speculative_decoding_token_rejection_gb300 as sv
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_token_rejection_gb300 import _build
+    _build.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = (ROOT / "include" / "spec_verify.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_verify_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(sv.EXPORTED) == set(names)
+
+
+def test_abi_description(lib):
+    assert lib.spec_verify_abi_version() == 1
+    assert lib.spec_verify_sizeof_args() == ctypes.sizeof(sv.SpecVerifyArgs)
+    assert lib.spec_verify_sizeof_config() == ctypes.sizeof(sv.SpecVerifyConfig)
+
+
+def test_status_strings(lib):
+    assert [sv.spec_verify_status_string(c) for c in range(5)] == [
+        "SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_UNSUPPORTED", "SV_ERR_CUDA", "SV_ERR_CAPACITY"]
+
+
+FAKE = 0x10000  # never dereferenced: check_args only looks at pointer presence
+
+
+def good_args(N=4, G=3, V=1000):
+    a = sv.SpecVerifyArgs()
+    a.num_reqs, a.max_spec_len, a.vocab_size = N, G, V
+    a.entry, a.dtype = sv.SV_ENTRY_PROBS, sv.SV_F32
+    a.num_draft_tokens_total = N * G
+    a.draft_ids = FAKE
+    a.target, a.target_row_stride = FAKE, V
+    a.draft, a.draft_row_stride = FAKE, V
+    a.out_tokens = FAKE
+    a.num_accepted = FAKE
+    return a
+
+
+def cfg(**kw):
+    c = dict(max_num_reqs=8, max_spec_len=4, vocab_size=2000)
+    c.update(kw)
+    return sv.make_config(**c)
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda a: None, sv.SV_OK),
+    (lambda a: setattr(a, "num_reqs", 9), sv.SV_ERR_CAPACITY),
+    (lambda a: setattr(a, "num_reqs", -1), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "max_spec_len", 5), sv.SV_ERR_CAPACITY),
+    (lambda a: setattr(a, "vocab_size", 2001), sv.SV_ERR_CAPACITY),
+    (lambda a: setattr(a, "vocab_size", 0), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "entry", 7), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "dtype", sv.SV_BF16), sv.SV_ERR_UNSUPPORTED),  # probs entry is fp32 only
+    (lambda a: setattr(a, "reserved0", 1), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "num_draft_tokens_total", 11), sv.SV_ERR_INVALID_ARG),  # != N*G without cu
+    (lambda a: setattr(a, "draft_ids", None), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "target", None), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "target_row_stride", 999), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "draft_row_stride", 10), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "uniforms", FAKE), sv.SV_ERR_INVALID_ARG),  # without exponentials
+    (lambda a: (setattr(a, "uniforms", FAKE), setattr(a, "exponentials", FAKE),
+                setattr(a, "exponentials_row_stride", 1000)), sv.SV_OK),
+    (lambda a: (setattr(a, "uniforms", FAKE), setattr(a, "exponentials", FAKE),
+                setattr(a, "exponentials_row_stride", 10)), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "out_tokens", None), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "num_accepted", None), sv.SV_ERR_INVALID_ARG),
+    (lambda a: (setattr(a, "cu_num_draft_tokens", FAKE), setattr(a, "num_draft_tokens_total", 5)), sv.SV_OK),
+    (lambda a: (setattr(a, "cu_num_draft_tokens", FAKE), setattr(a, "num_draft_tokens_total", 13)),
+     sv.SV_ERR_INVALID_ARG),  # T > N*G
+    (lambda a: (setattr(a, "num_reqs", 0), setattr(a, "num_draft_tokens_total", 0),
+                setattr(a, "target", None)), sv.SV_OK),  # empty batch: no pointers needed
+])
+def test_check_args(lib, mutate, code):
+    a = good_args()
+    mutate(a)
+    assert sv.spec_verify_check_args(cfg(), a) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(max_num_reqs=0), sv.SV_ERR_INVALID_ARG),
+    (dict(max_spec_len=257), sv.SV_ERR_INVALID_ARG),
+    (dict(vocab_size=0), sv.SV_ERR_INVALID_ARG),
+    (dict(cluster_ctas=3), sv.SV_ERR_INVALID_ARG),
+    (dict(cluster_ctas=16), sv.SV_OK),
+])
+def test_check_config(lib, kw, code):
+    assert sv.spec_verify_check_args(cfg(**kw), good_args()) == code
+
+
+def test_null_pointers_rejected(lib):
+    assert lib.spec_verify_check_args(None, None) == sv.SV_ERR_INVALID_ARG
+    c = cfg()
+    assert lib.spec_verify_check_args(ctypes.byref(c), None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_run(None, None, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_destroy(None) == sv.SV_OK
+    h = ctypes.c_void_p()
+    assert lib.spec_verify_create(None, ctypes.byref(h)) == sv.SV_ERR_INVALID_ARG
+
+
+def test_create_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(sv.SpecVerifyError) as ei:
+        sv.spec_verify_create(4, 4, 1000)
+    assert ei.value.code == sv.SV_ERR_CUDA

@@ -181,50 +181,64 @@ def _top_support_softmax(rows_f32: np.ndarray, temp: float, k: int):
     """For each row: indices of its ``k`` largest values and a float32 softmax of
     value/temp over them (input synthesis for the sparse fused workload)."""
     import torch
-    x = torch.from_numpy(rows_f32)
+    x = torch.from_numpy(np.ascontiguousarray(rows_f32))
     vals, idx = torch.topk(x, k, dim=-1, largest=True, sorted=True)
     w = torch.softmax(vals / temp, dim=-1, dtype=torch.float32)
     return idx.numpy().astype(np.int64), w.numpy()
 
 
 def _fused(name, rng, N, G, V):
+    """Chunks of requests are generated in parallel threads, each from its own
+    child stream of the workload seed, so the result does not depend on the
+    thread count."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
     temp, k, top_p = 0.8, 50, 0.9
     gammas = np.full(N, G, dtype=np.int64)
     T = N * G
+    kk = min(k, V)
     t_bits = np.empty((N, G + 1, V), dtype=np.uint16)
     d_bits = np.empty((N, G, V), dtype=np.uint16)
-    step = 32
-    for r0 in range(0, N, step):  # chunked to bound temporaries
-        r1 = min(N, r0 + step)
-        tl = rng.standard_normal((r1 - r0, G + 1, V), dtype=np.float32) * np.float32(2.5)
+    ids = np.zeros((N, G), dtype=np.int32)
+    probs = name == "fused_probs"
+    if probs:
+        p = np.zeros((N, G + 1, V), dtype=np.float32)
+        q = np.zeros((N, G, V), dtype=np.float32)
+    step = 16
+    chunk_seeds = rng.integers(0, 2 ** 63 - 1, size=(N + step - 1) // step)
+
+    def work(c):
+        r0, r1 = c * step, min(N, (c + 1) * step)
+        crng = np.random.default_rng(int(chunk_seeds[c]))
+        tl = crng.standard_normal((r1 - r0, G + 1, V), dtype=np.float32) * np.float32(2.5)
         t_bits[r0:r1] = _to_bf16_bits(tl)
         dl = bf16_bits_to_f32(t_bits[r0:r1, :G]) + \
-            rng.standard_normal((r1 - r0, G, V), dtype=np.float32) * np.float32(0.7)
+            crng.standard_normal((r1 - r0, G, V), dtype=np.float32) * np.float32(0.7)
         d_bits[r0:r1] = _to_bf16_bits(dl)
-    t_bits = t_bits.reshape(T + N, V)
-    d_bits = d_bits.reshape(T, V)
-    kk = min(k, V)
-    d_idx, d_w = _top_support_softmax(bf16_bits_to_f32(d_bits), temp, kk) if T else (None, None)
-    if T:
-        pick = _inverse_cdf(rng, d_w)
-        ids = d_idx[np.arange(T), pick].astype(np.int32)
-    else:
-        ids = np.zeros(0, np.int32)
+        if G:
+            d32 = bf16_bits_to_f32(d_bits[r0:r1]).reshape(-1, V)
+            d_idx, d_w = _top_support_softmax(d32, temp, kk)
+            pick = _inverse_cdf(crng, d_w)
+            ids[r0:r1] = d_idx[np.arange(d_idx.shape[0]), pick].reshape(r1 - r0, G)
+            if probs:
+                np.put_along_axis(q[r0:r1].reshape(-1, V), d_idx, d_w, axis=-1)
+        if probs:
+            t_idx, t_w = _top_support_softmax(bf16_bits_to_f32(t_bits[r0:r1]).reshape(-1, V), temp, kk)
+            np.put_along_axis(p[r0:r1].reshape(-1, V), t_idx, t_w, axis=-1)
+
+    nchunks = len(chunk_seeds)
+    with ThreadPoolExecutor(max_workers=min(nchunks, os.cpu_count() or 1, 16)) as ex:
+        list(ex.map(work, range(nchunks)))
     ncomp, slots, _ = _kv_bookkeeping(rng, gammas)
-    out = dict(T=T, draft_ids=ids, cu_num_draft_tokens=None,
+    out = dict(T=T, draft_ids=ids.reshape(-1), cu_num_draft_tokens=None,
                temperature=np.full(N, temp, np.float32), top_k=np.full(N, k, np.int32),
                top_p=np.full(N, top_p, np.float32), num_computed_tokens=ncomp, slot_mapping=slots)
-    if name == "fused":
-        out.update(entry="logits", dtype="bf16", target=t_bits, draft=d_bits)
+    if not probs:
+        out.update(entry="logits", dtype="bf16", target=t_bits.reshape(T + N, V), draft=d_bits.reshape(T, V))
         return out
     # fused_probs: sparse fp32 probability rows with the same support size
-    t_idx, t_w = _top_support_softmax(bf16_bits_to_f32(t_bits), temp, kk)
-    p = np.zeros((T + N, V), dtype=np.float32)
-    np.put_along_axis(p, t_idx, t_w, axis=-1)
-    q = np.zeros((T, V), dtype=np.float32)
-    if T:
-        np.put_along_axis(q, d_idx, d_w, axis=-1)
-    out.update(entry="probs", dtype="f32", target=p, draft=q, top_k=None, top_p=None)
+    out.update(entry="probs", dtype="f32", target=p.reshape(T + N, V), draft=q.reshape(T, V), top_k=None,
+               top_p=None)
     return out
 
 
