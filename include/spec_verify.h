@@ -112,9 +112,9 @@ typedef struct spec_verify_args {
   const int32_t *top_k;     /* [N] or NULL; <= 0 or >= V disables (logits entry only) */
   const float *top_p;       /* [N] or NULL; >= 1 disables; must be > 0 (logits entry only) */
 
-  /* Randomness.  Test mode: both pointers set; u [T] in [0, 1) and E [N rows,
-   * exponentials_row_stride] > 0 are read as given.  Production mode: both
-   * NULL; u and E come from Philox4x32-10 (Salmon et al., SC'11) with key
+  /* Randomness.  Test mode: exponentials set (and uniforms, unless T = 0);
+   * u [T] in [0, 1) and E [N rows, exponentials_row_stride] > 0 are read as
+   * given.  Production mode: both NULL; u and E come from Philox4x32-10 (Salmon et al., SC'11) with key
    * (seed) and counters (j/4, 2r+1, offset) for u_j and (x/4, 2r, offset) for
    * E(x), r = rng_request_base + i; u = (w >> 8) 2^-24, E = -ln((2(w >> 9)+1) 2^-24). */
   const float *uniforms;

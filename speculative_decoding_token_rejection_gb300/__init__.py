@@ -162,7 +162,9 @@ def _rows(t, name, device, V, nrows, dtypes):
         raise ValueError(f"{name} must have shape [{nrows}, {V}], got {tuple(t.shape)}")
     if t.dtype not in dtypes:
         raise TypeError(f"{name} dtype {t.dtype} not in {dtypes}")
-    if t.stride(1) != 1 or (nrows > 1 and t.stride(0) < V):
+    if nrows == 0:
+        return None, V  # nothing to read; torch gives empty dims arbitrary strides
+    if (V > 1 and t.stride(1) != 1) or (nrows > 1 and t.stride(0) < V):
         raise ValueError(f"{name} rows must be unit-stride and non-overlapping")
     if t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")

@@ -111,8 +111,10 @@ sv_status spec_verify_check_args(const spec_verify_config *c, const spec_verify_
   if (a->target_row_stride < a->vocab_size) return fail(SV_ERR_INVALID_ARG, "target_row_stride < vocab_size");
   if (a->draft && a->draft_row_stride < a->vocab_size)
     return fail(SV_ERR_INVALID_ARG, "draft_row_stride < vocab_size");
-  if ((a->uniforms == nullptr) != (a->exponentials == nullptr))
-    return fail(SV_ERR_INVALID_ARG, "uniforms and exponentials must be given together (test mode) or not at all");
+  if (a->uniforms && !a->exponentials)
+    return fail(SV_ERR_INVALID_ARG, "uniforms without exponentials: test mode needs both");
+  if (a->exponentials && !a->uniforms && a->num_draft_tokens_total > 0)
+    return fail(SV_ERR_INVALID_ARG, "test mode with draft tokens needs uniforms");
   if (a->exponentials && a->exponentials_row_stride < a->vocab_size)
     return fail(SV_ERR_INVALID_ARG, "exponentials_row_stride < vocab_size");
   if (!a->out_tokens || !a->num_accepted) return fail(SV_ERR_INVALID_ARG, "out_tokens / num_accepted is NULL");

@@ -386,7 +386,7 @@ cudaError_t enable_probs_kernels(int max_cluster) {
 }
 
 cudaError_t launch_probs(const VerifyParams &p, int cluster, bool vec, cudaStream_t stream) {
-  const bool test = p.uniforms != nullptr;
+  const bool test = p.exponentials != nullptr;
   if (test) return vec ? launch_one<true, true>(p, cluster, stream) : launch_one<true, false>(p, cluster, stream);
   return vec ? launch_one<false, true>(p, cluster, stream) : launch_one<false, false>(p, cluster, stream);
 }

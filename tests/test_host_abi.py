@@ -85,6 +85,10 @@ def cfg(**kw):
                 setattr(a, "exponentials_row_stride", 1000)), sv.SV_OK),
     (lambda a: (setattr(a, "uniforms", FAKE), setattr(a, "exponentials", FAKE),
                 setattr(a, "exponentials_row_stride", 10)), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "exponentials", FAKE), sv.SV_ERR_INVALID_ARG),  # test mode, T > 0, no uniforms
+    (lambda a: (setattr(a, "exponentials", FAKE), setattr(a, "exponentials_row_stride", 1000),
+                setattr(a, "num_reqs", 2), setattr(a, "max_spec_len", 0),
+                setattr(a, "num_draft_tokens_total", 0)), sv.SV_OK),  # T = 0: uniforms may be absent
     (lambda a: setattr(a, "out_tokens", None), sv.SV_ERR_INVALID_ARG),
     (lambda a: setattr(a, "num_accepted", None), sv.SV_ERR_INVALID_ARG),
     (lambda a: (setattr(a, "cu_num_draft_tokens", FAKE), setattr(a, "num_draft_tokens_total", 5)), sv.SV_OK),
@@ -127,3 +131,29 @@ def test_create_without_gpu_reports_cuda_error(lib):
     with pytest.raises(sv.SpecVerifyError) as ei:
         sv.spec_verify_create(4, 4, 1000)
     assert ei.value.code == sv.SV_ERR_CUDA
+
+
+def test_gpu_test_workloads_pass_host_marshalling(lib):
+    """Every workload the GPU tests send goes through the binding's tensor
+    checks and the library's host validation without error (CPU tensors: the
+    pointers are only checked for presence)."""
+    import torch
+    import workloads
+    import test_gpu_probs as tg
+    cases = list(tg.edge_cases().values())
+    cases += [workloads.make(n, **kw) for n, kw in tg.CASES if n != "fused_probs" or kw]
+    cfg_ = sv.make_config(1 << 20, sv.SV_MAX_SPEC_LEN, 1 << 18)
+    for w in cases:
+        t = workloads.as_torch(w, "cpu")
+        N, G, T = w["N"], w["gamma"], w["T"]
+        for production in (False, True):
+            a = sv.build_args(
+                entry=w["entry"], draft_ids=t["draft_ids"], target=t["target"], draft=t["draft"],
+                cu_num_draft_tokens=t["cu_num_draft_tokens"], temperature=t["temperature"],
+                uniforms=None if production else t["uniforms"],
+                exponentials=None if production else t["exponentials"],
+                out_tokens=torch.empty((N, G + 1), dtype=torch.int32), num_accepted=torch.empty(N, dtype=torch.int32),
+                num_computed_tokens=t.get("num_computed_tokens"), slot_mapping=t.get("slot_mapping"),
+                dbg_py=torch.empty(T), dbg_qy=torch.empty(T), status=torch.zeros(1, dtype=torch.int32))
+            assert sv.spec_verify_check_args(cfg_, a) == sv.SV_OK, (w.get("name"), production,
+                                                                   lib.spec_verify_last_error())
