@@ -296,7 +296,7 @@ def run_ours(args, world, rank, local_rank):
                      "kernel_source_sha": kernel_source_hash(), "traffic_source_sha": traffic_sha},
         "acceptance": {"rate": float(acc.sum() / (gammas.sum() * K)),
                        "mean_accepted": float(acc.mean()),
-                       "committed_tokens_per_s": world * float((acc + 1).sum()) / K / (total_ms / 1e3) * 1.0,
+                       "committed_tokens_per_s": world * float((acc + 1).sum()) / (total_ms / 1e3),
                        "A_hist": np.bincount(acc.reshape(-1), minlength=G + 1).tolist()},
         "gpu_launches": K,
         "clocks": clocks.summary(t0, t1),

@@ -195,3 +195,30 @@ __device__ __forceinline__ void chunk_of(int V, uint32_t rank, uint32_t ncta, in
 }
 
 }  // namespace sv
+
+namespace sv {
+
+// Committed tokens, num_accepted and the KV rollback of request i, written by
+// the whole CTA that calls it (the cluster's first CTA).  tok(k) yields the
+// k-th committed token for k <= A.  ("Rejection sampling ... RejectionSampler":
+// output [batch, max_spec_len + 1] padded with -1; "How speculative decoding
+// interacts with the KV cache" 3.1: num_computed_tokens -= gamma - A when > 0;
+// rejected drafts' slots -> PADDING_SLOT_ID.)
+template <typename TokFn>
+__device__ __forceinline__ void emit_request(int i, int G, int g, int A, bool valid, int64_t tb, uint32_t req_bits,
+                                             TokFn tok, int32_t *out, int32_t *nacc, int32_t *ncomp,
+                                             int64_t *slots, int32_t *status) {
+  const int tid = threadIdx.x;
+  const int row_len = G + 1;
+  int32_t *orow = out + static_cast<int64_t>(i) * row_len;
+  for (int k = tid; k < row_len; k += kThreads) orow[k] = (valid && k <= A) ? tok(k) : -1;
+  if (valid && slots)
+    for (int j = A + 1 + tid; j <= g; j += kThreads) slots[tb + j] = -1;
+  if (tid == 0) {
+    nacc[i] = valid ? A : 0;
+    if (valid && ncomp && ncomp[i] > 0) ncomp[i] -= (g - A);
+    if (req_bits && status) atomicOr(status, static_cast<int>(req_bits));
+  }
+}
+
+}  // namespace sv

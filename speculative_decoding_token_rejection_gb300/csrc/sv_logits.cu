@@ -1,0 +1,764 @@
+// sv_logits.cu -- verifier kernel for the logits entry (bf16 or fp32 logits).
+//
+// The target and draft logits go through the same transform before the test
+// ("vLLM source walk-through (10)", section "Rejection sampling: the two
+// branches of RejectionSampler": temperature, top-k, top-p on both sides;
+// "Speculative Decoding: propose, verify, accept", section 06: identical
+// transforms are required for exactness):
+//   p(x) = exp((l(x) - l_max) / T) / Z'  for l(x) in the kept set, else 0,
+// where the kept set is {x : key(x) >= tau_k} (tau_k = k-th largest logit,
+// ties kept) cut further by top-p to the shortest descending prefix whose
+// mass reaches top_p (ties at the cut kept), and Z' sums the kept terms.
+//
+// One thread-block cluster per request.  A random request walks its positions
+// in order, as a sequential verifier reads them: position j loads the target
+// and draft row chunks once from HBM into the CTAs' shared memory, computes
+// the row statistics there (max, exact radix-select threshold for top-k,
+// fixed-point mass radix-select for the top-p cut, normaliser), tests
+// fl32(u * q(y)) < p(y), and either moves on or runs the exponential race of
+// the residual max(p - q, 0) over the rows already in shared memory.  When all
+// drafts pass, the bonus row is raced over p.  Rows after the first rejection
+// are never read.  Greedy requests stream target rows from HBM and take the
+// cluster argmax of the raw logits, stopping at the first mismatch.
+//
+// All sums are deterministic: integer histograms and fixed-point (2^-40)
+// masses use atomics whose order cannot change the result, and float sums
+// use a fixed reduction tree and rank order across the cluster.
+#include <cmath>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point scale of the top-p masses
+
+// ---------------------------------------------------------------------------
+// element types: raw bits in shared memory, order-preserving integer keys
+// (-0 folded onto +0, so equal values have equal keys)
+// ---------------------------------------------------------------------------
+template <typename TIn>
+struct Elem;
+
+template <>
+struct Elem<uint16_t> {  // bf16 bit patterns
+  static constexpr int kBits = 16;
+  __device__ static float val(uint32_t b) { return __uint_as_float(b << 16); }
+  __device__ static uint32_t key(uint32_t b) {
+    if (b == 0x8000u) b = 0u;
+    return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+  }
+  __device__ static float val_of_key(uint32_t k) {
+    const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return val(b);
+  }
+  __device__ static bool is_nan(uint32_t b) { return (b & 0x7F80u) == 0x7F80u && (b & 0x7Fu) != 0u; }
+  __device__ static bool is_pinf(uint32_t b) { return b == 0x7F80u; }
+  __device__ static bool finite(uint32_t b) { return (b & 0x7F80u) != 0x7F80u; }
+};
+
+template <>
+struct Elem<float> {  // fp32 values (bits handled as uint32)
+  static constexpr int kBits = 32;
+  __device__ static float val(uint32_t b) { return __uint_as_float(b); }
+  __device__ static uint32_t key(uint32_t b) {
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  __device__ static float val_of_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+  }
+  __device__ static bool is_nan(uint32_t b) { return (b & 0x7F800000u) == 0x7F800000u && (b & 0x7FFFFFu) != 0u; }
+  __device__ static bool is_pinf(uint32_t b) { return b == 0x7F800000u; }
+  __device__ static bool finite(uint32_t b) { return (b & 0x7F800000u) != 0x7F800000u; }
+};
+
+template <typename TIn>
+__device__ __forceinline__ uint32_t bits_at(const TIn *row, int x) {
+  return static_cast<uint32_t>(row[x]);
+}
+template <>
+__device__ __forceinline__ uint32_t bits_at<float>(const float *row, int x) {
+  return __float_as_uint(row[x]);
+}
+
+// ---------------------------------------------------------------------------
+// shared memory
+// ---------------------------------------------------------------------------
+constexpr uint32_t kFlagBad = 1u;     // NaN or +inf in a random row
+constexpr uint32_t kFlagFinite = 2u;  // at least one finite logit
+
+struct StatPart {  // one CTA's partials of one reduction round, for up to 2 rows
+  uint32_t maxkey[2];
+  uint32_t flags[2];
+  float z[2];
+  uint32_t cnt[2][256];
+  unsigned long long mass[2][256];
+};
+
+struct RowStats {
+  uint32_t cut;  // kept set: key >= cut
+  float vmax;    // largest logit
+  float c2;      // log2(e) / T
+  float zp;      // normaliser over the kept set
+};
+
+struct Select {  // result of one radix digit choice, per row
+  uint32_t prefix[2];
+  unsigned long long need[2];
+};
+
+struct LogitsSmem {
+  ReduceSmem red;
+  StatPart part[2];
+  StatPart sum;
+  float wz[2][kWarps];
+  Select sel;
+  int32_t tok[SV_MAX_SPEC_LEN + 1];
+};
+
+enum : uint32_t { kRMax = 1u, kRCnt = 2u, kRMass = 4u, kRZ = 8u };
+
+__device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
+  const int tid = threadIdx.x;
+  if (what & kRCnt)
+    for (int t = tid; t < nr * 256; t += kThreads) p.cnt[t >> 8][t & 255] = 0u;
+  if (what & kRMass)
+    for (int t = tid; t < nr * 256; t += kThreads) p.mass[t >> 8][t & 255] = 0ull;
+  if (tid < 2) {
+    p.maxkey[tid] = 0u;
+    p.flags[tid] = 0u;
+    p.z[tid] = 0.0f;
+  }
+}
+
+// Combine every CTA's part[par] into sum (the same in every CTA of the cluster).
+__device__ __forceinline__ void stat_reduce(LogitsSmem &sm, int par, uint32_t what, int nr, uint32_t ncta) {
+  __syncthreads();
+  cluster_sync();
+  const int tid = threadIdx.x;
+  StatPart &p = sm.part[par];
+  if (what & kRCnt) {
+    for (int t = tid; t < nr * 256; t += kThreads) {
+      const uint32_t a = smem_addr(&p.cnt[t >> 8][t & 255]);
+      uint32_t s = 0;
+      for (uint32_t c = 0; c < ncta; ++c) s += ld_dsmem_u32(map_to_rank(a, c));
+      sm.sum.cnt[t >> 8][t & 255] = s;
+    }
+  }
+  if (what & kRMass) {
+    for (int t = tid; t < nr * 256; t += kThreads) {
+      const uint32_t a = smem_addr(&p.mass[t >> 8][t & 255]);
+      unsigned long long s = 0;
+      for (uint32_t c = 0; c < ncta; ++c) s += ld_dsmem_u64(map_to_rank(a, c));
+      sm.sum.mass[t >> 8][t & 255] = s;
+    }
+  }
+  if (tid < nr) {
+    if (what & kRMax) {
+      uint32_t mk = 0, fl = 0;
+      for (uint32_t c = 0; c < ncta; ++c) {
+        mk = max(mk, ld_dsmem_u32(map_to_rank(smem_addr(&p.maxkey[tid]), c)));
+        fl |= ld_dsmem_u32(map_to_rank(smem_addr(&p.flags[tid]), c));
+      }
+      sm.sum.maxkey[tid] = mk;
+      sm.sum.flags[tid] = fl;
+    }
+    if (what & kRZ) {
+      float z = 0.0f;
+      for (uint32_t c = 0; c < ncta; ++c) z += __uint_as_float(ld_dsmem_u32(map_to_rank(smem_addr(&p.z[tid]), c)));
+      sm.sum.z[tid] = z;
+    }
+  }
+  __syncthreads();
+}
+
+// Deterministic block sum of one float per thread per row into part.z[r].
+__device__ __forceinline__ void block_sum_z(LogitsSmem &sm, StatPart &p, const float v[2], int nr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int r = 0; r < nr; ++r) {
+    float s = v[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) sm.wz[r][warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < nr) {
+    float s = 0.0f;
+    for (int w = 0; w < kWarps; ++w) s += sm.wz[threadIdx.x][w];
+    p.z[threadIdx.x] = s;
+  }
+}
+
+// Pick the radix digit of row r: walking bins from 255 down, the first bin b
+// where (mass above b) + h[b] >= need.  Run by one warp; writes sm.sel.
+template <typename H>
+__device__ __forceinline__ void select_digit(LogitsSmem &sm, int r, const H *h, int shift) {
+  const int lane = threadIdx.x & 31;
+  // lane L owns bins [8L, 8L+8)
+  unsigned long long own = 0;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) own += static_cast<unsigned long long>(h[8 * lane + t]);
+  // inclusive suffix sum over lanes (bins above included)
+  unsigned long long suf = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long v = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+    if (lane + o < 32) suf += v;
+  }
+  const unsigned long long above_lane = suf - own;  // bins of higher lanes
+  const unsigned long long need = sm.sel.need[r];
+  int found = -1;
+  unsigned long long above = 0;
+  if (above_lane < need && suf >= need) {
+    unsigned long long acc = above_lane;
+    for (int t = 7; t >= 0; --t) {
+      const unsigned long long hv = static_cast<unsigned long long>(h[8 * lane + t]);
+      if (acc + hv >= need) {
+        found = 8 * lane + t;
+        above = acc;
+        break;
+      }
+      acc += hv;
+    }
+  }
+  const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0);
+  const int src = ball ? (__ffs(ball) - 1) : 0;
+  const int d = __shfl_sync(0xFFFFFFFFu, found, src);
+  const unsigned long long ab = __shfl_sync(0xFFFFFFFFu, above, src);
+  if (lane == 0) {
+    const int dd = d < 0 ? 0 : d;  // need > total cannot happen for valid inputs
+    sm.sel.prefix[r] |= static_cast<uint32_t>(dd) << shift;
+    sm.sel.need[r] = need - ab;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// row statistics of one position (target row, and draft row when nr == 2)
+// ---------------------------------------------------------------------------
+template <typename TIn, bool kVec>
+__device__ bool position_stats(LogitsSmem &sm, const TIn *const grow[2], TIn *const srow[2], int nr, int n,
+                               float c2, int topk, float topp, RowStats st[2], int &step, uint32_t ncta) {
+  using E = Elem<TIn>;
+  constexpr int kB = E::kBits;
+  const int tid = threadIdx.x;
+  const bool use_k = topk > 0;
+  const bool use_p = topp < 1.0f;
+
+  // pass 1: HBM -> shared memory, max key, value checks, top-digit counts
+  int par = step & 1;
+  zero_part(sm.part[par], kRMax | (use_k ? kRCnt : 0u), nr);
+  __syncthreads();
+  for (int r = 0; r < nr; ++r) {
+    uint32_t mk = 0, fl = 0;
+    const TIn *g = grow[r];
+    TIn *s = srow[r];
+    constexpr int kPer = 16 / sizeof(TIn);
+    int xs = 0;
+    if (kVec) {
+      const int nv = n / kPer;
+      const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
+      uint4 *s4 = reinterpret_cast<uint4 *>(s);
+      for (int v = tid; v < nv; v += kThreads) {
+        uint4 d;
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+                     : "l"(g4 + v));
+        s4[v] = d;
+        const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+#pragma unroll
+          for (int h = 0; h < (kB == 16 ? 2 : 1); ++h) {
+            const uint32_t b = (kB == 16) ? ((w[t] >> (16 * h)) & 0xFFFFu) : w[t];
+            const uint32_t k = E::key(b);
+            if (E::is_nan(b) || E::is_pinf(b)) fl |= kFlagBad;
+            if (E::finite(b)) fl |= kFlagFinite;
+            mk = max(mk, k);
+            if (use_k) atomicAdd(&sm.part[par].cnt[r][k >> (kB - 8)], 1u);
+          }
+        }
+      }
+      xs = nv * kPer;
+    }
+    for (int x = xs + tid; x < n; x += kThreads) {
+      const TIn e = g[x];
+      s[x] = e;
+      const uint32_t b = bits_at(s, x);
+      const uint32_t k = E::key(b);
+      if (E::is_nan(b) || E::is_pinf(b)) fl |= kFlagBad;
+      if (E::finite(b)) fl |= kFlagFinite;
+      mk = max(mk, k);
+      if (use_k) atomicAdd(&sm.part[par].cnt[r][k >> (kB - 8)], 1u);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
+      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+    }
+    if ((tid & 31) == 0) {
+      atomicMax(&sm.part[par].maxkey[r], mk);
+      atomicOr(&sm.part[par].flags[r], fl);
+    }
+  }
+  stat_reduce(sm, par, kRMax | (use_k ? kRCnt : 0u), nr, ncta);
+  ++step;
+  for (int r = 0; r < nr; ++r) {
+    const uint32_t f = sm.sum.flags[r];
+    if ((f & kFlagBad) || !(f & kFlagFinite)) return false;
+    st[r].vmax = E::val_of_key(sm.sum.maxkey[r]);
+    st[r].c2 = c2;
+  }
+
+  // top-k: exact k-th largest key by radix digits (ties kept)
+  uint32_t tau[2] = {0u, 0u};
+  if (use_k) {
+    if (tid < 2) {
+      sm.sel.prefix[tid] = 0u;
+      sm.sel.need[tid] = static_cast<unsigned long long>(topk);
+    }
+    __syncthreads();
+    for (int shift = kB - 8;; shift -= 8) {
+      if ((tid >> 5) < nr) select_digit(sm, tid >> 5, sm.sum.cnt[tid >> 5], shift);
+      __syncthreads();
+      if (shift == 0) break;
+      par = step & 1;
+      zero_part(sm.part[par], kRCnt, nr);
+      __syncthreads();
+      for (int r = 0; r < nr; ++r) {
+        const uint32_t hi = sm.sel.prefix[r] >> (shift);
+        const TIn *s = srow[r];
+        for (int x = tid; x < n; x += kThreads) {
+          const uint32_t k = E::key(bits_at(s, x));
+          if ((k >> shift) == hi) atomicAdd(&sm.part[par].cnt[r][(k >> (shift - 8)) & 255u], 1u);
+        }
+      }
+      stat_reduce(sm, par, kRCnt, nr, ncta);
+      ++step;
+    }
+    for (int r = 0; r < nr; ++r) tau[r] = sm.sel.prefix[r];
+  }
+
+  // normaliser over the top-k set, and the top digit of the top-p masses
+  par = step & 1;
+  zero_part(sm.part[par], kRZ | (use_p ? kRMass : 0u), nr);
+  __syncthreads();
+  {
+    float zt[2] = {0.0f, 0.0f};
+    for (int r = 0; r < nr; ++r) {
+      const TIn *s = srow[r];
+      float sum = 0.0f, comp = 0.0f;
+      for (int x = tid; x < n; x += kThreads) {
+        const uint32_t b = bits_at(s, x);
+        const uint32_t k = E::key(b);
+        if (k < tau[r]) continue;
+        const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2));
+        const float y = e - comp;  // Kahan
+        const float t = sum + y;
+        comp = (t - sum) - y;
+        sum = t;
+        if (use_p)
+          atomicAdd(&sm.part[par].mass[r][k >> (kB - 8)], static_cast<unsigned long long>(__float2ull_rn(e * kMassScale)));
+      }
+      zt[r] = sum;
+    }
+    block_sum_z(sm, sm.part[par], zt, nr);
+  }
+  stat_reduce(sm, par, kRZ | (use_p ? kRMass : 0u), nr, ncta);
+  ++step;
+  for (int r = 0; r < nr; ++r) {
+    st[r].cut = tau[r];
+    st[r].zp = sm.sum.z[r];
+  }
+
+  // top-p: largest key c with mass(key >= c) >= top_p * total, by radix digits
+  if (use_p) {
+    if (tid < nr) {
+      unsigned long long tot = 0;
+      for (int b = 0; b < 256; ++b) tot += sm.sum.mass[tid][b];
+      sm.sel.prefix[tid] = 0u;
+      unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(tot));
+      sm.sel.need[tid] = need > 0 ? need : 1ull;
+    }
+    __syncthreads();
+    for (int shift = kB - 8;; shift -= 8) {
+      if ((tid >> 5) < nr) select_digit(sm, tid >> 5, sm.sum.mass[tid >> 5], shift);
+      __syncthreads();
+      if (shift == 0) break;
+      par = step & 1;
+      zero_part(sm.part[par], kRMass, nr);
+      __syncthreads();
+      for (int r = 0; r < nr; ++r) {
+        const uint32_t hi = sm.sel.prefix[r] >> shift;
+        const TIn *s = srow[r];
+        for (int x = tid; x < n; x += kThreads) {
+          const uint32_t b = bits_at(s, x);
+          const uint32_t k = E::key(b);
+          if (k < tau[r] || (k >> shift) != hi) continue;
+          const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2));
+          atomicAdd(&sm.part[par].mass[r][(k >> (shift - 8)) & 255u],
+                    static_cast<unsigned long long>(__float2ull_rn(e * kMassScale)));
+        }
+      }
+      stat_reduce(sm, par, kRMass, nr, ncta);
+      ++step;
+    }
+    // normaliser over the final kept set
+    par = step & 1;
+    zero_part(sm.part[par], kRZ, nr);
+    __syncthreads();
+    float zt[2] = {0.0f, 0.0f};
+    for (int r = 0; r < nr; ++r) {
+      const uint32_t cut = max(tau[r], sm.sel.prefix[r]);
+      st[r].cut = cut;
+      const TIn *s = srow[r];
+      float sum = 0.0f, comp = 0.0f;
+      for (int x = tid; x < n; x += kThreads) {
+        const uint32_t b = bits_at(s, x);
+        if (E::key(b) < cut) continue;
+        const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2));
+        const float y = e - comp;
+        const float t = sum + y;
+        comp = (t - sum) - y;
+        sum = t;
+      }
+      zt[r] = sum;
+    }
+    block_sum_z(sm, sm.part[par], zt, nr);
+    stat_reduce(sm, par, kRZ, nr, ncta);
+    ++step;
+    for (int r = 0; r < nr; ++r) st[r].zp = sm.sum.z[r];
+  }
+  return true;
+}
+
+// Probability of one logit under a row's statistics (0 outside the kept set).
+template <typename TIn>
+__device__ __forceinline__ float prob_of(uint32_t b, const RowStats &st) {
+  using E = Elem<TIn>;
+  if (E::key(b) < st.cut) return 0.0f;
+  const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st.vmax), st.c2));
+  return __fdiv_rn(e, st.zp);
+}
+
+// ---------------------------------------------------------------------------
+// race over the rows in shared memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void consider_drawn_l(float w, uint32_t word, int x, float &bk, int &bx) {
+  const float U = e_word_to_open_uniform(word);
+  const float om = 1.0f - U;
+  if (__fmaf_rn(bk, om, -w) > 0.0f) return;  // w / (1-U) < bk and E >= 1-U: cannot win
+  const float E = -logf(U);
+  const float key = __fdiv_rn(w, E);
+  if (key > bk) {
+    bk = key;
+    bx = x;
+  }
+}
+
+template <typename TIn, bool kTest, bool kResidual>
+__device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const RowStats &ps, const RowStats &qs,
+                                          int x0, int n, const float *Erow, const RngKey &rk, uint32_t rs, float &bk,
+                                          int &bx, uint32_t &flags) {
+  const int tid = threadIdx.x;
+  for (int q4 = tid; 4 * q4 < n; q4 += kThreads) {
+    float w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int x = 4 * q4 + t;
+      w[t] = 0.0f;
+      if (x < n) {
+        const float p = prob_of<TIn>(bits_at(sp, x), ps);
+        if (kResidual) {
+          const float q = prob_of<TIn>(bits_at(sq, x), qs);
+          const float d = __fsub_rn(p, q);
+          w[t] = d > 0.0f ? d : 0.0f;
+        } else {
+          w[t] = p > 0.0f ? p : 0.0f;
+        }
+      }
+    }
+    if (!(w[0] > 0.0f || w[1] > 0.0f || w[2] > 0.0f || w[3] > 0.0f)) continue;
+    const int xg = x0 + 4 * q4;  // global vocabulary index of this quad (x0 is a multiple of 8)
+    if (kTest) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (!(w[t] > 0.0f)) continue;
+        const float E = Erow[xg + t];
+        if (!(E > 0.0f)) {
+          flags |= SV_DATA_BAD_EXPONENTIAL;
+          continue;
+        }
+        const float key = __fdiv_rn(w[t], E);
+        if (key > bk) {
+          bk = key;
+          bx = xg + t;
+        }
+      }
+    } else {
+      const uint4 wd = draw_e_words(rk, rs, static_cast<uint32_t>(xg) >> 2);
+      if (w[0] > 0.0f) consider_drawn_l(w[0], wd.x, xg + 0, bk, bx);
+      if (w[1] > 0.0f) consider_drawn_l(w[1], wd.y, xg + 1, bk, bx);
+      if (w[2] > 0.0f) consider_drawn_l(w[2], wd.z, xg + 2, bk, bx);
+      if (w[3] > 0.0f) consider_drawn_l(w[3], wd.w, xg + 3, bk, bx);
+    }
+  }
+}
+
+// Greedy: thread-local argmax of raw logits of a global row chunk.
+template <typename TIn, bool kVec>
+__device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsigned long long &best, uint32_t &flags) {
+  using E = Elem<TIn>;
+  const int tid = threadIdx.x;
+  auto take = [&](uint32_t b, int x) {
+    if (E::is_nan(b)) {
+      flags |= SV_DATA_BAD_VALUES;
+      return;
+    }
+    const unsigned long long k =
+        (static_cast<unsigned long long>(E::key(b)) << 32) | static_cast<unsigned long long>(~static_cast<uint32_t>(x0 + x));
+    best = umax64(best, k);
+  };
+  int xs = 0;
+  if (kVec) {
+    constexpr int kPer = 16 / sizeof(TIn);
+    const int nv = n / kPer;
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
+    for (int v = tid; v < nv; v += kThreads) {
+      uint4 d;
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+                   : "l"(g4 + v));
+      const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (E::kBits == 16) {
+          take(w[t] & 0xFFFFu, v * kPer + 2 * t);
+          take(w[t] >> 16, v * kPer + 2 * t + 1);
+        } else {
+          take(w[t], v * kPer + t);
+        }
+      }
+    }
+    xs = nv * kPer;
+  }
+  for (int x = xs + tid; x < n; x += kThreads) take(bits_at(g, x), x);
+}
+
+template <typename TIn, bool kTest, bool kVec>
+__global__ void __launch_bounds__(kThreads) logits_kernel(const VerifyParams P, int chunk) {
+  using E = Elem<TIn>;
+  extern __shared__ __align__(16) unsigned char dyn_smem[];
+  __shared__ LogitsSmem sm;
+  TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem) + chunk};
+
+  const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
+  const int i = static_cast<int>(blockIdx.x / ncta);
+  const int tid = threadIdx.x;
+  const int G = P.G, V = P.V;
+  const TIn *tgt = static_cast<const TIn *>(P.target);
+  const TIn *drf = static_cast<const TIn *>(P.draft);
+  const int64_t ts = P.target_stride, ds = P.draft_stride;
+  const int x0 = min(V, static_cast<int>(rank) * chunk);
+  const int n = min(V, x0 + chunk) - x0;
+
+  // a0: ragged decode
+  int64_t s, e;
+  if (P.cu) {
+    s = i ? P.cu[i - 1] : 0;
+    e = P.cu[i];
+  } else {
+    s = static_cast<int64_t>(i) * G;
+    e = s + G;
+  }
+  uint32_t req_bits = 0;
+  bool valid = true;
+  if (s < 0 || e < s || e > P.T || e - s > G) {
+    req_bits |= SV_DATA_BAD_CU;
+    valid = false;
+  }
+  const int g = valid ? static_cast<int>(e - s) : 0;
+  const int64_t tb = s + i;
+  const float temp = P.temperature ? P.temperature[i] : 1.0f;
+  if (valid && (!(temp >= 0.0f) || isinf(temp))) {
+    req_bits |= SV_DATA_BAD_PARAM;
+    valid = false;
+  }
+  const bool greedy = valid && temp == 0.0f;
+  int A = 0;
+  int32_t last_tok = -1;
+  int step = 0;
+
+  if (greedy) {
+    for (int j = 0;; ++j) {
+      unsigned long long best = 0;
+      uint32_t fl = 0;
+      argmax_logits<TIn, kVec>(tgt + (tb + j) * ts + x0, x0, n, best, fl);
+      const KeyFlags r = cluster_reduce(KeyFlags{best, fl}, sm.red, step++, ncta);
+      if (r.flags & SV_DATA_BAD_VALUES) {
+        req_bits |= SV_DATA_BAD_VALUES;
+        valid = false;
+        break;
+      }
+      const int gj = static_cast<int>(key_index(r.key));
+      if (tid == 0) sm.tok[j] = gj;
+      if (j == g) {
+        A = g;
+        break;
+      }
+      const int y = P.ids[s + j];
+      if (y < 0 || y >= V) {
+        req_bits |= SV_DATA_BAD_DRAFT_ID;
+        valid = false;
+        break;
+      }
+      if (y != gj) {
+        A = j;
+        break;
+      }
+    }
+  } else if (valid) {
+    int topk = P.top_k ? P.top_k[i] : 0;
+    if (topk >= V) topk = 0;
+    if (topk < 0) topk = 0;
+    const float topp = P.top_p ? P.top_p[i] : 1.0f;
+    if (!(topp > 0.0f)) {
+      req_bits |= SV_DATA_BAD_PARAM;
+      valid = false;
+    } else {
+      const float c2 = __fdiv_rn(kLog2e, temp);
+      const RngKey rk{P.seed_lo, P.seed_hi, P.off_lo, P.off_hi};
+      const uint32_t rs = P.req_base + static_cast<uint32_t>(i);
+      const float *Erow = kTest ? P.exponentials + static_cast<int64_t>(i) * P.exp_stride : nullptr;
+      RowStats st[2];
+      for (int j = 0;; ++j) {
+        const int nr = (j < g) ? 2 : 1;
+        if (nr == 2 && drf == nullptr) {
+          req_bits |= SV_DATA_MISSING_DRAFT;
+          valid = false;
+          break;
+        }
+        const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
+        if (!position_stats<TIn, kVec>(sm, grow, srow, nr, n, c2, topk, topp, st, step, ncta)) {
+          req_bits |= SV_DATA_BAD_VALUES;
+          valid = false;
+          break;
+        }
+        float bk = 0.0f;
+        int bx = -1;
+        uint32_t fl = 0;
+        bool residual = false;
+        if (j < g) {
+          const int y = P.ids[s + j];
+          if (y < 0 || y >= V) {
+            req_bits |= SV_DATA_BAD_DRAFT_ID;
+            valid = false;
+            break;
+          }
+          const float py = prob_of<TIn>(bits_at(tgt + (tb + j) * ts, y), st[0]);
+          const float qy = prob_of<TIn>(bits_at(drf + (s + j) * ds, y), st[1]);
+          if (rank == 0 && tid == 0) {
+            if (P.dbg_py) P.dbg_py[s + j] = py;
+            if (P.dbg_qy) P.dbg_qy[s + j] = qy;
+          }
+          const float u = kTest ? P.uniforms[s + j] : draw_uniform(rk, rs, static_cast<uint32_t>(j));
+          if (__fmul_rn(u, qy) < py) {
+            if (tid == 0) sm.tok[j] = y;
+            continue;  // accepted: next position
+          }
+          residual = true;
+          race_smem<TIn, kTest, true>(srow[0], srow[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl);
+        } else {
+          race_smem<TIn, kTest, false>(srow[0], srow[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
+        }
+        KeyFlags r = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
+        if (r.key == 0ull && residual) {  // no positive residual key: race over p with the same E
+          bk = 0.0f;
+          bx = -1;
+          fl = 0;
+          race_smem<TIn, kTest, false>(srow[0], srow[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
+          const KeyFlags r2 = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
+          r.key = r2.key;
+          r.flags |= r2.flags;
+        }
+        req_bits |= r.flags;
+        if (r.key == 0ull) {
+          req_bits |= SV_DATA_EMPTY_DISTRIBUTION;
+          last_tok = 0;
+        } else {
+          last_tok = static_cast<int32_t>(key_index(r.key));
+        }
+        A = j;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  if (rank == 0) {
+    auto tok = [&](int k) -> int32_t { return (k == A && !greedy) ? last_tok : sm.tok[k]; };
+    emit_request(i, G, g, A, valid, tb, req_bits, tok, P.out, P.nacc, P.ncomp, P.slots, P.status);
+  }
+  cluster_sync();
+}
+
+template <typename TIn, bool kTest, bool kVec>
+cudaError_t launch_one(const VerifyParams &p, int cluster, int chunk, size_t dyn, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.N) * static_cast<unsigned>(cluster), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, logits_kernel<TIn, kTest, kVec>, p, chunk);
+}
+
+template <typename TIn, bool kTest, bool kVec>
+cudaError_t enable_one(int max_cluster, int max_dyn) {
+  cudaError_t e = cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+  if (e != cudaSuccess) return e;
+  if (max_cluster > 8)
+    return cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t logits_static_smem() { return sizeof(LogitsSmem); }
+
+cudaError_t enable_logits_kernels(int max_cluster, int max_dyn) {
+  cudaError_t e;
+  if ((e = enable_one<uint16_t, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<uint16_t, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<uint16_t, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<uint16_t, false, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<float, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<float, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<float, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_one<float, false, false>(max_cluster, max_dyn);
+}
+
+cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
+  const bool test = p.exponentials != nullptr;
+  const size_t dyn = 2 * static_cast<size_t>(chunk) * (bf16 ? 2 : 4);
+  if (bf16) {
+    if (test) return vec ? launch_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
+                         : launch_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);
+    return vec ? launch_one<uint16_t, false, true>(p, cluster, chunk, dyn, stream)
+               : launch_one<uint16_t, false, false>(p, cluster, chunk, dyn, stream);
+  }
+  if (test) return vec ? launch_one<float, true, true>(p, cluster, chunk, dyn, stream)
+                       : launch_one<float, true, false>(p, cluster, chunk, dyn, stream);
+  return vec ? launch_one<float, false, true>(p, cluster, chunk, dyn, stream)
+             : launch_one<float, false, false>(p, cluster, chunk, dyn, stream);
+}
+
+}  // namespace sv

@@ -330,23 +330,8 @@ __global__ void __launch_bounds__(kThreads) probs_kernel(const VerifyParams P) {
 
   // a6 / a7: outputs and KV rollback, written by the cluster's first CTA
   if (rank == 0) {
-    const int row_len = G + 1;
-    int32_t *orow = P.out + static_cast<int64_t>(i) * row_len;
-    for (int k = tid; k < row_len; k += kThreads) {
-      int32_t v = SV_PLACEHOLDER_TOKEN_ID;
-      if (valid && k <= A) {
-        if (greedy) v = sm.tok[k];
-        else v = (k == A) ? last_tok : P.ids[s + k];
-      }
-      orow[k] = v;
-    }
-    if (valid && P.slots)
-      for (int j = A + 1 + tid; j <= g; j += kThreads) P.slots[tb + j] = SV_PADDING_SLOT_ID;
-    if (tid == 0) {
-      P.nacc[i] = valid ? A : 0;
-      if (valid && P.ncomp && P.ncomp[i] > 0) P.ncomp[i] -= (g - A);
-      if (req_bits && P.status) atomicOr(P.status, static_cast<int>(req_bits));
-    }
+    auto tok = [&](int k) -> int32_t { return greedy ? sm.tok[k] : (k == A ? last_tok : P.ids[s + k]); };
+    emit_request(i, G, g, A, valid, tb, req_bits, tok, P.out, P.nacc, P.ncomp, P.slots, P.status);
   }
   cluster_sync();  // peers may still be reading this CTA's reduction slot
 }
