@@ -7,6 +7,12 @@ request and one row at a time, see that file's header for the pages it
 follows); this module only compiles it with gcc and marshals numpy arrays
 through ctypes.
 
+Diagnostics (``diag`` columns): DIAG_ACCEPT_MARGIN and DIAG_RACE_FLIP are
+"flip indices" -- the perturbation of p and q needed to change that decision,
+in units of the tolerance (1e-6 absolute and 1e-5 relative); below 1 means a
+perturbation inside both bounds could flip it.  DIAG_RACE_RELGAP is the
+relative gap between the winning race key and the runner-up.
+
 Status bits mirror the library's documented meaning: 1 bad cu range, 2 draft id
 outside [0, V), 4 bad exponential draw, 8 empty distribution, 16 NaN/inf
 values, 32 bad sampling parameter, 64 draft rows missing.

@@ -85,10 +85,14 @@
 #define ORC_BF16 1
 
 /* per-request diagnostics written when diag != NULL (tests use them to name
- * the decisions that sit within the stated tolerance of a flip) */
+ * the decisions that sit within the stated tolerance of a flip).  A "flip
+ * index" is max(needed_abs / 1e-6, needed_rel / 1e-5): the perturbation of p
+ * and q needed to change the decision, in units of the tolerance -- 1e-6
+ * absolute (the contract on probabilities) and 1e-5 relative.  An index < 1
+ * means a perturbation inside both bounds could flip the decision. */
 #define ORC_NDIAG 6
-#define DIAG_ACCEPT_MARGIN 0 /* min |u*q - p| over examined positions (double)        */
-#define DIAG_RACE_FLIP 1     /* min (k1 - k_x) / (1/E1 + 1/E_x) over supported x != x1 */
+#define DIAG_ACCEPT_MARGIN 0 /* min over examined positions of the flip index of the test */
+#define DIAG_RACE_FLIP 1     /* min over supported x != x1 of the flip index of the race */
 #define DIAG_RACE_RELGAP 2   /* min (k1 - k_x) / k1 over supported x != x1             */
 #define DIAG_TOPP_EDGE 3     /* 1 if a cumulative sum at a top-p cut is within 1e-6   */
 #define DIAG_FALLBACK 4      /* 1 if the residual race had no positive key            */
@@ -321,22 +325,34 @@ static int race(race_ctx *c, const float *w, float *kmax) {
 }
 
 /* diagnostics of a finished race: how far the winner is from a flip */
-static void race_diag(race_ctx *c, const float *w, const float *supp_a, const float *supp_b, int win,
-                      double *flip, double *relgap) {
+static double flip_index(double needed_abs, double needed_rel) {
+  double a = needed_abs / 1e-6, r = needed_rel / 1e-5;
+  return a > r ? a : r;
+}
+
+/* how far a finished race is from a flip: the winner x1 against every x in the
+ * support of p or q.  A weight w = max(p - q, 0) (or p) moves by at most
+ * delta absolute or eps*(p+q) relative, so keys k = w/E can swap when
+ * k1 - k_x <= delta*(1/E1 + 1/E_x) and k1 - k_x <= eps*((p1+q1)/E1 + (p_x+q_x)/E_x). */
+static void race_diag(race_ctx *c, const float *w, const float *pa, const float *qa, int win, double *flip,
+                      double *relgap) {
   double k1 = 0, e1 = 1;
   if (w[win] > 0.0f) {
     e1 = (double)E_at(c, win);
     k1 = (double)(w[win] / (float)e1);
   }
+  double m1 = (double)pa[win] + (qa ? (double)qa[win] : 0.0);
   double fmin = INFINITY, rmin = INFINITY;
   for (int x = 0; x < c->V; ++x) {
     if (x == win) continue;
-    int supported = (supp_a && supp_a[x] > 0.0f) || (supp_b && supp_b[x] > 0.0f);
+    int supported = (pa[x] > 0.0f) || (qa && qa[x] > 0.0f);
     if (!supported) continue;
     double ex = (double)E_at(c, x);
     double kx = (w[x] > 0.0f && ex > 0) ? (double)(w[x] / (float)ex) : 0.0;
     double d = k1 - kx;
-    double f = d / (1.0 / e1 + 1.0 / ex);
+    double mx = (double)pa[x] + (qa ? (double)qa[x] : 0.0);
+    double den_rel = m1 / e1 + mx / ex;
+    double f = flip_index(d / (1.0 / e1 + 1.0 / ex), den_rel > 0 ? d / den_rel : INFINITY);
     if (f < fmin) fmin = f;
     double r = k1 > 0 ? d / k1 : 0.0;
     if (r < rmin) rmin = r;
@@ -489,8 +505,9 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
     if (a->dbg_py) a->dbg_py[s + j] = py;
     if (a->dbg_qy) a->dbg_qy[s + j] = qy;
     float u = rc->test_mode ? a->uniforms[s + j] : oracle_uniform(a->seed, a->offset, rc->rng_req, (uint32_t)j);
-    if (dg) {
-      double mg = fabs((double)u * (double)qy - (double)py);
+    if (dg) { /* flip index of the test u*q < p (exact zeros on both sides cannot flip) */
+      double uq = (double)u * (double)qy, gap = fabs(uq - (double)py), scale = uq + (double)py;
+      double mg = scale > 0 ? flip_index(gap, gap / scale) : INFINITY;
       if (mg < dg[DIAG_ACCEPT_MARGIN]) dg[DIAG_ACCEPT_MARGIN] = mg;
     }
     float uq = u * qy; /* fp32 product, then a strict fp32 comparison */

@@ -33,12 +33,30 @@ void set_last_error(const char *fmt, ...) {
 
 int choose_cluster(const spec_verify_ctx *ctx, int N, int V) {
   if (ctx->cfg.cluster_ctas > 0) return ctx->cfg.cluster_ctas;
-  // Enough CTAs for several resident waves, but chunks of at least 4096
-  // elements so the per-CTA scan and reduction stay a small share of the work.
-  const long long target = 8LL * ctx->num_sms;
+  // Split a request over more CTAs only while the batch alone gives fewer than
+  // two CTAs per SM, and keep chunks of at least 4096 elements: every extra CTA
+  // repeats the request's scan and adds a reduction (measured on GB300 at
+  // N=512, V=151936: one CTA per request streams at 0.99 of the copy
+  // bandwidth, four per request at 0.89).
+  const long long target = 2LL * ctx->num_sms;
   int c = 1;
   while (c < ctx->max_cluster && static_cast<long long>(N) * c < target && V / (2 * c) >= 4096) c *= 2;
   return c;
+}
+
+bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk) {
+  // Rows of the current position live in the cluster's shared memory (target
+  // and draft chunk per CTA).  Prefer the CTA count of the probability entry,
+  // grow it until the two row chunks fit in ~100 KB so two CTAs share an SM.
+  auto chunk_for = [&](int c) { return ((V + c - 1) / c + 7) & ~7; };
+  auto bytes_for = [&](int c) { return 2LL * chunk_for(c) * elem_bytes; };
+  int c = ctx->cfg.cluster_ctas > 0 ? ctx->cfg.cluster_ctas : choose_cluster(ctx, N, V);
+  if (ctx->cfg.cluster_ctas == 0)
+    while (c < ctx->max_cluster && bytes_for(c) > 100 * 1024) c *= 2;
+  if (bytes_for(c) > ctx->max_dyn_smem) return false;
+  *cluster = c;
+  *chunk = chunk_for(c);
+  return true;
 }
 
 }  // namespace sv
@@ -97,7 +115,6 @@ sv_status spec_verify_check_args(const spec_verify_config *c, const spec_verify_
   if (a->dtype != SV_F32 && a->dtype != SV_BF16) return fail(SV_ERR_INVALID_ARG, "bad dtype");
   if (a->entry == SV_ENTRY_PROBS && a->dtype != SV_F32)
     return fail(SV_ERR_UNSUPPORTED, "the probability entry takes fp32 rows");
-  if (a->entry == SV_ENTRY_LOGITS) return fail(SV_ERR_UNSUPPORTED, "the logits entry is not built in this library");
   if (a->reserved0 != 0 || a->reserved1 != 0) return fail(SV_ERR_INVALID_ARG, "reserved fields must be 0");
   if (a->num_draft_tokens_total < 0) return fail(SV_ERR_INVALID_ARG, "num_draft_tokens_total < 0");
   if (!a->cu_num_draft_tokens &&
@@ -136,15 +153,19 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, config->device);
   sv_status result = SV_OK;
   int max_cluster = 16;
+  int max_dyn = 0;
   if (e != cudaSuccess) {
     result = fail(SV_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
   } else if (major != 10 || minor != 3) {
     result = fail(SV_ERR_UNSUPPORTED, "built for sm_103a only; device %d is sm_%d%d", config->device, major, minor);
   } else {
-    if (sv::enable_probs_kernels(16) != cudaSuccess) {
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, config->device);
+    max_dyn = optin - static_cast<int>(sv::logits_static_smem()) - 1024;
+    if (sv::enable_probs_kernels(16) != cudaSuccess || sv::enable_logits_kernels(16, max_dyn) != cudaSuccess) {
       cudaGetLastError();
       max_cluster = 8;
-      if ((e = sv::enable_probs_kernels(8)) != cudaSuccess)
+      if ((e = sv::enable_probs_kernels(8)) != cudaSuccess || (e = sv::enable_logits_kernels(8, max_dyn)) != cudaSuccess)
         result = fail(SV_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(e));
     }
     if (config->cluster_ctas > max_cluster)
@@ -157,6 +178,7 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
   h->cfg = *config;
   h->num_sms = sms;
   h->max_cluster = max_cluster;
+  h->max_dyn_smem = max_dyn;
   *out = h;
   return SV_OK;
 }
@@ -201,10 +223,24 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
   p.dbg_qy = a->dbg_qy;
   p.status = a->status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int cluster = sv::choose_cluster(h, p.N, p.V);
-  const bool vec = sv::aligned16(a->target) && (a->target_row_stride % 4 == 0) &&
-                   (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % 4 == 0));
-  const cudaError_t e = sv::launch_probs(p, cluster, vec, s);
+  cudaError_t e;
+  if (a->entry == SV_ENTRY_PROBS) {
+    const int cluster = sv::choose_cluster(h, p.N, p.V);
+    const bool vec = sv::aligned16(a->target) && (a->target_row_stride % 4 == 0) &&
+                     (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % 4 == 0));
+    e = sv::launch_probs(p, cluster, vec, s);
+  } else {
+    const bool bf16 = a->dtype == SV_BF16;
+    const int eb = bf16 ? 2 : 4;
+    const int per16 = 16 / eb;  // elements per 16-byte vector
+    int cluster = 0, chunk = 0;
+    if (!sv::choose_logits_layout(h, p.N, p.V, eb, &cluster, &chunk))
+      return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for the rows to fit in the cluster's shared memory",
+                  p.V);
+    const bool vec = sv::aligned16(a->target) && (a->target_row_stride % per16 == 0) &&
+                     (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % per16 == 0));
+    e = sv::launch_logits(p, bf16, cluster, chunk, vec, s);
+  }
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "verifier launch: %s", cudaGetErrorString(e));
   return SV_OK;
 }

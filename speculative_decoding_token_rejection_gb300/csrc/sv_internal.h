@@ -10,6 +10,7 @@ struct spec_verify_ctx {
   spec_verify_config cfg;
   int num_sms;
   int max_cluster;  // largest cluster size the kernels were enabled for (8 or 16)
+  int max_dyn_smem; // dynamic shared memory the logits kernels may request per CTA
 };
 
 namespace sv {
@@ -46,6 +47,14 @@ int choose_cluster(const spec_verify_ctx *ctx, int N, int V);
 
 cudaError_t enable_probs_kernels(int max_cluster);
 cudaError_t launch_probs(const VerifyParams &p, int cluster, bool vec, cudaStream_t stream);
+
+size_t logits_static_smem();
+cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);
+cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
+
+// Cluster size and per-CTA row chunk (elements, a multiple of 8) for the
+// logits entry; returns false if no cluster size fits the rows in shared memory.
+bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk);
 
 void set_last_error(const char *fmt, ...);
 

@@ -74,6 +74,8 @@ def cfg(**kw):
     (lambda a: setattr(a, "vocab_size", 0), sv.SV_ERR_INVALID_ARG),
     (lambda a: setattr(a, "entry", 7), sv.SV_ERR_INVALID_ARG),
     (lambda a: setattr(a, "dtype", sv.SV_BF16), sv.SV_ERR_UNSUPPORTED),  # probs entry is fp32 only
+    (lambda a: (setattr(a, "entry", sv.SV_ENTRY_LOGITS), setattr(a, "dtype", sv.SV_BF16)), sv.SV_OK),
+    (lambda a: setattr(a, "entry", sv.SV_ENTRY_LOGITS), sv.SV_OK),  # fp32 logits
     (lambda a: setattr(a, "reserved0", 1), sv.SV_ERR_INVALID_ARG),
     (lambda a: setattr(a, "num_draft_tokens_total", 11), sv.SV_ERR_INVALID_ARG),  # != N*G without cu
     (lambda a: setattr(a, "draft_ids", None), sv.SV_ERR_INVALID_ARG),
@@ -142,6 +144,8 @@ def test_gpu_test_workloads_pass_host_marshalling(lib):
     import test_gpu_probs as tg
     cases = list(tg.edge_cases().values())
     cases += [workloads.make(n, **kw) for n, kw in tg.CASES if n != "fused_probs" or kw]
+    cases += [workloads.make("greedy", N=7, V=3001), workloads.make("ragged", N=40, V=3001),
+              workloads.make("fused", N=24, V=8192)]
     cfg_ = sv.make_config(1 << 20, sv.SV_MAX_SPEC_LEN, 1 << 18)
     for w in cases:
         t = workloads.as_torch(w, "cpu")
@@ -150,6 +154,7 @@ def test_gpu_test_workloads_pass_host_marshalling(lib):
             a = sv.build_args(
                 entry=w["entry"], draft_ids=t["draft_ids"], target=t["target"], draft=t["draft"],
                 cu_num_draft_tokens=t["cu_num_draft_tokens"], temperature=t["temperature"],
+                top_k=t.get("top_k"), top_p=t.get("top_p"),
                 uniforms=None if production else t["uniforms"],
                 exponentials=None if production else t["exponentials"],
                 out_tokens=torch.empty((N, G + 1), dtype=torch.int32), num_accepted=torch.empty(N, dtype=torch.int32),
