@@ -72,7 +72,9 @@ enum sv_data_status {
   SV_DATA_EMPTY_DISTRIBUTION = 8, /* a draw found no positive key; token 0 emitted */
   SV_DATA_BAD_VALUES = 16,        /* NaN (greedy) or NaN/+inf/no finite logit (random logits) in a read row */
   SV_DATA_BAD_PARAM = 32,         /* temperature < 0/NaN/inf, or top_p <= 0/NaN */
-  SV_DATA_MISSING_DRAFT = 64      /* draft == NULL but a random request needs draft rows */
+  SV_DATA_MISSING_DRAFT = 64,     /* draft == NULL but a random request needs draft rows */
+  SV_DATA_COPY_TIMEOUT = 128      /* a bulk row copy did not complete within its wait limit (request
+                                     emits nothing); never expected on a healthy GPU */
 };
 
 typedef struct spec_verify_ctx *spec_verify_t;

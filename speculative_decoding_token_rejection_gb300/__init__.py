@@ -28,7 +28,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_MAX_SPEC_LEN = 256
 DATA_STATUS_BITS = {
     "BAD_CU": 1, "BAD_DRAFT_ID": 2, "BAD_EXPONENTIAL": 4, "EMPTY_DISTRIBUTION": 8,
-    "BAD_VALUES": 16, "BAD_PARAM": 32, "MISSING_DRAFT": 64,
+    "BAD_VALUES": 16, "BAD_PARAM": 32, "MISSING_DRAFT": 64, "COPY_TIMEOUT": 128,
 }
 
 _P = ctypes.c_void_p

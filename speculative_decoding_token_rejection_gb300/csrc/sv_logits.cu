@@ -87,13 +87,17 @@ __device__ __forceinline__ uint32_t bits_at<float>(const float *row, int x) {
 // ---------------------------------------------------------------------------
 // shared memory
 // ---------------------------------------------------------------------------
-constexpr uint32_t kFlagBad = 1u;     // NaN or +inf in a random row
-constexpr uint32_t kFlagFinite = 2u;  // at least one finite logit
+constexpr uint32_t kFlagBad = 1u;      // NaN or +inf in a random row
+constexpr uint32_t kFlagFinite = 2u;   // at least one finite logit
+constexpr uint32_t kFlagTimeout = 4u;  // the row's bulk copy did not complete in time
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kNearBins = 255;         // near-max bins: distances 0..254 from the row's largest key
 
 struct StatPart {  // one CTA's partials of one reduction round, for up to 2 rows
   uint32_t maxkey[2];
   uint32_t flags[2];
   float z[2];
+  unsigned long long tot[2];
   uint32_t cnt[2][256];
   unsigned long long mass[2][256];
 };
@@ -105,9 +109,13 @@ struct RowStats {
   float zp;      // normaliser over the kept set
 };
 
-struct Select {  // result of one radix digit choice, per row
-  uint32_t prefix[2];
-  unsigned long long need[2];
+struct Select {  // running state of a radix selection, per row
+  uint32_t prefix[2];          // key bits fixed so far
+  int known_lo[2];             // bits [kB-1, known_lo) of prefix are fixed
+  unsigned long long need[2];  // rank (counts) or mass still to cover inside the prefix range
+  unsigned long long above[2]; // count / mass of keys above the prefix range
+  unsigned long long last[2];  // count / mass of the last selected bin
+  int ok[2];
 };
 
 struct LogitsSmem {
@@ -115,11 +123,13 @@ struct LogitsSmem {
   StatPart part[2];
   StatPart sum;
   float wz[2][kWarps];
+  unsigned long long wt[2][kWarps];
   Select sel;
+  uint64_t bar;
   int32_t tok[SV_MAX_SPEC_LEN + 1];
 };
 
-enum : uint32_t { kRMax = 1u, kRCnt = 2u, kRMass = 4u, kRZ = 8u };
+enum : uint32_t { kRMax = 1u, kRCnt = 2u, kRMass = 4u, kRZ = 8u, kRTot = 16u };
 
 __device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
   const int tid = threadIdx.x;
@@ -131,6 +141,7 @@ __device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
     p.maxkey[tid] = 0u;
     p.flags[tid] = 0u;
     p.z[tid] = 0.0f;
+    p.tot[tid] = 0ull;
   }
 }
 
@@ -171,11 +182,16 @@ __device__ __forceinline__ void stat_reduce(LogitsSmem &sm, int par, uint32_t wh
       for (uint32_t c = 0; c < ncta; ++c) z += __uint_as_float(ld_dsmem_u32(map_to_rank(smem_addr(&p.z[tid]), c)));
       sm.sum.z[tid] = z;
     }
+    if (what & kRTot) {
+      unsigned long long t = 0;
+      for (uint32_t c = 0; c < ncta; ++c) t += ld_dsmem_u64(map_to_rank(smem_addr(&p.tot[tid]), c));
+      sm.sum.tot[tid] = t;
+    }
   }
   __syncthreads();
 }
 
-// Deterministic block sum of one float per thread per row into part.z[r].
+// Deterministic block sums (fixed shuffle tree, then warps in order) into part.
 __device__ __forceinline__ void block_sum_z(LogitsSmem &sm, StatPart &p, const float v[2], int nr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int r = 0; r < nr; ++r) {
@@ -191,107 +207,157 @@ __device__ __forceinline__ void block_sum_z(LogitsSmem &sm, StatPart &p, const f
     p.z[threadIdx.x] = s;
   }
 }
+__device__ __forceinline__ void block_sum_tot(LogitsSmem &sm, StatPart &p, const unsigned long long v[2], int nr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int r = 0; r < nr; ++r) {
+    unsigned long long s = v[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) sm.wt[r][warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < nr) {
+    unsigned long long s = 0;
+    for (int w = 0; w < kWarps; ++w) s += sm.wt[threadIdx.x][w];
+    p.tot[threadIdx.x] = s;
+  }
+}
 
-// Pick the radix digit of row r: walking bins from 255 down, the first bin b
-// where (mass above b) + h[b] >= need.  Run by one warp; writes sm.sel.
-template <typename H>
-__device__ __forceinline__ void select_digit(LogitsSmem &sm, int r, const H *h, int shift) {
+// One warp picks a bin of row r.  Bins are walked from the largest keys
+// down: logical bin L is physical bin L for near-max histograms (distance from
+// the largest key) and 255 - L for digit histograms.  The chosen bin is the
+// first whose running total reaches `need`; records what lies above it.
+template <bool kNear, typename H>
+__device__ __forceinline__ void select_bin(LogitsSmem &sm, int r, const H *h, int lo, uint32_t near_base) {
   const int lane = threadIdx.x & 31;
-  // lane L owns bins [8L, 8L+8)
+  auto hv = [&](int L) -> unsigned long long { return static_cast<unsigned long long>(h[kNear ? L : 255 - L]); };
   unsigned long long own = 0;
 #pragma unroll
-  for (int t = 0; t < 8; ++t) own += static_cast<unsigned long long>(h[8 * lane + t]);
-  // inclusive suffix sum over lanes (bins above included)
-  unsigned long long suf = own;
+  for (int t = 0; t < 8; ++t) own += hv(8 * lane + t);
+  unsigned long long inc = own;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long v = __shfl_down_sync(0xFFFFFFFFu, suf, o);
-    if (lane + o < 32) suf += v;
+    const unsigned long long v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= o) inc += v;
   }
-  const unsigned long long above_lane = suf - own;  // bins of higher lanes
+  const unsigned long long before = inc - own;
   const unsigned long long need = sm.sel.need[r];
   int found = -1;
-  unsigned long long above = 0;
-  if (above_lane < need && suf >= need) {
-    unsigned long long acc = above_lane;
-    for (int t = 7; t >= 0; --t) {
-      const unsigned long long hv = static_cast<unsigned long long>(h[8 * lane + t]);
-      if (acc + hv >= need) {
+  unsigned long long above = 0, last = 0;
+  if (before < need && inc >= need) {
+    unsigned long long acc = before;
+    for (int t = 0; t < 8; ++t) {
+      const unsigned long long x = hv(8 * lane + t);
+      if (acc + x >= need) {
         found = 8 * lane + t;
         above = acc;
+        last = x;
         break;
       }
-      acc += hv;
+      acc += x;
     }
   }
   const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0);
-  const int src = ball ? (__ffs(ball) - 1) : 0;
-  const int d = __shfl_sync(0xFFFFFFFFu, found, src);
-  const unsigned long long ab = __shfl_sync(0xFFFFFFFFu, above, src);
+  if (ball == 0) {
+    if (lane == 0) sm.sel.ok[r] = 0;
+    return;
+  }
+  const int src = __ffs(ball) - 1;
+  const int L = __shfl_sync(0xFFFFFFFFu, found, src);
+  above = __shfl_sync(0xFFFFFFFFu, above, src);
+  last = __shfl_sync(0xFFFFFFFFu, last, src);
   if (lane == 0) {
-    const int dd = d < 0 ? 0 : d;  // need > total cannot happen for valid inputs
-    sm.sel.prefix[r] |= static_cast<uint32_t>(dd) << shift;
-    sm.sel.need[r] = need - ab;
+    if (kNear) {
+      sm.sel.prefix[r] = (near_base - static_cast<uint32_t>(L)) << lo;  // the top 16 key bits
+    } else {
+      sm.sel.prefix[r] |= static_cast<uint32_t>(255 - L) << lo;
+    }
+    sm.sel.known_lo[r] = lo;
+    sm.sel.need[r] = need - above;
+    sm.sel.above[r] += above;
+    sm.sel.last[r] = last;
+    sm.sel.ok[r] = 1;
+  }
+}
+
+template <typename TIn>
+__device__ __forceinline__ uint32_t key16_of(uint32_t k) {
+  return Elem<TIn>::kBits == 16 ? k : (k >> 16);
+}
+
+__device__ __forceinline__ unsigned long long to_fixed(float e) {
+  return static_cast<unsigned long long>(__float2ull_rn(e * kMassScale));
+}
+
+// Refine the selection of every row whose prefix is not complete, one 8-bit
+// digit per level (counts, or fixed-point masses of keys >= tau).
+template <typename TIn, bool kMass>
+__device__ void radix_refine(LogitsSmem &sm, TIn *const srow[2], int nr, int n, const uint32_t tau[2],
+                             const RowStats st[2], int &step, uint32_t ncta) {
+  using E = Elem<TIn>;
+  constexpr int kB = E::kBits;
+  const int tid = threadIdx.x;
+  for (int lo = kB - 8; lo >= 0; lo -= 8) {
+    bool any = false;
+    for (int r = 0; r < nr; ++r) any |= sm.sel.known_lo[r] > lo;
+    if (!any) continue;
+    const int par = step & 1;
+    zero_part(sm.part[par], kMass ? kRMass : kRCnt, nr);
+    __syncthreads();
+    for (int r = 0; r < nr; ++r) {
+      if (sm.sel.known_lo[r] <= lo) continue;
+      const int hi_shift = lo + 8;
+      const uint32_t hi = hi_shift >= 32 ? 0u : (sm.sel.prefix[r] >> hi_shift);
+      const TIn *s = srow[r];
+      for (int x = tid; x < n; x += kThreads) {
+        const uint32_t b = bits_at(s, x);
+        const uint32_t k = E::key(b);
+        if (hi_shift < 32 && (k >> hi_shift) != hi) continue;
+        if (kMass) {
+          if (k < tau[r]) continue;
+          const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), st[r].c2));
+          atomicAdd(&sm.part[par].mass[r][(k >> lo) & 255u], to_fixed(e));
+        } else {
+          atomicAdd(&sm.part[par].cnt[r][(k >> lo) & 255u], 1u);
+        }
+      }
+    }
+    stat_reduce(sm, par, kMass ? kRMass : kRCnt, nr, ncta);
+    ++step;
+    const int warp = tid >> 5;
+    if (warp < nr && sm.sel.known_lo[warp] > lo) {
+      if (kMass) select_bin<false>(sm, warp, sm.sum.mass[warp], lo, 0u);
+      else select_bin<false>(sm, warp, sm.sum.cnt[warp], lo, 0u);
+    }
+    __syncthreads();
   }
 }
 
 // ---------------------------------------------------------------------------
-// row statistics of one position (target row, and draft row when nr == 2)
+// row statistics of one position (target row, and draft row when nr == 2),
+// the rows already in shared memory
 // ---------------------------------------------------------------------------
-template <typename TIn, bool kVec>
-__device__ bool position_stats(LogitsSmem &sm, const TIn *const grow[2], TIn *const srow[2], int nr, int n,
-                               float c2, int topk, float topp, RowStats st[2], int &step, uint32_t ncta) {
+template <typename TIn>
+__device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n, float c2, int topk, float topp,
+                               uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step, uint32_t ncta) {
   using E = Elem<TIn>;
   constexpr int kB = E::kBits;
   const int tid = threadIdx.x;
   const bool use_k = topk > 0;
   const bool use_p = topp < 1.0f;
 
-  // pass 1: HBM -> shared memory, max key, value checks, top-digit counts
+  // pass 1: max key and value checks
   int par = step & 1;
-  zero_part(sm.part[par], kRMax | (use_k ? kRCnt : 0u), nr);
+  zero_part(sm.part[par], kRMax, nr);
   __syncthreads();
   for (int r = 0; r < nr; ++r) {
-    uint32_t mk = 0, fl = 0;
-    const TIn *g = grow[r];
-    TIn *s = srow[r];
-    constexpr int kPer = 16 / sizeof(TIn);
-    int xs = 0;
-    if (kVec) {
-      const int nv = n / kPer;
-      const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
-      uint4 *s4 = reinterpret_cast<uint4 *>(s);
-      for (int v = tid; v < nv; v += kThreads) {
-        uint4 d;
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
-                     : "l"(g4 + v));
-        s4[v] = d;
-        const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-#pragma unroll
-          for (int h = 0; h < (kB == 16 ? 2 : 1); ++h) {
-            const uint32_t b = (kB == 16) ? ((w[t] >> (16 * h)) & 0xFFFFu) : w[t];
-            const uint32_t k = E::key(b);
-            if (E::is_nan(b) || E::is_pinf(b)) fl |= kFlagBad;
-            if (E::finite(b)) fl |= kFlagFinite;
-            mk = max(mk, k);
-            if (use_k) atomicAdd(&sm.part[par].cnt[r][k >> (kB - 8)], 1u);
-          }
-        }
-      }
-      xs = nv * kPer;
-    }
-    for (int x = xs + tid; x < n; x += kThreads) {
-      const TIn e = g[x];
-      s[x] = e;
+    uint32_t mk = 0, fl = load_flags;
+    const TIn *s = srow[r];
+    for (int x = tid; x < n; x += kThreads) {
       const uint32_t b = bits_at(s, x);
-      const uint32_t k = E::key(b);
       if (E::is_nan(b) || E::is_pinf(b)) fl |= kFlagBad;
       if (E::finite(b)) fl |= kFlagFinite;
-      mk = max(mk, k);
-      if (use_k) atomicAdd(&sm.part[par].cnt[r][k >> (kB - 8)], 1u);
+      mk = max(mk, E::key(b));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -303,123 +369,67 @@ __device__ bool position_stats(LogitsSmem &sm, const TIn *const grow[2], TIn *co
       atomicOr(&sm.part[par].flags[r], fl);
     }
   }
-  stat_reduce(sm, par, kRMax | (use_k ? kRCnt : 0u), nr, ncta);
+  stat_reduce(sm, par, kRMax, nr, ncta);
   ++step;
   for (int r = 0; r < nr; ++r) {
     const uint32_t f = sm.sum.flags[r];
-    if ((f & kFlagBad) || !(f & kFlagFinite)) return false;
+    if (f & kFlagTimeout) *req_bits |= SV_DATA_COPY_TIMEOUT;
+    if ((f & (kFlagBad | kFlagTimeout)) || !(f & kFlagFinite)) return false;
     st[r].vmax = E::val_of_key(sm.sum.maxkey[r]);
     st[r].c2 = c2;
   }
+  uint32_t maxk16[2] = {0u, 0u};
+  for (int r = 0; r < nr; ++r) maxk16[r] = key16_of<TIn>(sm.sum.maxkey[r]);
 
-  // top-k: exact k-th largest key by radix digits (ties kept)
+  // top-k: the k-th largest key (ties kept).  First count the keys within
+  // kNearBins steps of the largest (where the threshold almost always lies),
+  // then refine or fall back to a full radix selection.
   uint32_t tau[2] = {0u, 0u};
   if (use_k) {
+    par = step & 1;
+    zero_part(sm.part[par], kRCnt, nr);
     if (tid < 2) {
       sm.sel.prefix[tid] = 0u;
+      sm.sel.known_lo[tid] = kB;
       sm.sel.need[tid] = static_cast<unsigned long long>(topk);
+      sm.sel.above[tid] = 0ull;
     }
     __syncthreads();
-    for (int shift = kB - 8;; shift -= 8) {
-      if ((tid >> 5) < nr) select_digit(sm, tid >> 5, sm.sum.cnt[tid >> 5], shift);
-      __syncthreads();
-      if (shift == 0) break;
-      par = step & 1;
-      zero_part(sm.part[par], kRCnt, nr);
-      __syncthreads();
-      for (int r = 0; r < nr; ++r) {
-        const uint32_t hi = sm.sel.prefix[r] >> (shift);
-        const TIn *s = srow[r];
-        for (int x = tid; x < n; x += kThreads) {
-          const uint32_t k = E::key(bits_at(s, x));
-          if ((k >> shift) == hi) atomicAdd(&sm.part[par].cnt[r][(k >> (shift - 8)) & 255u], 1u);
-        }
+    for (int r = 0; r < nr; ++r) {
+      const TIn *s = srow[r];
+      for (int x = tid; x < n; x += kThreads) {
+        const uint32_t d = maxk16[r] - key16_of<TIn>(E::key(bits_at(s, x)));
+        if (d < static_cast<uint32_t>(kNearBins)) atomicAdd(&sm.part[par].cnt[r][d], 1u);
       }
-      stat_reduce(sm, par, kRCnt, nr, ncta);
-      ++step;
     }
+    stat_reduce(sm, par, kRCnt, nr, ncta);
+    ++step;
+    if ((tid >> 5) < nr) select_bin<true>(sm, tid >> 5, sm.sum.cnt[tid >> 5], kB - 16, maxk16[tid >> 5]);
+    __syncthreads();
+    if (tid < nr && !sm.sel.ok[tid]) {  // threshold farther than the near bins: full selection
+      sm.sel.prefix[tid] = 0u;
+      sm.sel.known_lo[tid] = kB;
+      sm.sel.need[tid] = static_cast<unsigned long long>(topk);
+      sm.sel.above[tid] = 0ull;
+    }
+    __syncthreads();
+    radix_refine<TIn, false>(sm, srow, nr, n, tau, st, step, ncta);
     for (int r = 0; r < nr; ++r) tau[r] = sm.sel.prefix[r];
   }
 
-  // normaliser over the top-k set, and the top digit of the top-p masses
-  par = step & 1;
-  zero_part(sm.part[par], kRZ | (use_p ? kRMass : 0u), nr);
-  __syncthreads();
-  {
-    float zt[2] = {0.0f, 0.0f};
-    for (int r = 0; r < nr; ++r) {
-      const TIn *s = srow[r];
-      float sum = 0.0f, comp = 0.0f;
-      for (int x = tid; x < n; x += kThreads) {
-        const uint32_t b = bits_at(s, x);
-        const uint32_t k = E::key(b);
-        if (k < tau[r]) continue;
-        const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2));
-        const float y = e - comp;  // Kahan
-        const float t = sum + y;
-        comp = (t - sum) - y;
-        sum = t;
-        if (use_p)
-          atomicAdd(&sm.part[par].mass[r][k >> (kB - 8)], static_cast<unsigned long long>(__float2ull_rn(e * kMassScale)));
-      }
-      zt[r] = sum;
-    }
-    block_sum_z(sm, sm.part[par], zt, nr);
-  }
-  stat_reduce(sm, par, kRZ | (use_p ? kRMass : 0u), nr, ncta);
-  ++step;
-  for (int r = 0; r < nr; ++r) {
-    st[r].cut = tau[r];
-    st[r].zp = sm.sum.z[r];
-  }
-
-  // top-p: largest key c with mass(key >= c) >= top_p * total, by radix digits
-  if (use_p) {
-    if (tid < nr) {
-      unsigned long long tot = 0;
-      for (int b = 0; b < 256; ++b) tot += sm.sum.mass[tid][b];
-      sm.sel.prefix[tid] = 0u;
-      unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(tot));
-      sm.sel.need[tid] = need > 0 ? need : 1ull;
-    }
-    __syncthreads();
-    for (int shift = kB - 8;; shift -= 8) {
-      if ((tid >> 5) < nr) select_digit(sm, tid >> 5, sm.sum.mass[tid >> 5], shift);
-      __syncthreads();
-      if (shift == 0) break;
-      par = step & 1;
-      zero_part(sm.part[par], kRMass, nr);
-      __syncthreads();
-      for (int r = 0; r < nr; ++r) {
-        const uint32_t hi = sm.sel.prefix[r] >> shift;
-        const TIn *s = srow[r];
-        for (int x = tid; x < n; x += kThreads) {
-          const uint32_t b = bits_at(s, x);
-          const uint32_t k = E::key(b);
-          if (k < tau[r] || (k >> shift) != hi) continue;
-          const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2));
-          atomicAdd(&sm.part[par].mass[r][(k >> (shift - 8)) & 255u],
-                    static_cast<unsigned long long>(__float2ull_rn(e * kMassScale)));
-        }
-      }
-      stat_reduce(sm, par, kRMass, nr, ncta);
-      ++step;
-    }
-    // normaliser over the final kept set
+  if (!use_p) {  // normaliser over the top-k set
     par = step & 1;
     zero_part(sm.part[par], kRZ, nr);
     __syncthreads();
     float zt[2] = {0.0f, 0.0f};
     for (int r = 0; r < nr; ++r) {
-      const uint32_t cut = max(tau[r], sm.sel.prefix[r]);
-      st[r].cut = cut;
       const TIn *s = srow[r];
       float sum = 0.0f, comp = 0.0f;
       for (int x = tid; x < n; x += kThreads) {
         const uint32_t b = bits_at(s, x);
-        if (E::key(b) < cut) continue;
+        if (E::key(b) < tau[r]) continue;
         const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2));
-        const float y = e - comp;
+        const float y = e - comp;  // Kahan
         const float t = sum + y;
         comp = (t - sum) - y;
         sum = t;
@@ -429,7 +439,64 @@ __device__ bool position_stats(LogitsSmem &sm, const TIn *const grow[2], TIn *co
     block_sum_z(sm, sm.part[par], zt, nr);
     stat_reduce(sm, par, kRZ, nr, ncta);
     ++step;
-    for (int r = 0; r < nr; ++r) st[r].zp = sm.sum.z[r];
+    for (int r = 0; r < nr; ++r) {
+      st[r].cut = tau[r];
+      st[r].zp = sm.sum.z[r];
+    }
+    return true;
+  }
+
+  // top-p: the largest key c with mass(key >= c) >= top_p * mass(top-k set),
+  // masses in 2^-40 fixed point; near-max bins first, then refine / fall back.
+  par = step & 1;
+  zero_part(sm.part[par], kRMass | kRTot, nr);
+  __syncthreads();
+  {
+    unsigned long long tt[2] = {0ull, 0ull};
+    for (int r = 0; r < nr; ++r) {
+      const TIn *s = srow[r];
+      unsigned long long tot = 0;
+      for (int x = tid; x < n; x += kThreads) {
+        const uint32_t b = bits_at(s, x);
+        const uint32_t k = E::key(b);
+        if (k < tau[r]) continue;
+        const unsigned long long m = to_fixed(exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2)));
+        tot += m;
+        const uint32_t d = maxk16[r] - key16_of<TIn>(k);
+        if (d < static_cast<uint32_t>(kNearBins)) atomicAdd(&sm.part[par].mass[r][d], m);
+      }
+      tt[r] = tot;
+    }
+    block_sum_tot(sm, sm.part[par], tt, nr);
+  }
+  stat_reduce(sm, par, kRMass | kRTot, nr, ncta);
+  ++step;
+  if (tid < 2) {
+    const unsigned long long tot = sm.sum.tot[tid < nr ? tid : 0];
+    unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(tot));
+    sm.sel.prefix[tid] = 0u;
+    sm.sel.known_lo[tid] = kB;
+    sm.sel.need[tid] = need > 0 ? need : 1ull;
+    sm.sel.above[tid] = 0ull;
+    sm.sel.last[tid] = 0ull;
+  }
+  __syncthreads();
+  if ((tid >> 5) < nr) select_bin<true>(sm, tid >> 5, sm.sum.mass[tid >> 5], kB - 16, maxk16[tid >> 5]);
+  __syncthreads();
+  if (tid < nr && !sm.sel.ok[tid]) {
+    const unsigned long long tot = sm.sum.tot[tid];
+    const unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(tot));
+    sm.sel.prefix[tid] = 0u;
+    sm.sel.known_lo[tid] = kB;
+    sm.sel.need[tid] = need > 0 ? need : 1ull;
+    sm.sel.above[tid] = 0ull;
+  }
+  __syncthreads();
+  radix_refine<TIn, true>(sm, srow, nr, n, tau, st, step, ncta);
+  for (int r = 0; r < nr; ++r) {
+    st[r].cut = max(tau[r], sm.sel.prefix[r]);
+    const unsigned long long kept = sm.sel.above[r] + sm.sel.last[r];  // mass of keys >= cut
+    st[r].zp = static_cast<float>(static_cast<double>(kept) * (1.0 / static_cast<double>(kMassScale)));
   }
   return true;
 }
@@ -507,6 +574,41 @@ __device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const Ro
   }
 }
 
+// Load this CTA's chunk of nr rows into shared memory.  Aligned rows arrive
+// through one bulk copy per row (TMA, completing on the CTA's mbarrier), with
+// plain loads only for a last partial 16-byte group; other rows use plain
+// loads.  Returns kFlagTimeout if the copy did not complete in time.
+template <typename TIn, bool kVec>
+__device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *const srow[2], int nr, int n,
+                              uint32_t &phase) {
+  const int tid = threadIdx.x;
+  fence_proxy_async_smem();  // earlier reads of the rows before the async overwrite
+  __syncthreads();
+  uint32_t flags = 0;
+  if (kVec) {
+    const uint32_t body = (static_cast<uint32_t>(n) * sizeof(TIn)) & ~15u;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&sm.bar, body * static_cast<uint32_t>(nr));
+      if (body)
+        for (int r = 0; r < nr; ++r) bulk_g2s(srow[r], grow[r], body, &sm.bar);
+    }
+    const int nb = static_cast<int>(body / sizeof(TIn));
+    for (int r = 0; r < nr; ++r)
+      for (int x = nb + tid; x < n; x += kThreads) srow[r][x] = grow[r][x];
+    __syncthreads();
+    if (!mbar_wait_bounded(&sm.bar, phase, kWaitLimit)) {
+      flags = kFlagTimeout;
+      mbar_wait_bounded(&sm.bar, phase, kWaitLimit);  // give the copies in flight one more bound
+    }
+    phase ^= 1u;
+  } else {
+    for (int r = 0; r < nr; ++r)
+      for (int x = tid; x < n; x += kThreads) srow[r][x] = grow[r][x];
+    __syncthreads();
+  }
+  return flags;
+}
+
 // Greedy: thread-local argmax of raw logits of a global row chunk.
 template <typename TIn, bool kVec>
 __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsigned long long &best, uint32_t &flags) {
@@ -548,7 +650,7 @@ __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsig
 }
 
 template <typename TIn, bool kTest, bool kVec>
-__global__ void __launch_bounds__(kThreads) logits_kernel(const VerifyParams P, int chunk) {
+__global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams P, int chunk) {
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ LogitsSmem sm;
@@ -590,6 +692,12 @@ __global__ void __launch_bounds__(kThreads) logits_kernel(const VerifyParams P, 
   int A = 0;
   int32_t last_tok = -1;
   int step = 0;
+  uint32_t phase = 0;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
 
   if (greedy) {
     for (int j = 0;; ++j) {
@@ -641,7 +749,8 @@ __global__ void __launch_bounds__(kThreads) logits_kernel(const VerifyParams P, 
           break;
         }
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
-        if (!position_stats<TIn, kVec>(sm, grow, srow, nr, n, c2, topk, topp, st, step, ncta)) {
+        const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, nr, n, phase);
+        if (!position_stats<TIn>(sm, srow, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta)) {
           req_bits |= SV_DATA_BAD_VALUES;
           valid = false;
           break;
