@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--requests", type=int, default=0, help="override the batch size (profiling runs only)")
+    ap.add_argument("--logits-steps", type=int, default=300)
+    ap.add_argument("--no-logits", action="store_true")
     return ap.parse_args()
 
 
@@ -168,6 +170,83 @@ def algorithmic_bytes(nacc, gammas, V, G):
     return int(per.sum())
 
 
+def logits_algorithmic_bytes(nacc, gammas, temps, V, G, elem=2):
+    """Minimal bytes of one logits-entry call: the logits rows a sequential
+    verifier must read -- target rows 0..A, and for random requests draft rows
+    0..min(A, gamma-1) -- plus ids, parameters, outputs and KV bookkeeping."""
+    import numpy as np
+    A = nacc.astype(np.int64)
+    g = gammas.astype(np.int64)
+    rows = np.where(temps == 0, A + 1, (A + 1) + np.minimum(A + 1, g))
+    per = rows * V * elem + 4 * g + 12 + 4 * (G + 1) + 4 + 8 + 8 * (g - A)
+    return int(per.sum())
+
+
+def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
+    """The logits entry on the same batch shape: bf16 target/draft logits with
+    T=0.8, top-k 50, top-p 0.9 per request (production Philox)."""
+    import numpy as np
+    import torch
+    import workloads
+    w = workloads.make("fused", seed=3 + 1000 * rank, test_mode=False, N=args.requests or None)
+    N, G, V, T = w["N"], w["gamma"], w["V"], w["T"]
+    gam = workloads.gammas_of(w)
+    t = workloads.as_torch(w, dev)
+    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster)
+    K = max(3, min(args.steps, args.logits_steps))
+    W = args.warmup
+    nacc = torch.empty((K + W, N), dtype=torch.int32, device=dev)
+    out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = sv.build_args(entry="logits", draft_ids=t["draft_ids"], target=t["target"], draft=t["draft"],
+                      temperature=t["temperature"], top_k=t["top_k"], top_p=t["top_p"], out_tokens=out,
+                      num_accepted=nacc[0], num_computed_tokens=t["num_computed_tokens"].clone(),
+                      slot_mapping=t["slot_mapping"].clone(), status=status, seed=20240602,
+                      rng_request_base=rank * N)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    h = ctypes.c_void_p(ver.handle)
+
+    def step(k):
+        a.offset = k
+        a.num_accepted = nacc.data_ptr() + 4 * N * k
+        if lib.spec_verify_run(h, ctypes.byref(a), sptr) != 0:
+            raise RuntimeError(lib.spec_verify_last_error().decode())
+
+    for k in range(W):
+        step(k)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    ev[0].record(stream)
+    for k in range(K):
+        step(W + k)
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    total_ms = ev[0].elapsed_time(ev[K])
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    na = nacc[W:].cpu().numpy()
+    alg = float(np.mean([logits_algorithmic_bytes(na[k], gam, w["temperature"], V, G) for k in range(K)]))
+    ms = total_ms / K
+    peak, src = measured_peak()
+    full = (2 * T + N) * V * 2
+    ver.close()
+    return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
+            "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k 50, top-p 0.9, "
+                                   "production Philox", "entry": "logits"},
+            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg, "full_tensor_bytes": full,
+                         "full_tensor_frac": full / (ms / 1e3) / 1e9 / peak},
+            "acceptance": {"mean_accepted": float(na.mean()),
+                           "A_hist": np.bincount(na.reshape(-1), minlength=G + 1).tolist()},
+            "gpu_launches": K}
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -253,6 +332,7 @@ def run_ours(args, world, rank, local_rank):
     torch.cuda.synchronize()
     t1 = time.time()
     barrier()
+    logits = None if args.no_logits else time_logits_entry(args, sv, lib, dev, world, rank, dist, stream)
     clocks.stop()
     total_ms = ev[0].elapsed_time(ev[K])
     per_launch = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
@@ -301,6 +381,8 @@ def run_ours(args, world, rank, local_rank):
         "gpu_launches": K,
         "clocks": clocks.summary(t0, t1),
     }
+    if logits:
+        line["logits_entry"] = logits
     if e2e:
         line["e2e"] = e2e
     if cpu:

@@ -24,6 +24,8 @@
 // All sums are deterministic: integer histograms and fixed-point (2^-40)
 // masses use atomics whose order cannot change the result, and float sums
 // use a fixed reduction tree and rank order across the cluster.
+#include <cuda_bf16.h>
+
 #include <cmath>
 
 #include "sv_device.cuh"
@@ -84,6 +86,46 @@ __device__ __forceinline__ uint32_t bits_at<float>(const float *row, int x) {
   return __float_as_uint(row[x]);
 }
 
+// Visit this thread's elements of a shared-memory row chunk through 16-byte
+// reads (8 bf16 or 4 fp32 per read), then the tail; f(bits, x).
+template <typename TIn, typename F>
+__device__ __forceinline__ void for_each_elem(const TIn *s, int n, F f) {
+  constexpr int kPer = 16 / sizeof(TIn);
+  const int nv = n / kPer;
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(s);
+  for (int v = threadIdx.x; v < nv; v += kThreads) {
+    const uint4 d = s4[v];
+    const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (sizeof(TIn) == 2) {
+        f(w[t] & 0xFFFFu, v * kPer + 2 * t);
+        f(w[t] >> 16, v * kPer + 2 * t + 1);
+      } else {
+        f(w[t], v * kPer + t);
+      }
+    }
+  }
+  for (int x = nv * kPer + threadIdx.x; x < n; x += kThreads) f(bits_at(s, x), x);
+}
+
+// bf16 pairs with native bf16x2 instructions.  max.NaN propagates NaN, so
+// one running max per thread also reveals NaN and +inf in the chunk.
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// 0xFFFF in each half of w that is >= the bf16 value in both halves of t2
+// (false for NaN halves).
+__device__ __forceinline__ uint32_t bf16x2_ge_mask(uint32_t w, uint32_t t2) {
+  return __hge2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w), *reinterpret_cast<const __nv_bfloat162 *>(&t2));
+}
+// bf16 bits of an order key (inverse of Elem<uint16_t>::key).
+__device__ __forceinline__ uint32_t bf16_bits_of_key(uint32_t k) {
+  return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+}
+
 // ---------------------------------------------------------------------------
 // shared memory
 // ---------------------------------------------------------------------------
@@ -91,7 +133,9 @@ constexpr uint32_t kFlagBad = 1u;      // NaN or +inf in a random row
 constexpr uint32_t kFlagFinite = 2u;   // at least one finite logit
 constexpr uint32_t kFlagTimeout = 4u;  // the row's bulk copy did not complete in time
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kNearBins = 255;         // near-max bins: distances 0..254 from the row's largest key
+constexpr int kNearBins = 128;         // near-max bins: distances 0..127 from the row's largest key
+constexpr int kMaxCluster = 16;
+constexpr int kQueue = 192;  // per-warp candidate queue
 
 struct StatPart {  // one CTA's partials of one reduction round, for up to 2 rows
   uint32_t maxkey[2];
@@ -100,6 +144,7 @@ struct StatPart {  // one CTA's partials of one reduction round, for up to 2 row
   unsigned long long tot[2];
   uint32_t cnt[2][256];
   unsigned long long mass[2][256];
+  float massf[2][kNearBins];  // fast path: window masses relative to this CTA's max
 };
 
 struct RowStats {
@@ -118,10 +163,26 @@ struct Select {  // running state of a radix selection, per row
   int ok[2];
 };
 
+struct NearSum {  // cluster-wide near-max histograms on the global maximum, per row
+  unsigned long long cnt[2][kNearBins];
+  unsigned long long mass[2][kNearBins];  // 2^-40 fixed point
+  float z[2];                             // dense normaliser
+  unsigned long long tot[2];              // fixed-point mass of every element
+  uint32_t gmax[2];
+  uint32_t flags[2];
+  uint32_t pkey[2][kMaxCluster];    // each peer's largest finite key
+  uint32_t pflags[2][kMaxCluster];  // each peer's value flags
+  int delta[2][kMaxCluster];        // global minus peer 16-bit max key (-1: peer has no finite value)
+  float scale[2][kMaxCluster];      // exp2((peer max - global max) * c2)
+};
+
 struct LogitsSmem {
   ReduceSmem red;
+  uint32_t queue[kWarps][kQueue];  // per-warp queue of window candidates
+  uint32_t qcount[kWarps];
   StatPart part[2];
   StatPart sum;
+  NearSum near;
   float wz[2][kWarps];
   unsigned long long wt[2][kWarps];
   Select sel;
@@ -129,10 +190,12 @@ struct LogitsSmem {
   int32_t tok[SV_MAX_SPEC_LEN + 1];
 };
 
-enum : uint32_t { kRMax = 1u, kRCnt = 2u, kRMass = 4u, kRZ = 8u, kRTot = 16u };
+enum : uint32_t { kRMax = 1u, kRCnt = 2u, kRMass = 4u, kRZ = 8u, kRTot = 16u, kRMassF = 32u };
 
 __device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
   const int tid = threadIdx.x;
+  if (what & kRMassF)
+    for (int t = tid; t < nr * kNearBins; t += kThreads) p.massf[t / kNearBins][t % kNearBins] = 0.0f;
   if (what & kRCnt)
     for (int t = tid; t < nr * 256; t += kThreads) p.cnt[t >> 8][t & 255] = 0u;
   if (what & kRMass)
@@ -154,37 +217,63 @@ __device__ __forceinline__ void stat_reduce(LogitsSmem &sm, int par, uint32_t wh
   if (what & kRCnt) {
     for (int t = tid; t < nr * 256; t += kThreads) {
       const uint32_t a = smem_addr(&p.cnt[t >> 8][t & 255]);
+      uint32_t v[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) v[c] = c < static_cast<int>(ncta) ? ld_dsmem_u32(map_to_rank(a, c)) : 0u;
       uint32_t s = 0;
-      for (uint32_t c = 0; c < ncta; ++c) s += ld_dsmem_u32(map_to_rank(a, c));
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) s += v[c];
       sm.sum.cnt[t >> 8][t & 255] = s;
     }
   }
   if (what & kRMass) {
     for (int t = tid; t < nr * 256; t += kThreads) {
       const uint32_t a = smem_addr(&p.mass[t >> 8][t & 255]);
+      unsigned long long v[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) v[c] = c < static_cast<int>(ncta) ? ld_dsmem_u64(map_to_rank(a, c)) : 0ull;
       unsigned long long s = 0;
-      for (uint32_t c = 0; c < ncta; ++c) s += ld_dsmem_u64(map_to_rank(a, c));
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) s += v[c];
       sm.sum.mass[t >> 8][t & 255] = s;
     }
   }
-  if (tid < nr) {
+  if (tid < nr) {  // every remote load is issued before any is consumed
     if (what & kRMax) {
-      uint32_t mk = 0, fl = 0;
-      for (uint32_t c = 0; c < ncta; ++c) {
-        mk = max(mk, ld_dsmem_u32(map_to_rank(smem_addr(&p.maxkey[tid]), c)));
-        fl |= ld_dsmem_u32(map_to_rank(smem_addr(&p.flags[tid]), c));
+      uint32_t mk[kMaxCluster], fl[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) {
+        const bool in = c < static_cast<int>(ncta);
+        mk[c] = in ? ld_dsmem_u32(map_to_rank(smem_addr(&p.maxkey[tid]), c)) : 0u;
+        fl[c] = in ? ld_dsmem_u32(map_to_rank(smem_addr(&p.flags[tid]), c)) : 0u;
       }
-      sm.sum.maxkey[tid] = mk;
-      sm.sum.flags[tid] = fl;
+      uint32_t m = 0, f = 0;
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) {
+        m = max(m, mk[c]);
+        f |= fl[c];
+      }
+      sm.sum.maxkey[tid] = m;
+      sm.sum.flags[tid] = f;
     }
     if (what & kRZ) {
+      uint32_t zb[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c)
+        zb[c] = c < static_cast<int>(ncta) ? ld_dsmem_u32(map_to_rank(smem_addr(&p.z[tid]), c)) : 0u;
       float z = 0.0f;
-      for (uint32_t c = 0; c < ncta; ++c) z += __uint_as_float(ld_dsmem_u32(map_to_rank(smem_addr(&p.z[tid]), c)));
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) z += __uint_as_float(zb[c]);
       sm.sum.z[tid] = z;
     }
     if (what & kRTot) {
+      unsigned long long tv[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c)
+        tv[c] = c < static_cast<int>(ncta) ? ld_dsmem_u64(map_to_rank(smem_addr(&p.tot[tid]), c)) : 0ull;
       unsigned long long t = 0;
-      for (uint32_t c = 0; c < ncta; ++c) t += ld_dsmem_u64(map_to_rank(smem_addr(&p.tot[tid]), c));
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) t += tv[c];
       sm.sum.tot[tid] = t;
     }
   }
@@ -334,52 +423,20 @@ __device__ void radix_refine(LogitsSmem &sm, TIn *const srow[2], int nr, int n, 
 }
 
 // ---------------------------------------------------------------------------
-// row statistics of one position (target row, and draft row when nr == 2),
-// the rows already in shared memory
+// row statistics, multi-pass path: exact radix selections over the rows in
+// shared memory, one cluster reduction per 8-bit digit.  Used when the
+// threshold or cut lies beyond the near-max window, for fp32 logits, and for
+// top-p without top-k over a wide nucleus.  st[r].vmax / c2 are already set.
 // ---------------------------------------------------------------------------
 template <typename TIn>
-__device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n, float c2, int topk, float topp,
-                               uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step, uint32_t ncta) {
+__device__ bool stats_slow(LogitsSmem &sm, TIn *const srow[2], int nr, int n, float c2, int topk, float topp,
+                           const uint32_t maxk16[2], RowStats st[2], int &step, uint32_t ncta) {
   using E = Elem<TIn>;
   constexpr int kB = E::kBits;
   const int tid = threadIdx.x;
   const bool use_k = topk > 0;
   const bool use_p = topp < 1.0f;
-
-  // pass 1: max key and value checks
-  int par = step & 1;
-  zero_part(sm.part[par], kRMax, nr);
-  __syncthreads();
-  for (int r = 0; r < nr; ++r) {
-    uint32_t mk = 0, fl = load_flags;
-    const TIn *s = srow[r];
-    for (int x = tid; x < n; x += kThreads) {
-      const uint32_t b = bits_at(s, x);
-      if (E::is_nan(b) || E::is_pinf(b)) fl |= kFlagBad;
-      if (E::finite(b)) fl |= kFlagFinite;
-      mk = max(mk, E::key(b));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
-      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
-    }
-    if ((tid & 31) == 0) {
-      atomicMax(&sm.part[par].maxkey[r], mk);
-      atomicOr(&sm.part[par].flags[r], fl);
-    }
-  }
-  stat_reduce(sm, par, kRMax, nr, ncta);
-  ++step;
-  for (int r = 0; r < nr; ++r) {
-    const uint32_t f = sm.sum.flags[r];
-    if (f & kFlagTimeout) *req_bits |= SV_DATA_COPY_TIMEOUT;
-    if ((f & (kFlagBad | kFlagTimeout)) || !(f & kFlagFinite)) return false;
-    st[r].vmax = E::val_of_key(sm.sum.maxkey[r]);
-    st[r].c2 = c2;
-  }
-  uint32_t maxk16[2] = {0u, 0u};
-  for (int r = 0; r < nr; ++r) maxk16[r] = key16_of<TIn>(sm.sum.maxkey[r]);
+  int par;
 
   // top-k: the k-th largest key (ties kept).  First count the keys within
   // kNearBins steps of the largest (where the threshold almost always lies),
@@ -501,6 +558,384 @@ __device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// row statistics of one position (target row, and draft row when nr == 2),
+// the rows already in shared memory.
+//
+// Fast path, one cluster reduction: every CTA measures its chunk against its
+// own largest key -- value checks, and for top-k/top-p the counts and
+// fixed-point masses exp2((v - local max) * c2) of the keys within kNearBins
+// steps of that maximum (dense rows: the local normaliser).  The reduction
+// moves each peer's histogram onto the global maximum (shift by the distance
+// between the maxima, scale by exp2 of their difference) and sums in rank
+// order, which resolves the k-th largest key, the top-p cut and the
+// normaliser whenever they lie in the near window (bf16 keys).
+// ---------------------------------------------------------------------------
+// One warp: first near bin (walking from distance 0) whose running total
+// reaches `need`, within [0, limit).  Returns the bin or -1; *incl = total up
+// to and including it.  Integer sums: the choice is the same in every CTA.
+constexpr int kBinsPerLane = kNearBins / 32;
+__device__ __forceinline__ int near_pick(const unsigned long long *h, int limit, unsigned long long need,
+                                         unsigned long long *incl) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long own = 0;
+#pragma unroll
+  for (int t = 0; t < kBinsPerLane; ++t) {
+    const int d = kBinsPerLane * lane + t;
+    own += d < limit ? h[d] : 0ull;
+  }
+  unsigned long long inc = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  const unsigned long long before = inc - own;
+  int found = -1;
+  unsigned long long in = 0;
+  if (before < need && inc >= need) {
+    unsigned long long acc = before;
+#pragma unroll
+    for (int t = 0; t < kBinsPerLane; ++t) {
+      const int d = kBinsPerLane * lane + t;
+      const unsigned long long x = d < limit ? h[d] : 0ull;
+      if (found < 0 && acc + x >= need) {
+        found = d;
+        in = acc + x;
+      }
+      acc += x;
+    }
+  }
+  const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0);
+  if (!ball) return -1;
+  const int src = __ffs(ball) - 1;
+  *incl = __shfl_sync(0xFFFFFFFFu, in, src);
+  return __shfl_sync(0xFFFFFFFFu, found, src);
+}
+
+// One warp: sum of h over bins [0, limit).
+__device__ __forceinline__ unsigned long long near_sum(const unsigned long long *h, int limit) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long s = 0;
+#pragma unroll
+  for (int t = 0; t < kBinsPerLane; ++t) {
+    const int d = kBinsPerLane * lane + t;
+    s += d < limit ? h[d] : 0ull;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  return s;
+}
+
+template <typename TIn>
+__device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n, float c2, int topk, float topp,
+                               uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step, uint32_t ncta) {
+  using E = Elem<TIn>;
+  constexpr int kB = E::kBits;
+  const int tid = threadIdx.x;
+  const bool use_k = topk > 0;
+  const bool use_p = topp < 1.0f;
+  const bool near = use_k || use_p;
+  const int par = step & 1;
+  StatPart &lp = sm.part[par];
+
+  // local pass A: largest key and value checks of this CTA's chunk
+  zero_part(lp, near ? (kRCnt | kRMassF) : 0u, nr);
+  __syncthreads();
+  for (int r = 0; r < nr; ++r) {
+    uint32_t mk = 0, fl = load_flags;
+    if (kB == 16) {
+      // pairs of bf16 through one NaN-propagating bf16x2 max per pair
+      const int nw = n >> 1;
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
+      uint32_t acc = 0xFF80FF80u;  // (-inf, -inf)
+      for (int v = tid; v < (nw >> 2); v += kThreads) {
+        const uint4 d = s4[v];
+        acc = bf16x2_max_nan(acc, d.x);
+        acc = bf16x2_max_nan(acc, d.y);
+        acc = bf16x2_max_nan(acc, d.z);
+        acc = bf16x2_max_nan(acc, d.w);
+      }
+      for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) acc = bf16x2_max_nan(acc, bits_at(srow[r], x) | 0xFF800000u);
+      acc = bf16x2_max_nan(acc, (acc >> 16) | (acc << 16));
+      const uint32_t mb = acc & 0xFFFFu;  // this thread's largest value, NaN if it saw one
+      if (E::is_nan(mb) || E::is_pinf(mb)) fl |= kFlagBad;
+      if (E::finite(mb)) {
+        fl |= kFlagFinite;
+        mk = E::key(mb);
+      }
+    } else {
+      for_each_elem(srow[r], n, [&](uint32_t b, int) {
+        if (E::is_nan(b) || E::is_pinf(b)) fl |= kFlagBad;
+        if (E::finite(b)) {
+          fl |= kFlagFinite;
+          mk = max(mk, E::key(b));  // largest finite key
+        }
+      });
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
+      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+    }
+    if ((tid & 31) == 0) {
+      atomicMax(&lp.maxkey[r], mk);
+      atomicOr(&lp.flags[r], fl);
+    }
+  }
+  __syncthreads();
+
+  // local pass B: near-max counts and masses, or the dense local normaliser
+  {
+    float zt[2] = {0.0f, 0.0f};
+    unsigned long long tt[2] = {0ull, 0ull};
+    for (int r = 0; r < nr; ++r) {
+      if (!(lp.flags[r] & kFlagFinite)) continue;  // empty or no finite value: contributes nothing
+      const uint32_t lk = lp.maxkey[r];
+      const uint32_t lk16 = key16_of<TIn>(lk);
+      const float lv = E::val_of_key(lk);
+      float sum = 0.0f, comp = 0.0f;
+      unsigned long long tot = 0;
+      if (kB == 16 && use_k) {
+        // top-k rows: only keys within the window matter; test pairs of keys
+        // against the window's lower edge and visit single elements rarely
+        const uint32_t lo = lk16 - (kNearBins - 1);  // window's smallest key; below key(-inf): all finite pass
+        const uint32_t lob = (lk16 >= static_cast<uint32_t>(kNearBins - 1) && lo > 0x007Fu) ? bf16_bits_of_key(lo)
+                                                                                              : 0xFF80u;
+        const uint32_t lo2 = lob | (lob << 16);
+        auto take = [&](uint32_t b) {
+          if (!E::finite(b)) return;
+          const uint32_t d = lk16 - E::key(b);
+          if (d >= static_cast<uint32_t>(kNearBins)) return;
+          atomicAdd(&lp.cnt[r][d], 1u);
+          atomicAdd(&lp.massf[r][d], exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2)));
+        };
+        // Candidates are rare (a few percent): each thread appends its own to
+        // its warp's queue, and the warp treats a full queue (or the rest at
+        // the end) with all 32 lanes at once.
+        const int nw = n >> 1;
+        const int ng = nw >> 2;  // 16-byte groups
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
+        const int lane = tid & 31, warp = tid >> 5;
+        uint32_t *q = sm.queue[warp];
+        if (lane == 0) sm.qcount[warp] = 0u;
+        __syncwarp();
+        auto flush = [&]() {
+          __syncwarp();
+          const uint32_t total = sm.qcount[warp];
+          for (uint32_t i = lane; i < total; i += 32) take(q[i]);
+          __syncwarp();
+          if (lane == 0) sm.qcount[warp] = 0u;
+          __syncwarp();
+        };
+        for (int vb = warp * 32; vb < ng; vb += kThreads) {  // warp-uniform trip count
+          const int v = vb + lane;
+          uint32_t w[4] = {0u, 0u, 0u, 0u}, m[4] = {0u, 0u, 0u, 0u};
+          if (v < ng) {
+            const uint4 dv = s4[v];
+            w[0] = dv.x; w[1] = dv.y; w[2] = dv.z; w[3] = dv.w;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) m[t] = bf16x2_ge_mask(w[t], lo2);
+          }
+          // each true half contributes 16 set bits
+          const uint32_t mine = (__popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3])) >> 4;
+          const uint32_t here = __reduce_add_sync(0xFFFFFFFFu, mine);
+          if (here == 0u) continue;
+          if (here > static_cast<uint32_t>(kQueue)) {  // too many at once: every lane takes its own
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              if (m[t] & 0xFFFFu) take(w[t] & 0xFFFFu);
+              if (m[t] >> 16) take(w[t] >> 16);
+            }
+            continue;
+          }
+          if (sm.qcount[warp] + here > static_cast<uint32_t>(kQueue)) flush();
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if (m[t] & 0xFFFFu) q[atomicAdd(&sm.qcount[warp], 1u)] = w[t] & 0xFFFFu;
+            if (m[t] >> 16) q[atomicAdd(&sm.qcount[warp], 1u)] = w[t] >> 16;
+          }
+          __syncwarp();
+        }
+        flush();
+        for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) take(bits_at(srow[r], x));
+        zt[r] = 0.0f;
+        tt[r] = 0ull;
+        continue;
+      }
+      for_each_elem(srow[r], n, [&](uint32_t b, int) {
+        if (!E::finite(b)) return;  // -inf adds nothing (NaN/+inf already flagged)
+        const uint32_t k = E::key(b);
+        const uint32_t d = lk16 - key16_of<TIn>(k);
+        const bool in_near = d < static_cast<uint32_t>(kNearBins);
+        if (!near || in_near || (use_p && !use_k)) {
+          const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2));
+          if (!near) {
+            const float y = e - comp;  // Kahan
+            const float t = sum + y;
+            comp = (t - sum) - y;
+            sum = t;
+          } else {
+            if (use_p && !use_k) tot += to_fixed(e);
+            if (in_near) {
+              if (use_k) atomicAdd(&lp.cnt[r][d], 1u);
+              atomicAdd(&lp.massf[r][d], e);
+            }
+          }
+        }
+      });
+      zt[r] = sum;
+      tt[r] = tot;
+    }
+    if (!near) block_sum_z(sm, lp, zt, nr);
+    else if (use_p && !use_k) block_sum_tot(sm, lp, tt, nr);
+  }
+
+  // the one cluster reduction
+  __syncthreads();
+  cluster_sync();
+  ++step;
+  NearSum &ns = sm.near;
+  if (tid < nr * kMaxCluster) {
+    const int r = tid / kMaxCluster, c = tid % kMaxCluster;
+    if (c < static_cast<int>(ncta)) {
+      ns.pkey[r][c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.maxkey[r]), c));
+      ns.pflags[r][c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.flags[r]), c));
+    }
+  }
+  __syncthreads();
+  if (tid < nr) {
+    const int r = tid;
+    uint32_t gk = 0, fl = 0;
+    for (int c = 0; c < static_cast<int>(ncta); ++c) {
+      const uint32_t pf = ns.pflags[r][c];
+      fl |= pf;
+      if (pf & kFlagFinite) gk = max(gk, ns.pkey[r][c]);
+    }
+    ns.gmax[r] = gk;
+    ns.flags[r] = fl;
+  }
+  __syncthreads();
+  if (tid < nr * kMaxCluster) {  // one thread per (row, peer): shift and scale onto the global max
+    const int r = tid / kMaxCluster, c = tid % kMaxCluster;
+    const uint32_t pf = c < static_cast<int>(ncta) ? ns.pflags[r][c] : 0u;
+    if ((pf & kFlagFinite) && (ns.flags[r] & kFlagFinite)) {
+      const uint32_t pk = ns.pkey[r][c];
+      ns.delta[r][c] = static_cast<int>(key16_of<TIn>(ns.gmax[r]) - key16_of<TIn>(pk));
+      ns.scale[r][c] = exp2f(__fmul_rn(__fsub_rn(E::val_of_key(pk), E::val_of_key(ns.gmax[r])), c2));
+    } else {
+      ns.delta[r][c] = -1;
+      ns.scale[r][c] = 0.0f;
+    }
+  }
+  __syncthreads();
+  if (near && tid < nr * kNearBins) {  // one thread per (row, bin) of the window
+    const int r = tid / kNearBins, d = tid % kNearBins;
+    uint32_t cv[kMaxCluster], mv[kMaxCluster];
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {  // every load is issued (from a valid address), then masked
+      const int dl = d - ns.delta[r][c];    // delta is -1 for absent peers
+      const bool ok = c < static_cast<int>(ncta) && ns.delta[r][c] >= 0 && dl >= 0;
+      const int cc = ok ? c : 0, dd = ok ? dl : 0;
+      cv[c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.cnt[r][dd]), cc));
+      mv[c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.massf[r][dd]), cc));
+      if (!ok) cv[c] = mv[c] = 0u;
+    }
+    // peers' masses rescaled onto the global maximum and summed in rank
+    // order, then held in 2^-40 fixed point for the integer selection
+    unsigned long long cs = 0;
+    float ms = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      cs += use_k ? cv[c] : 0u;
+      ms += __uint_as_float(mv[c]) * ns.scale[r][c];
+    }
+    ns.cnt[r][d] = cs;
+    ns.mass[r][d] = to_fixed(ms);
+  }
+  if (tid < nr) {  // remote loads first, then the fixed-order sums
+    const int r = tid;
+    float z = 0.0f;
+    unsigned long long tot = 0;
+    if (!near) {
+      uint32_t zb[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c)
+        zb[c] = (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0) ? ld_dsmem_u32(map_to_rank(smem_addr(&lp.z[r]), c)) : 0u;
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c)
+        if (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0) z += __uint_as_float(zb[c]) * ns.scale[r][c];
+    } else if (use_p && !use_k) {
+      unsigned long long tv[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c)
+        tv[c] = (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0) ? ld_dsmem_u64(map_to_rank(smem_addr(&lp.tot[r]), c)) : 0ull;
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c)
+        if (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0 && tv[c])
+          tot += __float2ull_rn(__ull2float_rn(tv[c]) * ns.scale[r][c]);
+    }
+    ns.z[r] = z;
+    ns.tot[r] = tot;
+  }
+  __syncthreads();
+
+  for (int r = 0; r < nr; ++r) {
+    const uint32_t f = ns.flags[r];
+    if (f & kFlagTimeout) *req_bits |= SV_DATA_COPY_TIMEOUT;
+    if ((f & (kFlagBad | kFlagTimeout)) || !(f & kFlagFinite)) return false;
+    st[r].vmax = E::val_of_key(ns.gmax[r]);
+    st[r].c2 = c2;
+    st[r].cut = 0u;
+    st[r].zp = ns.z[r];
+  }
+  if (!near) return true;
+
+  // resolve the threshold, the cut and the normaliser from the near bins
+  const int warp = tid >> 5;
+  if (warp < nr) {
+    const int r = warp;
+    int ok = 1, lim = kNearBins;
+    unsigned long long kept = 0;
+    if (use_k) {
+      unsigned long long in;
+      const int L = near_pick(ns.cnt[r], kNearBins, static_cast<unsigned long long>(topk), &in);
+      if (L < 0) ok = 0;
+      else lim = L + 1;
+      kept = near_sum(ns.mass[r], lim);  // mass of the top-k set
+    } else {
+      kept = ns.tot[r];
+    }
+    int Lc = lim - 1;
+    if (ok && use_p) {
+      unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(kept));
+      unsigned long long in = 0;
+      Lc = near_pick(ns.mass[r], lim, need > 0ull ? need : 1ull, &in);
+      if (Lc < 0) ok = 0;
+      else kept = in;
+    }
+    if ((threadIdx.x & 31) == 0) {
+      sm.sel.ok[r] = ok && (kB == 16);  // fp32 keys need the low 16 bits refined: multi-pass path
+      sm.sel.prefix[r] = key16_of<TIn>(ns.gmax[r]) - static_cast<uint32_t>(Lc < 0 ? 0 : Lc);
+      ns.z[r] = static_cast<float>(static_cast<double>(kept) * (1.0 / static_cast<double>(kMassScale)));
+    }
+  }
+  __syncthreads();
+  bool all_ok = true;
+  for (int r = 0; r < nr; ++r) all_ok &= sm.sel.ok[r] != 0;
+  if (all_ok) {
+    for (int r = 0; r < nr; ++r) {
+      st[r].cut = sm.sel.prefix[r];
+      st[r].zp = ns.z[r];
+    }
+    return true;
+  }
+  uint32_t maxk16[2] = {0u, 0u};
+  for (int r = 0; r < nr; ++r) maxk16[r] = key16_of<TIn>(ns.gmax[r]);
+  __syncthreads();
+  return stats_slow<TIn>(sm, srow, nr, n, c2, topk, topp, maxk16, st, step, ncta);
+}
+
 // Probability of one logit under a row's statistics (0 outside the kept set).
 template <typename TIn>
 __device__ __forceinline__ float prob_of(uint32_t b, const RowStats &st) {
@@ -525,52 +960,97 @@ __device__ __forceinline__ void consider_drawn_l(float w, uint32_t word, int x, 
   }
 }
 
+// Race candidates of one quad (4 consecutive entries starting at a multiple of
+// 4): E from the test-mode row or from one Philox call.
+template <bool kTest>
+__device__ __forceinline__ void race_quad_l(const float w[4], int xg, const float *Erow, const RngKey &rk,
+                                            uint32_t rs, float &bk, int &bx, uint32_t &flags) {
+  if (!(w[0] > 0.0f || w[1] > 0.0f || w[2] > 0.0f || w[3] > 0.0f)) return;
+  if (kTest) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (!(w[t] > 0.0f)) continue;
+      const float E = Erow[xg + t];
+      if (!(E > 0.0f)) {
+        flags |= SV_DATA_BAD_EXPONENTIAL;
+        continue;
+      }
+      const float key = __fdiv_rn(w[t], E);
+      if (key > bk) {
+        bk = key;
+        bx = xg + t;
+      }
+    }
+  } else {
+    const uint4 wd = draw_e_words(rk, rs, static_cast<uint32_t>(xg) >> 2);
+    if (w[0] > 0.0f) consider_drawn_l(w[0], wd.x, xg + 0, bk, bx);
+    if (w[1] > 0.0f) consider_drawn_l(w[1], wd.y, xg + 1, bk, bx);
+    if (w[2] > 0.0f) consider_drawn_l(w[2], wd.z, xg + 2, bk, bx);
+    if (w[3] > 0.0f) consider_drawn_l(w[3], wd.w, xg + 3, bk, bx);
+  }
+}
+
+template <typename TIn, bool kResidual>
+__device__ __forceinline__ float race_w(uint32_t bp, uint32_t bq, const RowStats &ps, const RowStats &qs) {
+  const float p = prob_of<TIn>(bp, ps);
+  if (kResidual) {
+    const float d = __fsub_rn(p, prob_of<TIn>(bq, qs));
+    return d > 0.0f ? d : 0.0f;
+  }
+  return p > 0.0f ? p : 0.0f;
+}
+
+// The race over this CTA's rows in shared memory.  Each thread takes 16-byte
+// groups in increasing order (then the tail quads), so its strict '>' keeps
+// its lowest index on ties.
 template <typename TIn, bool kTest, bool kResidual>
 __device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const RowStats &ps, const RowStats &qs,
                                           int x0, int n, const float *Erow, const RngKey &rk, uint32_t rs, float &bk,
                                           int &bx, uint32_t &flags) {
-  const int tid = threadIdx.x;
-  for (int q4 = tid; 4 * q4 < n; q4 += kThreads) {
+  constexpr int kPer = 16 / sizeof(TIn);  // 8 bf16 or 4 fp32 = 2 or 1 quads
+  const int nv = n / kPer;
+  const uint4 *p4 = reinterpret_cast<const uint4 *>(sp);
+  const uint4 *q4 = reinterpret_cast<const uint4 *>(kResidual ? sq : sp);
+  // bf16 rows with a cut: pairs of keys are tested against the cuts first, so
+  // entries outside both kept sets cost two SIMD compares per pair
+  const uint32_t cpb = bf16_bits_of_key(ps.cut), cqb = bf16_bits_of_key(qs.cut);
+  const uint32_t cp2 = cpb | (cpb << 16), cq2 = cqb | (cqb << 16);
+  const bool packed_test = sizeof(TIn) == 2 && (ps.cut > 0x007Fu) && (!kResidual || qs.cut > 0x007Fu);
+  for (int v = threadIdx.x; v < nv; v += kThreads) {
+    const uint4 dp = p4[v];
+    const uint4 dq = kResidual ? q4[v] : dp;
+    const uint32_t wp[4] = {dp.x, dp.y, dp.z, dp.w}, wq[4] = {dq.x, dq.y, dq.z, dq.w};
+    if (packed_test) {
+      uint32_t any = 0u;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        any |= bf16x2_ge_mask(wp[t], cp2);
+        if (kResidual) any |= bf16x2_ge_mask(wq[t], cq2);
+      }
+      if (any == 0u) continue;  // no kept entry in these 8: every weight is 0
+    }
+    float w[kPer];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (sizeof(TIn) == 2) {
+        w[2 * t] = race_w<TIn, kResidual>(wp[t] & 0xFFFFu, wq[t] & 0xFFFFu, ps, qs);
+        w[2 * t + 1] = race_w<TIn, kResidual>(wp[t] >> 16, wq[t] >> 16, ps, qs);
+      } else {
+        w[t] = race_w<TIn, kResidual>(wp[t], wq[t], ps, qs);
+      }
+    }
+#pragma unroll
+    for (int qd = 0; qd < kPer / 4; ++qd)
+      race_quad_l<kTest>(&w[4 * qd], x0 + v * kPer + 4 * qd, Erow, rk, rs, bk, bx, flags);
+  }
+  for (int q = nv * (kPer / 4) + threadIdx.x; 4 * q < n; q += kThreads) {
     float w[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const int x = 4 * q4 + t;
-      w[t] = 0.0f;
-      if (x < n) {
-        const float p = prob_of<TIn>(bits_at(sp, x), ps);
-        if (kResidual) {
-          const float q = prob_of<TIn>(bits_at(sq, x), qs);
-          const float d = __fsub_rn(p, q);
-          w[t] = d > 0.0f ? d : 0.0f;
-        } else {
-          w[t] = p > 0.0f ? p : 0.0f;
-        }
-      }
+      const int x = 4 * q + t;
+      w[t] = x < n ? race_w<TIn, kResidual>(bits_at(sp, x), kResidual ? bits_at(sq, x) : 0u, ps, qs) : 0.0f;
     }
-    if (!(w[0] > 0.0f || w[1] > 0.0f || w[2] > 0.0f || w[3] > 0.0f)) continue;
-    const int xg = x0 + 4 * q4;  // global vocabulary index of this quad (x0 is a multiple of 8)
-    if (kTest) {
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (!(w[t] > 0.0f)) continue;
-        const float E = Erow[xg + t];
-        if (!(E > 0.0f)) {
-          flags |= SV_DATA_BAD_EXPONENTIAL;
-          continue;
-        }
-        const float key = __fdiv_rn(w[t], E);
-        if (key > bk) {
-          bk = key;
-          bx = xg + t;
-        }
-      }
-    } else {
-      const uint4 wd = draw_e_words(rk, rs, static_cast<uint32_t>(xg) >> 2);
-      if (w[0] > 0.0f) consider_drawn_l(w[0], wd.x, xg + 0, bk, bx);
-      if (w[1] > 0.0f) consider_drawn_l(w[1], wd.y, xg + 1, bk, bx);
-      if (w[2] > 0.0f) consider_drawn_l(w[2], wd.z, xg + 2, bk, bx);
-      if (w[3] > 0.0f) consider_drawn_l(w[3], wd.w, xg + 3, bk, bx);
-    }
+    race_quad_l<kTest>(w, x0 + 4 * q, Erow, rk, rs, bk, bx, flags);
   }
 }
 
@@ -748,6 +1228,19 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
           valid = false;
           break;
         }
+        // the draft id, its two logits and u are fetched now, so their latency
+        // hides behind the row copy and the statistics
+        int y = -1;
+        uint32_t bty = 0u, bdy = 0u;
+        float u = 0.0f;
+        if (j < g) {
+          y = P.ids[s + j];
+          if (y >= 0 && y < V) {
+            bty = bits_at(tgt + (tb + j) * ts, y);
+            bdy = bits_at(drf + (s + j) * ds, y);
+          }
+          u = kTest ? P.uniforms[s + j] : draw_uniform(rk, rs, static_cast<uint32_t>(j));
+        }
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
         const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, nr, n, phase);
         if (!position_stats<TIn>(sm, srow, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta)) {
@@ -760,19 +1253,17 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
         uint32_t fl = 0;
         bool residual = false;
         if (j < g) {
-          const int y = P.ids[s + j];
           if (y < 0 || y >= V) {
             req_bits |= SV_DATA_BAD_DRAFT_ID;
             valid = false;
             break;
           }
-          const float py = prob_of<TIn>(bits_at(tgt + (tb + j) * ts, y), st[0]);
-          const float qy = prob_of<TIn>(bits_at(drf + (s + j) * ds, y), st[1]);
+          const float py = prob_of<TIn>(bty, st[0]);
+          const float qy = prob_of<TIn>(bdy, st[1]);
           if (rank == 0 && tid == 0) {
             if (P.dbg_py) P.dbg_py[s + j] = py;
             if (P.dbg_qy) P.dbg_qy[s + j] = qy;
           }
-          const float u = kTest ? P.uniforms[s + j] : draw_uniform(rk, rs, static_cast<uint32_t>(j));
           if (__fmul_rn(u, qy) < py) {
             if (tid == 0) sm.tok[j] = y;
             continue;  // accepted: next position
