@@ -143,8 +143,16 @@ struct StatPart {  // one CTA's partials of one reduction round, for up to 2 row
   float z[2];
   unsigned long long tot[2];
   uint32_t cnt[2][256];
-  unsigned long long mass[2][256];
-  float massf[2][kNearBins];  // fast path: window masses relative to this CTA's max
+  float massf[2][256];  // masses (fast path: the window, relative to this CTA's max)
+};
+
+struct StatSum {  // cluster totals of a reduction round (the same in every CTA)
+  uint32_t maxkey[2];
+  uint32_t flags[2];
+  float z[2];
+  unsigned long long tot[2];
+  uint32_t cnt[2][256];
+  unsigned long long mass[2][256];  // 2^-40 fixed point, from the peers' fp32 masses in rank order
 };
 
 struct RowStats {
@@ -181,7 +189,7 @@ struct LogitsSmem {
   uint32_t queue[kWarps][kQueue];  // per-warp queue of window candidates
   uint32_t qcount[kWarps];
   StatPart part[2];
-  StatPart sum;
+  StatSum sum;
   NearSum near;
   float wz[2][kWarps];
   unsigned long long wt[2][kWarps];
@@ -196,16 +204,20 @@ __device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
   const int tid = threadIdx.x;
   if (what & kRMassF)
     for (int t = tid; t < nr * kNearBins; t += kThreads) p.massf[t / kNearBins][t % kNearBins] = 0.0f;
+  if (what & kRMass)
+    for (int t = tid; t < nr * 256; t += kThreads) p.massf[t >> 8][t & 255] = 0.0f;
   if (what & kRCnt)
     for (int t = tid; t < nr * 256; t += kThreads) p.cnt[t >> 8][t & 255] = 0u;
-  if (what & kRMass)
-    for (int t = tid; t < nr * 256; t += kThreads) p.mass[t >> 8][t & 255] = 0ull;
   if (tid < 2) {
     p.maxkey[tid] = 0u;
     p.flags[tid] = 0u;
     p.z[tid] = 0.0f;
     p.tot[tid] = 0ull;
   }
+}
+
+__device__ __forceinline__ unsigned long long to_fixed(float e) {
+  return static_cast<unsigned long long>(__float2ull_rn(e * kMassScale));
 }
 
 // Combine every CTA's part[par] into sum (the same in every CTA of the cluster).
@@ -228,13 +240,13 @@ __device__ __forceinline__ void stat_reduce(LogitsSmem &sm, int par, uint32_t wh
   }
   if (what & kRMass) {
     for (int t = tid; t < nr * 256; t += kThreads) {
-      const uint32_t a = smem_addr(&p.mass[t >> 8][t & 255]);
-      unsigned long long v[kMaxCluster];
+      const uint32_t a = smem_addr(&p.massf[t >> 8][t & 255]);
+      uint32_t v[kMaxCluster];
 #pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c) v[c] = c < static_cast<int>(ncta) ? ld_dsmem_u64(map_to_rank(a, c)) : 0ull;
+      for (int c = 0; c < kMaxCluster; ++c) v[c] = c < static_cast<int>(ncta) ? ld_dsmem_u32(map_to_rank(a, c)) : 0u;
       unsigned long long s = 0;
 #pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c) s += v[c];
+      for (int c = 0; c < kMaxCluster; ++c) s += to_fixed(__uint_as_float(v[c]));  // exact integer sum
       sm.sum.mass[t >> 8][t & 255] = s;
     }
   }
@@ -374,9 +386,6 @@ __device__ __forceinline__ uint32_t key16_of(uint32_t k) {
   return Elem<TIn>::kBits == 16 ? k : (k >> 16);
 }
 
-__device__ __forceinline__ unsigned long long to_fixed(float e) {
-  return static_cast<unsigned long long>(__float2ull_rn(e * kMassScale));
-}
 
 // Refine the selection of every row whose prefix is not complete, one 8-bit
 // digit per level (counts, or fixed-point masses of keys >= tau).
@@ -405,7 +414,7 @@ __device__ void radix_refine(LogitsSmem &sm, TIn *const srow[2], int nr, int n, 
         if (kMass) {
           if (k < tau[r]) continue;
           const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), st[r].c2));
-          atomicAdd(&sm.part[par].mass[r][(k >> lo) & 255u], to_fixed(e));
+          atomicAdd(&sm.part[par].massf[r][(k >> lo) & 255u], e);
         } else {
           atomicAdd(&sm.part[par].cnt[r][(k >> lo) & 255u], 1u);
         }
@@ -517,10 +526,10 @@ __device__ bool stats_slow(LogitsSmem &sm, TIn *const srow[2], int nr, int n, fl
         const uint32_t b = bits_at(s, x);
         const uint32_t k = E::key(b);
         if (k < tau[r]) continue;
-        const unsigned long long m = to_fixed(exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2)));
-        tot += m;
+        const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st[r].vmax), c2));
+        tot += to_fixed(e);
         const uint32_t d = maxk16[r] - key16_of<TIn>(k);
-        if (d < static_cast<uint32_t>(kNearBins)) atomicAdd(&sm.part[par].mass[r][d], m);
+        if (d < static_cast<uint32_t>(kNearBins)) atomicAdd(&sm.part[par].massf[r][d], e);
       }
       tt[r] = tot;
     }
@@ -648,14 +657,21 @@ __device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n
       // pairs of bf16 through one NaN-propagating bf16x2 max per pair
       const int nw = n >> 1;
       const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
-      uint32_t acc = 0xFF80FF80u;  // (-inf, -inf)
-      for (int v = tid; v < (nw >> 2); v += kThreads) {
-        const uint4 d = s4[v];
-        acc = bf16x2_max_nan(acc, d.x);
-        acc = bf16x2_max_nan(acc, d.y);
-        acc = bf16x2_max_nan(acc, d.z);
-        acc = bf16x2_max_nan(acc, d.w);
+      uint32_t acc = 0xFF80FF80u, acc2 = 0xFF80FF80u;  // (-inf, -inf); two chains
+      const int ng = nw >> 2;
+      int v = tid;
+      for (; v + 3 * kThreads < ng; v += 4 * kThreads) {  // four 16-byte loads in flight
+        const uint4 d0 = s4[v], d1 = s4[v + kThreads], d2 = s4[v + 2 * kThreads], d3 = s4[v + 3 * kThreads];
+        acc = bf16x2_max_nan(acc, bf16x2_max_nan(bf16x2_max_nan(d0.x, d0.y), bf16x2_max_nan(d0.z, d0.w)));
+        acc2 = bf16x2_max_nan(acc2, bf16x2_max_nan(bf16x2_max_nan(d1.x, d1.y), bf16x2_max_nan(d1.z, d1.w)));
+        acc = bf16x2_max_nan(acc, bf16x2_max_nan(bf16x2_max_nan(d2.x, d2.y), bf16x2_max_nan(d2.z, d2.w)));
+        acc2 = bf16x2_max_nan(acc2, bf16x2_max_nan(bf16x2_max_nan(d3.x, d3.y), bf16x2_max_nan(d3.z, d3.w)));
       }
+      for (; v < ng; v += kThreads) {
+        const uint4 d = s4[v];
+        acc = bf16x2_max_nan(acc, bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w)));
+      }
+      acc = bf16x2_max_nan(acc, acc2);
       for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) acc = bf16x2_max_nan(acc, bits_at(srow[r], x) | 0xFF800000u);
       acc = bf16x2_max_nan(acc, (acc >> 16) | (acc << 16));
       const uint32_t mb = acc & 0xFFFFu;  // this thread's largest value, NaN if it saw one
@@ -728,32 +744,39 @@ __device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n
           if (lane == 0) sm.qcount[warp] = 0u;
           __syncwarp();
         };
-        for (int vb = warp * 32; vb < ng; vb += kThreads) {  // warp-uniform trip count
-          const int v = vb + lane;
-          uint32_t w[4] = {0u, 0u, 0u, 0u}, m[4] = {0u, 0u, 0u, 0u};
-          if (v < ng) {
-            const uint4 dv = s4[v];
-            w[0] = dv.x; w[1] = dv.y; w[2] = dv.z; w[3] = dv.w;
+        for (int vb = warp * 32; vb < ng; vb += 2 * kThreads) {  // warp-uniform trip count, 2 groups
+          uint32_t w[8], m[8];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) m[t] = bf16x2_ge_mask(w[t], lo2);
+          for (int h = 0; h < 2; ++h) {
+            const int v = vb + h * kThreads + lane;
+            uint4 dv = make_uint4(0u, 0u, 0u, 0u);
+            if (v < ng) dv = s4[v];
+            w[4 * h + 0] = dv.x; w[4 * h + 1] = dv.y; w[4 * h + 2] = dv.z; w[4 * h + 3] = dv.w;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) m[4 * h + t] = v < ng ? bf16x2_ge_mask(w[4 * h + t], lo2) : 0u;
           }
-          // each true half contributes 16 set bits
-          const uint32_t mine = (__popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3])) >> 4;
+          uint32_t pc = 0u;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) pc += __popc(m[t]);
+          const uint32_t mine = pc >> 4;  // each true half contributes 16 set bits
           const uint32_t here = __reduce_add_sync(0xFFFFFFFFu, mine);
           if (here == 0u) continue;
           if (here > static_cast<uint32_t>(kQueue)) {  // too many at once: every lane takes its own
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
+            for (int t = 0; t < 8; ++t) {
               if (m[t] & 0xFFFFu) take(w[t] & 0xFFFFu);
               if (m[t] >> 16) take(w[t] >> 16);
             }
             continue;
           }
           if (sm.qcount[warp] + here > static_cast<uint32_t>(kQueue)) flush();
+          if (mine) {
+            uint32_t idx = atomicAdd(&sm.qcount[warp], mine);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (m[t] & 0xFFFFu) q[atomicAdd(&sm.qcount[warp], 1u)] = w[t] & 0xFFFFu;
-            if (m[t] >> 16) q[atomicAdd(&sm.qcount[warp], 1u)] = w[t] >> 16;
+            for (int t = 0; t < 8; ++t) {
+              if (m[t] & 0xFFFFu) q[idx++] = w[t] & 0xFFFFu;
+              if (m[t] >> 16) q[idx++] = w[t] >> 16;
+            }
           }
           __syncwarp();
         }
