@@ -24,7 +24,10 @@
  *
  * Memory and execution model: every pointer in spec_verify_args is a DEVICE
  * pointer on the handle's device, owned by the caller (the library allocates
- * nothing per call).  spec_verify_run only validates on the host and enqueues
+ * nothing per call).  For the probability entry, target/draft/exponentials may
+ * also point into pinned host memory mapped into the device address space
+ * (unified addressing): the kernel then reads only the rows a call needs over
+ * the host link (NVLink-C2C on GB300).  The logits entry needs device rows.  spec_verify_run only validates on the host and enqueues
  * kernels on the caller's stream; it never synchronises.  Errors visible on
  * the host are returned before anything is enqueued.  Errors in the data are
  * reported through the optional device word `status` (bitwise OR of

@@ -154,8 +154,11 @@ def _ptr(t, dtype, name, device, numel=None, ndim=None, contiguous=True):
     return t.data_ptr()
 
 
-def _rows(t, name, device, V, nrows, dtypes):
-    """A [rows, >=V] tensor whose rows are unit-stride; returns (ptr, row_stride)."""
+def _rows(t, name, device, V, nrows, dtypes, host_ok=False):
+    """A [rows, >=V] tensor whose rows are unit-stride; returns (ptr, row_stride).
+    With host_ok, a pinned host tensor is accepted too: its address is valid on
+    the device (unified addressing) and the kernel reads the rows it needs
+    directly from host memory."""
     if t is None:
         return None, 0
     if t.dim() != 2 or t.shape[1] != V or t.shape[0] != nrows:
@@ -166,20 +169,33 @@ def _rows(t, name, device, V, nrows, dtypes):
         return None, V  # nothing to read; torch gives empty dims arbitrary strides
     if (V > 1 and t.stride(1) != 1) or (nrows > 1 and t.stride(0) < V):
         raise ValueError(f"{name} rows must be unit-stride and non-overlapping")
-    if t.device != device:
-        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.device != device and not (host_ok and t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError(f"{name} is on {t.device}, expected {device}" +
+                         (" or pinned host memory" if host_ok else ""))
     return t.data_ptr(), (t.stride(0) if nrows > 1 else V)
 
 
 def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft=None, cu_num_draft_tokens=None,
                temperature=None, top_k=None, top_p=None, uniforms=None, exponentials=None, seed: int = 0,
                offset: int = 0, rng_request_base: int = 0, num_computed_tokens=None, slot_mapping=None,
-               dbg_py=None, dbg_qy=None, status=None, device=None) -> SpecVerifyArgs:
-    """Validate tensors and fill a SpecVerifyArgs (no device work)."""
+               dbg_py=None, dbg_qy=None, status=None, device=None,
+               host_rows: bool = False) -> SpecVerifyArgs:
+    """Validate tensors and fill a SpecVerifyArgs (no device work).
+
+    ``host_rows=True`` (probability entry only) lets ``target``/``draft``/
+    ``exponentials`` live in pinned host memory: the kernel then pulls only
+    the rows a call needs over the host link instead of the caller copying
+    every row first.  ``device`` must then be given (the GPU running the call)."""
     import torch
     if entry not in ("probs", "logits"):
         raise ValueError("entry must be 'probs' or 'logits'")
-    device = target.device if device is None else torch.device(device)
+    if host_rows and entry != "probs":
+        raise ValueError("host_rows is supported by the probability entry only")
+    if device is None:
+        if host_rows:
+            raise ValueError("host_rows needs an explicit device")
+        device = target.device
+    device = torch.device(device)
     N = out_tokens.shape[0]
     G = out_tokens.shape[1] - 1
     V = target.shape[-1]
@@ -198,15 +214,15 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
     a.num_draft_tokens_total = T
     a.draft_ids = _ptr(draft_ids, torch.int32, "draft_ids", device)
     a.cu_num_draft_tokens = _ptr(cu_num_draft_tokens, torch.int32, "cu_num_draft_tokens", device, numel=N)
-    a.target, a.target_row_stride = _rows(target, "target", device, V, T + N, dts)
-    a.draft, a.draft_row_stride = _rows(draft, "draft", device, V, T, dts)
+    a.target, a.target_row_stride = _rows(target, "target", device, V, T + N, dts, host_rows)
+    a.draft, a.draft_row_stride = _rows(draft, "draft", device, V, T, dts, host_rows)
     a.temperature = _ptr(temperature, torch.float32, "temperature", device, numel=N)
     a.top_k = _ptr(top_k, torch.int32, "top_k", device, numel=N)
     a.top_p = _ptr(top_p, torch.float32, "top_p", device, numel=N)
     a.uniforms = _ptr(uniforms, torch.float32, "uniforms", device, numel=T)
     if exponentials is not None:
         a.exponentials, a.exponentials_row_stride = _rows(exponentials, "exponentials", device, V, N,
-                                                          (torch.float32,))
+                                                          (torch.float32,), host_rows)
     a.seed, a.offset, a.rng_request_base = int(seed), int(offset), int(rng_request_base)
     a.out_tokens = _ptr(out_tokens, torch.int32, "out_tokens", device, ndim=2)
     a.num_accepted = _ptr(num_accepted, torch.int32, "num_accepted", device, numel=N)
@@ -224,7 +240,7 @@ def spec_verify_run(handle: int, stream=None, **kw) -> None:
     import torch
     a = build_args(**kw)
     if stream is None:
-        stream = torch.cuda.current_stream(kw["target"].device)
+        stream = torch.cuda.current_stream(kw.get("device") or kw["target"].device)
     s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     _check(load_library().spec_verify_run(ctypes.c_void_p(handle), ctypes.byref(a), ctypes.c_void_p(s)))
 

@@ -244,3 +244,33 @@ def test_production_chi_square_v8_first_token():
     first = np.bincount(g["out_tokens"][:, 0], minlength=V)
     expect = p[0].astype(np.float64) / p[0].astype(np.float64).sum()
     assert scipy.stats.chisquare(first, n * expect).pvalue > 0.01
+
+
+def test_pinned_host_rows_zero_copy():
+    """Probability rows left in pinned host memory give the same outputs as
+    rows copied to the device (the kernel reads them over the host link)."""
+    import torch
+    import speculative_decoding_token_rejection_gb300 as sv
+    w = workloads.make("fused_probs", N=48, V=16384)
+    dev = torch.device("cuda:0")
+    ref = H().run_gpu(w)
+    t = workloads.as_torch(w, dev)
+    hp = torch.from_numpy(w["target"]).pin_memory()
+    hq = torch.from_numpy(w["draft"]).pin_memory()
+    hE = torch.from_numpy(w["exponentials"]).pin_memory()
+    N, G, T = w["N"], w["gamma"], w["T"]
+    out = torch.full((N, G + 1), -7, dtype=torch.int32, device=dev)
+    nacc = torch.full((N,), -7, dtype=torch.int32, device=dev)
+    ncomp = t["num_computed_tokens"].clone()
+    slots = t["slot_mapping"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sv.spec_verify_run(H().verifier().handle, entry="probs", draft_ids=t["draft_ids"], target=hp, draft=hq,
+                       temperature=t["temperature"], uniforms=t["uniforms"], exponentials=hE, out_tokens=out,
+                       num_accepted=nacc, num_computed_tokens=ncomp, slot_mapping=slots, status=status,
+                       device=dev, host_rows=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), ref["out_tokens"])
+    np.testing.assert_array_equal(nacc.cpu().numpy(), ref["num_accepted"])
+    np.testing.assert_array_equal(ncomp.cpu().numpy(), ref["num_computed_tokens"])
+    np.testing.assert_array_equal(slots.cpu().numpy(), ref["slot_mapping"])
+    assert int(status.item()) == 0
