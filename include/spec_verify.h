@@ -140,6 +140,43 @@ typedef struct spec_verify_args {
   int32_t *status;              /* [1] or NULL: SV_DATA_* bits OR-ed in */
 } spec_verify_args;
 
+/* Draft-side sampler ("vLLM source walk-through (10)", section "propose()
+ * multi-step loop": each draft step samples its token from the draft model's
+ * distribution and keeps that distribution for the rejection sampler).  One
+ * token per logits row: the row goes through the verifier's own transform
+ * (temperature, top-k, softmax, top-p) and the token is drawn by the same
+ * exponential race; temperature 0 takes the argmax (lowest index).  The
+ * transformed fp32 row can be written out, ready to be the q input of the
+ * probability entry.  R = num_rows, V = vocab_size.  Production draws use the
+ * verifier's E counters under the key (seed_lo, seed_hi ^ 0x53414D50), so a
+ * sampler call and a verifier call with the same seed never share a stream. */
+typedef struct spec_verify_sample_args {
+  int32_t num_rows;   /* R >= 0 (0 is a no-op); at most the handle's max_num_reqs */
+  int32_t vocab_size; /* V, at most the handle's vocab_size */
+  int32_t dtype;      /* SV_F32 or SV_BF16 logits */
+  int32_t reserved0;  /* must be 0 */
+  const void *logits; /* [R rows, row_stride] */
+  int64_t row_stride; /* elements between rows (>= V) */
+  const float *temperature; /* [R] or NULL (= 1) */
+  const int32_t *top_k;     /* [R] or NULL */
+  const float *top_p;       /* [R] or NULL */
+  const float *exponentials; /* test mode: [R rows, exponentials_row_stride] E > 0; NULL = Philox */
+  int64_t exponentials_row_stride;
+  uint64_t seed;
+  uint64_t offset;
+  uint32_t rng_row_base; /* stream of row r: rng_row_base + r */
+  uint32_t reserved1;    /* must be 0 */
+  int32_t *tokens;       /* [R] out: sampled token, -1 for an invalid row */
+  float *probs;          /* [R rows, probs_row_stride] out or NULL: the transformed row (random rows only) */
+  int64_t probs_row_stride;
+  int32_t *status;       /* [1] or NULL: SV_DATA_* bits OR-ed in */
+} spec_verify_sample_args;
+
+sv_status spec_verify_sample(spec_verify_t handle, const spec_verify_sample_args *args, void *stream);
+
+/* Host-only validation of sampler arguments against `config`. */
+sv_status spec_verify_check_sample_args(const spec_verify_config *config, const spec_verify_sample_args *args);
+
 /* Create a handle.  Queries the device and sets kernel attributes on it
  * (temporarily making `device` current).  *out is set only on SV_OK. */
 sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *out);
@@ -165,6 +202,7 @@ const char *spec_verify_last_error(void);
 uint32_t spec_verify_abi_version(void);
 size_t spec_verify_sizeof_config(void);
 size_t spec_verify_sizeof_args(void);
+size_t spec_verify_sizeof_sample_args(void);
 
 #ifdef __cplusplus
 }

@@ -85,6 +85,9 @@ def _lib():
         lib.oracle_exponential.restype = ctypes.c_float
         lib.oracle_logits_to_probs.argtypes = [_P, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float,
                                                _P, _P]
+        lib.oracle_sample_rows.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int64,
+                                           _P, _P, _P, _P, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
+                                           ctypes.c_uint32, _P, _P, _P, _P]
         assert lib.oracle_sizeof_args() == ctypes.sizeof(_Args), "oracle_args layout mismatch"
         _LIB = lib
     return _LIB
@@ -183,3 +186,28 @@ def verify(w: dict, *, production: bool = False, seed: int = 0, offset: int = 0,
         raise RuntimeError(f"oracle_verify failed with {rc}")
     return dict(out_tokens=out, num_accepted=nacc, num_computed_tokens=ncomp, slot_mapping=slots,
                 dbg_py=dpy[:T], dbg_qy=dqy[:T], status=int(status[0]), diag=diag)
+
+
+def sample_rows(logits, *, temperature=None, top_k=None, top_p=None, exponentials=None, seed=0, offset=0,
+                rng_row_base=0, with_probs=True):
+    """Draft-side sampler: one token per logits row (fp32 array [R, V] or bf16
+    bits uint16 [R, V]).  Test mode when ``exponentials`` is given.  Returns
+    dict(tokens [R], probs [R, V] or None, status, diag [R, 2] = race flip
+    index, top-p edge flag)."""
+    lib = _lib()
+    bf16 = logits.dtype == np.uint16
+    l = _c(logits, np.uint16 if bf16 else np.float32)
+    R, V = l.shape
+    temp = _c(temperature, np.float32)
+    tk = _c(top_k, np.int32)
+    tp = _c(top_p, np.float32)
+    E = _c(exponentials, np.float32)
+    tokens = np.full(R, -7, np.int32)
+    probs = np.zeros((R, V), np.float32) if with_probs else None
+    status = np.zeros(1, np.int32)
+    diag = np.zeros((R, 2), np.float64)
+    rc = lib.oracle_sample_rows(R, V, 1 if bf16 else 0, _ptr(l), V, _ptr(temp), _ptr(tk), _ptr(tp), _ptr(E), V,
+                                seed, offset, rng_row_base, _ptr(tokens), _ptr(probs), _ptr(status), _ptr(diag))
+    if rc != 0:
+        raise RuntimeError(f"oracle_sample_rows failed with {rc}")
+    return dict(tokens=tokens, probs=probs, status=int(status[0]), diag=diag)

@@ -586,3 +586,100 @@ int oracle_verify_range(const oracle_args *a, int req_begin, int req_end) {
 int oracle_verify(const oracle_args *a) { return oracle_verify_range(a, 0, a->num_reqs); }
 
 int oracle_sizeof_args(void) { return (int)sizeof(oracle_args); }
+
+/* ------------------------------------------------------------------------ */
+/* draft-side sampler: one token per logits row from the transformed row     */
+/* ("vLLM source walk-through (10)", section "propose() multi-step loop":    */
+/* _sample_draft_tokens draws each draft token from the draft distribution;  */
+/* "Speculative Decoding: propose, verify, accept", section 02: the draft    */
+/* keeps every step's distribution q_i).  Same transform as the verifier's    */
+/* rows, same exponential race; temperature 0 takes the argmax.  Production  */
+/* draws use the verifier's E counter under the key (seed_lo, seed_hi ^      */
+/* 0x53414D50) so the sampler and the verifier never share a stream.          */
+/* ------------------------------------------------------------------------ */
+int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logits, int64_t row_stride,
+                       const float *temperature, const int32_t *top_k, const float *top_p,
+                       const float *exponentials, int64_t exp_stride, uint64_t seed, uint64_t offset,
+                       uint32_t rng_row_base, int32_t *tokens, float *probs_out, int32_t *status,
+                       double *diag /* [rows, 2]: race flip index, top-p edge */) {
+  float *l = (float *)malloc(sizeof(float) * (size_t)V);
+  float *p = (float *)malloc(sizeof(float) * (size_t)V);
+  float *E = (float *)malloc(sizeof(float) * (size_t)V);
+  if (!l || !p || !E) {
+    free(l); free(p); free(E);
+    return -2;
+  }
+  const uint64_t skey = seed ^ ((uint64_t)0x53414D50u << 32);
+  for (int r = 0; r < rows; ++r) {
+    load_row(logits, dtype, r, row_stride, V, l);
+    float temp = temperature ? temperature[r] : 1.0f;
+    if (diag) {
+      diag[2 * r] = INFINITY;
+      diag[2 * r + 1] = 0;
+    }
+    if (!(temp >= 0.0f) || isinf(temp)) {
+      *status |= ORC_BAD_PARAM;
+      tokens[r] = -1;
+      continue;
+    }
+    if (temp == 0.0f) { /* greedy drafting: argmax of the raw logits */
+      int g = argmax_row(l, V);
+      if (g < 0) *status |= ORC_BAD_VALUES;
+      tokens[r] = g;
+      continue;
+    }
+    int k = top_k ? top_k[r] : 0;
+    float tp = top_p ? top_p[r] : 1.0f;
+    if (!(tp > 0.0f)) {
+      *status |= ORC_BAD_PARAM;
+      tokens[r] = -1;
+      continue;
+    }
+    int edge = 0;
+    if (oracle_logits_to_probs(l, V, temp, k, tp, p, &edge)) {
+      *status |= ORC_BAD_VALUES;
+      tokens[r] = -1;
+      continue;
+    }
+    for (int x = 0; x < V; ++x) {
+      if (exponentials) {
+        E[x] = exponentials[(int64_t)r * exp_stride + x];
+      } else {
+        uint32_t w = philox_word(skey, offset, (uint32_t)x / 4u, 2u * (rng_row_base + (uint32_t)r), (int)(x % 4u));
+        E[x] = (float)(-log((double)((float)(2u * (w >> 9) + 1u) * 0x1p-24f)));
+      }
+    }
+    int best = -1;
+    float bk = 0.0f;
+    for (int x = 0; x < V; ++x) {
+      float key = 0.0f;
+      if (p[x] > 0.0f) {
+        if (E[x] > 0.0f) key = p[x] / E[x];
+        else *status |= ORC_BAD_EXPONENTIAL;
+      }
+      if (best < 0 || key > bk) {
+        bk = key;
+        best = x;
+      }
+    }
+    if (bk == 0.0f) *status |= ORC_EMPTY_DISTRIBUTION;
+    tokens[r] = best;
+    if (probs_out)
+      for (int x = 0; x < V; ++x) probs_out[(int64_t)r * V + x] = p[x];
+    if (diag) {
+      double k1 = (double)bk, e1 = (double)E[best], m1 = (double)p[best], fmin = INFINITY;
+      for (int x = 0; x < V; ++x) {
+        if (x == best || !(p[x] > 0.0f)) continue;
+        double kx = (E[x] > 0) ? (double)(p[x] / E[x]) : 0.0, d = k1 - kx;
+        double f = flip_index(d / (1.0 / e1 + 1.0 / (double)E[x]), d / (m1 / e1 + (double)p[x] / (double)E[x]));
+        if (f < fmin) fmin = f;
+      }
+      diag[2 * r] = fmin;
+      diag[2 * r + 1] = edge;
+    }
+  }
+  free(l);
+  free(p);
+  free(E);
+  return 0;
+}

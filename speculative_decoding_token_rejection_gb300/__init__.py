@@ -57,6 +57,19 @@ class SpecVerifyArgs(ctypes.Structure):
     ]
 
 
+class SpecVerifySampleArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_rows", ctypes.c_int32), ("vocab_size", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("logits", _P), ("row_stride", ctypes.c_int64),
+        ("temperature", _P), ("top_k", _P), ("top_p", _P),
+        ("exponentials", _P), ("exponentials_row_stride", ctypes.c_int64),
+        ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+        ("rng_row_base", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
+        ("tokens", _P), ("probs", _P), ("probs_row_stride", ctypes.c_int64), ("status", _P),
+    ]
+
+
 class NativeLibraryMissing(RuntimeError):
     pass
 
@@ -70,7 +83,8 @@ class SpecVerifyError(RuntimeError):
 _LIB = None
 EXPORTED = ("spec_verify_create", "spec_verify_run", "spec_verify_destroy", "spec_verify_check_args",
             "spec_verify_status_string", "spec_verify_last_error", "spec_verify_abi_version",
-            "spec_verify_sizeof_config", "spec_verify_sizeof_args")
+            "spec_verify_sizeof_config", "spec_verify_sizeof_args", "spec_verify_sample",
+            "spec_verify_check_sample_args", "spec_verify_sizeof_sample_args")
 
 
 def load_library(path: Optional[str] = None):
@@ -97,8 +111,15 @@ def load_library(path: Optional[str] = None):
     lib.spec_verify_abi_version.restype = ctypes.c_uint32
     lib.spec_verify_sizeof_config.restype = ctypes.c_size_t
     lib.spec_verify_sizeof_args.restype = ctypes.c_size_t
+    lib.spec_verify_sample.argtypes = [ctypes.c_void_p, ctypes.POINTER(SpecVerifySampleArgs), ctypes.c_void_p]
+    lib.spec_verify_sample.restype = ctypes.c_int
+    lib.spec_verify_check_sample_args.argtypes = [ctypes.POINTER(SpecVerifyConfig),
+                                                  ctypes.POINTER(SpecVerifySampleArgs)]
+    lib.spec_verify_check_sample_args.restype = ctypes.c_int
+    lib.spec_verify_sizeof_sample_args.restype = ctypes.c_size_t
     if lib.spec_verify_sizeof_config() != ctypes.sizeof(SpecVerifyConfig) or \
-            lib.spec_verify_sizeof_args() != ctypes.sizeof(SpecVerifyArgs):
+            lib.spec_verify_sizeof_args() != ctypes.sizeof(SpecVerifyArgs) or \
+            lib.spec_verify_sizeof_sample_args() != ctypes.sizeof(SpecVerifySampleArgs):
         raise RuntimeError("spec_verify struct layout differs from the binding")
     if path is None:
         _LIB = lib
@@ -243,6 +264,51 @@ def spec_verify_run(handle: int, stream=None, **kw) -> None:
         stream = torch.cuda.current_stream(kw.get("device") or kw["target"].device)
     s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     _check(load_library().spec_verify_run(ctypes.c_void_p(handle), ctypes.byref(a), ctypes.c_void_p(s)))
+
+
+def build_sample_args(*, logits, tokens, probs=None, temperature=None, top_k=None, top_p=None, exponentials=None,
+                      seed: int = 0, offset: int = 0, rng_row_base: int = 0, status=None) -> SpecVerifySampleArgs:
+    """Validate tensors and fill a SpecVerifySampleArgs (no device work)."""
+    import torch
+    device = logits.device
+    R, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = SV_BF16
+    elif logits.dtype == torch.float32:
+        dt = SV_F32
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    a = SpecVerifySampleArgs()
+    a.num_rows, a.vocab_size, a.dtype = R, V, dt
+    a.logits, a.row_stride = _rows(logits, "logits", device, V, R, (logits.dtype,))
+    a.temperature = _ptr(temperature, torch.float32, "temperature", device, numel=R)
+    a.top_k = _ptr(top_k, torch.int32, "top_k", device, numel=R)
+    a.top_p = _ptr(top_p, torch.float32, "top_p", device, numel=R)
+    if exponentials is not None:
+        a.exponentials, a.exponentials_row_stride = _rows(exponentials, "exponentials", device, V, R,
+                                                          (torch.float32,))
+    a.seed, a.offset, a.rng_row_base = int(seed), int(offset), int(rng_row_base)
+    a.tokens = _ptr(tokens, torch.int32, "tokens", device, numel=R)
+    if probs is not None:
+        a.probs, a.probs_row_stride = _rows(probs, "probs", device, V, R, (torch.float32,))
+    a.status = _ptr(status, torch.int32, "status", device, numel=1)
+    return a
+
+
+def spec_verify_sample(handle: int, stream=None, **kw) -> None:
+    """Enqueue the draft-side sampler on ``stream`` (default: torch's current
+    stream).  Keyword arguments are those of ``build_sample_args``."""
+    import torch
+    a = build_sample_args(**kw)
+    if stream is None:
+        stream = torch.cuda.current_stream(kw["logits"].device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(load_library().spec_verify_sample(ctypes.c_void_p(handle), ctypes.byref(a), ctypes.c_void_p(s)))
+
+
+def spec_verify_check_sample_args(config: SpecVerifyConfig, args: SpecVerifySampleArgs) -> int:
+    """Host-only validation of sampler arguments; returns the sv_status code."""
+    return int(load_library().spec_verify_check_sample_args(ctypes.byref(config), ctypes.byref(args)))
 
 
 def spec_verify_check_args(config: SpecVerifyConfig, args: SpecVerifyArgs) -> int:

@@ -81,6 +81,7 @@ const char *spec_verify_last_error(void) { return sv::g_last_error; }
 uint32_t spec_verify_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
 size_t spec_verify_sizeof_config(void) { return sizeof(spec_verify_config); }
 size_t spec_verify_sizeof_args(void) { return sizeof(spec_verify_args); }
+size_t spec_verify_sizeof_sample_args(void) { return sizeof(spec_verify_sample_args); }
 
 static sv_status check_config(const spec_verify_config *c) {
   if (!c) return fail(SV_ERR_INVALID_ARG, "config is NULL");
@@ -162,10 +163,12 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, config->device);
     max_dyn = optin - static_cast<int>(sv::logits_static_smem()) - 1024;
-    if (sv::enable_probs_kernels(16) != cudaSuccess || sv::enable_logits_kernels(16, max_dyn) != cudaSuccess) {
+    if (sv::enable_probs_kernels(16) != cudaSuccess || sv::enable_logits_kernels(16, max_dyn) != cudaSuccess ||
+        sv::enable_sample_kernels(16, max_dyn) != cudaSuccess) {
       cudaGetLastError();
       max_cluster = 8;
-      if ((e = sv::enable_probs_kernels(8)) != cudaSuccess || (e = sv::enable_logits_kernels(8, max_dyn)) != cudaSuccess)
+      if ((e = sv::enable_probs_kernels(8)) != cudaSuccess || (e = sv::enable_logits_kernels(8, max_dyn)) != cudaSuccess ||
+          (e = sv::enable_sample_kernels(8, max_dyn)) != cudaSuccess)
         result = fail(SV_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(e));
     }
     if (config->cluster_ctas > max_cluster)
@@ -242,6 +245,64 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
     e = sv::launch_logits(p, bf16, cluster, chunk, vec, s);
   }
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "verifier launch: %s", cudaGetErrorString(e));
+  return SV_OK;
+}
+
+sv_status spec_verify_check_sample_args(const spec_verify_config *c, const spec_verify_sample_args *a) {
+  sv_status st = check_config(c);
+  if (st != SV_OK) return st;
+  if (!a) return fail(SV_ERR_INVALID_ARG, "args is NULL");
+  if (a->num_rows < 0) return fail(SV_ERR_INVALID_ARG, "num_rows < 0");
+  if (a->vocab_size < 1) return fail(SV_ERR_INVALID_ARG, "vocab_size < 1");
+  if (a->num_rows > c->max_num_reqs) return fail(SV_ERR_CAPACITY, "num_rows %d > handle max %d", a->num_rows,
+                                                 c->max_num_reqs);
+  if (a->vocab_size > c->vocab_size)
+    return fail(SV_ERR_CAPACITY, "vocab_size %d > handle max %d", a->vocab_size, c->vocab_size);
+  if (a->dtype != SV_F32 && a->dtype != SV_BF16) return fail(SV_ERR_INVALID_ARG, "bad dtype");
+  if (a->reserved0 != 0 || a->reserved1 != 0) return fail(SV_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (a->num_rows == 0) return SV_OK;
+  if (!a->logits) return fail(SV_ERR_INVALID_ARG, "logits is NULL");
+  if (a->row_stride < a->vocab_size) return fail(SV_ERR_INVALID_ARG, "row_stride < vocab_size");
+  if (a->exponentials && a->exponentials_row_stride < a->vocab_size)
+    return fail(SV_ERR_INVALID_ARG, "exponentials_row_stride < vocab_size");
+  if (a->probs && a->probs_row_stride < a->vocab_size)
+    return fail(SV_ERR_INVALID_ARG, "probs_row_stride < vocab_size");
+  if (!a->tokens) return fail(SV_ERR_INVALID_ARG, "tokens is NULL");
+  return SV_OK;
+}
+
+sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, void *stream) {
+  if (!h) return fail(SV_ERR_INVALID_ARG, "handle is NULL");
+  sv_status st = spec_verify_check_sample_args(&h->cfg, a);
+  if (st != SV_OK) return st;
+  if (a->num_rows == 0) return SV_OK;
+  sv::SampleParams p{};
+  p.R = a->num_rows;
+  p.V = a->vocab_size;
+  p.logits = a->logits;
+  p.row_stride = a->row_stride;
+  p.temperature = a->temperature;
+  p.top_k = a->top_k;
+  p.top_p = a->top_p;
+  p.exponentials = a->exponentials;
+  p.exp_stride = a->exponentials_row_stride;
+  p.seed_lo = static_cast<uint32_t>(a->seed);
+  p.seed_hi = static_cast<uint32_t>(a->seed >> 32);
+  p.off_lo = static_cast<uint32_t>(a->offset);
+  p.off_hi = static_cast<uint32_t>(a->offset >> 32);
+  p.row_base = a->rng_row_base;
+  p.tokens = a->tokens;
+  p.probs = a->probs;
+  p.probs_stride = a->probs_row_stride;
+  p.status = a->status;
+  const bool bf16 = a->dtype == SV_BF16;
+  const int eb = bf16 ? 2 : 4;
+  int cluster = 0, chunk = 0;
+  if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk))
+    return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for a row to fit in the cluster's shared memory", p.V);
+  const bool vec = sv::aligned16(a->logits) && (a->row_stride % (16 / eb) == 0);
+  const cudaError_t e = sv::launch_sample(p, bf16, cluster, chunk, vec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "sampler launch: %s", cudaGetErrorString(e));
   return SV_OK;
 }
 

@@ -42,6 +42,24 @@ struct VerifyParams {
   int32_t *status;
 };
 
+// The draft-side sampler's parameters (device pointers, sizes).
+struct SampleParams {
+  int32_t R, V;
+  const void *logits;
+  int64_t row_stride;
+  const float *temperature;
+  const int32_t *top_k;
+  const float *top_p;
+  const float *exponentials;
+  int64_t exp_stride;
+  uint32_t seed_lo, seed_hi, off_lo, off_hi;
+  uint32_t row_base;
+  int32_t *tokens;
+  float *probs;
+  int64_t probs_stride;
+  int32_t *status;
+};
+
 // Picks the CTAs-per-request for a call (power of two, <= ctx->max_cluster).
 int choose_cluster(const spec_verify_ctx *ctx, int N, int V);
 
@@ -49,6 +67,8 @@ cudaError_t enable_probs_kernels(int max_cluster);
 cudaError_t launch_probs(const VerifyParams &p, int cluster, bool vec, cudaStream_t stream);
 
 size_t logits_static_smem();
+cudaError_t enable_sample_kernels(int max_cluster, int max_dyn);
+cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
 

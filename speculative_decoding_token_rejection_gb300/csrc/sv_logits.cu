@@ -1326,6 +1326,115 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
   cluster_sync();
 }
 
+// ---------------------------------------------------------------------------
+// draft-side sampler: one token per logits row from the transformed row
+// ("vLLM source walk-through (10)", section "propose() multi-step loop":
+// each draft step samples its token from the draft distribution and keeps the
+// distribution for the rejection sampler).  One cluster per row; the row is
+// transformed exactly like a verifier row, the token is drawn by the same
+// exponential race (argmax at temperature 0), and the fp32 probability row can
+// be written out for the probability entry.
+// ---------------------------------------------------------------------------
+template <typename TIn, bool kTest, bool kVec>
+__global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams P, int chunk) {
+  extern __shared__ __align__(16) unsigned char dyn_smem[];
+  __shared__ LogitsSmem sm;
+  TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem)};
+  const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
+  const int r = static_cast<int>(blockIdx.x / ncta);
+  const int tid = threadIdx.x;
+  const int V = P.V;
+  const TIn *row = static_cast<const TIn *>(P.logits) + static_cast<int64_t>(r) * P.row_stride;
+  const int x0 = min(V, static_cast<int>(rank) * chunk);
+  const int n = min(V, x0 + chunk) - x0;
+  uint32_t bits = 0;
+  int32_t token = -1;
+  int step = 0;
+  uint32_t phase = 0;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const float temp = P.temperature ? P.temperature[r] : 1.0f;
+  if (!(temp >= 0.0f) || isinf(temp)) {
+    bits |= SV_DATA_BAD_PARAM;
+  } else if (temp == 0.0f) {
+    unsigned long long best = 0;
+    uint32_t fl = 0;
+    argmax_logits<TIn, kVec>(row + x0, x0, n, best, fl);
+    const KeyFlags kr = cluster_reduce(KeyFlags{best, fl}, sm.red, step++, ncta);
+    if (kr.flags & SV_DATA_BAD_VALUES) bits |= SV_DATA_BAD_VALUES;
+    else token = static_cast<int32_t>(key_index(kr.key));
+  } else {
+    int topk = P.top_k ? P.top_k[r] : 0;
+    if (topk >= V || topk < 0) topk = 0;
+    const float topp = P.top_p ? P.top_p[r] : 1.0f;
+    if (!(topp > 0.0f)) {
+      bits |= SV_DATA_BAD_PARAM;
+    } else {
+      const TIn *grow[2] = {row + x0, nullptr};
+      const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase);
+      RowStats st[2];
+      if (!position_stats<TIn>(sm, srow, 1, n, __fdiv_rn(kLog2e, temp), topk, topp, lf, st, &bits, step, ncta)) {
+        bits |= SV_DATA_BAD_VALUES;
+      } else {
+        const RngKey rk{P.seed_lo, P.seed_hi ^ 0x53414D50u, P.off_lo, P.off_hi};  // the sampler's own streams
+        const float *Erow = kTest ? P.exponentials + static_cast<int64_t>(r) * P.exp_stride : nullptr;
+        float bk = 0.0f;
+        int bx = -1;
+        uint32_t fl = 0;
+        race_smem<TIn, kTest, false>(srow[0], srow[0], st[0], st[0], x0, n, Erow, rk,
+                                     P.row_base + static_cast<uint32_t>(r), bk, bx, fl);
+        const KeyFlags kr = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
+        bits |= kr.flags;
+        if (kr.key == 0ull) {
+          bits |= SV_DATA_EMPTY_DISTRIBUTION;
+          token = 0;
+        } else {
+          token = static_cast<int32_t>(key_index(kr.key));
+        }
+        if (P.probs) {  // this CTA's chunk of the transformed row
+          float *prow = P.probs + static_cast<int64_t>(r) * P.probs_stride + x0;
+          for (int x = tid; x < n; x += kThreads) prow[x] = prob_of<TIn>(bits_at(srow[0], x), st[0]);
+        }
+      }
+    }
+  }
+  if (rank == 0 && tid == 0) {
+    P.tokens[r] = token;
+    if (bits && P.status) atomicOr(P.status, static_cast<int>(bits));
+  }
+  cluster_sync();
+}
+
+template <typename TIn, bool kTest, bool kVec>
+cudaError_t launch_sample_one(const SampleParams &p, int cluster, int chunk, size_t dyn, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.R) * static_cast<unsigned>(cluster), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sample_kernel<TIn, kTest, kVec>, p, chunk);
+}
+
+template <typename TIn, bool kTest, bool kVec>
+cudaError_t enable_sample_one(int max_cluster, int max_dyn) {
+  cudaError_t e = cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+  if (e != cudaSuccess) return e;
+  if (max_cluster > 8)
+    return cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaSuccess;
+}
+
 template <typename TIn, bool kTest, bool kVec>
 cudaError_t launch_one(const VerifyParams &p, int cluster, int chunk, size_t dyn, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -1367,6 +1476,33 @@ cudaError_t enable_logits_kernels(int max_cluster, int max_dyn) {
   if ((e = enable_one<float, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
   if ((e = enable_one<float, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
   return enable_one<float, false, false>(max_cluster, max_dyn);
+}
+
+cudaError_t enable_sample_kernels(int max_cluster, int max_dyn) {
+  cudaError_t e;
+  if ((e = enable_sample_one<uint16_t, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<uint16_t, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<uint16_t, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<uint16_t, false, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<float, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<float, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<float, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_sample_one<float, false, false>(max_cluster, max_dyn);
+}
+
+cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
+  const bool test = p.exponentials != nullptr;
+  const size_t dyn = static_cast<size_t>(chunk) * (bf16 ? 2 : 4);
+  if (bf16) {
+    if (test) return vec ? launch_sample_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
+                         : launch_sample_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);
+    return vec ? launch_sample_one<uint16_t, false, true>(p, cluster, chunk, dyn, stream)
+               : launch_sample_one<uint16_t, false, false>(p, cluster, chunk, dyn, stream);
+  }
+  if (test) return vec ? launch_sample_one<float, true, true>(p, cluster, chunk, dyn, stream)
+                       : launch_sample_one<float, true, false>(p, cluster, chunk, dyn, stream);
+  return vec ? launch_sample_one<float, false, true>(p, cluster, chunk, dyn, stream)
+             : launch_sample_one<float, false, false>(p, cluster, chunk, dyn, stream);
 }
 
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {

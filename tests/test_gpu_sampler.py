@@ -1,0 +1,119 @@
+"""Parity of the CUDA draft-side sampler with the oracle (GPU required).
+
+Every transformed probability row must agree with the oracle's within 1e-6
+absolute (a full-row check of the logits transform shared with the verifier's
+logits entry); sampled tokens must agree except where the oracle reports a
+race a perturbation inside 1e-6 absolute and 1e-5 relative could flip, or a
+top-p edge.  Greedy rows are exact.  Production draws pass a chi-square test.
+"""
+import numpy as np
+import pytest
+import scipy.stats
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from speculative_decoding_token_rejection_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=False):
+    import torch
+    import gpu_harness
+    import speculative_decoding_token_rejection_gb300 as sv
+    dev = torch.device("cuda:0")
+    if bf16:
+        logits = torch.from_numpy(rows_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    else:
+        logits = torch.from_numpy(np.ascontiguousarray(rows_np, np.float32)).to(dev)
+    R, V = rows_np.shape
+    tokens = torch.full((R,), -7, dtype=torch.int32, device=dev)
+    probs = torch.zeros((R, V), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    t = lambda a, dt: None if a is None else torch.as_tensor(np.asarray(a), dtype=dt).to(dev)
+    sv.spec_verify_sample(gpu_harness.verifier().handle, logits=logits, tokens=tokens, probs=probs,
+                          temperature=t(temp, torch.float32), top_k=t(k, torch.int32), top_p=t(p, torch.float32),
+                          exponentials=t(E, torch.float32), seed=seed, offset=offset, rng_row_base=base,
+                          status=status)
+    torch.cuda.synchronize()
+    return tokens.cpu().numpy(), probs.cpu().numpy(), int(status.item())
+
+
+def check(rows, temp, k, p, E=None, production=False, bf16=False, budget=0.02, seed=0, offset=0, base=0):
+    o = oracle.sample_rows(rows, temperature=temp, top_k=k, top_p=p, exponentials=E, seed=seed, offset=offset,
+                           rng_row_base=base)
+    tok, pr, st = run_sampler(rows, temp, k, p, E, bf16=bf16, seed=seed, offset=offset, base=base)
+    assert st == o["status"]
+    temp = np.asarray(temp)
+    rnd = temp > 0
+    np.testing.assert_array_equal(tok[~rnd], o["tokens"][~rnd])  # greedy: exact
+    assert np.max(np.abs(pr[rnd] - o["probs"][rnd])) <= 1e-6
+    ex = (o["diag"][:, 0] < 1) | (o["diag"][:, 1] > 0)
+    keep = ~ex
+    np.testing.assert_array_equal(tok[keep], o["tokens"][keep])
+    assert ex.mean() <= budget, ex.sum()
+    return tok
+
+
+def fused_rows(R=64, V=151936):
+    w = workloads.make("fused", N=max(1, R // 7), V=V, test_mode=False)
+    return w["draft"][:R]
+
+
+@pytest.mark.parametrize("V", [151936, 5000, 4097])
+def test_sampler_fused_rows_test_mode(V):
+    rows = fused_rows(64, V)
+    R = rows.shape[0]
+    rng = np.random.default_rng(1)
+    E = rng.standard_exponential((R, V), dtype=np.float32)
+    check(rows, np.full(R, 0.8, np.float32), np.full(R, 50), np.full(R, 0.9, np.float32), E, bf16=True)
+
+
+@pytest.mark.parametrize("k,p,temp", [(0, 1.0, 1.0), (0, 0.95, 0.7), (200, 1.0, 1.3), (1, 1.0, 1.0)])
+def test_sampler_parameter_grid_fp32(k, p, temp):
+    rng = np.random.default_rng(2)
+    R, V = 48, 6000
+    rows = (rng.standard_normal((R, V)) * 2.0).astype(np.float32)
+    E = rng.standard_exponential((R, V), dtype=np.float32)
+    check(rows, np.full(R, temp, np.float32), np.full(R, k), np.full(R, p, np.float32), E, budget=0.05)
+
+
+def test_sampler_greedy_rows_and_status():
+    rng = np.random.default_rng(3)
+    rows = (rng.standard_normal((6, 300)) * 2).astype(np.float32)
+    rows[4, 17] = np.nan
+    temp = np.array([0, 1, 0, 0.5, 1, -2], np.float32)
+    E = rng.standard_exponential((6, 300), dtype=np.float32)
+    tok = check(rows, temp, np.zeros(6), np.ones(6, np.float32), E, budget=1.0)
+    assert tok[4] == -1 and tok[5] == -1
+
+
+def test_sampler_production_matches_oracle_philox():
+    rows = fused_rows(48, 20000)
+    R = rows.shape[0]
+    check(rows, np.full(R, 0.8, np.float32), np.full(R, 50), np.full(R, 0.9, np.float32), None, bf16=True,
+          seed=5, offset=2, base=9)
+
+
+def test_sampler_production_chi_square():
+    rng = np.random.default_rng(4)
+    V, R = 7, 1_000_000
+    l = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    probs, _, _ = oracle.logits_to_probs(l, 0.7, 4, 0.9)
+    tok, _, st = run_sampler(np.tile(l, (R, 1)), np.full(R, 0.7, np.float32), np.full(R, 4),
+                             np.full(R, 0.9, np.float32), None, seed=21, offset=3)
+    assert st == 0
+    cnt = np.bincount(tok, minlength=V)
+    e = probs.astype(np.float64)
+    assert np.all(cnt[e == 0] == 0)
+    nz = e > 0
+    assert scipy.stats.chisquare(cnt[nz], R * e[nz] / e[nz].sum()).pvalue > 0.01

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_exports_every_declared_function(lib):
     names = declared_functions()
-    assert len(names) >= 9
+    assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
     assert set(sv.EXPORTED) == set(names)
@@ -162,3 +162,31 @@ def test_gpu_test_workloads_pass_host_marshalling(lib):
                 dbg_py=torch.empty(T), dbg_qy=torch.empty(T), status=torch.zeros(1, dtype=torch.int32))
             assert sv.spec_verify_check_args(cfg_, a) == sv.SV_OK, (w.get("name"), production,
                                                                    lib.spec_verify_last_error())
+
+
+def _sample_args(R=4, V=1000):
+    a = sv.SpecVerifySampleArgs()
+    a.num_rows, a.vocab_size, a.dtype = R, V, sv.SV_BF16
+    a.logits, a.row_stride = FAKE, V
+    a.tokens = FAKE
+    return a
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda a: None, sv.SV_OK),
+    (lambda a: setattr(a, "num_rows", 9), sv.SV_ERR_CAPACITY),
+    (lambda a: setattr(a, "num_rows", -1), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "vocab_size", 2001), sv.SV_ERR_CAPACITY),
+    (lambda a: setattr(a, "dtype", 5), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "logits", None), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "row_stride", 999), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "tokens", None), sv.SV_ERR_INVALID_ARG),
+    (lambda a: (setattr(a, "probs", FAKE), setattr(a, "probs_row_stride", 10)), sv.SV_ERR_INVALID_ARG),
+    (lambda a: (setattr(a, "exponentials", FAKE), setattr(a, "exponentials_row_stride", 1000)), sv.SV_OK),
+    (lambda a: setattr(a, "reserved1", 3), sv.SV_ERR_INVALID_ARG),
+    (lambda a: (setattr(a, "num_rows", 0), setattr(a, "logits", None)), sv.SV_OK),
+])
+def test_check_sample_args(lib, mutate, code):
+    a = _sample_args()
+    mutate(a)
+    assert sv.spec_verify_check_sample_args(cfg(), a) == code
