@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 1u
+#define SPEC_VERIFY_ABI_VERSION 2u
 #define SV_PLACEHOLDER_TOKEN_ID (-1)
 #define SV_PADDING_SLOT_ID (-1)
 #define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
@@ -138,6 +138,15 @@ typedef struct spec_verify_args {
   float *dbg_py;                /* [T] or NULL: p_j(y_j) at examined positions j <= min(A, gamma_i - 1) */
   float *dbg_qy;                /* [T] or NULL: q_j(y_j) at the same positions */
   int32_t *status;              /* [1] or NULL: SV_DATA_* bits OR-ed in */
+
+  /* Synthetic acceptance ("vLLM source walk-through (10)", section "About
+   * synthetic / block verification": preset per-position rates, non-increasing,
+   * accept with "uniform < rate" instead of the probability test).  [G] device
+   * array in [0, 1], or NULL for the ordinary test.  Only the decision changes:
+   * rows before the stopping position are never read, the replacement or bonus
+   * draw there is the ordinary one, and dbg_py/dbg_qy are not written.  Rates
+   * outside [0, 1] or increasing over a request's positions: SV_DATA_BAD_PARAM. */
+  const float *synthetic_acceptance_rates;
 } spec_verify_args;
 
 /* Draft-side sampler ("vLLM source walk-through (10)", section "propose()

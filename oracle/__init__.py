@@ -54,7 +54,7 @@ class _Args(ctypes.Structure):
         ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
         ("rng_request_base", ctypes.c_uint32), ("pad1", ctypes.c_uint32),
         ("out_tokens", _P), ("num_accepted", _P), ("num_computed_tokens", _P), ("slot_mapping", _P),
-        ("dbg_py", _P), ("dbg_qy", _P), ("status", _P), ("diag", _P),
+        ("dbg_py", _P), ("dbg_qy", _P), ("status", _P), ("diag", _P), ("synthetic_rates", _P),
     ]
 
 
@@ -129,7 +129,8 @@ def logits_to_probs(logits, temperature: float, top_k: int = 0, top_p: float = 1
 
 
 def verify(w: dict, *, production: bool = False, seed: int = 0, offset: int = 0, rng_request_base: int = 0,
-           with_diag: bool = True, req_range=None, num_computed_tokens=None, slot_mapping=None) -> dict:
+           with_diag: bool = True, req_range=None, num_computed_tokens=None, slot_mapping=None,
+           synthetic_rates=None) -> dict:
     """Run the oracle on a workload dict (see ``workloads.make``).
 
     Test mode uses ``w['uniforms']`` / ``w['exponentials']``; ``production=True``
@@ -178,6 +179,8 @@ def verify(w: dict, *, production: bool = False, seed: int = 0, offset: int = 0,
     a.out_tokens, a.num_accepted = _ptr(out), _ptr(nacc)
     a.num_computed_tokens, a.slot_mapping = _ptr(ncomp), _ptr(slots)
     a.dbg_py, a.dbg_qy, a.status, a.diag = _ptr(dpy), _ptr(dqy), _ptr(status), _ptr(diag)
+    rates = _c(synthetic_rates, np.float32)
+    a.synthetic_rates = _ptr(rates)
     if req_range is None:
         rc = lib.oracle_verify(ctypes.byref(a))
     else:

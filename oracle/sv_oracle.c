@@ -51,6 +51,13 @@
  *    greedy path, NaN/+inf/no finite logit on the random logits path, missing
  *    draft rows) emits nothing: its output row stays -1, num_accepted = 0 and
  *    its KV bookkeeping is untouched;
+ *  - synthetic acceptance (page 1, "About synthetic / block verification":
+ *    preset per-position rates, non-increasing, "uniform < rate" accepts
+ *    without the target probabilities): only the test changes -- accept iff
+ *    u_j < rate_j; rows before the stopping position are not read (their
+ *    probabilities are never formed) and the replacement or bonus draw there
+ *    is the ordinary one; rates outside [0, 1] or increasing over the
+ *    request's positions are a bad parameter;
  *  - rejected KV slots are the verify tokens j in (A, gamma_i] of the request
  *    (the KV of the rejected drafts), so their count gamma_i - A equals the
  *    num_computed_tokens decrement [P3 s3.1, s3.2].
@@ -123,6 +130,7 @@ typedef struct {
   float *dbg_qy;
   int32_t *status;
   double *diag;
+  const float *synthetic_rates; /* [max_spec_len] or NULL */
 } oracle_args;
 
 /* ------------------------------------------------------------------------ */
@@ -479,8 +487,31 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
   rc->E_row = a->exponentials ? a->exponentials + (int64_t)i * a->exponentials_row_stride : NULL;
   if (!rc->test_mode) memset(rc->E_have, 0, (size_t)V);
 
+  int j0 = 0; /* first position whose rows are read */
+  if (a->synthetic_rates) {
+    for (int j = 0; j < g; ++j) {
+      float rj = a->synthetic_rates[j];
+      if (!(rj >= 0.0f && rj <= 1.0f) || (j > 0 && rj > a->synthetic_rates[j - 1])) {
+        *a->status |= ORC_BAD_PARAM;
+        emit_invalid(a, i);
+        return;
+      }
+    }
+    for (; j0 < g; ++j0) {
+      int32_t y = a->draft_ids[s + j0];
+      if (y < 0 || y >= V) {
+        *a->status |= ORC_BAD_DRAFT_ID;
+        emit_invalid(a, i);
+        return;
+      }
+      float u = rc->test_mode ? a->uniforms[s + j0]
+                              : oracle_uniform(a->seed, a->offset, rc->rng_req, (uint32_t)j0);
+      if (!(u < a->synthetic_rates[j0])) break; /* first synthetic rejection */
+      toks[j0] = y;
+    }
+  }
   int edge = 0;
-  for (int j = 0; j < g; ++j) {
+  for (int j = j0; j < g; ++j) {
     if (!a->draft) {
       *a->status |= ORC_MISSING_DRAFT;
       emit_invalid(a, i);
@@ -502,16 +533,17 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
       return;
     }
     float py = p[y], qy = q[y];
-    if (a->dbg_py) a->dbg_py[s + j] = py;
-    if (a->dbg_qy) a->dbg_qy[s + j] = qy;
+    if (a->dbg_py && !a->synthetic_rates) a->dbg_py[s + j] = py;
+    if (a->dbg_qy && !a->synthetic_rates) a->dbg_qy[s + j] = qy;
     float u = rc->test_mode ? a->uniforms[s + j] : oracle_uniform(a->seed, a->offset, rc->rng_req, (uint32_t)j);
-    if (dg) { /* flip index of the test u*q < p (exact zeros on both sides cannot flip) */
+    if (dg && !a->synthetic_rates) { /* flip index of the test u*q < p (exact zeros on both sides cannot flip) */
       double uq = (double)u * (double)qy, gap = fabs(uq - (double)py), scale = uq + (double)py;
       double mg = scale > 0 ? flip_index(gap, gap / scale) : INFINITY;
       if (mg < dg[DIAG_ACCEPT_MARGIN]) dg[DIAG_ACCEPT_MARGIN] = mg;
     }
     float uq = u * qy; /* fp32 product, then a strict fp32 comparison */
-    if (uq < py) {     /* accept y_j */
+    /* synthetic mode reaches the rows only at its first rejection */
+    if (!a->synthetic_rates && uq < py) { /* accept y_j */
       toks[j] = y;
       continue;
     }

@@ -53,7 +53,7 @@ class SpecVerifyArgs(ctypes.Structure):
         ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
         ("rng_request_base", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
         ("out_tokens", _P), ("num_accepted", _P), ("num_computed_tokens", _P), ("slot_mapping", _P),
-        ("dbg_py", _P), ("dbg_qy", _P), ("status", _P),
+        ("dbg_py", _P), ("dbg_qy", _P), ("status", _P), ("synthetic_acceptance_rates", _P),
     ]
 
 
@@ -200,7 +200,7 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
                temperature=None, top_k=None, top_p=None, uniforms=None, exponentials=None, seed: int = 0,
                offset: int = 0, rng_request_base: int = 0, num_computed_tokens=None, slot_mapping=None,
                dbg_py=None, dbg_qy=None, status=None, device=None,
-               host_rows: bool = False) -> SpecVerifyArgs:
+               host_rows: bool = False, synthetic_acceptance_rates=None) -> SpecVerifyArgs:
     """Validate tensors and fill a SpecVerifyArgs (no device work).
 
     ``host_rows=True`` (probability entry only) lets ``target``/``draft``/
@@ -252,6 +252,8 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
     a.dbg_py = _ptr(dbg_py, torch.float32, "dbg_py", device, numel=T)
     a.dbg_qy = _ptr(dbg_qy, torch.float32, "dbg_qy", device, numel=T)
     a.status = _ptr(status, torch.int32, "status", device, numel=1)
+    a.synthetic_acceptance_rates = _ptr(synthetic_acceptance_rates, torch.float32, "synthetic_acceptance_rates",
+                                        device, numel=G)
     return a
 
 

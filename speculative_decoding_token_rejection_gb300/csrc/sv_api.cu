@@ -225,6 +225,7 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
   p.dbg_py = a->dbg_py;
   p.dbg_qy = a->dbg_qy;
   p.status = a->status;
+  p.rates = a->synthetic_acceptance_rates;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (a->entry == SV_ENTRY_PROBS) {

@@ -40,6 +40,7 @@ struct VerifyParams {
   float *dbg_py;
   float *dbg_qy;
   int32_t *status;
+  const float *rates;  // synthetic acceptance rates [G] or nullptr
 };
 
 // The draft-side sampler's parameters (device pointers, sizes).

@@ -1244,7 +1244,32 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
       const uint32_t rs = P.req_base + static_cast<uint32_t>(i);
       const float *Erow = kTest ? P.exponentials + static_cast<int64_t>(i) * P.exp_stride : nullptr;
       RowStats st[2];
-      for (int j = 0;; ++j) {
+      // synthetic acceptance: the stopping position follows from u_j < rate_j
+      // alone; the rows of the positions before it are never read
+      int j_start = 0;
+      if (P.rates) {
+        bool bad_rates = false;
+        for (int j = 0; j < g; ++j) {
+          const float rj = P.rates[j];
+          if (!(rj >= 0.0f && rj <= 1.0f) || (j > 0 && rj > P.rates[j - 1])) bad_rates = true;
+        }
+        if (bad_rates) {
+          req_bits |= SV_DATA_BAD_PARAM;
+          valid = false;
+        }
+        for (; valid && j_start < g; ++j_start) {
+          const int y = P.ids[s + j_start];
+          if (y < 0 || y >= V) {
+            req_bits |= SV_DATA_BAD_DRAFT_ID;
+            valid = false;
+            break;
+          }
+          const float u = kTest ? P.uniforms[s + j_start] : draw_uniform(rk, rs, static_cast<uint32_t>(j_start));
+          if (!(u < P.rates[j_start])) break;
+          if (tid == 0) sm.tok[j_start] = y;
+        }
+      }
+      for (int j = j_start; valid; ++j) {
         const int nr = (j < g) ? 2 : 1;
         if (nr == 2 && drf == nullptr) {
           req_bits |= SV_DATA_MISSING_DRAFT;
@@ -1283,11 +1308,11 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
           }
           const float py = prob_of<TIn>(bty, st[0]);
           const float qy = prob_of<TIn>(bdy, st[1]);
-          if (rank == 0 && tid == 0) {
+          if (rank == 0 && tid == 0 && !P.rates) {
             if (P.dbg_py) P.dbg_py[s + j] = py;
             if (P.dbg_qy) P.dbg_qy[s + j] = qy;
           }
-          if (__fmul_rn(u, qy) < py) {
+          if (!P.rates && __fmul_rn(u, qy) < py) {  // (synthetic mode reaches here only at its rejection)
             if (tid == 0) sm.tok[j] = y;
             continue;  // accepted: next position
           }

@@ -37,8 +37,9 @@ constexpr int kUnroll = 4;  // float4 loads in flight per row per thread
 
 struct ProbsSmem {
   ReduceSmem red;
-  int stop;      // first position whose test stops the scan (gamma_i if none)
-  int stop_bad;  // that position has an invalid draft id
+  int stop;       // first position whose test stops the scan (gamma_i if none)
+  int stop_bad;   // that position has an invalid draft id
+  int bad_rates;  // synthetic rates outside [0, 1] or increasing
   int32_t tok[SV_MAX_SPEC_LEN + 1];
 };
 
@@ -265,19 +266,26 @@ __global__ void __launch_bounds__(kThreads) probs_kernel(const VerifyParams P) {
       if (tid == 0) {
         sm.stop = g;
         sm.stop_bad = 0;
+        sm.bad_rates = 0;
       }
       __syncthreads();
-      // a2: gather-and-accept scan, all positions at once
+      // a2: gather-and-accept scan, all positions at once (synthetic mode:
+      // the preset rate replaces the probability test and nothing is gathered)
+      const float *rates = P.rates;
       float py = 0.0f, qy = 0.0f;
       bool bad = false;
       if (tid < g) {
         const int y = P.ids[s + tid];
         bad = (y < 0 || y >= V);
         bool stop = bad;
-        if (!bad) {
+        const float u = kTest ? P.uniforms[s + tid] : draw_uniform(rk, rs, static_cast<uint32_t>(tid));
+        if (rates) {
+          const float rj = rates[tid];
+          if (!(rj >= 0.0f && rj <= 1.0f) || (tid > 0 && rj > rates[tid - 1])) sm.bad_rates = 1;
+          if (!bad) stop = !(u < rj);
+        } else if (!bad) {
           py = p[(tb + tid) * ts + y];
           qy = q[(s + tid) * ds + y];
-          const float u = kTest ? P.uniforms[s + tid] : draw_uniform(rk, rs, static_cast<uint32_t>(tid));
           stop = !(__fmul_rn(u, qy) < py);
         }
         if (stop) atomicMin(&sm.stop, tid);
@@ -286,12 +294,15 @@ __global__ void __launch_bounds__(kThreads) probs_kernel(const VerifyParams P) {
       const int a = sm.stop;
       if (tid == a && bad) sm.stop_bad = 1;
       __syncthreads();
-      if (sm.stop_bad) {
+      if (sm.bad_rates) {
+        req_bits |= SV_DATA_BAD_PARAM;
+        valid = false;
+      } else if (sm.stop_bad) {
         req_bits |= SV_DATA_BAD_DRAFT_ID;
         valid = false;
       } else {
         A = a;
-        if (rank == 0 && tid < g && tid <= A) {
+        if (rank == 0 && tid < g && tid <= A && !rates) {
           if (P.dbg_py) P.dbg_py[s + tid] = py;
           if (P.dbg_qy) P.dbg_qy[s + tid] = qy;
         }

@@ -249,3 +249,13 @@ def test_production_logits_chi_square():
     assert np.all(first[expect == 0] == 0)
     nz = expect > 0
     assert scipy.stats.chisquare(first[nz], n * expect[nz] / expect[nz].sum()).pvalue > 0.01
+
+
+@pytest.mark.parametrize("rates", [[0.9, 0.8, 0.5, 0.5, 0.3, 0.3, 0.1], [1.0] * 7, [0.3, 0.4, 0, 0, 0, 0, 0]])
+def test_synthetic_acceptance_logits(rates):
+    w = workloads.make("fused", N=24, V=8192, seed=5)
+    o = oracle.verify(w, synthetic_rates=np.array(rates, np.float32))
+    g = H().run_gpu(w, synthetic_rates=rates)
+    compare_logits(g, o, w)
+    if rates[1] > rates[0]:
+        assert o["status"] == oracle.BAD_PARAM

@@ -274,3 +274,15 @@ def test_pinned_host_rows_zero_copy():
     np.testing.assert_array_equal(ncomp.cpu().numpy(), ref["num_computed_tokens"])
     np.testing.assert_array_equal(slots.cpu().numpy(), ref["slot_mapping"])
     assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("rates", [[0.9, 0.7, 0.7, 0.2], [1.0, 1.0, 1.0, 1.0], [0.0, 0.0, 0.0, 0.0],
+                                   [0.5, 0.6, 0.1, 0.0]])
+@pytest.mark.parametrize("production", [False, True])
+def test_synthetic_acceptance_probs(rates, production):
+    """Synthetic mode (preset non-increasing rates): bit-exact with the oracle,
+    including the bad-rates status for the increasing set."""
+    w = workloads.make("random", N=40, V=6000, seed=17, test_mode=not production)
+    o = oracle.verify(w, production=production, seed=3, offset=1, synthetic_rates=np.array(rates, np.float32))
+    g = H().run_gpu(w, production=production, seed=3, offset=1, synthetic_rates=rates)
+    H().assert_same(g, o)

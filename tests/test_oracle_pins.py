@@ -506,3 +506,37 @@ def test_logits_entry_matches_probs_entry_on_softmax_rows(oracle_mod):
     close = (rl["diag"][:, 0] < 1e-6) | (rl["diag"][:, 1] < 1e-6)
     assert np.all(same | close)
     assert same.mean() > 0.9
+
+
+# ----------------------------------------------------------------------------
+# Page 1, "About synthetic / block verification": preset acceptance rates
+# ----------------------------------------------------------------------------
+def test_synthetic_acceptance_lengths_follow_the_rates(oracle_mod):
+    """With u on a uniform grid, the fraction of requests accepting at least k
+    drafts is exactly prod_{j<k} rate_j, whatever p and q are."""
+    import workloads
+    n, G, V = 1000, 3, 50
+    w = workloads.make("random", N=n, gamma=G, V=V, seed=3)
+    rates = np.array([0.9, 0.6, 0.5], np.float32)
+    # per-position u grids, shuffled independently so positions are uncorrelated
+    rng = np.random.default_rng(0)
+    u = np.stack([rng.permutation(U_GRID) for _ in range(G)], axis=1).reshape(-1)
+    w["uniforms"] = u
+    r = oracle_mod.verify(w, synthetic_rates=rates)
+    A = r["num_accepted"]
+    assert (A >= 1).mean() == pytest.approx(0.9, abs=0)
+    # later positions: conditional rates hold on the exact grid counts
+    assert ((A >= 2).sum()) == int(((u.reshape(n, G)[:, 0] < 0.9) & (u.reshape(n, G)[:, 1] < 0.6)).sum())
+    acc = r["out_tokens"]
+    for i in range(n):  # accepted tokens are the drafts; the next one is a residual draw (not the draft)
+        assert acc[i, :A[i]].tolist() == w["draft_ids"][i * G:i * G + A[i]].tolist()
+    assert np.all(np.isnan(r["dbg_py"]))  # the synthetic test uses no p(y), q(y): none are reported
+
+
+def test_synthetic_rates_must_be_non_increasing(oracle_mod):
+    import workloads
+    w = workloads.make("tiny")
+    r = oracle_mod.verify(w, synthetic_rates=np.array([0.5, 0.7, 0.2, 0.1], np.float32))
+    assert r["status"] == oracle_mod.BAD_PARAM and np.all(r["out_tokens"] == -1)
+    r = oracle_mod.verify(w, synthetic_rates=np.array([1.0, 1.0, 1.0, 1.0], np.float32))
+    assert np.all(r["num_accepted"] == 4)  # u < 1 always: every draft kept, bonus drawn

@@ -169,7 +169,7 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
     assert not _run_pins_against_current(oracle_mod)  # the unmodified oracle passes them all
     src = (oracle_mod._SRC).read_text()
     mutants = {
-        "accept <= ": ("if (uq < py) {", "if (uq <= py) {"),
+        "accept <= ": ("if (!a->synthetic_rates && uq < py) {", "if (!a->synthetic_rates && uq <= py) {"),
         "residual q-p": ("float d = p[x] - q[x];", "float d = q[x] - p[x];"),
         "target row s_i": ("const int64_t tb = s + i;", "const int64_t tb = s;"),
         "race highest index": ("if (best < 0 || key > bk) {", "if (best < 0 || key >= bk) {"),
