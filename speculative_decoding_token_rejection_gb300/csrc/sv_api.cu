@@ -49,11 +49,14 @@ bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_byt
   // and draft chunk per CTA).  Prefer the CTA count of the probability entry,
   // grow it until the two row chunks fit in ~100 KB so two CTAs share an SM.
   auto chunk_for = [&](int c) { return ((V + c - 1) / c + 7) & ~7; };
-  auto bytes_for = [&](int c) { return 2LL * chunk_for(c) * elem_bytes; };
+  auto bytes_for = [&](int c) {
+    return 2LL * chunk_for(c) * elem_bytes + static_cast<long long>(logits_inbox_bytes(c));
+  };
   int c = ctx->cfg.cluster_ctas > 0 ? ctx->cfg.cluster_ctas : choose_cluster(ctx, N, V);
   if (ctx->cfg.cluster_ctas == 0)
     while (c < ctx->max_cluster && bytes_for(c) > 100 * 1024) c *= 2;
-  if (bytes_for(c) > ctx->max_dyn_smem) return false;
+  // (window bins are 16-bit counts of one CTA's chunk)
+  if (bytes_for(c) > ctx->max_dyn_smem || chunk_for(c) > 65535) return false;
   *cluster = c;
   *chunk = chunk_for(c);
   return true;

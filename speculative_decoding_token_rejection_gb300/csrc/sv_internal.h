@@ -68,6 +68,9 @@ cudaError_t enable_probs_kernels(int max_cluster);
 cudaError_t launch_probs(const VerifyParams &p, int cluster, bool vec, cudaStream_t stream);
 
 size_t logits_static_smem();
+// Dynamic shared memory a logits-entry CTA needs besides its row chunks: the
+// double-buffered inboxes of the one-barrier row-statistics reduction.
+size_t logits_inbox_bytes(int cluster);
 cudaError_t enable_sample_kernels(int max_cluster, int max_dyn);
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);

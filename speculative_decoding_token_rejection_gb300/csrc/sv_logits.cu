@@ -135,7 +135,7 @@ constexpr uint32_t kFlagTimeout = 4u;  // the row's bulk copy did not complete i
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kNearBins = 128;         // near-max bins: distances 0..127 from the row's largest key
 constexpr int kMaxCluster = 16;
-constexpr int kQueue = 192;  // per-warp candidate queue
+constexpr int kWalkGroups = 8;  // 16-byte groups a lane tests per window-scan step
 
 struct StatPart {  // one CTA's partials of one reduction round, for up to 2 rows
   uint32_t maxkey[2];
@@ -178,16 +178,25 @@ struct NearSum {  // cluster-wide near-max histograms on the global maximum, per
   unsigned long long tot[2];              // fixed-point mass of every element
   uint32_t gmax[2];
   uint32_t flags[2];
-  uint32_t pkey[2][kMaxCluster];    // each peer's largest finite key
-  uint32_t pflags[2][kMaxCluster];  // each peer's value flags
-  int delta[2][kMaxCluster];        // global minus peer 16-bit max key (-1: peer has no finite value)
-  float scale[2][kMaxCluster];      // exp2((peer max - global max) * c2)
 };
+
+// One CTA's contribution to a fast-path reduction round, as stored into every
+// peer's shared memory (slot [parity][sender rank]).  Window bins count the
+// keys at distance d below the sender's largest key; a CTA's chunk never holds
+// more than 65535 elements, so 16-bit counts suffice.
+struct Inbox {
+  uint32_t maxkey[2];
+  uint32_t flags[2];
+  float z[2];
+  uint32_t pad[2];
+  unsigned long long tot[2];
+  uint16_t cnt[2][kNearBins];
+};
+constexpr int kInboxWords = sizeof(Inbox) / 16;  // 16-byte stores per sender per peer
+static_assert(sizeof(Inbox) % 16 == 0, "inbox slots are written with 16-byte stores");
 
 struct LogitsSmem {
   ReduceSmem red;
-  uint32_t queue[kWarps][kQueue];  // per-warp queue of window candidates
-  uint32_t qcount[kWarps];
   StatPart part[2];
   StatSum sum;
   NearSum near;
@@ -198,12 +207,10 @@ struct LogitsSmem {
   int32_t tok[SV_MAX_SPEC_LEN + 1];
 };
 
-enum : uint32_t { kRMax = 1u, kRCnt = 2u, kRMass = 4u, kRZ = 8u, kRTot = 16u, kRMassF = 32u };
+enum : uint32_t { kRMax = 1u, kRCnt = 2u, kRMass = 4u, kRZ = 8u, kRTot = 16u };
 
 __device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
   const int tid = threadIdx.x;
-  if (what & kRMassF)
-    for (int t = tid; t < nr * kNearBins; t += kThreads) p.massf[t / kNearBins][t % kNearBins] = 0.0f;
   if (what & kRMass)
     for (int t = tid; t < nr * 256; t += kThreads) p.massf[t >> 8][t & 255] = 0.0f;
   if (what & kRCnt)
@@ -637,8 +644,9 @@ __device__ __forceinline__ unsigned long long near_sum(const unsigned long long 
 }
 
 template <typename TIn>
-__device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n, float c2, int topk, float topp,
-                               uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step, uint32_t ncta) {
+__device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], int nr, int n, float c2, int topk,
+                               float topp, uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step,
+                               uint32_t ncta, uint32_t rank) {
   using E = Elem<TIn>;
   constexpr int kB = E::kBits;
   const int tid = threadIdx.x;
@@ -649,7 +657,7 @@ __device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n
   StatPart &lp = sm.part[par];
 
   // local pass A: largest key and value checks of this CTA's chunk
-  zero_part(lp, near ? (kRCnt | kRMassF) : 0u, nr);
+  zero_part(lp, (kB == 16 && near) ? kRCnt : 0u, nr);
   __syncthreads();
   for (int r = 0; r < nr; ++r) {
     uint32_t mk = 0, fl = load_flags;
@@ -701,205 +709,165 @@ __device__ bool position_stats(LogitsSmem &sm, TIn *const srow[2], int nr, int n
   }
   __syncthreads();
 
-  // local pass B: near-max counts and masses, or the dense local normaliser
-  {
-    float zt[2] = {0.0f, 0.0f};
+  // local pass B.  bf16 top-k/top-p rows: count the keys within the window
+  // below this CTA's largest key (a bin is one bf16 value, so its mass is its
+  // count times one weight, formed after the reduction); top-p without top-k
+  // also sums every kept weight.  Dense rows: the local normaliser.  fp32
+  // top-k/top-p rows are left to the multi-pass path.
+  if (kB == 16 && near) {
     unsigned long long tt[2] = {0ull, 0ull};
+    const int lane = tid & 31, warp = tid >> 5;
     for (int r = 0; r < nr; ++r) {
       if (!(lp.flags[r] & kFlagFinite)) continue;  // empty or no finite value: contributes nothing
-      const uint32_t lk = lp.maxkey[r];
-      const uint32_t lk16 = key16_of<TIn>(lk);
-      const float lv = E::val_of_key(lk);
-      float sum = 0.0f, comp = 0.0f;
-      unsigned long long tot = 0;
-      if (kB == 16 && use_k) {
-        // top-k rows: only keys within the window matter; test pairs of keys
-        // against the window's lower edge and visit single elements rarely
-        const uint32_t lo = lk16 - (kNearBins - 1);  // window's smallest key; below key(-inf): all finite pass
-        const uint32_t lob = (lk16 >= static_cast<uint32_t>(kNearBins - 1) && lo > 0x007Fu) ? bf16_bits_of_key(lo)
-                                                                                              : 0xFF80u;
-        const uint32_t lo2 = lob | (lob << 16);
-        auto take = [&](uint32_t b) {
-          if (!E::finite(b)) return;
-          const uint32_t d = lk16 - E::key(b);
-          if (d >= static_cast<uint32_t>(kNearBins)) return;
-          atomicAdd(&lp.cnt[r][d], 1u);
-          atomicAdd(&lp.massf[r][d], exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2)));
-        };
-        // Candidates are rare (a few percent): each thread appends its own to
-        // its warp's queue, and the warp treats a full queue (or the rest at
-        // the end) with all 32 lanes at once.
-        const int nw = n >> 1;
-        const int ng = nw >> 2;  // 16-byte groups
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
-        const int lane = tid & 31, warp = tid >> 5;
-        uint32_t *q = sm.queue[warp];
-        if (lane == 0) sm.qcount[warp] = 0u;
-        __syncwarp();
-        auto flush = [&]() {
-          __syncwarp();
-          const uint32_t total = sm.qcount[warp];
-          for (uint32_t i = lane; i < total; i += 32) take(q[i]);
-          __syncwarp();
-          if (lane == 0) sm.qcount[warp] = 0u;
-          __syncwarp();
-        };
-        for (int vb = warp * 32; vb < ng; vb += 2 * kThreads) {  // warp-uniform trip count, 2 groups
-          uint32_t w[8], m[8];
+      const uint32_t lk16 = key16_of<TIn>(lp.maxkey[r]);
+      const uint32_t lo = lk16 - (kNearBins - 1);  // window's smallest key; below key(-inf): all finite pass
+      const uint32_t lob = (lk16 >= static_cast<uint32_t>(kNearBins - 1) && lo > 0x007Fu) ? bf16_bits_of_key(lo)
+                                                                                            : 0xFF80u;
+      const uint32_t lo2 = lob | (lob << 16);
+      uint32_t *cnt = lp.cnt[r];
+      const TIn *row = srow[r];
+      const int nw = n >> 1;
+      const int ng = nw >> 2;  // 16-byte groups
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
+      // Candidates are a few percent of the keys.  A lane tests eight 16-byte
+      // groups at once (packed compares, every load in flight together) into
+      // one 64-bit candidate mask, then the warp walks the set bits in step:
+      // each trip counts at most one candidate per lane, so the trips are the
+      // largest per-lane count, not the number of element slots.
+      for (int vb = warp * 32; vb < ng; vb += kWalkGroups * kThreads) {
+        unsigned long long M = 0ull;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int v = vb + h * kThreads + lane;
-            uint4 dv = make_uint4(0u, 0u, 0u, 0u);
-            if (v < ng) dv = s4[v];
-            w[4 * h + 0] = dv.x; w[4 * h + 1] = dv.y; w[4 * h + 2] = dv.z; w[4 * h + 3] = dv.w;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) m[4 * h + t] = v < ng ? bf16x2_ge_mask(w[4 * h + t], lo2) : 0u;
+        for (int h = 0; h < kWalkGroups; ++h) {
+          const int v = vb + h * kThreads + lane;
+          if (v < ng) {
+            const uint4 dv = s4[v];
+            uint32_t g = (bf16x2_ge_mask(dv.x, lo2) & 0x00010001u) | ((bf16x2_ge_mask(dv.y, lo2) & 0x00010001u) << 1) |
+                         ((bf16x2_ge_mask(dv.z, lo2) & 0x00010001u) << 2) |
+                         ((bf16x2_ge_mask(dv.w, lo2) & 0x00010001u) << 3);
+            g = (g | (g >> 12)) & 0xFFu;  // bit t: low half of word t; bit 4 + t: its high half
+            M |= static_cast<unsigned long long>(g) << (8 * h);
           }
-          uint32_t pc = 0u;
-#pragma unroll
-          for (int t = 0; t < 8; ++t) pc += __popc(m[t]);
-          const uint32_t mine = pc >> 4;  // each true half contributes 16 set bits
-          const uint32_t here = __reduce_add_sync(0xFFFFFFFFu, mine);
-          if (here == 0u) continue;
-          if (here > static_cast<uint32_t>(kQueue)) {  // too many at once: every lane takes its own
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              if (m[t] & 0xFFFFu) take(w[t] & 0xFFFFu);
-              if (m[t] >> 16) take(w[t] >> 16);
-            }
-            continue;
-          }
-          if (sm.qcount[warp] + here > static_cast<uint32_t>(kQueue)) flush();
-          if (mine) {
-            uint32_t idx = atomicAdd(&sm.qcount[warp], mine);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              if (m[t] & 0xFFFFu) q[idx++] = w[t] & 0xFFFFu;
-              if (m[t] >> 16) q[idx++] = w[t] >> 16;
-            }
-          }
-          __syncwarp();
         }
-        flush();
-        for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) take(bits_at(srow[r], x));
-        zt[r] = 0.0f;
-        tt[r] = 0ull;
-        continue;
+        while (__any_sync(0xFFFFFFFFu, M != 0ull)) {
+          if (M != 0ull) {
+            const int pos = __ffsll(static_cast<long long>(M)) - 1;
+            M &= M - 1ull;
+            const int x = 8 * (vb + (pos >> 3) * kThreads + lane) + 2 * (pos & 3) + ((pos >> 2) & 1);
+            const uint32_t b = bits_at(row, x);
+            const uint32_t d = lk16 - E::key(b);
+            if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
+          }
+        }
       }
+      for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) {
+        const uint32_t b = bits_at(srow[r], x);
+        const uint32_t d = lk16 - E::key(b);
+        if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
+      }
+      if (use_p && !use_k) {  // top-p alone: the whole row is kept before the cut
+        const float lv = E::val_of_key(lp.maxkey[r]);
+        unsigned long long tot = 0;
+        for_each_elem(srow[r], n, [&](uint32_t b, int) {
+          if (E::finite(b)) tot += to_fixed(exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2)));
+        });
+        tt[r] = tot;
+      }
+    }
+    if (use_p && !use_k) block_sum_tot(sm, lp, tt, nr);
+  } else if (!near) {
+    float zt[2] = {0.0f, 0.0f};
+    for (int r = 0; r < nr; ++r) {
+      if (!(lp.flags[r] & kFlagFinite)) continue;
+      const float lv = E::val_of_key(lp.maxkey[r]);
+      float sum = 0.0f, comp = 0.0f;
       for_each_elem(srow[r], n, [&](uint32_t b, int) {
         if (!E::finite(b)) return;  // -inf adds nothing (NaN/+inf already flagged)
-        const uint32_t k = E::key(b);
-        const uint32_t d = lk16 - key16_of<TIn>(k);
-        const bool in_near = d < static_cast<uint32_t>(kNearBins);
-        if (!near || in_near || (use_p && !use_k)) {
-          const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2));
-          if (!near) {
-            const float y = e - comp;  // Kahan
-            const float t = sum + y;
-            comp = (t - sum) - y;
-            sum = t;
-          } else {
-            if (use_p && !use_k) tot += to_fixed(e);
-            if (in_near) {
-              if (use_k) atomicAdd(&lp.cnt[r][d], 1u);
-              atomicAdd(&lp.massf[r][d], e);
-            }
-          }
-        }
+        const float y = exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2)) - comp;  // Kahan
+        const float t = sum + y;
+        comp = (t - sum) - y;
+        sum = t;
       });
       zt[r] = sum;
-      tt[r] = tot;
     }
-    if (!near) block_sum_z(sm, lp, zt, nr);
-    else if (use_p && !use_k) block_sum_tot(sm, lp, tt, nr);
+    block_sum_z(sm, lp, zt, nr);
   }
 
-  // the one cluster reduction
+  // The one cluster reduction.  Every CTA stores its header and window bins
+  // into its slot of every peer's inbox, then one cluster barrier makes them
+  // visible; the sums below read local shared memory only.
   __syncthreads();
+  Inbox *const ibx = inbox + par * static_cast<int>(ncta);
+  {
+    const int nwords = (kB == 16 && near) ? kInboxWords : 3;  // header only unless bins are used
+    for (int t = tid; t < nwords * static_cast<int>(ncta); t += kThreads) {
+      const int c = t / nwords, wd = t % nwords;
+      uint4 v;
+      if (wd == 0) {
+        v = make_uint4(lp.maxkey[0], lp.maxkey[1], lp.flags[0], lp.flags[1]);
+      } else if (wd == 1) {
+        v = make_uint4(__float_as_uint(lp.z[0]), __float_as_uint(lp.z[1]), 0u, 0u);
+      } else if (wd == 2) {
+        v = make_uint4(static_cast<uint32_t>(lp.tot[0]), static_cast<uint32_t>(lp.tot[0] >> 32),
+                       static_cast<uint32_t>(lp.tot[1]), static_cast<uint32_t>(lp.tot[1] >> 32));
+      } else {  // eight 16-bit bins per word
+        const int r = (wd - 3) / (kNearBins / 8), d0 = ((wd - 3) % (kNearBins / 8)) * 8;
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
+        if (r < nr) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) h[k] = lp.cnt[r][d0 + 2 * k] | (lp.cnt[r][d0 + 2 * k + 1] << 16);
+        }
+        v = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+      st_dsmem_v4(map_to_rank(smem_addr(reinterpret_cast<uint4 *>(&ibx[rank]) + wd), static_cast<uint32_t>(c)), v);
+    }
+  }
   cluster_sync();
   ++step;
   NearSum &ns = sm.near;
-  if (tid < nr * kMaxCluster) {
-    const int r = tid / kMaxCluster, c = tid % kMaxCluster;
-    if (c < static_cast<int>(ncta)) {
-      ns.pkey[r][c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.maxkey[r]), c));
-      ns.pflags[r][c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.flags[r]), c));
-    }
-  }
-  __syncthreads();
-  if (tid < nr) {
-    const int r = tid;
+  if (tid < nr * kNearBins) {  // one thread per (row, bin) of the window
+    const int r = tid / kNearBins, d = tid % kNearBins;
     uint32_t gk = 0, fl = 0;
     for (int c = 0; c < static_cast<int>(ncta); ++c) {
-      const uint32_t pf = ns.pflags[r][c];
+      const uint32_t pf = ibx[c].flags[r];
       fl |= pf;
-      if (pf & kFlagFinite) gk = max(gk, ns.pkey[r][c]);
+      if (pf & kFlagFinite) gk = max(gk, ibx[c].maxkey[r]);
     }
-    ns.gmax[r] = gk;
-    ns.flags[r] = fl;
-  }
-  __syncthreads();
-  if (tid < nr * kMaxCluster) {  // one thread per (row, peer): shift and scale onto the global max
-    const int r = tid / kMaxCluster, c = tid % kMaxCluster;
-    const uint32_t pf = c < static_cast<int>(ncta) ? ns.pflags[r][c] : 0u;
-    if ((pf & kFlagFinite) && (ns.flags[r] & kFlagFinite)) {
-      const uint32_t pk = ns.pkey[r][c];
-      ns.delta[r][c] = static_cast<int>(key16_of<TIn>(ns.gmax[r]) - key16_of<TIn>(pk));
-      ns.scale[r][c] = exp2f(__fmul_rn(__fsub_rn(E::val_of_key(pk), E::val_of_key(ns.gmax[r])), c2));
-    } else {
-      ns.delta[r][c] = -1;
-      ns.scale[r][c] = 0.0f;
+    const uint32_t g16 = key16_of<TIn>(gk);
+    if (d == 0) {
+      ns.gmax[r] = gk;
+      ns.flags[r] = fl;
     }
-  }
-  __syncthreads();
-  if (near && tid < nr * kNearBins) {  // one thread per (row, bin) of the window
-    const int r = tid / kNearBins, d = tid % kNearBins;
-    uint32_t cv[kMaxCluster], mv[kMaxCluster];
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {  // every load is issued (from a valid address), then masked
-      const int dl = d - ns.delta[r][c];    // delta is -1 for absent peers
-      const bool ok = c < static_cast<int>(ncta) && ns.delta[r][c] >= 0 && dl >= 0;
-      const int cc = ok ? c : 0, dd = ok ? dl : 0;
-      cv[c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.cnt[r][dd]), cc));
-      mv[c] = ld_dsmem_u32(map_to_rank(smem_addr(&lp.massf[r][dd]), cc));
-      if (!ok) cv[c] = mv[c] = 0u;
+    if (kB == 16 && near) {
+      // peers' bins shifted onto the global maximum, summed as integers; the
+      // bin's mass is its count times the weight of its one bf16 value
+      uint32_t cs = 0;
+      if (fl & kFlagFinite) {
+        for (int c = 0; c < static_cast<int>(ncta); ++c) {
+          if (!(ibx[c].flags[r] & kFlagFinite)) continue;
+          const int dl = d - static_cast<int>(g16 - key16_of<TIn>(ibx[c].maxkey[r]));
+          if (dl >= 0) cs += ibx[c].cnt[r][dl];
+        }
+      }
+      ns.cnt[r][d] = cs;
+      ns.mass[r][d] = cs ? cs * to_fixed(exp2f(__fmul_rn(__fsub_rn(E::val_of_key(g16 - static_cast<uint32_t>(d)),
+                                                                      E::val_of_key(gk)), c2)))
+                         : 0ull;
     }
-    // peers' masses rescaled onto the global maximum and summed in rank
-    // order, then held in 2^-40 fixed point for the integer selection
-    unsigned long long cs = 0;
-    float ms = 0.0f;
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {
-      cs += use_k ? cv[c] : 0u;
-      ms += __uint_as_float(mv[c]) * ns.scale[r][c];
+    if (d == 0) {  // rescale the peers' sums onto the global maximum, in rank order
+      float z = 0.0f;
+      unsigned long long tot = 0;
+      if ((fl & kFlagFinite) && (!near || (use_p && !use_k))) {
+        const float gv = E::val_of_key(gk);
+        for (int c = 0; c < static_cast<int>(ncta); ++c) {
+          if (!(ibx[c].flags[r] & kFlagFinite)) continue;
+          const float scale = exp2f(__fmul_rn(__fsub_rn(E::val_of_key(ibx[c].maxkey[r]), gv), c2));
+          if (!near) z += ibx[c].z[r] * scale;
+          else if (ibx[c].tot[r]) tot += __float2ull_rn(__ull2float_rn(ibx[c].tot[r]) * scale);
+        }
+      }
+      ns.z[r] = z;
+      ns.tot[r] = tot;
     }
-    ns.cnt[r][d] = cs;
-    ns.mass[r][d] = to_fixed(ms);
-  }
-  if (tid < nr) {  // remote loads first, then the fixed-order sums
-    const int r = tid;
-    float z = 0.0f;
-    unsigned long long tot = 0;
-    if (!near) {
-      uint32_t zb[kMaxCluster];
-#pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c)
-        zb[c] = (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0) ? ld_dsmem_u32(map_to_rank(smem_addr(&lp.z[r]), c)) : 0u;
-#pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c)
-        if (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0) z += __uint_as_float(zb[c]) * ns.scale[r][c];
-    } else if (use_p && !use_k) {
-      unsigned long long tv[kMaxCluster];
-#pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c)
-        tv[c] = (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0) ? ld_dsmem_u64(map_to_rank(smem_addr(&lp.tot[r]), c)) : 0ull;
-#pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c)
-        if (c < static_cast<int>(ncta) && ns.delta[r][c] >= 0 && tv[c])
-          tot += __float2ull_rn(__ull2float_rn(tv[c]) * ns.scale[r][c]);
-    }
-    ns.z[r] = z;
-    ns.tot[r] = tot;
   }
   __syncthreads();
 
@@ -1158,6 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ LogitsSmem sm;
   TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem) + chunk};
+  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + 2 * static_cast<size_t>(chunk) * sizeof(TIn));
 
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int i = static_cast<int>(blockIdx.x / ncta);
@@ -1201,8 +1170,18 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
     fence_mbar_init();
   }
   __syncthreads();
+  // Peers' shared memory may be written only once every CTA of the cluster
+  // runs: arrive now, wait before the first store into a peer (the first row
+  // copy proceeds meanwhile).
+  cluster_arrive_relaxed();
+  bool joined = false;
+  auto join = [&]() {
+    if (!joined) cluster_wait_acquire();
+    joined = true;
+  };
 
   if (greedy) {
+    join();
     for (int j = 0;; ++j) {
       unsigned long long best = 0;
       uint32_t fl = 0;
@@ -1291,7 +1270,8 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
         }
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
         const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, nr, n, phase);
-        if (!position_stats<TIn>(sm, srow, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta)) {
+        join();
+        if (!position_stats<TIn>(sm, inbox, srow, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta, rank)) {
           req_bits |= SV_DATA_BAD_VALUES;
           valid = false;
           break;
@@ -1343,6 +1323,7 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
       }
     }
   }
+  join();
   __syncthreads();
   if (rank == 0) {
     auto tok = [&](int k) -> int32_t { return (k == A && !greedy) ? last_tok : sm.tok[k]; };
@@ -1365,6 +1346,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ LogitsSmem sm;
   TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem)};
+  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + static_cast<size_t>(chunk) * sizeof(TIn));
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int r = static_cast<int>(blockIdx.x / ncta);
   const int tid = threadIdx.x;
@@ -1381,6 +1363,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
     fence_mbar_init();
   }
   __syncthreads();
+  cluster_sync();  // every CTA of the cluster runs before any store into a peer
   const float temp = P.temperature ? P.temperature[r] : 1.0f;
   if (!(temp >= 0.0f) || isinf(temp)) {
     bits |= SV_DATA_BAD_PARAM;
@@ -1401,7 +1384,8 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
       const TIn *grow[2] = {row + x0, nullptr};
       const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase);
       RowStats st[2];
-      if (!position_stats<TIn>(sm, srow, 1, n, __fdiv_rn(kLog2e, temp), topk, topp, lf, st, &bits, step, ncta)) {
+      if (!position_stats<TIn>(sm, inbox, srow, 1, n, __fdiv_rn(kLog2e, temp), topk, topp, lf, st, &bits, step,
+                               ncta, rank)) {
         bits |= SV_DATA_BAD_VALUES;
       } else {
         const RngKey rk{P.seed_lo, P.seed_hi ^ 0x53414D50u, P.off_lo, P.off_hi};  // the sampler's own streams
@@ -1490,6 +1474,7 @@ cudaError_t enable_one(int max_cluster, int max_dyn) {
 }  // namespace
 
 size_t logits_static_smem() { return sizeof(LogitsSmem); }
+size_t logits_inbox_bytes(int cluster) { return 2 * static_cast<size_t>(cluster) * sizeof(Inbox); }
 
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn) {
   cudaError_t e;
@@ -1517,7 +1502,7 @@ cudaError_t enable_sample_kernels(int max_cluster, int max_dyn) {
 
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
   const bool test = p.exponentials != nullptr;
-  const size_t dyn = static_cast<size_t>(chunk) * (bf16 ? 2 : 4);
+  const size_t dyn = static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster);
   if (bf16) {
     if (test) return vec ? launch_sample_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
                          : launch_sample_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);
@@ -1532,7 +1517,7 @@ cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chu
 
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
   const bool test = p.exponentials != nullptr;
-  const size_t dyn = 2 * static_cast<size_t>(chunk) * (bf16 ? 2 : 4);
+  const size_t dyn = 2 * static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster);
   if (bf16) {
     if (test) return vec ? launch_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
                          : launch_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);
