@@ -136,10 +136,12 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kNearBins = 128;         // near-max bins: distances 0..127 from the row's largest key
 constexpr int kMaxCluster = 16;
 constexpr int kWalkGroups = 8;  // 16-byte groups a lane tests per window-scan step
+constexpr int kGroupWords = 8;  // registers of packed group maxima per row and thread (2 groups each)
 
 struct StatPart {  // one CTA's partials of one reduction round, for up to 2 rows
   uint32_t maxkey[2];
   uint32_t flags[2];
+  uint32_t floor[2];  // lower bound of the row's top-k threshold (key), from the thread maxima
   float z[2];
   unsigned long long tot[2];
   uint32_t cnt[2][256];
@@ -218,6 +220,7 @@ __device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
   if (tid < 2) {
     p.maxkey[tid] = 0u;
     p.flags[tid] = 0u;
+    p.floor[tid] = 0xFFFFFFFFu;
     p.z[tid] = 0.0f;
     p.tot[tid] = 0ull;
   }
@@ -579,68 +582,99 @@ __device__ bool stats_slow(LogitsSmem &sm, TIn *const srow[2], int nr, int n, fl
 // the rows already in shared memory.
 //
 // Fast path, one cluster reduction: every CTA measures its chunk against its
-// own largest key -- value checks, and for top-k/top-p the counts and
-// fixed-point masses exp2((v - local max) * c2) of the keys within kNearBins
-// steps of that maximum (dense rows: the local normaliser).  The reduction
-// moves each peer's histogram onto the global maximum (shift by the distance
-// between the maxima, scale by exp2 of their difference) and sums in rank
-// order, which resolves the k-th largest key, the top-p cut and the
-// normaliser whenever they lie in the near window (bf16 keys).
+// own largest key -- value checks, and for bf16 top-k/top-p rows the count of
+// each key within kNearBins steps below that maximum (and not below a floor
+// the k-th largest key cannot undercut); dense rows: the local normaliser.
+// Each CTA stores these into every peer's inbox; after one cluster barrier
+// every CTA shifts the peers' bins onto the global maximum, sums them as
+// integers and weighs each bin (one bf16 value) by exp2((v - max) * c2) in
+// 2^-40 fixed point.  That resolves the k-th largest key, the top-p cut and
+// the normaliser whenever they lie in the window.
 // ---------------------------------------------------------------------------
-// One warp: first near bin (walking from distance 0) whose running total
-// reaches `need`, within [0, limit).  Returns the bin or -1; *incl = total up
-// to and including it.  Integer sums: the choice is the same in every CTA.
+// One warp resolves a row's kept set from its near bins (walking from
+// distance 0, the largest key): the top-k bin L (the first whose running
+// count reaches k; all 128 bins when top-k is off) and, for top-p, the first
+// bin at or above L whose running mass reaches top_p times the mass kept so
+// far.  `total` is the mass of every key of the row (used when top-k is
+// off).  Counts and masses share one prefix scan; all sums are integers, so
+// every CTA of the cluster chooses alike.  Returns false when a bin lies
+// outside the window.
 constexpr int kBinsPerLane = kNearBins / 32;
-__device__ __forceinline__ int near_pick(const unsigned long long *h, int limit, unsigned long long need,
-                                         unsigned long long *incl) {
+struct NearChoice {
+  int last;                 // last kept bin (distance from the largest key)
+  unsigned long long kept;  // fixed-point mass of bins 0..last
+};
+__device__ __forceinline__ bool near_select(const unsigned long long *cnt, const unsigned long long *mass, int topk,
+                                            bool use_p, float topp, unsigned long long total, NearChoice *out) {
   const int lane = threadIdx.x & 31;
-  unsigned long long own = 0;
+  unsigned long long c[kBinsPerLane], m[kBinsPerLane], cs = 0, ms = 0;
 #pragma unroll
   for (int t = 0; t < kBinsPerLane; ++t) {
-    const int d = kBinsPerLane * lane + t;
-    own += d < limit ? h[d] : 0ull;
+    c[t] = cnt[kBinsPerLane * lane + t];
+    m[t] = mass[kBinsPerLane * lane + t];
+    cs += c[t];
+    ms += m[t];
   }
-  unsigned long long inc = own;
+  unsigned long long ci = cs, mi = ms;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  const unsigned long long before = inc - own;
-  int found = -1;
-  unsigned long long in = 0;
-  if (before < need && inc >= need) {
-    unsigned long long acc = before;
-#pragma unroll
-    for (int t = 0; t < kBinsPerLane; ++t) {
-      const int d = kBinsPerLane * lane + t;
-      const unsigned long long x = d < limit ? h[d] : 0ull;
-      if (found < 0 && acc + x >= need) {
-        found = d;
-        in = acc + x;
-      }
-      acc += x;
+    const unsigned long long vc = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+    const unsigned long long vm = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+    if (lane >= o) {
+      ci += vc;
+      mi += vm;
     }
   }
-  const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0);
-  if (!ball) return -1;
-  const int src = __ffs(ball) - 1;
-  *incl = __shfl_sync(0xFFFFFFFFu, in, src);
-  return __shfl_sync(0xFFFFFFFFu, found, src);
-}
-
-// One warp: sum of h over bins [0, limit).
-__device__ __forceinline__ unsigned long long near_sum(const unsigned long long *h, int limit) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long s = 0;
+  const unsigned long long cb = ci - cs, mb = mi - ms;  // totals before this lane's bins
+  int last = kNearBins - 1;
+  unsigned long long kept = total;
+  if (topk > 0) {
+    const unsigned long long k = static_cast<unsigned long long>(topk);
+    int found = -1;
+    unsigned long long kin = 0;
+    if (cb < k && ci >= k) {
+      unsigned long long acc = cb, macc = mb;
 #pragma unroll
-  for (int t = 0; t < kBinsPerLane; ++t) {
-    const int d = kBinsPerLane * lane + t;
-    s += d < limit ? h[d] : 0ull;
+      for (int t = 0; t < kBinsPerLane; ++t) {
+        acc += c[t];
+        macc += m[t];
+        if (found < 0 && acc >= k) {
+          found = kBinsPerLane * lane + t;
+          kin = macc;
+        }
+      }
+    }
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0);
+    if (!ball) return false;
+    const int src = __ffs(ball) - 1;
+    last = __shfl_sync(0xFFFFFFFFu, found, src);
+    kept = __shfl_sync(0xFFFFFFFFu, kin, src);
   }
+  if (use_p) {
+    unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(kept));
+    if (need == 0ull) need = 1ull;
+    int found = -1;
+    unsigned long long in = 0;
+    if (mb < need && mi >= need) {
+      unsigned long long acc = mb;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-  return s;
+      for (int t = 0; t < kBinsPerLane; ++t) {
+        acc += m[t];
+        if (found < 0 && acc >= need) {
+          found = kBinsPerLane * lane + t;
+          in = acc;
+        }
+      }
+    }
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0 && found <= last);
+    if (!ball) return false;
+    const int src = __ffs(ball) - 1;
+    last = __shfl_sync(0xFFFFFFFFu, found, src);
+    kept = __shfl_sync(0xFFFFFFFFu, in, src);
+  }
+  out->last = last;
+  out->kept = kept;
+  return true;
 }
 
 template <typename TIn>
@@ -653,15 +687,52 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   const bool use_k = topk > 0;
   const bool use_p = topp < 1.0f;
   const bool near = use_k || use_p;
+  // top-k rows with k <= 32 * kWarps: a per-CTA lower bound of the threshold
+  // narrows the window scan (keys below it cannot be among the top k)
+  const bool use_floor = kB == 16 && use_k && topk <= 32 * kWarps;
   const int par = step & 1;
   StatPart &lp = sm.part[par];
 
   // local pass A: largest key and value checks of this CTA's chunk
   zero_part(lp, (kB == 16 && near) ? kRCnt : 0u, nr);
   __syncthreads();
+  uint32_t mk[2] = {0u, 0u}, fl[2] = {load_flags, load_flags};  // this thread's largest finite key, flags
+  // bf16 rows whose chunk gives a thread at most 2 * kGroupWords 16-byte
+  // groups keep each group's largest value in registers (two per word, NaN
+  // for absent groups), so the window pass re-reads only groups that hold a
+  // candidate
+  const int ng_all = n >> 3;
+  const bool reg_groups = kB == 16 && ng_all <= 2 * kGroupWords * kThreads;
+  uint32_t gw[2][kGroupWords];
   for (int r = 0; r < nr; ++r) {
-    uint32_t mk = 0, fl = load_flags;
-    if (kB == 16) {
+    if (kB == 16 && reg_groups) {
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
+      uint32_t acc = 0xFF80FF80u;  // (-inf, -inf)
+#pragma unroll
+      for (int i = 0; i < kGroupWords; ++i) {
+        uint32_t half[2] = {0x7FFFu, 0x7FFFu};  // NaN: never a window candidate
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int v = tid + (2 * i + h) * kThreads;
+          if (v < ng_all) {
+            const uint4 d = s4[v];
+            uint32_t p2 = bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w));
+            p2 = bf16x2_max_nan(p2, (p2 >> 16) | (p2 << 16));
+            acc = bf16x2_max_nan(acc, p2);
+            half[h] = p2 & 0xFFFFu;
+          }
+        }
+        gw[r][i] = half[0] | (half[1] << 16);
+      }
+      for (int x = (ng_all << 3) + tid; x < n; x += kThreads) acc = bf16x2_max_nan(acc, bits_at(srow[r], x) | 0xFF800000u);
+      acc = bf16x2_max_nan(acc, (acc >> 16) | (acc << 16));
+      const uint32_t mb = acc & 0xFFFFu;  // this thread's largest value, NaN if it saw one
+      if (E::is_nan(mb) || E::is_pinf(mb)) fl[r] |= kFlagBad;
+      if (E::finite(mb)) {
+        fl[r] |= kFlagFinite;
+        mk[r] = E::key(mb);
+      }
+    } else if (kB == 16) {
       // pairs of bf16 through one NaN-propagating bf16x2 max per pair
       const int nw = n >> 1;
       const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
@@ -683,28 +754,64 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) acc = bf16x2_max_nan(acc, bits_at(srow[r], x) | 0xFF800000u);
       acc = bf16x2_max_nan(acc, (acc >> 16) | (acc << 16));
       const uint32_t mb = acc & 0xFFFFu;  // this thread's largest value, NaN if it saw one
-      if (E::is_nan(mb) || E::is_pinf(mb)) fl |= kFlagBad;
+      if (E::is_nan(mb) || E::is_pinf(mb)) fl[r] |= kFlagBad;
       if (E::finite(mb)) {
-        fl |= kFlagFinite;
-        mk = E::key(mb);
+        fl[r] |= kFlagFinite;
+        mk[r] = E::key(mb);
       }
     } else {
       for_each_elem(srow[r], n, [&](uint32_t b, int) {
-        if (E::is_nan(b) || E::is_pinf(b)) fl |= kFlagBad;
+        if (E::is_nan(b) || E::is_pinf(b)) fl[r] |= kFlagBad;
         if (E::finite(b)) {
-          fl |= kFlagFinite;
-          mk = max(mk, E::key(b));  // largest finite key
+          fl[r] |= kFlagFinite;
+          mk[r] = max(mk[r], E::key(b));  // largest finite key
         }
       });
     }
+  }
+  // warp maxima and flags of both rows (the two shuffle chains interleave)
+  uint32_t wk[2] = {mk[0], mk[1]}, wf[2] = {fl[0], fl[1]};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
-      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      wk[r] = max(wk[r], __shfl_xor_sync(0xFFFFFFFFu, wk[r], o));
+      wf[r] |= __shfl_xor_sync(0xFFFFFFFFu, wf[r], o);
     }
-    if ((tid & 31) == 0) {
-      atomicMax(&lp.maxkey[r], mk);
-      atomicOr(&lp.flags[r], fl);
+  }
+  uint32_t wfloor[2] = {0u, 0u};
+  if (use_floor) {
+    // The thread maxima are distinct elements of disjoint subsets: if f is the
+    // j-th largest of a warp's 32, that warp holds j elements >= f, so the
+    // smallest f over the kWarps warps (j = ceil(k / kWarps)) has at least k
+    // elements at or above it and cannot exceed the k-th largest key of the
+    // chunk, nor therefore of the row.  The j-th largest is searched as the
+    // j-th smallest distance below the warp's maximum, clamped to 255: a
+    // clamped result lies more than kNearBins below the CTA's maximum, under
+    // the window's own lower edge, so it never narrows the window.
+    const int need = (topk + kWarps - 1) / kWarps;
+    uint32_t near_key[2], f[2] = {0u, 0u};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) near_key[r] = 255u - min(wk[r] - mk[r], 255u);  // larger = nearer the maximum
+#pragma unroll
+    for (int bit = 7; bit >= 0; --bit) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t t = f[r] | (1u << bit);
+        if (__popc(__ballot_sync(0xFFFFFFFFu, near_key[r] >= t)) >= need) f[r] = t;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t dist = 255u - f[r];
+      wfloor[r] = wk[r] > dist ? wk[r] - dist : 0u;
+    }
+  }
+  if ((tid & 31) == 0) {
+    for (int r = 0; r < nr; ++r) {
+      atomicMax(&lp.maxkey[r], wk[r]);
+      atomicOr(&lp.flags[r], wf[r]);
+      if (use_floor) atomicMin(&lp.floor[r], wfloor[r]);
     }
   }
   __syncthreads();
@@ -720,33 +827,69 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
     for (int r = 0; r < nr; ++r) {
       if (!(lp.flags[r] & kFlagFinite)) continue;  // empty or no finite value: contributes nothing
       const uint32_t lk16 = key16_of<TIn>(lp.maxkey[r]);
-      const uint32_t lo = lk16 - (kNearBins - 1);  // window's smallest key; below key(-inf): all finite pass
-      const uint32_t lob = (lk16 >= static_cast<uint32_t>(kNearBins - 1) && lo > 0x007Fu) ? bf16_bits_of_key(lo)
-                                                                                            : 0xFF80u;
+      // window's smallest key (at most kNearBins - 1 below the largest, and not
+      // below the threshold's floor); at or below key(-inf): every finite key
+      uint32_t lo = lk16 >= static_cast<uint32_t>(kNearBins - 1) ? lk16 - (kNearBins - 1) : 0u;
+      if (use_floor) lo = max(lo, lp.floor[r]);
+      const uint32_t lob = lo > 0x007Fu ? bf16_bits_of_key(lo) : 0xFF80u;
       const uint32_t lo2 = lob | (lob << 16);
       uint32_t *cnt = lp.cnt[r];
       const TIn *row = srow[r];
       const int nw = n >> 1;
       const int ng = nw >> 2;  // 16-byte groups
       const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
-      // Candidates are a few percent of the keys.  A lane tests eight 16-byte
-      // groups at once (packed compares, every load in flight together) into
-      // one 64-bit candidate mask, then the warp walks the set bits in step:
-      // each trip counts at most one candidate per lane, so the trips are the
-      // largest per-lane count, not the number of element slots.
-      for (int vb = warp * 32; vb < ng; vb += kWalkGroups * kThreads) {
+      // Counting one candidate: the warp walks the set bits of per-lane masks
+      // in step, one candidate per lane per trip.
+      auto count_group = [&](int v, uint32_t em) {
+        while (__any_sync(0xFFFFFFFFu, em != 0u)) {
+          if (em != 0u) {
+            const int pos = __ffs(em) - 1;
+            em &= em - 1u;
+            const int x = 8 * v + 2 * (pos & 3) + (pos >> 2);
+            const uint32_t b = bits_at(row, x);
+            const uint32_t d = lk16 - E::key(b);
+            if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
+          }
+        }
+      };
+      // 8-bit candidate mask of one 16-byte group: bit t is the low half of
+      // word t, bit 4 + t its high half
+      auto group_mask = [&](const uint4 &dv) {
+        uint32_t g = (bf16x2_ge_mask(dv.x, lo2) & 0x00010001u) | ((bf16x2_ge_mask(dv.y, lo2) & 0x00010001u) << 1) |
+                     ((bf16x2_ge_mask(dv.z, lo2) & 0x00010001u) << 2) |
+                     ((bf16x2_ge_mask(dv.w, lo2) & 0x00010001u) << 3);
+        return (g | (g >> 12)) & 0xFFu;
+      };
+      if (reg_groups) {
+        // groups whose largest value reaches the window, two per compare; only
+        // those are read again
+        uint32_t cg = 0u;
+#pragma unroll
+        for (int i = 0; i < kGroupWords; ++i) {
+          const uint32_t m = bf16x2_ge_mask(gw[r][i], lo2);
+          cg |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * i);
+        }
+        while (__any_sync(0xFFFFFFFFu, cg != 0u)) {
+          int v = 0;
+          uint32_t em = 0u;
+          if (cg != 0u) {
+            const int pos = __ffs(cg) - 1;
+            cg &= cg - 1u;
+            v = tid + pos * kThreads;
+            em = group_mask(s4[v]);
+          }
+          count_group(v, em);
+        }
+      }
+      // Otherwise a lane tests eight 16-byte groups at once (packed compares,
+      // every load in flight together) into one 64-bit candidate mask and the
+      // warp walks its set bits.
+      for (int vb = warp * 32; !reg_groups && vb < ng; vb += kWalkGroups * kThreads) {
         unsigned long long M = 0ull;
 #pragma unroll
         for (int h = 0; h < kWalkGroups; ++h) {
           const int v = vb + h * kThreads + lane;
-          if (v < ng) {
-            const uint4 dv = s4[v];
-            uint32_t g = (bf16x2_ge_mask(dv.x, lo2) & 0x00010001u) | ((bf16x2_ge_mask(dv.y, lo2) & 0x00010001u) << 1) |
-                         ((bf16x2_ge_mask(dv.z, lo2) & 0x00010001u) << 2) |
-                         ((bf16x2_ge_mask(dv.w, lo2) & 0x00010001u) << 3);
-            g = (g | (g >> 12)) & 0xFFu;  // bit t: low half of word t; bit 4 + t: its high half
-            M |= static_cast<unsigned long long>(g) << (8 * h);
-          }
+          if (v < ng) M |= static_cast<unsigned long long>(group_mask(s4[v])) << (8 * h);
         }
         while (__any_sync(0xFFFFFFFFu, M != 0ull)) {
           if (M != 0ull) {
@@ -762,7 +905,7 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) {
         const uint32_t b = bits_at(srow[r], x);
         const uint32_t d = lk16 - E::key(b);
-        if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
+        if (E::finite(b) && E::key(b) >= lo && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
       }
       if (use_p && !use_k) {  // top-p alone: the whole row is kept before the cut
         const float lv = E::val_of_key(lp.maxkey[r]);
@@ -886,29 +1029,12 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   const int warp = tid >> 5;
   if (warp < nr) {
     const int r = warp;
-    int ok = 1, lim = kNearBins;
-    unsigned long long kept = 0;
-    if (use_k) {
-      unsigned long long in;
-      const int L = near_pick(ns.cnt[r], kNearBins, static_cast<unsigned long long>(topk), &in);
-      if (L < 0) ok = 0;
-      else lim = L + 1;
-      kept = near_sum(ns.mass[r], lim);  // mass of the top-k set
-    } else {
-      kept = ns.tot[r];
-    }
-    int Lc = lim - 1;
-    if (ok && use_p) {
-      unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(kept));
-      unsigned long long in = 0;
-      Lc = near_pick(ns.mass[r], lim, need > 0ull ? need : 1ull, &in);
-      if (Lc < 0) ok = 0;
-      else kept = in;
-    }
-    if ((threadIdx.x & 31) == 0) {
+    NearChoice ch;
+    const bool ok = near_select(ns.cnt[r], ns.mass[r], use_k ? topk : 0, use_p, topp, ns.tot[r], &ch);
+    if ((tid & 31) == 0) {
       sm.sel.ok[r] = ok && (kB == 16);  // fp32 keys need the low 16 bits refined: multi-pass path
-      sm.sel.prefix[r] = key16_of<TIn>(ns.gmax[r]) - static_cast<uint32_t>(Lc < 0 ? 0 : Lc);
-      ns.z[r] = static_cast<float>(static_cast<double>(kept) * (1.0 / static_cast<double>(kMassScale)));
+      sm.sel.prefix[r] = key16_of<TIn>(ns.gmax[r]) - static_cast<uint32_t>(ok ? ch.last : 0);
+      ns.z[r] = static_cast<float>(static_cast<double>(ok ? ch.kept : 0ull) * (1.0 / static_cast<double>(kMassScale)));
     }
   }
   __syncthreads();

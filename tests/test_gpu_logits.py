@@ -259,3 +259,34 @@ def test_synthetic_acceptance_logits(rates):
     compare_logits(g, o, w)
     if rates[1] > rates[0]:
         assert o["status"] == oracle.BAD_PARAM
+
+
+@pytest.mark.parametrize("shape", ["normal", "ties", "spiky", "monotone"])
+@pytest.mark.parametrize("top_k", [1, 8, 9, 100, 255, 256, 257])
+def test_top_k_threshold_bound_cases(shape, top_k):
+    """Rows chosen so the threshold sits at every kind of place relative to a
+    CTA's largest keys: heavy ties, a few spikes over a flat floor, and a
+    monotone row whose top k all lie in one CTA's chunk; k on both sides of
+    32 x warps (where the per-CTA threshold bound switches off)."""
+    N, V = 6, 40000
+    w = workloads.make("fused", N=N, V=V, seed=41)
+    rng = np.random.default_rng(top_k * 7 + len(shape))
+    G = w["gamma"]
+    rows = N * (G + 1) + N * G
+    if shape == "normal":
+        l = rng.standard_normal((rows, V)).astype(np.float32) * 2.5
+    elif shape == "ties":
+        l = rng.integers(0, 6, size=(rows, V)).astype(np.float32)
+    elif shape == "spiky":
+        l = np.full((rows, V), -5.0, np.float32)
+        l[:, rng.integers(0, V, size=3)] = 10.0
+        l += rng.integers(0, 2, size=(rows, V)).astype(np.float32) * 0.5
+    else:
+        l = np.tile(-np.arange(V, dtype=np.float32) * 0.01, (rows, 1))
+        l += rng.standard_normal((rows, V)).astype(np.float32) * 0.02
+    bits = workloads._to_bf16_bits(l)
+    w["target"] = bits[:N * (G + 1)]
+    w["draft"] = bits[N * (G + 1):]
+    w["top_k"] = np.full(N, top_k, np.int32)
+    w["top_p"] = np.full(N, 0.95 if top_k > 8 else 1.0, np.float32)
+    compare_logits(H().run_gpu(w), oracle.verify(w), w, max_exempt_frac=0.5)
