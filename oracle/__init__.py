@@ -88,6 +88,8 @@ def _lib():
         lib.oracle_sample_rows.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int64,
                                            _P, _P, _P, _P, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
                                            ctypes.c_uint32, _P, _P, _P, _P]
+        lib.oracle_ngram_propose.argtypes = [ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int64, _P, _P]
         assert lib.oracle_sizeof_args() == ctypes.sizeof(_Args), "oracle_args layout mismatch"
         _LIB = lib
     return _LIB
@@ -214,3 +216,17 @@ def sample_rows(logits, *, temperature=None, top_k=None, top_p=None, exponential
     if rc != 0:
         raise RuntimeError(f"oracle_sample_rows failed with {rc}")
     return dict(tokens=tokens, probs=probs, status=int(status[0]), diag=diag)
+
+
+def ngram_propose(tokens, cu_num_tokens, *, min_ngram: int, max_ngram: int, k: int, max_model_len: int):
+    """N-gram proposals for a ragged batch of token histories (request q owns
+    tokens[cu[q-1]:cu[q]]).  Returns dict(draft_token_ids [R, k] with -1
+    padding, num_draft_tokens [R], status)."""
+    t = _c(np.asarray(tokens), np.int32)
+    cu = _c(np.asarray(cu_num_tokens), np.int64)
+    R = int(cu.shape[0])
+    out = np.full((R, max(k, 0)), -1, np.int32)
+    num = np.zeros(R, np.int32)
+    st = _lib().oracle_ngram_propose(R, _ptr(t), _ptr(cu), int(t.shape[0]), int(min_ngram), int(max_ngram), int(k),
+                                     int(max_model_len), _ptr(out), _ptr(num))
+    return dict(draft_token_ids=out, num_draft_tokens=num, status=int(st))

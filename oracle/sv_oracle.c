@@ -715,3 +715,67 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
   free(E);
   return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * N-gram proposer ("vLLM source walk-through (10)", section "NgramProposer":
+ * no draft model; the history is read backwards so that "the current tail
+ * seen earlier" becomes a prefix match, KMP-style, with match lengths capped
+ * at max_ngram; the longest match with length in [min_ngram, max_ngram]
+ * proposes the k tokens that followed it).
+ *
+ * Written out as its definition: r[j] = t[L-1-j] is the history read
+ * backwards.  For each end index i in [1, L), m(i) is the largest
+ * m <= min(max_ngram, i) with r[i-m+1 .. i] == r[0 .. m-1], i.e. the
+ * occurrence t[L-1-i .. L-1-i+m) equals the last m tokens and is followed by
+ * at least one token.  m* = max_i m(i); nothing is proposed if m* < min_ngram.
+ * Otherwise i* is the smallest i with m(i) = m* -- the first match a scan of
+ * r meets, the most recent occurrence in t -- and the proposal is
+ * t[start .. start + k'), start = L - 1 - i* + m*, k' = min(k, max_model_len - L,
+ * L - start).  Requests use the verifier's ragged layout: request q owns
+ * tokens [cu[q-1], cu[q]) (cu[-1] = 0).  Output rows are [R, k], -1 after the
+ * proposal; num[q] = k'.  Returns the status bits (1: bad cu range).
+ * ------------------------------------------------------------------------ */
+int oracle_ngram_propose(int32_t R, const int32_t *tokens, const int64_t *cu, int64_t total, int32_t min_ngram,
+                         int32_t max_ngram, int32_t k, int64_t max_model_len, int32_t *out, int32_t *num) {
+  int status = 0;
+  for (int32_t q = 0; q < R; ++q) {
+    int32_t *row = out + (int64_t)q * k;
+    for (int32_t c = 0; c < k; ++c) row[c] = -1;
+    num[q] = 0;
+    const int64_t s = q ? cu[q - 1] : 0, e = cu[q];
+    if (s < 0 || e < s || e > total) {
+      status |= ORC_BAD_CU;
+      continue;
+    }
+    const int32_t *t = tokens + s;
+    const int64_t L = e - s;
+    if (L < min_ngram) continue;
+    int64_t kk = k;
+    if (max_model_len - L < kk) kk = max_model_len - L;
+    if (kk <= 0) continue;
+    int64_t best_m = 0, best_i = -1;
+    for (int64_t i = 1; i < L; ++i) {
+      int64_t cap = i < max_ngram ? i : max_ngram;
+      int64_t m = 0;
+      for (int64_t len = cap; len >= 1; --len) { /* largest len whose windows agree */
+        int same = 1;
+        for (int64_t j = 0; j < len && same; ++j)
+          if (t[L - 1 - (i - len + 1 + j)] != t[L - 1 - j]) same = 0;
+        if (same) {
+          m = len;
+          break;
+        }
+      }
+      if (m > best_m) { /* strictly longer only: the earliest i keeps a tie */
+        best_m = m;
+        best_i = i;
+      }
+    }
+    if (best_m < min_ngram) continue;
+    const int64_t start = L - 1 - best_i + best_m;
+    if (L - start < kk) kk = L - start;
+    for (int64_t c = 0; c < kk; ++c) row[c] = t[start + c];
+    num[q] = (int32_t)kk;
+  }
+  return status;
+}
