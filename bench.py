@@ -11,7 +11,8 @@ inserted.
 
 Prints one JSON line: verified draft tokens/s for the whole job, the roofline
 of the verifier kernel against the measured HBM copy bandwidth, the logits
-entry on the same batch shape, end-to-end figures through the C ABI with
+entry on the same batch shape, the n-gram proposer on its own batch,
+end-to-end figures through the C ABI with
 inputs in pinned host memory (zero-copy rows, and full copies), the CPU oracle
 as a reported baseline, and the SM clocks sampled during the timed region.
 
@@ -57,6 +58,8 @@ def parse_args():
     ap.add_argument("--requests", type=int, default=0, help="override the batch size (profiling runs only)")
     ap.add_argument("--logits-steps", type=int, default=300)
     ap.add_argument("--no-logits", action="store_true")
+    ap.add_argument("--ngram-steps", type=int, default=200)
+    ap.add_argument("--no-ngram", action="store_true")
     return ap.parse_args()
 
 
@@ -248,6 +251,61 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
             "gpu_launches": K}
 
 
+def time_ngram(args, sv, dev, world, rank, dist, stream):
+    """The batched n-gram proposer on its default batch (512 repetitive
+    histories of 1024..16384 tokens, min/max n-gram 5, k = 7).  The histories
+    (~18 MB) fit in L2, so every launch is timed on its own with a 256 MB
+    buffer written in between (outside the events) to flush L2."""
+    import numpy as np
+    import torch
+    import workloads
+    tokens, cu = workloads.make_histories(seed=workloads.NGRAM["seed"] + 1000 * rank)
+    R, k, n_min, n_max = len(cu), 7, 5, 5
+    t = torch.as_tensor(tokens).to(dev)
+    c = torch.as_tensor(cu).to(dev)
+    out = torch.empty((R, k), dtype=torch.int32, device=dev)
+    num = torch.empty((R,), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    h = sv.spec_verify_create(R, k, 1, device=dev.index)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    K = max(3, min(args.steps, args.ngram_steps))
+    kw = dict(token_ids=t, cu_num_tokens=c, draft_token_ids=out, num_draft_tokens=num, min_ngram=n_min,
+              max_ngram=n_max, max_model_len=1 << 20, status=status)
+    for _ in range(args.warmup):
+        sv.spec_verify_ngram_propose(h, stream=stream, **kw)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    times = []
+    for _ in range(K):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sv.spec_verify_ngram_propose(h, stream=stream, **kw)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = float(np.mean(times))
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    proposed = num.cpu().numpy()
+    sv.spec_verify_destroy(h)
+    alg = 4 * int(cu[-1]) + 8 * R + 4 * R * (k + 1)
+    peak, src = measured_peak()
+    return {"value": world * R / (ms / 1e3), "unit": "requests/s", "ms_per_step": ms, "steps": K,
+            "history_tokens_per_s": world * int(cu[-1]) / (ms / 1e3),
+            "config": {"workload": f"ngram: R={R} histories of 1024..16384 tokens (mean {int(cu[-1]) // R}), "
+                                   f"vocab 151936, half the segments repeated; min/max n-gram {n_min}/{n_max}, "
+                                   f"k={k}", "l2": "flushed before every launch (256 MB write, untimed)"},
+            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg},
+            "proposed_fraction": float((proposed > 0).mean()), "gpu_launches": K}
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -334,6 +392,7 @@ def run_ours(args, world, rank, local_rank):
     t1 = time.time()
     barrier()
     logits = None if args.no_logits else time_logits_entry(args, sv, lib, dev, world, rank, dist, stream)
+    ngram = None if args.no_ngram else time_ngram(args, sv, dev, world, rank, dist, stream)
     clocks.stop()
     total_ms = ev[0].elapsed_time(ev[K])
     per_launch = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
@@ -384,6 +443,8 @@ def run_ours(args, world, rank, local_rank):
     }
     if logits:
         line["logits_entry"] = logits
+    if ngram:
+        line["ngram_proposer"] = ngram
     if e2e:
         line["e2e"] = e2e
         line["e2e_full_copy"] = e2e_fc

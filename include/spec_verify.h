@@ -46,10 +46,11 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 2u
+#define SPEC_VERIFY_ABI_VERSION 3u
 #define SV_PLACEHOLDER_TOKEN_ID (-1)
 #define SV_PADDING_SLOT_ID (-1)
 #define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
+#define SV_MAX_NGRAM 64     /* largest max_ngram of the n-gram proposer */
 
 /* Host-visible result codes. */
 typedef enum sv_status {
@@ -186,6 +187,37 @@ sv_status spec_verify_sample(spec_verify_t handle, const spec_verify_sample_args
 /* Host-only validation of sampler arguments against `config`. */
 sv_status spec_verify_check_sample_args(const spec_verify_config *config, const spec_verify_sample_args *args);
 
+/* Batched n-gram proposer ("vLLM source walk-through (10)", section
+ * "NgramProposer": no draft model; the tail of a request's token history is
+ * looked up earlier in the history -- the history read backwards, match
+ * lengths capped at max_ngram -- and the longest match with a length in
+ * [min_ngram, max_ngram] proposes the tokens that followed it).  Exactly: for
+ * every end position E <= L - 2 of a request's history t[0 .. L), l(E) is the
+ * number of j = 0, 1, ... with t[E - j] == t[L - 1 - j], capped at max_ngram
+ * and at E + 1.  The proposal follows the E with the largest l(E), the latest
+ * such E on ties (the most recent occurrence), if that l is at least
+ * min_ngram: draft = t[E + 1 .. E + 1 + k'), k' = min(k, max_model_len - L,
+ * L - 1 - E).  Otherwise nothing is proposed.  R = num_reqs; one CTA per
+ * request reads its history once from HBM. */
+typedef struct spec_verify_ngram_args {
+  int32_t num_reqs;        /* R >= 0 (0 is a no-op); at most the handle's max_num_reqs */
+  int32_t min_ngram;       /* 1 <= min_ngram <= max_ngram */
+  int32_t max_ngram;       /* max_ngram <= SV_MAX_NGRAM */
+  int32_t num_spec_tokens; /* k: 0 .. the handle's max_spec_len */
+  int64_t max_model_len;   /* >= 1: a history of L tokens gets at most max_model_len - L */
+  int64_t num_tokens_total;              /* length of token_ids (>= 0) */
+  const int32_t *token_ids;              /* [num_tokens_total] histories, request after request */
+  const int64_t *cu_num_tokens;          /* [R] inclusive prefix sums: request q owns [cu[q-1], cu[q]), cu[-1] = 0 */
+  int32_t *draft_token_ids;              /* [R, k] out: the proposal, then -1 (may be NULL when k == 0) */
+  int32_t *num_draft_tokens;             /* [R] out: k' (0 when nothing is proposed or the range is bad) */
+  int32_t *status;                       /* [1] or NULL: SV_DATA_BAD_CU OR-ed in for a bad range */
+} spec_verify_ngram_args;
+
+sv_status spec_verify_ngram_propose(spec_verify_t handle, const spec_verify_ngram_args *args, void *stream);
+
+/* Host-only validation of n-gram proposer arguments against `config`. */
+sv_status spec_verify_check_ngram_args(const spec_verify_config *config, const spec_verify_ngram_args *args);
+
 /* Create a handle.  Queries the device and sets kernel attributes on it
  * (temporarily making `device` current).  *out is set only on SV_OK. */
 sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *out);
@@ -212,6 +244,7 @@ uint32_t spec_verify_abi_version(void);
 size_t spec_verify_sizeof_config(void);
 size_t spec_verify_sizeof_args(void);
 size_t spec_verify_sizeof_sample_args(void);
+size_t spec_verify_sizeof_ngram_args(void);
 
 #ifdef __cplusplus
 }

@@ -70,6 +70,15 @@ class SpecVerifySampleArgs(ctypes.Structure):
     ]
 
 
+class SpecVerifyNgramArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_reqs", ctypes.c_int32), ("min_ngram", ctypes.c_int32), ("max_ngram", ctypes.c_int32),
+        ("num_spec_tokens", ctypes.c_int32), ("max_model_len", ctypes.c_int64),
+        ("num_tokens_total", ctypes.c_int64), ("token_ids", _P), ("cu_num_tokens", _P),
+        ("draft_token_ids", _P), ("num_draft_tokens", _P), ("status", _P),
+    ]
+
+
 class NativeLibraryMissing(RuntimeError):
     pass
 
@@ -84,7 +93,8 @@ _LIB = None
 EXPORTED = ("spec_verify_create", "spec_verify_run", "spec_verify_destroy", "spec_verify_check_args",
             "spec_verify_status_string", "spec_verify_last_error", "spec_verify_abi_version",
             "spec_verify_sizeof_config", "spec_verify_sizeof_args", "spec_verify_sample",
-            "spec_verify_check_sample_args", "spec_verify_sizeof_sample_args")
+            "spec_verify_check_sample_args", "spec_verify_sizeof_sample_args", "spec_verify_ngram_propose",
+            "spec_verify_check_ngram_args", "spec_verify_sizeof_ngram_args")
 
 
 def load_library(path: Optional[str] = None):
@@ -117,9 +127,15 @@ def load_library(path: Optional[str] = None):
                                                   ctypes.POINTER(SpecVerifySampleArgs)]
     lib.spec_verify_check_sample_args.restype = ctypes.c_int
     lib.spec_verify_sizeof_sample_args.restype = ctypes.c_size_t
+    lib.spec_verify_ngram_propose.argtypes = [ctypes.c_void_p, ctypes.POINTER(SpecVerifyNgramArgs), ctypes.c_void_p]
+    lib.spec_verify_ngram_propose.restype = ctypes.c_int
+    lib.spec_verify_check_ngram_args.argtypes = [ctypes.POINTER(SpecVerifyConfig), ctypes.POINTER(SpecVerifyNgramArgs)]
+    lib.spec_verify_check_ngram_args.restype = ctypes.c_int
+    lib.spec_verify_sizeof_ngram_args.restype = ctypes.c_size_t
     if lib.spec_verify_sizeof_config() != ctypes.sizeof(SpecVerifyConfig) or \
             lib.spec_verify_sizeof_args() != ctypes.sizeof(SpecVerifyArgs) or \
-            lib.spec_verify_sizeof_sample_args() != ctypes.sizeof(SpecVerifySampleArgs):
+            lib.spec_verify_sizeof_sample_args() != ctypes.sizeof(SpecVerifySampleArgs) or \
+            lib.spec_verify_sizeof_ngram_args() != ctypes.sizeof(SpecVerifyNgramArgs):
         raise RuntimeError("spec_verify struct layout differs from the binding")
     if path is None:
         _LIB = lib
@@ -311,6 +327,44 @@ def spec_verify_sample(handle: int, stream=None, **kw) -> None:
 def spec_verify_check_sample_args(config: SpecVerifyConfig, args: SpecVerifySampleArgs) -> int:
     """Host-only validation of sampler arguments; returns the sv_status code."""
     return int(load_library().spec_verify_check_sample_args(ctypes.byref(config), ctypes.byref(args)))
+
+
+def build_ngram_args(*, token_ids, cu_num_tokens, draft_token_ids, num_draft_tokens, min_ngram: int, max_ngram: int,
+                     max_model_len: int, status=None) -> SpecVerifyNgramArgs:
+    """Validate tensors and fill a SpecVerifyNgramArgs (no device work).  The
+    number of proposed tokens k is draft_token_ids.shape[1]."""
+    import torch
+    device = cu_num_tokens.device
+    R = int(cu_num_tokens.numel())
+    if draft_token_ids.dim() != 2 or draft_token_ids.shape[0] != R:
+        raise ValueError(f"draft_token_ids must have shape [{R}, k], got {tuple(draft_token_ids.shape)}")
+    a = SpecVerifyNgramArgs()
+    a.num_reqs, a.min_ngram, a.max_ngram = R, int(min_ngram), int(max_ngram)
+    a.num_spec_tokens = int(draft_token_ids.shape[1])
+    a.max_model_len = int(max_model_len)
+    a.num_tokens_total = int(token_ids.numel())
+    a.token_ids = _ptr(token_ids, torch.int32, "token_ids", device, ndim=1) if token_ids.numel() else None
+    a.cu_num_tokens = _ptr(cu_num_tokens, torch.int64, "cu_num_tokens", device, ndim=1) if R else None
+    a.draft_token_ids = _ptr(draft_token_ids, torch.int32, "draft_token_ids", device) if draft_token_ids.numel() else None
+    a.num_draft_tokens = _ptr(num_draft_tokens, torch.int32, "num_draft_tokens", device, numel=R) if R else None
+    a.status = _ptr(status, torch.int32, "status", device, numel=1)
+    return a
+
+
+def spec_verify_ngram_propose(handle: int, stream=None, **kw) -> None:
+    """Enqueue the batched n-gram proposer on ``stream`` (default: torch's
+    current stream).  Keyword arguments are those of ``build_ngram_args``."""
+    import torch
+    a = build_ngram_args(**kw)
+    if stream is None:
+        stream = torch.cuda.current_stream(kw["cu_num_tokens"].device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(load_library().spec_verify_ngram_propose(ctypes.c_void_p(handle), ctypes.byref(a), ctypes.c_void_p(s)))
+
+
+def spec_verify_check_ngram_args(config: SpecVerifyConfig, args: SpecVerifyNgramArgs) -> int:
+    """Host-only validation of n-gram proposer arguments; returns the sv_status code."""
+    return int(load_library().spec_verify_check_ngram_args(ctypes.byref(config), ctypes.byref(args)))
 
 
 def spec_verify_check_args(config: SpecVerifyConfig, args: SpecVerifyArgs) -> int:

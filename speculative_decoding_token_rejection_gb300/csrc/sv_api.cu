@@ -85,6 +85,7 @@ uint32_t spec_verify_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
 size_t spec_verify_sizeof_config(void) { return sizeof(spec_verify_config); }
 size_t spec_verify_sizeof_args(void) { return sizeof(spec_verify_args); }
 size_t spec_verify_sizeof_sample_args(void) { return sizeof(spec_verify_sample_args); }
+size_t spec_verify_sizeof_ngram_args(void) { return sizeof(spec_verify_ngram_args); }
 
 static sv_status check_config(const spec_verify_config *c) {
   if (!c) return fail(SV_ERR_INVALID_ARG, "config is NULL");
@@ -307,6 +308,51 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   const bool vec = sv::aligned16(a->logits) && (a->row_stride % (16 / eb) == 0);
   const cudaError_t e = sv::launch_sample(p, bf16, cluster, chunk, vec, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "sampler launch: %s", cudaGetErrorString(e));
+  return SV_OK;
+}
+
+sv_status spec_verify_check_ngram_args(const spec_verify_config *c, const spec_verify_ngram_args *a) {
+  sv_status st = check_config(c);
+  if (st != SV_OK) return st;
+  if (!a) return fail(SV_ERR_INVALID_ARG, "args is NULL");
+  if (a->num_reqs < 0) return fail(SV_ERR_INVALID_ARG, "num_reqs < 0");
+  if (a->num_reqs > c->max_num_reqs)
+    return fail(SV_ERR_CAPACITY, "num_reqs %d > handle max %d", a->num_reqs, c->max_num_reqs);
+  if (a->num_spec_tokens < 0) return fail(SV_ERR_INVALID_ARG, "num_spec_tokens < 0");
+  if (a->num_spec_tokens > c->max_spec_len)
+    return fail(SV_ERR_CAPACITY, "num_spec_tokens %d > handle max_spec_len %d", a->num_spec_tokens, c->max_spec_len);
+  if (a->min_ngram < 1 || a->max_ngram < a->min_ngram)
+    return fail(SV_ERR_INVALID_ARG, "need 1 <= min_ngram <= max_ngram (got %d, %d)", a->min_ngram, a->max_ngram);
+  if (a->max_ngram > SV_MAX_NGRAM) return fail(SV_ERR_UNSUPPORTED, "max_ngram %d > %d", a->max_ngram, SV_MAX_NGRAM);
+  if (a->max_model_len < 1) return fail(SV_ERR_INVALID_ARG, "max_model_len < 1");
+  if (a->num_tokens_total < 0) return fail(SV_ERR_INVALID_ARG, "num_tokens_total < 0");
+  if (a->num_reqs == 0) return SV_OK;
+  if (!a->cu_num_tokens) return fail(SV_ERR_INVALID_ARG, "cu_num_tokens is NULL");
+  if (!a->token_ids && a->num_tokens_total > 0) return fail(SV_ERR_INVALID_ARG, "token_ids is NULL");
+  if (!a->num_draft_tokens) return fail(SV_ERR_INVALID_ARG, "num_draft_tokens is NULL");
+  if (!a->draft_token_ids && a->num_spec_tokens > 0) return fail(SV_ERR_INVALID_ARG, "draft_token_ids is NULL");
+  return SV_OK;
+}
+
+sv_status spec_verify_ngram_propose(spec_verify_t h, const spec_verify_ngram_args *a, void *stream) {
+  if (!h) return fail(SV_ERR_INVALID_ARG, "handle is NULL");
+  sv_status st = spec_verify_check_ngram_args(&h->cfg, a);
+  if (st != SV_OK) return st;
+  if (a->num_reqs == 0) return SV_OK;
+  sv::NgramParams p{};
+  p.R = a->num_reqs;
+  p.min_n = a->min_ngram;
+  p.max_n = a->max_ngram;
+  p.k = a->num_spec_tokens;
+  p.max_model_len = a->max_model_len;
+  p.total = a->num_tokens_total;
+  p.tokens = a->token_ids;
+  p.cu = a->cu_num_tokens;
+  p.out = a->draft_token_ids;
+  p.num = a->num_draft_tokens;
+  p.status = a->status;
+  const cudaError_t e = sv::launch_ngram(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "n-gram proposer launch: %s", cudaGetErrorString(e));
   return SV_OK;
 }
 

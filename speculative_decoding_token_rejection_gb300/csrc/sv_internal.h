@@ -61,6 +61,18 @@ struct SampleParams {
   int32_t *status;
 };
 
+// The n-gram proposer's parameters (device pointers, sizes).
+struct NgramParams {
+  int32_t R, min_n, max_n, k;
+  int64_t max_model_len, total;
+  const int32_t *tokens;
+  const int64_t *cu;
+  int32_t *out;
+  int32_t *num;
+  int32_t *status;
+};
+cudaError_t launch_ngram(const NgramParams &p, cudaStream_t stream);
+
 // Picks the CTAs-per-request for a call (power of two, <= ctx->max_cluster).
 int choose_cluster(const spec_verify_ctx *ctx, int N, int V);
 

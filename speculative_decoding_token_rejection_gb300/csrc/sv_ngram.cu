@@ -1,0 +1,115 @@
+// sv_ngram.cu -- batched n-gram proposer ("vLLM source walk-through (10)",
+// section "NgramProposer": the tail of a request's history looked up earlier
+// in the history, match lengths capped at max_ngram, the longest match with a
+// length in [min_ngram, max_ngram] proposing the tokens that followed it).
+//
+// One CTA per request.  The CTA streams the request's history from HBM with
+// 16-byte loads, up to kLoads per thread in flight, and compares each token
+// with the last one; only the rare equal tokens E (E <= L - 2, so a token
+// follows) start the backward comparison t[E - j] == t[L - 1 - j] against the
+// tail held in shared memory.  The CTA keeps the largest (length, E) -- the
+// longest match, then the most recent occurrence -- and copies the proposal.
+#include <cstdint>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kLoads = 8;  // 16-byte loads in flight per thread
+
+__global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
+  __shared__ int32_t tail[SV_MAX_NGRAM];
+  __shared__ unsigned long long warp_best[kWarps];
+  const int q = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t *row = P.out ? P.out + static_cast<int64_t>(q) * P.k : nullptr;
+  const int64_t s = q ? P.cu[q - 1] : 0, e = P.cu[q];
+  if (s < 0 || e < s || e > P.total || e - s > 0x7FFFFFFF) {
+    for (int c = tid; c < P.k; c += kThreads) row[c] = -1;
+    if (tid == 0) {
+      P.num[q] = 0;
+      if (P.status) atomicOr(P.status, static_cast<int>(SV_DATA_BAD_CU));
+    }
+    return;
+  }
+  const int64_t L = e - s;
+  const int32_t *t = P.tokens + s;
+  int64_t kk = P.k;
+  if (P.max_model_len - L < kk) kk = P.max_model_len - L;
+  unsigned long long best = 0ull;  // (length << 32) | E; 0 = no match
+  if (L >= P.min_n && kk > 0) {
+    // candidate ends occupy global positions [s, s + L - 2]; 16-byte groups
+    // start at the aligned position at or below s
+    const int64_t g0 = s & ~static_cast<int64_t>(3), g_end = s + L - 1;  // exclusive end
+    const int64_t ngroups = (g_end - g0 + 3) >> 2;
+    const bool vec = (reinterpret_cast<uintptr_t>(P.tokens) & 15u) == 0;
+    int4 d[kLoads];
+    auto load_round = [&](int64_t vb) {
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int64_t v = vb + u * kThreads + tid;
+        const int64_t g = g0 + 4 * v;
+        if (v < ngroups && vec && g + 3 < P.total) {
+          d[u] = __ldg(reinterpret_cast<const int4 *>(P.tokens + g));
+        } else {
+          int32_t w[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[c] = (v < ngroups && g + c < P.total) ? P.tokens[g + c] : 0;
+          d[u] = make_int4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    };
+    load_round(0);  // in flight together with the tail
+    const int span = static_cast<int>(min(static_cast<int64_t>(P.max_n), L));
+    for (int j = tid; j < span; j += kThreads) tail[j] = t[L - 1 - j];
+    __syncthreads();
+    const int32_t last = tail[0];
+    auto extend = [&](int64_t E) {  // t[E] == t[L - 1]: how far back does the match run?
+      const int cap = static_cast<int>(min(static_cast<int64_t>(P.max_n), E + 1));
+      int len = 1;
+      while (len < cap && __ldg(t + E - len) == tail[len]) ++len;
+      if (len >= P.min_n) best = umax64(best, (static_cast<unsigned long long>(len) << 32) | static_cast<uint64_t>(E));
+    };
+    for (int64_t vb = 0; vb < ngroups; vb += static_cast<int64_t>(kLoads) * kThreads) {
+      if (vb > 0) load_round(vb);
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int64_t E0 = g0 + 4 * (vb + u * kThreads + tid) - s;
+        const int32_t w[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)  // (groups past the end fail the range test)
+          if (w[c] == last && E0 + c >= 0 && E0 + c <= L - 2) extend(E0 + c);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+  if (lane == 0) warp_best[warp] = best;
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < kWarps ? warp_best[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    if (lane == 0) warp_best[0] = best;
+  }
+  __syncthreads();
+  best = warp_best[0];
+  int64_t start = 0, n = 0;
+  if (best != 0ull) {
+    start = static_cast<int64_t>(best & 0xFFFFFFFFull) + 1;
+    n = min(kk, L - start);
+  }
+  for (int c = tid; c < P.k; c += kThreads) row[c] = c < n ? t[start + c] : -1;
+  if (tid == 0) P.num[q] = static_cast<int32_t>(n);
+}
+
+}  // namespace
+
+cudaError_t launch_ngram(const NgramParams &p, cudaStream_t stream) {
+  ngram_kernel<<<p.R, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sv

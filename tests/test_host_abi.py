@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_description(lib):
-    assert lib.spec_verify_abi_version() == 2
+    assert lib.spec_verify_abi_version() == 3
     assert lib.spec_verify_sizeof_args() == ctypes.sizeof(sv.SpecVerifyArgs)
     assert lib.spec_verify_sizeof_config() == ctypes.sizeof(sv.SpecVerifyConfig)
 
@@ -190,3 +190,26 @@ def test_check_sample_args(lib, mutate, code):
     a = _sample_args()
     mutate(a)
     assert sv.spec_verify_check_sample_args(cfg(), a) == code
+
+
+def _ngram_args(sv, **kw):
+    a = sv.SpecVerifyNgramArgs()
+    a.num_reqs, a.min_ngram, a.max_ngram, a.num_spec_tokens = 4, 2, 5, 3
+    a.max_model_len, a.num_tokens_total = 100, 50
+    a.token_ids, a.cu_num_tokens, a.draft_token_ids, a.num_draft_tokens = 0x1000, 0x2000, 0x3000, 0x4000
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("mutate,code", [
+    ({}, 0), (dict(num_reqs=0, token_ids=None, cu_num_tokens=None), 0), (dict(num_reqs=-1), 1),
+    (dict(num_reqs=1 << 20), 4), (dict(num_spec_tokens=-1), 1), (dict(num_spec_tokens=9), 4),
+    (dict(min_ngram=0), 1), (dict(max_ngram=1), 1), (dict(min_ngram=3, max_ngram=65), 2),
+    (dict(max_model_len=0), 1), (dict(num_tokens_total=-1), 1), (dict(cu_num_tokens=None), 1),
+    (dict(token_ids=None), 1), (dict(token_ids=None, num_tokens_total=0), 0), (dict(num_draft_tokens=None), 1),
+    (dict(draft_token_ids=None), 1), (dict(draft_token_ids=None, num_spec_tokens=0), 0)])
+def test_check_ngram_args(lib, mutate, code):
+    import speculative_decoding_token_rejection_gb300 as sv
+    cfg = sv.make_config(64, 8, 1000)
+    assert sv.spec_verify_check_ngram_args(cfg, _ngram_args(sv, **mutate)) == code

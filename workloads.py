@@ -37,6 +37,14 @@ Recipes (one per named workload; sizes can be shrunk for parity tests):
   without top-k/top-p; num_computed_tokens_i ~ U[gamma_i+1, 4096]; a random
   block table with block_size 16 gives int64 slot_mapping entries for the
   gamma_i+1 verify tokens at positions ncomp_i-gamma_i-1 .. ncomp_i-1.
+
+N-gram proposer histories (``make_histories``; "vLLM source walk-through
+(10)", section "NgramProposer": useful on repetitive text such as code,
+formatted output and chat templates): each request's history starts with 32
+fresh tokens; then, segment after segment (lengths U{8..64}), with probability
+``p_copy`` an earlier stretch of the same history is repeated, else fresh tokens
+are drawn uniformly from ``vocab`` ids.  Lengths are U{min_len..max_len}; the
+``ngram`` batch is R=512, lengths 1024..16384, vocab 151936, p_copy 0.5.
 """
 from __future__ import annotations
 
@@ -301,3 +309,33 @@ def as_torch(w: dict, device="cpu", pin: bool = False) -> dict:
         else:
             out[k] = v
     return out
+
+
+NGRAM = dict(R=512, min_len=1024, max_len=16384, vocab=151936, p_copy=0.5, seed=9)
+
+
+def make_histories(R: int = NGRAM["R"], *, min_len: int = NGRAM["min_len"], max_len: int = NGRAM["max_len"],
+                   vocab: int = NGRAM["vocab"], p_copy: float = NGRAM["p_copy"], seed: int = NGRAM["seed"]):
+    """Token histories for the n-gram proposer: returns (tokens int32 [total],
+    cu_num_tokens int64 [R] inclusive prefix sums).  Pure input synthesis."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(min_len, max_len + 1, size=R)
+    hist = []
+    for L in lens:
+        h = np.empty(int(L), np.int32)
+        n0 = min(32, int(L))
+        h[:n0] = rng.integers(0, vocab, size=n0)
+        pos = n0
+        while pos < L:
+            seg = min(int(rng.integers(8, 65)), int(L) - pos)
+            if pos >= 16 and rng.random() < p_copy:
+                src = int(rng.integers(0, pos - 8))
+                for c in range(seg):  # element by element: a repeat may run into itself
+                    h[pos + c] = h[src + c]
+            else:
+                h[pos:pos + seg] = rng.integers(0, vocab, size=seg)
+            pos += seg
+        hist.append(h)
+    tokens = np.concatenate(hist) if hist else np.zeros(0, np.int32)
+    cu = np.cumsum(lens).astype(np.int64)
+    return tokens, cu
