@@ -15,7 +15,13 @@ relative gap between the winning race key and the runner-up.
 
 Status bits mirror the library's documented meaning: 1 bad cu range, 2 draft id
 outside [0, V), 4 bad exponential draw, 8 empty distribution, 16 NaN/inf
-values, 32 bad sampling parameter, 64 draft rows missing.
+values, 32 bad sampling parameter, 64 draft rows missing, 256 bad processor or
+stop list range.
+
+Logits processors and stop tokens come with the workload dict (optional keys):
+``repetition_penalty`` [N], ``penalty_cu``/``penalty_ids`` (each request's
+context tokens), ``banned_cu``/``banned_ids`` and ``stop_cu``/``stop_ids``
+(inclusive prefix sums into the id arrays, like ``cu_num_draft_tokens``).
 """
 from __future__ import annotations
 
@@ -37,6 +43,7 @@ DIAG_ACCEPT_MARGIN, DIAG_RACE_FLIP, DIAG_RACE_RELGAP, DIAG_TOPP_EDGE, DIAG_FALLB
 
 BAD_CU, BAD_DRAFT_ID, BAD_EXPONENTIAL, EMPTY_DISTRIBUTION, BAD_VALUES, BAD_PARAM, MISSING_DRAFT = (
     1, 2, 4, 8, 16, 32, 64)
+BAD_LIST = 256
 
 _P = ctypes.c_void_p
 
@@ -55,6 +62,9 @@ class _Args(ctypes.Structure):
         ("rng_request_base", ctypes.c_uint32), ("pad1", ctypes.c_uint32),
         ("out_tokens", _P), ("num_accepted", _P), ("num_computed_tokens", _P), ("slot_mapping", _P),
         ("dbg_py", _P), ("dbg_qy", _P), ("status", _P), ("diag", _P), ("synthetic_rates", _P),
+        ("repetition_penalty", _P), ("penalty_cu", _P), ("penalty_ids", _P), ("penalty_total", ctypes.c_int64),
+        ("banned_cu", _P), ("banned_ids", _P), ("banned_total", ctypes.c_int64),
+        ("stop_cu", _P), ("stop_ids", _P), ("stop_total", ctypes.c_int64),
     ]
 
 
@@ -183,6 +193,17 @@ def verify(w: dict, *, production: bool = False, seed: int = 0, offset: int = 0,
     a.dbg_py, a.dbg_qy, a.status, a.diag = _ptr(dpy), _ptr(dqy), _ptr(status), _ptr(diag)
     rates = _c(synthetic_rates, np.float32)
     a.synthetic_rates = _ptr(rates)
+    keep = []
+    theta = _c(w.get("repetition_penalty"), np.float32)
+    keep.append(theta)
+    a.repetition_penalty = _ptr(theta)
+    for name in ("penalty", "banned", "stop"):
+        cu_l = _c(w.get(f"{name}_cu"), np.int64)
+        ids_l = _c(w.get(f"{name}_ids"), np.int32)
+        keep += [cu_l, ids_l]
+        setattr(a, f"{name}_cu", _ptr(cu_l))
+        setattr(a, f"{name}_ids", _ptr(ids_l))
+        setattr(a, f"{name}_total", 0 if ids_l is None else int(ids_l.shape[0]))
     if req_range is None:
         rc = lib.oracle_verify(ctypes.byref(a))
     else:

@@ -97,6 +97,7 @@
  * and q needed to change the decision, in units of the tolerance -- 1e-6
  * absolute (the contract on probabilities) and 1e-5 relative.  An index < 1
  * means a perturbation inside both bounds could flip the decision. */
+#define ORC_BAD_LIST 256 /* a processor or stop list range of the request is invalid */
 #define ORC_NDIAG 6
 #define DIAG_ACCEPT_MARGIN 0 /* min over examined positions of the flip index of the test */
 #define DIAG_RACE_FLIP 1     /* min over supported x != x1 of the flip index of the race */
@@ -131,6 +132,18 @@ typedef struct {
   int32_t *status;
   double *diag;
   const float *synthetic_rates; /* [max_spec_len] or NULL */
+  /* logits processors and stop tokens (per-request lists: request i owns
+   * entries [cu[i-1], cu[i]) of the ids array) */
+  const float *repetition_penalty; /* [N] theta, or NULL */
+  const int64_t *penalty_cu;
+  const int32_t *penalty_ids;
+  int64_t penalty_total;
+  const int64_t *banned_cu;
+  const int32_t *banned_ids;
+  int64_t banned_total;
+  const int64_t *stop_cu;
+  const int32_t *stop_ids;
+  int64_t stop_total;
 } oracle_args;
 
 /* ------------------------------------------------------------------------ */
@@ -369,6 +382,74 @@ static void race_diag(race_ctx *c, const float *w, const float *pa, const float 
   *relgap = rmin;
 }
 
+/* ------------------------------------------------------------------------
+ * Logits processors ("Speculative Decoding: propose, verify, accept", section
+ * 06: the same banned tokens and repetition penalty on p and q at a position;
+ * "vLLM source walk-through (10)", section "Rejection sampling: the two
+ * branches of RejectionSampler": processors such as penalties applied to the
+ * verified logits).  Readings: a banned token's logit becomes -inf; the
+ * repetition penalty (Keskar et al., CTRL, 2019) divides a positive logit by
+ * theta and multiplies a non-positive one by it, once per distinct token of
+ * the request's context list plus the drafts y_0 .. y_{j-1} already committed
+ * when position j is verified; the result is rounded to the input type (bf16
+ * round-to-nearest-even).  Ids outside [0, V) are ignored; a banned token is
+ * not penalised.
+ * ------------------------------------------------------------------------ */
+static int list_range(const int64_t *cu, int64_t total, int i, int64_t *b, int64_t *e) {
+  *b = i ? cu[i - 1] : 0;
+  *e = cu[i];
+  return *b >= 0 && *e >= *b && *e <= total;
+}
+
+static float round_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) {
+    u |= 0x00400000u; /* NaN stays NaN */
+  } else {
+    u += 0x7FFFu + ((u >> 16) & 1u); /* round half to even on the dropped 16 bits */
+  }
+  u &= 0xFFFF0000u;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+static int has_processors(const oracle_args *a) {
+  return a->entry == ORC_ENTRY_LOGITS && (a->banned_cu || (a->repetition_penalty && a->penalty_cu));
+}
+
+static void process_row(const oracle_args *a, int i, int64_t s, int j, float *row) {
+  if (!has_processors(a)) return;
+  const int V = a->vocab_size;
+  unsigned char *mark = calloc((size_t)V, 1); /* 1 banned, 2 penalised */
+  int64_t b, e;
+  if (a->banned_cu && list_range(a->banned_cu, a->banned_total, i, &b, &e))
+    for (int64_t k = b; k < e; ++k) {
+      int32_t x = a->banned_ids[k];
+      if (x >= 0 && x < V) mark[x] = 1;
+    }
+  if (a->repetition_penalty && a->penalty_cu && list_range(a->penalty_cu, a->penalty_total, i, &b, &e)) {
+    for (int64_t k = b; k < e; ++k) {
+      int32_t x = a->penalty_ids[k];
+      if (x >= 0 && x < V && !mark[x]) mark[x] = 2;
+    }
+    for (int k = 0; k < j; ++k) {
+      int32_t x = a->draft_ids[s + k];
+      if (x >= 0 && x < V && !mark[x]) mark[x] = 2;
+    }
+  }
+  const float theta = a->repetition_penalty ? a->repetition_penalty[i] : 1.0f;
+  for (int x = 0; x < V; ++x) {
+    if (mark[x] == 1) {
+      row[x] = -INFINITY;
+    } else if (mark[x] == 2) {
+      float v = row[x] > 0.0f ? row[x] / theta : row[x] * theta;
+      row[x] = a->dtype == ORC_BF16 ? round_to_bf16(v) : v;
+    }
+  }
+  free(mark);
+}
+
 static void emit_invalid(const oracle_args *a, int i) {
   int G = a->max_spec_len;
   for (int k = 0; k <= G; ++k) a->out_tokens[(int64_t)i * (G + 1) + k] = -1;
@@ -378,6 +459,21 @@ static void emit_invalid(const oracle_args *a, int i) {
 
 static void emit(const oracle_args *a, int i, int64_t s, int64_t tb, int g, int A, const int32_t *toks) {
   int G = a->max_spec_len;
+  /* stop tokens are checked on the committed prefix only, token by token
+   * ("Speculative Decoding: propose, verify, accept", sections 13-14): the
+   * commit ends at the first one, and the KV rollback follows the shorter
+   * commit (reading: A becomes that token's index) */
+  int64_t b, e;
+  if (a->stop_cu && list_range(a->stop_cu, a->stop_total, i, &b, &e)) {
+    for (int m = 0; m <= A; ++m) {
+      int hit = 0;
+      for (int64_t k = b; k < e && !hit; ++k) hit = toks[m] == a->stop_ids[k];
+      if (hit) {
+        A = m;
+        break;
+      }
+    }
+  }
   for (int k = 0; k <= G; ++k) a->out_tokens[(int64_t)i * (G + 1) + k] = (k <= A) ? toks[k] : -1;
   a->num_accepted[i] = A;
   /* KV rollback [P3 s3.1]: num_computed_tokens -= gamma_i - A when > 0 */
@@ -390,7 +486,7 @@ static void emit(const oracle_args *a, int i, int64_t s, int64_t tb, int g, int 
 
 /* fetch probability row j of the target (is_target) or draft side */
 static int prob_row(const oracle_args *a, int is_target, int64_t row, float T, int top_k, float top_p,
-                    float *tmp, float *out, int *edge) {
+                    float *tmp, float *out, int *edge, int i, int64_t s, int j) {
   const void *base = is_target ? a->target : a->draft;
   int64_t stride = is_target ? a->target_row_stride : a->draft_row_stride;
   if (a->entry == ORC_ENTRY_PROBS) {
@@ -398,6 +494,7 @@ static int prob_row(const oracle_args *a, int is_target, int64_t row, float T, i
     return 0;
   }
   load_row(base, a->dtype, row, stride, a->vocab_size, tmp);
+  process_row(a, i, s, j, tmp);
   int e = 0;
   int rc = oracle_logits_to_probs(tmp, a->vocab_size, T, top_k, top_p, out, &e);
   if (edge && e) *edge = 1;
@@ -440,12 +537,30 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
     return;
   }
 
+  {
+    int64_t b, e;
+    if ((a->penalty_cu && !list_range(a->penalty_cu, a->penalty_total, i, &b, &e)) ||
+        (a->banned_cu && !list_range(a->banned_cu, a->banned_total, i, &b, &e)) ||
+        (a->stop_cu && !list_range(a->stop_cu, a->stop_total, i, &b, &e))) {
+      *a->status |= ORC_BAD_LIST;
+      emit_invalid(a, i);
+      return;
+    }
+    if (a->repetition_penalty && a->entry == ORC_ENTRY_LOGITS &&
+        !(a->repetition_penalty[i] > 0.0f && !isinf(a->repetition_penalty[i]))) {
+      *a->status |= ORC_BAD_PARAM;
+      emit_invalid(a, i);
+      return;
+    }
+  }
+
   /* ---- greedy path (temperature 0) [P1 "Greedy kernel"; P2 s03] ---- */
   if (temp == 0.0f) {
     if (dg) dg[DIAG_PATH] = 1;
     for (int j = 0; j <= g; ++j) {
       load_row(a->target, a->entry == ORC_ENTRY_PROBS ? ORC_F32 : a->dtype, tb + j, a->target_row_stride, V,
                bufA);
+      process_row(a, i, s, j, bufA);
       int gj = argmax_row(bufA, V);
       if (gj < 0) {
         *a->status |= ORC_BAD_VALUES;
@@ -518,8 +633,8 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
       return;
     }
     float *p = bufA, *q = bufB;
-    int bad = prob_row(a, 1, tb + j, temp, top_k, top_p, bufC, p, &edge);
-    bad |= prob_row(a, 0, s + j, temp, top_k, top_p, bufD, q, &edge);
+    int bad = prob_row(a, 1, tb + j, temp, top_k, top_p, bufC, p, &edge, i, s, j);
+    bad |= prob_row(a, 0, s + j, temp, top_k, top_p, bufD, q, &edge, i, s, j);
     if (bad) {
       *a->status |= ORC_BAD_VALUES;
       emit_invalid(a, i);
@@ -570,7 +685,7 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
   }
   /* every draft accepted: bonus token from the last target row [P1; P2 s06] */
   float *p = bufA;
-  if (prob_row(a, 1, tb + g, temp, top_k, top_p, bufC, p, &edge)) {
+  if (prob_row(a, 1, tb + g, temp, top_k, top_p, bufC, p, &edge, i, s, g)) {
     *a->status |= ORC_BAD_VALUES;
     emit_invalid(a, i);
     return;
