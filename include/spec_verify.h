@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 3u
+#define SPEC_VERIFY_ABI_VERSION 4u
 #define SV_PLACEHOLDER_TOKEN_ID (-1)
 #define SV_PADDING_SLOT_ID (-1)
 #define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
@@ -77,8 +77,9 @@ enum sv_data_status {
   SV_DATA_BAD_VALUES = 16,        /* NaN (greedy) or NaN/+inf/no finite logit (random logits) in a read row */
   SV_DATA_BAD_PARAM = 32,         /* temperature < 0/NaN/inf, or top_p <= 0/NaN */
   SV_DATA_MISSING_DRAFT = 64,     /* draft == NULL but a random request needs draft rows */
-  SV_DATA_COPY_TIMEOUT = 128      /* a bulk row copy did not complete within its wait limit (request
+  SV_DATA_COPY_TIMEOUT = 128,     /* a bulk row copy did not complete within its wait limit (request
                                      emits nothing); never expected on a healthy GPU */
+  SV_DATA_BAD_LIST = 256          /* a penalty, banned or stop list range of the request is invalid */
 };
 
 typedef struct spec_verify_ctx *spec_verify_t;
@@ -148,6 +149,38 @@ typedef struct spec_verify_args {
    * draw there is the ordinary one, and dbg_py/dbg_qy are not written.  Rates
    * outside [0, 1] or increasing over a request's positions: SV_DATA_BAD_PARAM. */
   const float *synthetic_acceptance_rates;
+
+  /* Logits processors, logits entry only ("Speculative Decoding: propose,
+   * verify, accept", section 06: the same banned tokens and repetition penalty
+   * on p and q at a position; "vLLM source walk-through (10)", section
+   * "Rejection sampling: the two branches of RejectionSampler").  Lists are
+   * per request, like cu_num_draft_tokens: request i owns entries
+   * [cu[i-1], cu[i]) (cu[-1] = 0) of the id array; ids outside [0, V) are
+   * ignored and repeats count once.  A banned token's logit becomes -inf on
+   * every row of the request.  With repetition_penalty, every distinct token
+   * of the request's penalty list, plus the drafts y_0 .. y_{j-1} when
+   * position j is verified, has its logit l replaced by l / theta if l > 0,
+   * else l * theta (fp32 arithmetic, rounded to the logits' type), on the
+   * target and the draft row alike; banned tokens are not penalised.  Theta
+   * must be > 0 and finite (else SV_DATA_BAD_PARAM).  The probability entry
+   * rejects these fields (its rows are already transformed). */
+  const float *repetition_penalty;    /* [N] theta, or NULL: no penalty */
+  const int64_t *penalty_cu;          /* [N] or NULL */
+  const int32_t *penalty_token_ids;   /* [penalty_total] */
+  int64_t penalty_total;
+  const int64_t *banned_cu;           /* [N] or NULL */
+  const int32_t *banned_token_ids;    /* [banned_total] */
+  int64_t banned_total;
+
+  /* Stop tokens, both entries ("Speculative Decoding: propose, verify,
+   * accept", sections 13-14: stop rules are checked on the committed prefix
+   * only, token by token).  If a committed token c_m (m <= A) is in the
+   * request's stop list, the commit ends at the first such m: out row
+   * c_0 .. c_m, num_accepted = m, and the KV rollback follows (gamma_i - m
+   * tokens, slots of verify tokens m+1 .. gamma_i). */
+  const int64_t *stop_cu;             /* [N] or NULL */
+  const int32_t *stop_token_ids;      /* [stop_total] */
+  int64_t stop_total;
 } spec_verify_args;
 
 /* Draft-side sampler ("vLLM source walk-through (10)", section "propose()

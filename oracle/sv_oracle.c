@@ -415,7 +415,7 @@ static float round_to_bf16(float f) {
 }
 
 static int has_processors(const oracle_args *a) {
-  return a->entry == ORC_ENTRY_LOGITS && (a->banned_cu || (a->repetition_penalty && a->penalty_cu));
+  return a->entry == ORC_ENTRY_LOGITS && (a->banned_cu || a->repetition_penalty);
 }
 
 static void process_row(const oracle_args *a, int i, int64_t s, int j, float *row) {
@@ -428,11 +428,12 @@ static void process_row(const oracle_args *a, int i, int64_t s, int j, float *ro
       int32_t x = a->banned_ids[k];
       if (x >= 0 && x < V) mark[x] = 1;
     }
-  if (a->repetition_penalty && a->penalty_cu && list_range(a->penalty_cu, a->penalty_total, i, &b, &e)) {
-    for (int64_t k = b; k < e; ++k) {
-      int32_t x = a->penalty_ids[k];
-      if (x >= 0 && x < V && !mark[x]) mark[x] = 2;
-    }
+  if (a->repetition_penalty) {
+    if (a->penalty_cu && list_range(a->penalty_cu, a->penalty_total, i, &b, &e))
+      for (int64_t k = b; k < e; ++k) {
+        int32_t x = a->penalty_ids[k];
+        if (x >= 0 && x < V && !mark[x]) mark[x] = 2;
+      }
     for (int k = 0; k < j; ++k) {
       int32_t x = a->draft_ids[s + k];
       if (x >= 0 && x < V && !mark[x]) mark[x] = 2;

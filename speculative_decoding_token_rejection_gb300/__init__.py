@@ -54,6 +54,9 @@ class SpecVerifyArgs(ctypes.Structure):
         ("rng_request_base", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
         ("out_tokens", _P), ("num_accepted", _P), ("num_computed_tokens", _P), ("slot_mapping", _P),
         ("dbg_py", _P), ("dbg_qy", _P), ("status", _P), ("synthetic_acceptance_rates", _P),
+        ("repetition_penalty", _P), ("penalty_cu", _P), ("penalty_token_ids", _P), ("penalty_total", ctypes.c_int64),
+        ("banned_cu", _P), ("banned_token_ids", _P), ("banned_total", ctypes.c_int64),
+        ("stop_cu", _P), ("stop_token_ids", _P), ("stop_total", ctypes.c_int64),
     ]
 
 
@@ -216,8 +219,14 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
                temperature=None, top_k=None, top_p=None, uniforms=None, exponentials=None, seed: int = 0,
                offset: int = 0, rng_request_base: int = 0, num_computed_tokens=None, slot_mapping=None,
                dbg_py=None, dbg_qy=None, status=None, device=None,
-               host_rows: bool = False, synthetic_acceptance_rates=None) -> SpecVerifyArgs:
+               host_rows: bool = False, synthetic_acceptance_rates=None, repetition_penalty=None,
+               penalty_cu=None, penalty_token_ids=None, banned_cu=None, banned_token_ids=None, stop_cu=None,
+               stop_token_ids=None) -> SpecVerifyArgs:
     """Validate tensors and fill a SpecVerifyArgs (no device work).
+
+    Logits processors (logits entry) and stop tokens (both entries) come as
+    per-request lists: ``*_cu`` int64 [N] inclusive prefix sums into the
+    int32 ``*_token_ids``; ``repetition_penalty`` float32 [N].
 
     ``host_rows=True`` (probability entry only) lets ``target``/``draft``/
     ``exponentials`` live in pinned host memory: the kernel then pulls only
@@ -270,6 +279,14 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
     a.status = _ptr(status, torch.int32, "status", device, numel=1)
     a.synthetic_acceptance_rates = _ptr(synthetic_acceptance_rates, torch.float32, "synthetic_acceptance_rates",
                                         device, numel=G)
+    a.repetition_penalty = _ptr(repetition_penalty, torch.float32, "repetition_penalty", device, numel=N)
+    for name, cu_l, ids_l in (("penalty", penalty_cu, penalty_token_ids), ("banned", banned_cu, banned_token_ids),
+                              ("stop", stop_cu, stop_token_ids)):
+        setattr(a, f"{name}_cu", _ptr(cu_l, torch.int64, f"{name}_cu", device, numel=N))
+        has_ids = ids_l is not None and ids_l.numel() > 0
+        setattr(a, f"{name}_token_ids", _ptr(ids_l, torch.int32, f"{name}_token_ids", device, ndim=1)
+                if has_ids else None)
+        setattr(a, f"{name}_total", int(ids_l.numel()) if ids_l is not None else 0)
     return a
 
 

@@ -44,13 +44,15 @@ int choose_cluster(const spec_verify_ctx *ctx, int N, int V) {
   return c;
 }
 
-bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk) {
+bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk,
+                          bool bitmaps) {
   // Rows of the current position live in the cluster's shared memory (target
   // and draft chunk per CTA).  Prefer the CTA count of the probability entry,
   // grow it until the two row chunks fit in ~100 KB so two CTAs share an SM.
   auto chunk_for = [&](int c) { return ((V + c - 1) / c + 7) & ~7; };
   auto bytes_for = [&](int c) {
-    return 2LL * chunk_for(c) * elem_bytes + static_cast<long long>(logits_inbox_bytes(c));
+    return 2LL * chunk_for(c) * elem_bytes + static_cast<long long>(logits_inbox_bytes(c)) +
+           (bitmaps ? static_cast<long long>(logits_bitmap_bytes(chunk_for(c))) : 0LL);
   };
   int c = ctx->cfg.cluster_ctas > 0 ? ctx->cfg.cluster_ctas : choose_cluster(ctx, N, V);
   if (ctx->cfg.cluster_ctas == 0)
@@ -140,6 +142,21 @@ sv_status spec_verify_check_args(const spec_verify_config *c, const spec_verify_
   if (a->exponentials && a->exponentials_row_stride < a->vocab_size)
     return fail(SV_ERR_INVALID_ARG, "exponentials_row_stride < vocab_size");
   if (!a->out_tokens || !a->num_accepted) return fail(SV_ERR_INVALID_ARG, "out_tokens / num_accepted is NULL");
+  if (a->entry == SV_ENTRY_PROBS && (a->repetition_penalty || a->penalty_cu || a->banned_cu))
+    return fail(SV_ERR_INVALID_ARG, "logits processors apply to the logits entry (probability rows are transformed)");
+  struct {
+    const char *name;
+    const int64_t *cu;
+    const int32_t *ids;
+    int64_t total;
+  } lists[3] = {{"penalty", a->penalty_cu, a->penalty_token_ids, a->penalty_total},
+                {"banned", a->banned_cu, a->banned_token_ids, a->banned_total},
+                {"stop", a->stop_cu, a->stop_token_ids, a->stop_total}};
+  for (const auto &l : lists) {
+    if (!l.cu) continue;
+    if (l.total < 0) return fail(SV_ERR_INVALID_ARG, "%s_total < 0", l.name);
+    if (l.total > 0 && !l.ids) return fail(SV_ERR_INVALID_ARG, "%s_token_ids is NULL", l.name);
+  }
   return SV_OK;
 }
 
@@ -230,6 +247,16 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
   p.dbg_qy = a->dbg_qy;
   p.status = a->status;
   p.rates = a->synthetic_acceptance_rates;
+  p.rep_penalty = a->repetition_penalty;
+  p.pen_cu = a->penalty_cu;
+  p.pen_ids = a->penalty_token_ids;
+  p.pen_total = a->penalty_total;
+  p.ban_cu = a->banned_cu;
+  p.ban_ids = a->banned_token_ids;
+  p.ban_total = a->banned_total;
+  p.stop_cu = a->stop_cu;
+  p.stop_ids = a->stop_token_ids;
+  p.stop_total = a->stop_total;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (a->entry == SV_ENTRY_PROBS) {
@@ -242,7 +269,8 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
     const int eb = bf16 ? 2 : 4;
     const int per16 = 16 / eb;  // elements per 16-byte vector
     int cluster = 0, chunk = 0;
-    if (!sv::choose_logits_layout(h, p.N, p.V, eb, &cluster, &chunk))
+    const bool procs = a->repetition_penalty || a->banned_cu;
+    if (!sv::choose_logits_layout(h, p.N, p.V, eb, &cluster, &chunk, procs))
       return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for the rows to fit in the cluster's shared memory",
                   p.V);
     const bool vec = sv::aligned16(a->target) && (a->target_row_stride % per16 == 0) &&
@@ -303,7 +331,7 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   const bool bf16 = a->dtype == SV_BF16;
   const int eb = bf16 ? 2 : 4;
   int cluster = 0, chunk = 0;
-  if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk))
+  if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk, false))
     return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for a row to fit in the cluster's shared memory", p.V);
   const bool vec = sv::aligned16(a->logits) && (a->row_stride % (16 / eb) == 0);
   const cudaError_t e = sv::launch_sample(p, bf16, cluster, chunk, vec, static_cast<cudaStream_t>(stream));

@@ -215,6 +215,34 @@ namespace sv {
 // output [batch, max_spec_len + 1] padded with -1; "How speculative decoding
 // interacts with the KV cache" 3.1: num_computed_tokens -= gamma - A when > 0;
 // rejected drafts' slots -> PADDING_SLOT_ID.)
+// Stop tokens checked on the committed prefix only ("Speculative Decoding:
+// propose, verify, accept", sections 13-14): the commit c_0 .. c_A ends at
+// the first c_m in the request's stop list [b, e).  Called by every thread of
+// the emitting CTA; returns the new A.  *first is one shared-memory word.
+template <typename TokFn>
+__device__ __forceinline__ int stop_commit(int A, TokFn tok, const int32_t *ids, int64_t b, int64_t e, int *first) {
+  if (threadIdx.x == 0) *first = A;
+  __syncthreads();
+  for (int m = threadIdx.x; m <= A; m += kThreads) {
+    const int32_t t = tok(m);
+    for (int64_t k = b; k < e; ++k)
+      if (ids[k] == t) {
+        atomicMin(first, m);
+        break;
+      }
+  }
+  __syncthreads();
+  return *first;
+}
+
+// A per-request list range [b, e) (inclusive prefix sums, like
+// cu_num_draft_tokens); false if it is not inside [0, total].
+__device__ __forceinline__ bool list_range(const int64_t *cu, int64_t total, int i, int64_t &b, int64_t &e) {
+  b = i ? cu[i - 1] : 0;
+  e = cu[i];
+  return b >= 0 && e >= b && e <= total;
+}
+
 template <typename TokFn>
 __device__ __forceinline__ void emit_request(int i, int G, int g, int A, bool valid, int64_t tb, uint32_t req_bits,
                                              TokFn tok, int32_t *out, int32_t *nacc, int32_t *ncomp,

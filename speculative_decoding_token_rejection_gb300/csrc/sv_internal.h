@@ -41,6 +41,17 @@ struct VerifyParams {
   float *dbg_qy;
   int32_t *status;
   const float *rates;  // synthetic acceptance rates [G] or nullptr
+  // logits processors and stop tokens (per-request lists, inclusive prefix sums)
+  const float *rep_penalty;
+  const int64_t *pen_cu;
+  const int32_t *pen_ids;
+  int64_t pen_total;
+  const int64_t *ban_cu;
+  const int32_t *ban_ids;
+  int64_t ban_total;
+  const int64_t *stop_cu;
+  const int32_t *stop_ids;
+  int64_t stop_total;
 };
 
 // The draft-side sampler's parameters (device pointers, sizes).
@@ -87,10 +98,13 @@ cudaError_t enable_sample_kernels(int max_cluster, int max_dyn);
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
+// Dynamic shared memory of the processor bitmaps (banned and penalised keys of a chunk).
+size_t logits_bitmap_bytes(int chunk);
 
 // Cluster size and per-CTA row chunk (elements, a multiple of 8) for the
 // logits entry; returns false if no cluster size fits the rows in shared memory.
-bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk);
+bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk,
+                          bool bitmaps);
 
 void set_last_error(const char *fmt, ...);
 

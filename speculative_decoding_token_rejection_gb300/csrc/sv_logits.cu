@@ -206,6 +206,8 @@ struct LogitsSmem {
   unsigned long long wt[2][kWarps];
   Select sel;
   uint64_t bar;
+  int stop_first;      // first committed stop token
+  uint32_t yproc[2];   // processed logits of the draft token (target, draft row), from its owner
   int32_t tok[SV_MAX_SPEC_LEN + 1];
 };
 
@@ -680,7 +682,8 @@ __device__ __forceinline__ bool near_select(const unsigned long long *cnt, const
 template <typename TIn>
 __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], int nr, int n, float c2, int topk,
                                float topp, uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step,
-                               uint32_t ncta, uint32_t rank) {
+                               uint32_t ncta, uint32_t rank, uint32_t ybits0 = 0u, uint32_t ybits1 = 0u,
+                               int y_owner = -1) {
   using E = Elem<TIn>;
   constexpr int kB = E::kBits;
   const int tid = threadIdx.x;
@@ -948,7 +951,7 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       if (wd == 0) {
         v = make_uint4(lp.maxkey[0], lp.maxkey[1], lp.flags[0], lp.flags[1]);
       } else if (wd == 1) {
-        v = make_uint4(__float_as_uint(lp.z[0]), __float_as_uint(lp.z[1]), 0u, 0u);
+        v = make_uint4(__float_as_uint(lp.z[0]), __float_as_uint(lp.z[1]), ybits0, ybits1);
       } else if (wd == 2) {
         v = make_uint4(static_cast<uint32_t>(lp.tot[0]), static_cast<uint32_t>(lp.tot[0] >> 32),
                        static_cast<uint32_t>(lp.tot[1]), static_cast<uint32_t>(lp.tot[1] >> 32));
@@ -1011,6 +1014,10 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       ns.z[r] = z;
       ns.tot[r] = tot;
     }
+  }
+  if (tid == 0 && y_owner >= 0) {  // the draft token's processed logits travel in its owner's header
+    sm.yproc[0] = ibx[y_owner].pad[0];
+    sm.yproc[1] = ibx[y_owner].pad[1];
   }
   __syncthreads();
 
@@ -1206,6 +1213,58 @@ __device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *con
   return flags;
 }
 
+// ---------------------------------------------------------------------------
+// logits processors on the rows in shared memory ("Speculative Decoding:
+// propose, verify, accept", section 06: the same banned tokens and repetition
+// penalty on the target and draft rows of a position).  Two bitmaps over this
+// CTA's chunk mark banned and penalised keys; after every row copy the marked
+// entries are rewritten: banned -> -inf, penalised -> l / theta if l > 0 else
+// l * theta (fp32, rounded to the row's type; Keskar et al., CTRL, 2019).
+// ---------------------------------------------------------------------------
+template <typename TIn>
+__device__ __forceinline__ void store_processed(TIn *row, int x, bool banned, float theta) {
+  using E = Elem<TIn>;
+  const float v = E::val(bits_at(row, x));
+  const float f = banned ? -INFINITY : (v > 0.0f ? __fdiv_rn(v, theta) : __fmul_rn(v, theta));
+  if constexpr (sizeof(TIn) == 2) {
+    row[x] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  } else {
+    row[x] = f;
+  }
+}
+
+template <typename TIn>
+__device__ __forceinline__ void apply_processors(TIn *const srow[2], int nr, int n, const uint32_t *pen,
+                                                 const uint32_t *ban, int words, float theta) {
+  for (int w = threadIdx.x; w < words; w += kThreads) {
+    uint32_t bits = pen[w] | ban[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int x = 32 * w + b;
+      if (x >= n) break;
+      const bool banned = (ban[w] >> b) & 1u;
+      for (int r = 0; r < nr; ++r) store_processed(srow[r], x, banned, theta);
+    }
+  }
+  __syncthreads();
+}
+
+// Greedy with processors: thread-local argmax of a row chunk in shared memory.
+template <typename TIn>
+__device__ __forceinline__ void argmax_smem(const TIn *row, int x0, int n, unsigned long long &best,
+                                            uint32_t &flags) {
+  using E = Elem<TIn>;
+  for_each_elem(row, n, [&](uint32_t b, int x) {
+    if (E::is_nan(b)) {
+      flags |= SV_DATA_BAD_VALUES;
+      return;
+    }
+    best = umax64(best, (static_cast<unsigned long long>(E::key(b)) << 32) |
+                            static_cast<unsigned long long>(~static_cast<uint32_t>(x0 + x)));
+  });
+}
+
 // Greedy: thread-local argmax of raw logits of a global row chunk.
 template <typename TIn, bool kVec>
 __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsigned long long &best, uint32_t &flags) {
@@ -1256,6 +1315,10 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
 
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int i = static_cast<int>(blockIdx.x / ncta);
+  // processor bitmaps (present only when the call has processors)
+  const int words = (chunk + 31) / 32;
+  uint32_t *const pen_bits = reinterpret_cast<uint32_t *>(inbox + 2 * ncta);
+  uint32_t *const ban_bits = pen_bits + words;
   const int tid = threadIdx.x;
   const int G = P.G, V = P.V;
   const TIn *tgt = static_cast<const TIn *>(P.target);
@@ -1286,11 +1349,28 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
     req_bits |= SV_DATA_BAD_PARAM;
     valid = false;
   }
+  int64_t pen_b = 0, pen_e = 0, ban_b = 0, ban_e = 0, stop_b = 0, stop_e = 0;
+  if (valid && ((P.pen_cu && !list_range(P.pen_cu, P.pen_total, i, pen_b, pen_e)) ||
+                (P.ban_cu && !list_range(P.ban_cu, P.ban_total, i, ban_b, ban_e)) ||
+                (P.stop_cu && !list_range(P.stop_cu, P.stop_total, i, stop_b, stop_e)))) {
+    req_bits |= SV_DATA_BAD_LIST;
+    valid = false;
+  }
+  float theta = 1.0f;
+  if (valid && P.rep_penalty) {
+    theta = P.rep_penalty[i];
+    if (!(theta > 0.0f) || isinf(theta)) {
+      req_bits |= SV_DATA_BAD_PARAM;
+      valid = false;
+    }
+  }
+  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
   const bool greedy = valid && temp == 0.0f;
   int A = 0;
   int32_t last_tok = -1;
   int step = 0;
   uint32_t phase = 0;
+  int added = 0;  // drafts already in the penalty bitmap
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     fence_mbar_init();
@@ -1306,15 +1386,42 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
     joined = true;
   };
 
+  auto mark = [&](uint32_t *bm, int32_t x) {
+    if (x >= x0 && x < x0 + n) atomicOr(&bm[(x - x0) >> 5], 1u << ((x - x0) & 31));
+  };
+  if (valid && procs) {  // this chunk's banned and penalised keys
+    for (int w = tid; w < 2 * words; w += kThreads) pen_bits[w] = 0u;
+    __syncthreads();
+    if (P.ban_cu)
+      for (int64_t k = ban_b + tid; k < ban_e; k += kThreads) mark(ban_bits, P.ban_ids[k]);
+    if (P.rep_penalty && P.pen_cu)
+      for (int64_t k = pen_b + tid; k < pen_e; k += kThreads) mark(pen_bits, P.pen_ids[k]);
+    __syncthreads();
+  }
+  // position j penalises the drafts y_0 .. y_{j-1} too (they are committed by then)
+  auto add_drafts = [&](int j) {
+    if (P.rep_penalty)
+      for (; added < j; ++added)
+        if (tid == 0) mark(pen_bits, P.ids[s + added]);
+  };
+
   if (greedy) {
     join();
     for (int j = 0;; ++j) {
       unsigned long long best = 0;
       uint32_t fl = 0;
-      argmax_logits<TIn, kVec>(tgt + (tb + j) * ts + x0, x0, n, best, fl);
+      if (procs) {  // the row goes through shared memory to be processed
+        add_drafts(j);
+        const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nullptr};
+        if (load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase) & kFlagTimeout) fl |= SV_DATA_COPY_TIMEOUT;
+        apply_processors(srow, 1, n, pen_bits, ban_bits, words, theta);
+        argmax_smem(srow[0], x0, n, best, fl);
+      } else {
+        argmax_logits<TIn, kVec>(tgt + (tb + j) * ts + x0, x0, n, best, fl);
+      }
       const KeyFlags r = cluster_reduce(KeyFlags{best, fl}, sm.red, step++, ncta);
-      if (r.flags & SV_DATA_BAD_VALUES) {
-        req_bits |= SV_DATA_BAD_VALUES;
+      if (r.flags & (SV_DATA_BAD_VALUES | SV_DATA_COPY_TIMEOUT)) {
+        req_bits |= r.flags & (SV_DATA_BAD_VALUES | SV_DATA_COPY_TIMEOUT);
         valid = false;
         break;
       }
@@ -1395,9 +1502,23 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
           u = kTest ? P.uniforms[s + j] : draw_uniform(rk, rs, static_cast<uint32_t>(j));
         }
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
+        if (procs) add_drafts(j);
         const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, nr, n, phase);
         join();
-        if (!position_stats<TIn>(sm, inbox, srow, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta, rank)) {
+        int y_owner = -1;
+        uint32_t yb0 = 0u, yb1 = 0u;
+        if (procs) {
+          apply_processors(srow, nr, n, pen_bits, ban_bits, words, theta);
+          if (j < g && y >= 0 && y < V) {  // the CTA holding y publishes its processed logits
+            y_owner = y / chunk;
+            if (static_cast<int>(rank) == y_owner) {
+              yb0 = bits_at(srow[0], y - x0);
+              yb1 = bits_at(srow[1], y - x0);
+            }
+          }
+        }
+        if (!position_stats<TIn>(sm, inbox, srow, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta, rank, yb0,
+                                 yb1, y_owner)) {
           req_bits |= SV_DATA_BAD_VALUES;
           valid = false;
           break;
@@ -1411,6 +1532,10 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
             req_bits |= SV_DATA_BAD_DRAFT_ID;
             valid = false;
             break;
+          }
+          if (procs) {
+            bty = sm.yproc[0];
+            bdy = sm.yproc[1];
           }
           const float py = prob_of<TIn>(bty, st[0]);
           const float qy = prob_of<TIn>(bdy, st[1]);
@@ -1452,7 +1577,9 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
   join();
   __syncthreads();
   if (rank == 0) {
-    auto tok = [&](int k) -> int32_t { return (k == A && !greedy) ? last_tok : sm.tok[k]; };
+    const int A0 = A;
+    auto tok = [&](int k) -> int32_t { return (k == A0 && !greedy) ? last_tok : sm.tok[k]; };
+    if (valid && P.stop_cu) A = stop_commit(A0, tok, P.stop_ids, stop_b, stop_e, &sm.stop_first);
     emit_request(i, G, g, A, valid, tb, req_bits, tok, P.out, P.nacc, P.ncomp, P.slots, P.status);
   }
   cluster_sync();
@@ -1601,6 +1728,7 @@ cudaError_t enable_one(int max_cluster, int max_dyn) {
 
 size_t logits_static_smem() { return sizeof(LogitsSmem); }
 size_t logits_inbox_bytes(int cluster) { return 2 * static_cast<size_t>(cluster) * sizeof(Inbox); }
+size_t logits_bitmap_bytes(int chunk) { return ((2 * static_cast<size_t>((chunk + 31) / 32) * 4) + 15) & ~size_t{15}; }
 
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn) {
   cudaError_t e;
@@ -1643,7 +1771,8 @@ cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chu
 
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
   const bool test = p.exponentials != nullptr;
-  const size_t dyn = 2 * static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster);
+  const size_t dyn = 2 * static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster) +
+                     ((p.rep_penalty || p.ban_cu) ? logits_bitmap_bytes(chunk) : 0);
   if (bf16) {
     if (test) return vec ? launch_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
                          : launch_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);

@@ -40,6 +40,7 @@ struct ProbsSmem {
   int stop;       // first position whose test stops the scan (gamma_i if none)
   int stop_bad;   // that position has an invalid draft id
   int bad_rates;  // synthetic rates outside [0, 1] or increasing
+  int stop_first; // first committed stop token
   int32_t tok[SV_MAX_SPEC_LEN + 1];
 };
 
@@ -188,7 +189,7 @@ __device__ __forceinline__ void argmax_chunk(const float *row, int x0, int x1, u
 }
 
 template <bool kTest, bool kVec>
-__global__ void __launch_bounds__(kThreads) probs_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(kThreads, 4) probs_kernel(const VerifyParams P) {
   __shared__ ProbsSmem sm;
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int i = static_cast<int>(blockIdx.x / ncta);
@@ -218,6 +219,11 @@ __global__ void __launch_bounds__(kThreads) probs_kernel(const VerifyParams P) {
   const float temp = P.temperature ? P.temperature[i] : 1.0f;
   if (valid && (!(temp >= 0.0f) || isinf(temp))) {
     req_bits |= SV_DATA_BAD_PARAM;
+    valid = false;
+  }
+  int64_t stop_b = 0, stop_e = 0;
+  if (valid && P.stop_cu && !list_range(P.stop_cu, P.stop_total, i, stop_b, stop_e)) {
+    req_bits |= SV_DATA_BAD_LIST;
     valid = false;
   }
   const bool greedy = valid && temp == 0.0f;
@@ -341,7 +347,9 @@ __global__ void __launch_bounds__(kThreads) probs_kernel(const VerifyParams P) {
 
   // a6 / a7: outputs and KV rollback, written by the cluster's first CTA
   if (rank == 0) {
-    auto tok = [&](int k) -> int32_t { return greedy ? sm.tok[k] : (k == A ? last_tok : P.ids[s + k]); };
+    const int A0 = A;
+    auto tok = [&](int k) -> int32_t { return greedy ? sm.tok[k] : (k == A0 ? last_tok : P.ids[s + k]); };
+    if (valid && P.stop_cu) A = stop_commit(A0, tok, P.stop_ids, stop_b, stop_e, &sm.stop_first);
     emit_request(i, G, g, A, valid, tb, req_bits, tok, P.out, P.nacc, P.ncomp, P.slots, P.status);
   }
   cluster_sync();  // peers may still be reading this CTA's reduction slot

@@ -16,6 +16,19 @@ def verifier(cluster_ctas=0):
     return _VERIFIERS[cluster_ctas]
 
 
+def processor_args(w, dev):
+    """Logits processors and stop tokens of a workload dict (optional keys, the
+    names the oracle reads) as binding keyword arguments."""
+    out = {}
+    if w.get("repetition_penalty") is not None:
+        out["repetition_penalty"] = torch.as_tensor(np.asarray(w["repetition_penalty"], np.float32)).to(dev)
+    for name, kw in (("penalty", "penalty"), ("banned", "banned"), ("stop", "stop")):
+        if w.get(f"{name}_cu") is not None:
+            out[f"{kw}_cu"] = torch.as_tensor(np.asarray(w[f"{name}_cu"], np.int64)).to(dev)
+            out[f"{kw}_token_ids"] = torch.as_tensor(np.asarray(w[f"{name}_ids"], np.int32)).to(dev)
+    return out
+
+
 def run_gpu(w, *, production=False, seed=0, offset=0, rng_request_base=0, cluster_ctas=0, stream=None,
             synthetic_rates=None):
     """Run the CUDA path on workload ``w``; returns numpy results like oracle.verify."""
@@ -39,7 +52,7 @@ def run_gpu(w, *, production=False, seed=0, offset=0, rng_request_base=0, cluste
         seed=seed, offset=offset, rng_request_base=rng_request_base, out_tokens=out, num_accepted=nacc,
         num_computed_tokens=ncomp, slot_mapping=slots, dbg_py=dpy, dbg_qy=dqy, status=status,
         synthetic_acceptance_rates=None if synthetic_rates is None else
-        torch.as_tensor(np.asarray(synthetic_rates, np.float32)).to(dev))
+        torch.as_tensor(np.asarray(synthetic_rates, np.float32)).to(dev), **processor_args(w, dev))
     torch.cuda.synchronize()
     cpu = lambda x: None if x is None else x.cpu().numpy()
     return dict(out_tokens=cpu(out), num_accepted=cpu(nacc), num_computed_tokens=cpu(ncomp),

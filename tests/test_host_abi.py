@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_description(lib):
-    assert lib.spec_verify_abi_version() == 3
+    assert lib.spec_verify_abi_version() == 4
     assert lib.spec_verify_sizeof_args() == ctypes.sizeof(sv.SpecVerifyArgs)
     assert lib.spec_verify_sizeof_config() == ctypes.sizeof(sv.SpecVerifyConfig)
 
@@ -98,6 +98,20 @@ def cfg(**kw):
      sv.SV_ERR_INVALID_ARG),  # T > N*G
     (lambda a: (setattr(a, "num_reqs", 0), setattr(a, "num_draft_tokens_total", 0),
                 setattr(a, "target", None)), sv.SV_OK),  # empty batch: no pointers needed
+    # processors belong to the logits entry; stop tokens to both
+    (lambda a: setattr(a, "repetition_penalty", FAKE), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "banned_cu", FAKE), sv.SV_ERR_INVALID_ARG),
+    (lambda a: (setattr(a, "entry", sv.SV_ENTRY_LOGITS), setattr(a, "repetition_penalty", FAKE),
+                setattr(a, "penalty_cu", FAKE), setattr(a, "penalty_token_ids", FAKE),
+                setattr(a, "penalty_total", 3)), sv.SV_OK),
+    (lambda a: (setattr(a, "entry", sv.SV_ENTRY_LOGITS), setattr(a, "banned_cu", FAKE),
+                setattr(a, "banned_total", 3)), sv.SV_ERR_INVALID_ARG),  # ids missing
+    (lambda a: (setattr(a, "entry", sv.SV_ENTRY_LOGITS), setattr(a, "banned_cu", FAKE),
+                setattr(a, "banned_total", 0)), sv.SV_OK),  # empty lists need no ids
+    (lambda a: (setattr(a, "stop_cu", FAKE), setattr(a, "stop_token_ids", FAKE), setattr(a, "stop_total", 2)),
+     sv.SV_OK),
+    (lambda a: (setattr(a, "stop_cu", FAKE), setattr(a, "stop_token_ids", FAKE), setattr(a, "stop_total", -1)),
+     sv.SV_ERR_INVALID_ARG),
 ])
 def test_check_args(lib, mutate, code):
     a = good_args()

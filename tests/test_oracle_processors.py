@@ -49,6 +49,16 @@ def test_golden_g1_commit_length():
     assert o["num_accepted"][0] == 1 and list(o["out_tokens"][0]) == [1, 0, -1]
 
 
+def test_penalty_without_context_list():
+    """g1's rows with theta 2 and no context list: position 0 is unprocessed
+    ([2.0 1.5 -1.0] -> argmax 0 != y0 = 1)... so take y0 = 0: accepted, then
+    position 1 penalises y0: [1.0 1.5 -1.0] -> argmax 1."""
+    g = load_golden("processors_examples.txt")
+    rows = _rows(g["g1_rows"])
+    o = _greedy(rows, [0, 0], repetition_penalty=np.array([2.0], np.float32))
+    assert o["num_accepted"][0] == 1 and list(o["out_tokens"][0, :2]) == [0, 1]
+
+
 def test_stop_token_truncates_commit_and_rollback():
     g = load_golden("processors_examples.txt")
     drafts = [int(x) for x in g["g4_drafts"]]
@@ -131,12 +141,15 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
     import ctypes  # noqa: F401
     import subprocess
     src = oracle_mod._SRC.read_text()
-    tests = (test_greedy_golden_cases, test_golden_g1_commit_length, test_stop_token_truncates_commit_and_rollback,
+    tests = (test_greedy_golden_cases, test_golden_g1_commit_length, test_penalty_without_context_list,
+             test_stop_token_truncates_commit_and_rollback,
              test_identical_processing_of_target_and_draft, test_bf16_rounding_of_penalised_logits)
     mutants = {
         "drafts not in the set": ("for (int k = 0; k < j; ++k) {", "for (int k = 0; k < j - 1; ++k) {"),
-        "penalty overrides ban": ("      if (x >= 0 && x < V && !mark[x]) mark[x] = 2;\n    }\n    for (int k = 0; k < j",
-                                  "      if (x >= 0 && x < V) mark[x] = 2;\n    }\n    for (int k = 0; k < j"),
+        "penalty overrides ban": ("        if (x >= 0 && x < V && !mark[x]) mark[x] = 2;\n      }\n    for (int k = 0; k < j",
+                                  "        if (x >= 0 && x < V) mark[x] = 2;\n      }\n    for (int k = 0; k < j"),
+        "drafts only with a context list": ("  if (a->repetition_penalty) {\n    if (a->penalty_cu",
+                                            "  if (a->repetition_penalty && a->penalty_cu) {\n    if (a->penalty_cu"),
         "no bf16 rounding": ("row[x] = a->dtype == ORC_BF16 ? round_to_bf16(v) : v;", "row[x] = v;"),
         "stop off by one": ("        A = m;\n        break;", "        A = m > 0 ? m - 1 : 0;\n        break;"),
         "draft side unprocessed": ("load_row(base, a->dtype, row, stride, a->vocab_size, tmp);\n  process_row(a, i, s, j, tmp);",
