@@ -74,21 +74,24 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s earlier GB300 copy measurement)"
 
 
-def kernel_source_hash() -> str:
+LOGITS_KERNEL_SOURCES = ["sv_logits.cu", "sv_device.cuh"]
+
+
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for n in KERNEL_SOURCES:
+    for n in (sources or KERNEL_SOURCES):
         h.update((ROOT / "speculative_decoding_token_rejection_gb300" / "csrc" / n).read_bytes())
     return h.hexdigest()[:16]
 
 
-def stored_traffic():
+def stored_traffic(name="verify_probs_fused_probs", sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
-    p = ROOT / "profiles" / "verify_probs_fused_probs.traffic.json"
+    p = ROOT / "profiles" / f"{name}.traffic.json"
     if not p.exists():
         return None, None
     d = json.loads(p.read_text())
-    if d.get("kernel_source_sha") != kernel_source_hash():
+    if d.get("kernel_source_sha") != kernel_source_hash(sources):
         return None, d.get("kernel_source_sha")
     return d.get("dram_bytes_per_launch"), d.get("kernel_source_sha")
 
@@ -238,14 +241,17 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
     ms = total_ms / K
     peak, src = measured_peak()
     full = (2 * T + N) * V * 2
+    traffic, traffic_sha = stored_traffic("verify_logits_fused", LOGITS_KERNEL_SOURCES)
     ver.close()
     return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
             "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k 50, top-p 0.9, "
                                    "production Philox", "entry": "logits"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
-                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
                          "algorithmic_bytes_per_launch": alg, "full_tensor_bytes": full,
-                         "full_tensor_frac": full / (ms / 1e3) / 1e9 / peak},
+                         "full_tensor_frac": full / (ms / 1e3) / 1e9 / peak,
+                         "kernel_source_sha": kernel_source_hash(LOGITS_KERNEL_SOURCES),
+                         "traffic_source_sha": traffic_sha},
             "acceptance": {"mean_accepted": float(na.mean()),
                            "A_hist": np.bincount(na.reshape(-1), minlength=G + 1).tolist()},
             "gpu_launches": K}
