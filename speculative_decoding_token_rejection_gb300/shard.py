@@ -8,7 +8,9 @@ request index, so production-mode draws -- keyed by the global request index
 -- are the same whichever way the batch is split.
 
 Works on dicts of numpy arrays or torch tensors with the keys used by
-``workloads.make`` (host bookkeeping only; no verifier arithmetic).
+``workloads.make`` plus the optional per-request processor and stop lists
+(host bookkeeping only; no verifier arithmetic).  The n-gram proposer's
+histories split the same way (``shard_histories``).
 """
 from __future__ import annotations
 
@@ -57,4 +59,26 @@ def shard_workload(w: dict, rank: int, world: int) -> dict:
         out["exponentials"] = w["exponentials"][r0:r1]
     if w.get("slot_mapping") is not None:
         out["slot_mapping"] = w["slot_mapping"][t0:t1]
+    if w.get("repetition_penalty") is not None:
+        out["repetition_penalty"] = w["repetition_penalty"][r0:r1]
+    for name in ("penalty", "banned", "stop"):  # per-request id lists, inclusive prefix sums
+        if w.get(f"{name}_cu") is not None:
+            out[f"{name}_cu"], out[f"{name}_ids"] = _shard_list(w[f"{name}_cu"], w[f"{name}_ids"], r0, r1)
     return out
+
+
+def _shard_list(cu, ids, r0: int, r1: int):
+    """Entries of requests [r0, r1) of a per-request list (inclusive prefix
+    sums ``cu`` into ``ids``), with ``cu`` re-based."""
+    b = int(cu[r0 - 1]) if r0 > 0 else 0
+    e = int(cu[r1 - 1]) if r1 > r0 else b
+    return cu[r0:r1] - b, ids[b:e]
+
+
+def shard_histories(tokens, cu_num_tokens, rank: int, world: int):
+    """The n-gram proposer's batch of ``rank``: its contiguous range of
+    request histories with ``cu_num_tokens`` re-based.  Returns (tokens, cu,
+    (r0, r1))."""
+    r0, r1 = shard_bounds(len(cu_num_tokens), rank, world)
+    c, t = _shard_list(cu_num_tokens, tokens, r0, r1)
+    return t, c, (r0, r1)

@@ -25,6 +25,23 @@ def _free_port():
     return p
 
 
+def _with_lists(w):
+    """Processor and stop lists on a workload (deterministic, per request)."""
+    rng = np.random.default_rng(11)
+    N, V = w["N"], w["V"]
+    for name, n in (("penalty", 30), ("banned", 5), ("stop", 2)):
+        lens = rng.integers(0, n, size=N)
+        w[f"{name}_cu"] = np.cumsum(lens).astype(np.int64)
+        w[f"{name}_ids"] = rng.integers(0, V, size=int(lens.sum())).astype(np.int32)
+    if w["entry"] != "logits":
+        for name in ("penalty", "banned"):
+            w.pop(f"{name}_cu")
+            w.pop(f"{name}_ids")
+    else:
+        w["repetition_penalty"] = rng.uniform(0.8, 1.6, size=N).astype(np.float32)
+    return w
+
+
 def _worker(rank, world, port, name, kw, q):
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -33,7 +50,10 @@ def _worker(rank, world, port, name, kw, q):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
+        lists = kw.pop("lists", False)
         w = workloads.make(name, test_mode=False, **kw)
+        if lists:
+            w = _with_lists(w)
         sh = shard_workload(w, rank, world)
         r = oracle.verify(sh, production=True, seed=5, offset=3, rng_request_base=sh["rng_request_base"],
                           with_diag=False)
@@ -52,7 +72,8 @@ def _worker(rank, world, port, name, kw, q):
 
 
 @pytest.mark.parametrize("name,kw", [("random", dict(N=9, V=3000)), ("ragged", dict(N=13, V=2000)),
-                                     ("fused", dict(N=6, V=4096))])
+                                     ("fused", dict(N=6, V=4096)), ("fused", dict(N=7, V=4096, lists=True)),
+                                     ("random", dict(N=9, V=3000, lists=True))])
 def test_two_rank_shards_equal_unsharded(name, kw):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
@@ -73,3 +94,40 @@ def test_shard_bounds_cover_the_batch():
             assert spans[0][0] == 0 and spans[-1][1] == n
             assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
             assert max(b - a for a, b in spans) - min(b - a for a, b in spans) <= 1
+
+
+def _ngram_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import oracle
+    import workloads
+    from speculative_decoding_token_rejection_gb300.shard import shard_histories
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        tokens, cu = workloads.make_histories(11, min_len=20, max_len=300, vocab=7, seed=4)
+        t, c, _ = shard_histories(tokens, cu, rank, world)
+        r = oracle.ngram_propose(t, c, min_ngram=2, max_ngram=4, k=5, max_model_len=1000)
+        gathered = [None] * world
+        dist.all_gather_object(gathered, r)
+        if rank == 0:
+            full = oracle.ngram_propose(tokens, cu, min_ngram=2, max_ngram=4, k=5, max_model_len=1000)
+            ok = all(np.array_equal(np.concatenate([g[k] for g in gathered]), full[k])
+                     for k in ("draft_token_ids", "num_draft_tokens"))
+            q.put(ok and (full["num_draft_tokens"] > 0).any())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_ngram_shards_equal_unsharded():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ngram_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    ok = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert ok
