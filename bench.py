@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--logits-steps", type=int, default=300)
     ap.add_argument("--no-logits", action="store_true")
     ap.add_argument("--ngram-steps", type=int, default=200)
+    ap.add_argument("--logits-resident", action="store_true",
+                    help="keep both row chunks of the logits entry in shared memory (comparison runs)")
     ap.add_argument("--no-ngram", action="store_true")
     return ap.parse_args()
 
@@ -199,7 +201,8 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
     N, G, V, T = w["N"], w["gamma"], w["V"], w["T"]
     gam = workloads.gammas_of(w)
     t = workloads.as_torch(w, dev)
-    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster)
+    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster,
+                      flags=sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0)
     K = max(3, min(args.steps, args.logits_steps))
     W = args.warmup
     nacc = torch.empty((K + W, N), dtype=torch.int32, device=dev)
@@ -245,7 +248,8 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
     ver.close()
     return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
             "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k 50, top-p 0.9, "
-                                   "production Philox", "entry": "logits"},
+                                   "production Philox", "entry": "logits",
+                       "draft_rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
                          "algorithmic_bytes_per_launch": alg, "full_tensor_bytes": full,

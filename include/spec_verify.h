@@ -82,6 +82,13 @@ enum sv_data_status {
   SV_DATA_BAD_LIST = 256          /* a penalty, banned or stop list range of the request is invalid */
 };
 
+/* Handle flags.  SV_FLAG_RESIDENT_ROWS: the logits entry keeps both the target
+ * and the draft row chunk of a position in shared memory (two CTAs per SM).
+ * By default only the target chunk is copied and the draft chunk is read in
+ * place after an L2 prefetch (three CTAs per SM); calls with logits
+ * processors or unaligned rows always keep both.  Results are identical. */
+#define SV_FLAG_RESIDENT_ROWS 1u
+
 typedef struct spec_verify_ctx *spec_verify_t;
 
 /* Limits fixed at creation. */
@@ -91,7 +98,7 @@ typedef struct spec_verify_config {
   int32_t vocab_size;   /* largest vocab_size of any call (>= 1) */
   int32_t device;       /* CUDA device ordinal the handle's calls run on */
   int32_t cluster_ctas; /* CTAs cooperating on one request: 0 = automatic, else 1, 2, 4, 8 or 16 */
-  uint32_t flags;       /* reserved, must be 0 */
+  uint32_t flags;       /* 0, or SV_FLAG_RESIDENT_ROWS */
 } spec_verify_config;
 
 /* One verification call.  N = num_reqs, G = max_spec_len, V = vocab_size,

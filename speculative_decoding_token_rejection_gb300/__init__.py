@@ -34,6 +34,9 @@ DATA_STATUS_BITS = {
 _P = ctypes.c_void_p
 
 
+SV_FLAG_RESIDENT_ROWS = 1
+
+
 class SpecVerifyConfig(ctypes.Structure):
     _fields_ = [("max_num_reqs", ctypes.c_int32), ("max_spec_len", ctypes.c_int32),
                 ("vocab_size", ctypes.c_int32), ("device", ctypes.c_int32),
@@ -155,14 +158,14 @@ def _check(code: int):
 
 
 def make_config(max_num_reqs: int, max_spec_len: int, vocab_size: int, device: int = 0,
-                cluster_ctas: int = 0) -> SpecVerifyConfig:
+                cluster_ctas: int = 0, flags: int = 0) -> SpecVerifyConfig:
     return SpecVerifyConfig(int(max_num_reqs), int(max_spec_len), int(vocab_size), int(device),
-                            int(cluster_ctas), 0)
+                            int(cluster_ctas), int(flags))
 
 
 def spec_verify_create(max_num_reqs: int, max_spec_len: int, vocab_size: int, device: int = 0,
-                       cluster_ctas: int = 0) -> int:
-    cfg = make_config(max_num_reqs, max_spec_len, vocab_size, device, cluster_ctas)
+                       cluster_ctas: int = 0, flags: int = 0) -> int:
+    cfg = make_config(max_num_reqs, max_spec_len, vocab_size, device, cluster_ctas, flags)
     h = ctypes.c_void_p()
     _check(load_library().spec_verify_create(ctypes.byref(cfg), ctypes.byref(h)))
     return h.value
@@ -400,9 +403,9 @@ class Verifier:
     """A handle plus output allocation.  ``verify`` returns device tensors."""
 
     def __init__(self, max_num_reqs: int, max_spec_len: int, vocab_size: int, device: int = 0,
-                 cluster_ctas: int = 0):
+                 cluster_ctas: int = 0, flags: int = 0):
         self.device = device
-        self.handle = spec_verify_create(max_num_reqs, max_spec_len, vocab_size, device, cluster_ctas)
+        self.handle = spec_verify_create(max_num_reqs, max_spec_len, vocab_size, device, cluster_ctas, flags)
 
     def close(self):
         if self.handle:

@@ -45,18 +45,19 @@ int choose_cluster(const spec_verify_ctx *ctx, int N, int V) {
 }
 
 bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk,
-                          bool bitmaps) {
-  // Rows of the current position live in the cluster's shared memory (target
-  // and draft chunk per CTA).  Prefer the CTA count of the probability entry,
-  // grow it until the two row chunks fit in ~100 KB so two CTAs share an SM.
+                          bool bitmaps, bool resident) {
+  // The rows of the current position live in the cluster's shared memory (the
+  // target chunk, and the draft chunk too when resident).  Start from the
+  // CTA count of the probability entry and grow it until a CTA is small
+  // enough for two (resident) or three CTAs to share an SM.
   auto chunk_for = [&](int c) { return ((V + c - 1) / c + 7) & ~7; };
   auto bytes_for = [&](int c) {
-    return 2LL * chunk_for(c) * elem_bytes + static_cast<long long>(logits_inbox_bytes(c)) +
-           (bitmaps ? static_cast<long long>(logits_bitmap_bytes(chunk_for(c))) : 0LL);
+    return static_cast<long long>(logits_dyn_bytes(c, chunk_for(c), elem_bytes, resident, bitmaps));
   };
+  const long long per_cta = ctx->smem_per_sm / (resident ? 2 : 3) - 1024 - static_cast<long long>(logits_static_smem());
   int c = ctx->cfg.cluster_ctas > 0 ? ctx->cfg.cluster_ctas : choose_cluster(ctx, N, V);
   if (ctx->cfg.cluster_ctas == 0)
-    while (c < ctx->max_cluster && bytes_for(c) > 100 * 1024) c *= 2;
+    while (c < ctx->max_cluster && bytes_for(c) > per_cta) c *= 2;
   // (window bins are 16-bit counts of one CTA's chunk)
   if (bytes_for(c) > ctx->max_dyn_smem || chunk_for(c) > 65535) return false;
   *cluster = c;
@@ -99,7 +100,7 @@ static sv_status check_config(const spec_verify_config *c) {
   const int cc = c->cluster_ctas;
   if (!(cc == 0 || cc == 1 || cc == 2 || cc == 4 || cc == 8 || cc == 16))
     return fail(SV_ERR_INVALID_ARG, "cluster_ctas must be 0, 1, 2, 4, 8 or 16");
-  if (c->flags != 0) return fail(SV_ERR_INVALID_ARG, "flags must be 0");
+  if (c->flags & ~SV_FLAG_RESIDENT_ROWS) return fail(SV_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   if (static_cast<long long>(c->max_num_reqs) * (cc ? cc : 16) > INT_MAX)
     return fail(SV_ERR_INVALID_ARG, "max_num_reqs too large for one grid");
   return SV_OK;
@@ -169,7 +170,8 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if ((e = cudaSetDevice(config->device)) != cudaSuccess)
     return fail(SV_ERR_CUDA, "cudaSetDevice(%d): %s", config->device, cudaGetErrorString(e));
-  int major = 0, minor = 0, sms = 0;
+  int major = 0, minor = 0, sms = 0, smem_sm = 0;
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, config->device);
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, config->device);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, config->device);
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, config->device);
@@ -203,6 +205,7 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
   h->num_sms = sms;
   h->max_cluster = max_cluster;
   h->max_dyn_smem = max_dyn;
+  h->smem_per_sm = smem_sm;
   *out = h;
   return SV_OK;
 }
@@ -270,12 +273,13 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
     const int per16 = 16 / eb;  // elements per 16-byte vector
     int cluster = 0, chunk = 0;
     const bool procs = a->repetition_penalty || a->banned_cu;
-    if (!sv::choose_logits_layout(h, p.N, p.V, eb, &cluster, &chunk, procs))
-      return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for the rows to fit in the cluster's shared memory",
-                  p.V);
     const bool vec = sv::aligned16(a->target) && (a->target_row_stride % per16 == 0) &&
                      (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % per16 == 0));
-    e = sv::launch_logits(p, bf16, cluster, chunk, vec, s);
+    const bool resident = procs || !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
+    if (!sv::choose_logits_layout(h, p.N, p.V, eb, &cluster, &chunk, procs, resident))
+      return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for the rows to fit in the cluster's shared memory",
+                  p.V);
+    e = sv::launch_logits(p, bf16, cluster, chunk, vec, resident, s);
   }
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "verifier launch: %s", cudaGetErrorString(e));
   return SV_OK;
@@ -331,7 +335,7 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   const bool bf16 = a->dtype == SV_BF16;
   const int eb = bf16 ? 2 : 4;
   int cluster = 0, chunk = 0;
-  if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk, false))
+  if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk, false, true))
     return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for a row to fit in the cluster's shared memory", p.V);
   const bool vec = sv::aligned16(a->logits) && (a->row_stride % (16 / eb) == 0);
   const cudaError_t e = sv::launch_sample(p, bf16, cluster, chunk, vec, static_cast<cudaStream_t>(stream));

@@ -11,6 +11,7 @@ struct spec_verify_ctx {
   int num_sms;
   int max_cluster;  // largest cluster size the kernels were enabled for (8 or 16)
   int max_dyn_smem; // dynamic shared memory the logits kernels may request per CTA
+  int smem_per_sm;  // shared memory of one SM (for the CTAs-per-SM target of the layout)
 };
 
 namespace sv {
@@ -97,14 +98,19 @@ size_t logits_inbox_bytes(int cluster);
 cudaError_t enable_sample_kernels(int max_cluster, int max_dyn);
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);
-cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
+// resident: both row chunks of a position in shared memory (needed by the
+// processors and by unaligned rows); otherwise the draft chunk is read in place.
+cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
+                          cudaStream_t stream);
 // Dynamic shared memory of the processor bitmaps (banned and penalised keys of a chunk).
 size_t logits_bitmap_bytes(int chunk);
+// Dynamic shared memory of one logits-entry CTA.
+size_t logits_dyn_bytes(int cluster, int chunk, int elem_bytes, bool resident, bool bitmaps);
 
 // Cluster size and per-CTA row chunk (elements, a multiple of 8) for the
 // logits entry; returns false if no cluster size fits the rows in shared memory.
 bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk,
-                          bool bitmaps);
+                          bool bitmaps, bool resident);
 
 void set_last_error(const char *fmt, ...);
 

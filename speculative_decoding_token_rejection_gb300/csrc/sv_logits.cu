@@ -1181,23 +1181,27 @@ __device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const Ro
 // Load this CTA's chunk of nr rows into shared memory.  Aligned rows arrive
 // through one bulk copy per row (TMA, completing on the CTA's mbarrier), with
 // plain loads only for a last partial 16-byte group; other rows use plain
-// loads.  Returns kFlagTimeout if the copy did not complete in time.
-template <typename TIn, bool kVec>
+// loads.  With kRes false only the target row is copied: the draft row stays
+// in global memory and is only prefetched into L2 here.  Returns
+// kFlagTimeout if the copy did not complete in time.
+template <typename TIn, bool kVec, bool kRes = true>
 __device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *const srow[2], int nr, int n,
                               uint32_t &phase) {
   const int tid = threadIdx.x;
+  const int nc = kRes ? nr : 1;  // rows copied into shared memory
   fence_proxy_async_smem();  // earlier reads of the rows before the async overwrite
   __syncthreads();
   uint32_t flags = 0;
   if (kVec) {
     const uint32_t body = (static_cast<uint32_t>(n) * sizeof(TIn)) & ~15u;
     if (tid == 0) {
-      mbar_arrive_expect_tx(&sm.bar, body * static_cast<uint32_t>(nr));
+      if (!kRes && nr == 2 && body) prefetch_l2(grow[1], body);
+      mbar_arrive_expect_tx(&sm.bar, body * static_cast<uint32_t>(nc));
       if (body)
-        for (int r = 0; r < nr; ++r) bulk_g2s(srow[r], grow[r], body, &sm.bar);
+        for (int r = 0; r < nc; ++r) bulk_g2s(srow[r], grow[r], body, &sm.bar);
     }
     const int nb = static_cast<int>(body / sizeof(TIn));
-    for (int r = 0; r < nr; ++r)
+    for (int r = 0; r < nc; ++r)
       for (int x = nb + tid; x < n; x += kThreads) srow[r][x] = grow[r][x];
     __syncthreads();
     if (!mbar_wait_bounded(&sm.bar, phase, kWaitLimit)) {
@@ -1206,7 +1210,7 @@ __device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *con
     }
     phase ^= 1u;
   } else {
-    for (int r = 0; r < nr; ++r)
+    for (int r = 0; r < nc; ++r)
       for (int x = tid; x < n; x += kThreads) srow[r][x] = grow[r][x];
     __syncthreads();
   }
@@ -1305,13 +1309,19 @@ __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsig
   for (int x = xs + tid; x < n; x += kThreads) take(bits_at(g, x), x);
 }
 
-template <typename TIn, bool kTest, bool kVec>
-__global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams P, int chunk) {
+// kRes: both row chunks of a position live in shared memory (two CTAs per
+// SM).  Otherwise only the target chunk does; the draft chunk is read where
+// it lies (prefetched into L2 next to the target copy), which leaves room for
+// three CTAs per SM.  Calls with logits processors, which rewrite both rows,
+// always take the resident form.
+template <typename TIn, bool kTest, bool kVec, bool kRes>
+__global__ void __launch_bounds__(kThreads, kRes ? 2 : 3) logits_kernel(const VerifyParams P, int chunk) {
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ LogitsSmem sm;
-  TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem) + chunk};
-  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + 2 * static_cast<size_t>(chunk) * sizeof(TIn));
+  TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem) + (kRes ? chunk : 0)};
+  Inbox *const inbox =
+      reinterpret_cast<Inbox *>(dyn_smem + (kRes ? 2 : 1) * static_cast<size_t>(chunk) * sizeof(TIn));
 
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int i = static_cast<int>(blockIdx.x / ncta);
@@ -1364,7 +1374,7 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
       valid = false;
     }
   }
-  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
+  const bool procs = kRes && (P.rep_penalty != nullptr || P.ban_cu != nullptr);
   const bool greedy = valid && temp == 0.0f;
   int A = 0;
   int32_t last_tok = -1;
@@ -1503,21 +1513,23 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
         }
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
         if (procs) add_drafts(j);
-        const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, nr, n, phase);
+        const uint32_t lf = load_rows<TIn, kVec, kRes>(sm, grow, srow, nr, n, phase);
+        // this position's rows: the draft chunk in shared memory, or where it lies
+        TIn *const rows[2] = {srow[0], kRes ? srow[1] : const_cast<TIn *>(grow[1])};
         join();
         int y_owner = -1;
         uint32_t yb0 = 0u, yb1 = 0u;
         if (procs) {
-          apply_processors(srow, nr, n, pen_bits, ban_bits, words, theta);
+          apply_processors(rows, nr, n, pen_bits, ban_bits, words, theta);
           if (j < g && y >= 0 && y < V) {  // the CTA holding y publishes its processed logits
             y_owner = y / chunk;
             if (static_cast<int>(rank) == y_owner) {
-              yb0 = bits_at(srow[0], y - x0);
-              yb1 = bits_at(srow[1], y - x0);
+              yb0 = bits_at(rows[0], y - x0);
+              yb1 = bits_at(rows[1], y - x0);
             }
           }
         }
-        if (!position_stats<TIn>(sm, inbox, srow, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta, rank, yb0,
+        if (!position_stats<TIn>(sm, inbox, rows, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta, rank, yb0,
                                  yb1, y_owner)) {
           req_bits |= SV_DATA_BAD_VALUES;
           valid = false;
@@ -1548,16 +1560,16 @@ __global__ void __launch_bounds__(kThreads, 2) logits_kernel(const VerifyParams 
             continue;  // accepted: next position
           }
           residual = true;
-          race_smem<TIn, kTest, true>(srow[0], srow[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl);
+          race_smem<TIn, kTest, true>(rows[0], rows[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl);
         } else {
-          race_smem<TIn, kTest, false>(srow[0], srow[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
+          race_smem<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
         }
         KeyFlags r = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
         if (r.key == 0ull && residual) {  // no positive residual key: race over p with the same E
           bk = 0.0f;
           bx = -1;
           fl = 0;
-          race_smem<TIn, kTest, false>(srow[0], srow[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
+          race_smem<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
           const KeyFlags r2 = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
           r.key = r2.key;
           r.flags |= r2.flags;
@@ -1697,7 +1709,7 @@ cudaError_t enable_sample_one(int max_cluster, int max_dyn) {
   return cudaSuccess;
 }
 
-template <typename TIn, bool kTest, bool kVec>
+template <typename TIn, bool kTest, bool kVec, bool kRes>
 cudaError_t launch_one(const VerifyParams &p, int cluster, int chunk, size_t dyn, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.N) * static_cast<unsigned>(cluster), 1, 1);
@@ -1711,17 +1723,37 @@ cudaError_t launch_one(const VerifyParams &p, int cluster, int chunk, size_t dyn
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, logits_kernel<TIn, kTest, kVec>, p, chunk);
+  return cudaLaunchKernelEx(&cfg, logits_kernel<TIn, kTest, kVec, kRes>, p, chunk);
 }
 
-template <typename TIn, bool kTest, bool kVec>
+template <typename TIn, bool kTest, bool kVec, bool kRes>
 cudaError_t enable_one(int max_cluster, int max_dyn) {
-  cudaError_t e = cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec>,
+  cudaError_t e = cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec, kRes>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
   if (e != cudaSuccess) return e;
   if (max_cluster > 8)
-    return cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec, kRes>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return cudaSuccess;
+}
+
+// Forms built per element type and randomness: unaligned rows (resident),
+// aligned rows with both chunks resident, aligned rows with the draft chunk
+// read in place.
+template <typename TIn, bool kTest>
+cudaError_t enable_forms(int max_cluster, int max_dyn) {
+  cudaError_t e;
+  if ((e = enable_one<TIn, kTest, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<TIn, kTest, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_one<TIn, kTest, true, false>(max_cluster, max_dyn);
+}
+
+template <typename TIn, bool kTest>
+cudaError_t launch_form(const VerifyParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
+                        cudaStream_t stream) {
+  if (!vec) return launch_one<TIn, kTest, false, true>(p, cluster, chunk, dyn, stream);
+  return resident ? launch_one<TIn, kTest, true, true>(p, cluster, chunk, dyn, stream)
+                  : launch_one<TIn, kTest, true, false>(p, cluster, chunk, dyn, stream);
 }
 
 }  // namespace
@@ -1729,17 +1761,17 @@ cudaError_t enable_one(int max_cluster, int max_dyn) {
 size_t logits_static_smem() { return sizeof(LogitsSmem); }
 size_t logits_inbox_bytes(int cluster) { return 2 * static_cast<size_t>(cluster) * sizeof(Inbox); }
 size_t logits_bitmap_bytes(int chunk) { return ((2 * static_cast<size_t>((chunk + 31) / 32) * 4) + 15) & ~size_t{15}; }
+size_t logits_dyn_bytes(int cluster, int chunk, int elem_bytes, bool resident, bool bitmaps) {
+  return (resident ? 2 : 1) * static_cast<size_t>(chunk) * elem_bytes + logits_inbox_bytes(cluster) +
+         (bitmaps ? logits_bitmap_bytes(chunk) : 0);
+}
 
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn) {
   cudaError_t e;
-  if ((e = enable_one<uint16_t, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_one<uint16_t, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_one<uint16_t, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_one<uint16_t, false, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_one<float, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_one<float, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_one<float, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  return enable_one<float, false, false>(max_cluster, max_dyn);
+  if ((e = enable_forms<uint16_t, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_forms<uint16_t, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_forms<float, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_forms<float, false>(max_cluster, max_dyn);
 }
 
 cudaError_t enable_sample_kernels(int max_cluster, int max_dyn) {
@@ -1769,20 +1801,15 @@ cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chu
              : launch_sample_one<float, false, false>(p, cluster, chunk, dyn, stream);
 }
 
-cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
+cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
+                          cudaStream_t stream) {
   const bool test = p.exponentials != nullptr;
-  const size_t dyn = 2 * static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster) +
-                     ((p.rep_penalty || p.ban_cu) ? logits_bitmap_bytes(chunk) : 0);
-  if (bf16) {
-    if (test) return vec ? launch_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
-                         : launch_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);
-    return vec ? launch_one<uint16_t, false, true>(p, cluster, chunk, dyn, stream)
-               : launch_one<uint16_t, false, false>(p, cluster, chunk, dyn, stream);
-  }
-  if (test) return vec ? launch_one<float, true, true>(p, cluster, chunk, dyn, stream)
-                       : launch_one<float, true, false>(p, cluster, chunk, dyn, stream);
-  return vec ? launch_one<float, false, true>(p, cluster, chunk, dyn, stream)
-             : launch_one<float, false, false>(p, cluster, chunk, dyn, stream);
+  resident = resident || !vec;
+  const size_t dyn = logits_dyn_bytes(cluster, chunk, bf16 ? 2 : 4, resident, p.rep_penalty || p.ban_cu);
+  if (bf16) return test ? launch_form<uint16_t, true>(p, cluster, chunk, dyn, vec, resident, stream)
+                        : launch_form<uint16_t, false>(p, cluster, chunk, dyn, vec, resident, stream);
+  return test ? launch_form<float, true>(p, cluster, chunk, dyn, vec, resident, stream)
+              : launch_form<float, false>(p, cluster, chunk, dyn, vec, resident, stream);
 }
 
 }  // namespace sv

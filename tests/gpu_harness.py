@@ -9,11 +9,12 @@ import workloads
 _VERIFIERS = {}
 
 
-def verifier(cluster_ctas=0):
-    if cluster_ctas not in _VERIFIERS:
-        _VERIFIERS[cluster_ctas] = sv.Verifier(1 << 20, sv.SV_MAX_SPEC_LEN, 1 << 18, device=0,
-                                               cluster_ctas=cluster_ctas)
-    return _VERIFIERS[cluster_ctas]
+def verifier(cluster_ctas=0, flags=0):
+    key = (cluster_ctas, flags)
+    if key not in _VERIFIERS:
+        _VERIFIERS[key] = sv.Verifier(1 << 20, sv.SV_MAX_SPEC_LEN, 1 << 18, device=0, cluster_ctas=cluster_ctas,
+                                      flags=flags)
+    return _VERIFIERS[key]
 
 
 def processor_args(w, dev):
@@ -30,7 +31,7 @@ def processor_args(w, dev):
 
 
 def run_gpu(w, *, production=False, seed=0, offset=0, rng_request_base=0, cluster_ctas=0, stream=None,
-            synthetic_rates=None):
+            synthetic_rates=None, flags=0):
     """Run the CUDA path on workload ``w``; returns numpy results like oracle.verify."""
     dev = torch.device("cuda:0")
     t = workloads.as_torch(w, dev)
@@ -45,7 +46,7 @@ def run_gpu(w, *, production=False, seed=0, offset=0, rng_request_base=0, cluste
     ncomp = None if ncomp is None else ncomp.clone()
     slots = None if slots is None else slots.clone()
     sv.spec_verify_run(
-        verifier(cluster_ctas).handle, stream=stream, entry=w["entry"], draft_ids=t["draft_ids"],
+        verifier(cluster_ctas, flags).handle, stream=stream, entry=w["entry"], draft_ids=t["draft_ids"],
         target=t["target"], draft=t["draft"], cu_num_draft_tokens=t["cu_num_draft_tokens"],
         temperature=t["temperature"], top_k=t.get("top_k"), top_p=t.get("top_p"),
         uniforms=None if production else t["uniforms"], exponentials=None if production else t["exponentials"],

@@ -290,3 +290,20 @@ def test_top_k_threshold_bound_cases(shape, top_k):
     w["top_k"] = np.full(N, top_k, np.int32)
     w["top_p"] = np.full(N, 0.95 if top_k > 8 else 1.0, np.float32)
     compare_logits(H().run_gpu(w), oracle.verify(w), w, max_exempt_frac=0.5)
+
+
+@pytest.mark.parametrize("name,kw,production", [("fused", dict(N=40, V=151936), False),
+                                                ("fused", dict(N=24, V=12000), True),
+                                                ("ragged", dict(N=48, V=9000), False)])
+def test_draft_rows_in_place_and_resident_agree(name, kw, production):
+    """The two forms of the logits kernel -- draft row chunk read in place
+    (default) or copied into shared memory -- against the oracle and against
+    each other (identical except inside the tolerance band)."""
+    import speculative_decoding_token_rejection_gb300 as sv
+    w = workloads.make(name, test_mode=not production, **kw)
+    o = oracle.verify(w, production=production, seed=6, offset=1)
+    g_in_place = H().run_gpu(w, production=production, seed=6, offset=1)
+    g_res = H().run_gpu(w, production=production, seed=6, offset=1, flags=sv.SV_FLAG_RESIDENT_ROWS)
+    compare_logits(g_in_place, o, w, production=production, max_exempt_frac=0.05)
+    compare_logits(g_res, o, w, production=production, max_exempt_frac=0.05)
+    np.testing.assert_array_equal(g_in_place["num_accepted"], g_res["num_accepted"])

@@ -125,6 +125,8 @@ def test_check_args(lib, mutate, code):
     (dict(vocab_size=0), sv.SV_ERR_INVALID_ARG),
     (dict(cluster_ctas=3), sv.SV_ERR_INVALID_ARG),
     (dict(cluster_ctas=16), sv.SV_OK),
+    (dict(flags=sv.SV_FLAG_RESIDENT_ROWS), sv.SV_OK),
+    (dict(flags=2), sv.SV_ERR_INVALID_ARG),
 ])
 def test_check_config(lib, kw, code):
     assert sv.spec_verify_check_args(cfg(**kw), good_args()) == code
