@@ -142,11 +142,13 @@ struct StatPart {  // one CTA's partials of one reduction round, for up to 2 row
   uint32_t maxkey[2];
   uint32_t flags[2];
   uint32_t floor[2];  // lower bound of the row's top-k threshold (key), from the thread maxima
+  uint32_t nbins[2];  // window bins that can be non-zero (the window's width)
   float z[2];
   unsigned long long tot[2];
   uint32_t cnt[2][256];
   float massf[2][256];  // masses (fast path: the window, relative to this CTA's max)
 };
+constexpr int kBinsShift = 8;  // an inbox header carries nbins in the flags word above this bit
 
 struct StatSum {  // cluster totals of a reduction round (the same in every CTA)
   uint32_t maxkey[2];
@@ -223,6 +225,7 @@ __device__ __forceinline__ void zero_part(StatPart &p, uint32_t what, int nr) {
     p.maxkey[tid] = 0u;
     p.flags[tid] = 0u;
     p.floor[tid] = 0xFFFFFFFFu;
+    p.nbins[tid] = 0u;
     p.z[tid] = 0.0f;
     p.tot[tid] = 0ull;
   }
@@ -834,6 +837,7 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       // below the threshold's floor); at or below key(-inf): every finite key
       uint32_t lo = lk16 >= static_cast<uint32_t>(kNearBins - 1) ? lk16 - (kNearBins - 1) : 0u;
       if (use_floor) lo = max(lo, lp.floor[r]);
+      if (tid == 0) lp.nbins[r] = min(static_cast<uint32_t>(kNearBins), lk16 - lo + 1u);
       const uint32_t lob = lo > 0x007Fu ? bf16_bits_of_key(lo) : 0xFF80u;
       const uint32_t lo2 = lob | (lob << 16);
       uint32_t *cnt = lp.cnt[r];
@@ -944,12 +948,17 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   __syncthreads();
   Inbox *const ibx = inbox + par * static_cast<int>(ncta);
   {
-    const int nwords = (kB == 16 && near) ? kInboxWords : 3;  // header only unless bins are used
+    // header, then only the words of bins that can be non-zero (eight per word)
+    const int w0 = (kB == 16 && near) ? static_cast<int>((lp.nbins[0] + 7u) / 8u) : 0;
+    const int w1 = (kB == 16 && near) ? static_cast<int>((lp.nbins[1] + 7u) / 8u) : 0;
+    const int nwords = 3 + w0 + w1;
     for (int t = tid; t < nwords * static_cast<int>(ncta); t += kThreads) {
-      const int c = t / nwords, wd = t % nwords;
+      const int c = t / nwords, k = t % nwords;
+      const int wd = k < 3 + w0 ? k : k - w0 + kNearBins / 8;  // row 1's words start at 3 + kNearBins / 8
       uint4 v;
       if (wd == 0) {
-        v = make_uint4(lp.maxkey[0], lp.maxkey[1], lp.flags[0], lp.flags[1]);
+        v = make_uint4(lp.maxkey[0], lp.maxkey[1], lp.flags[0] | (lp.nbins[0] << kBinsShift),
+                       lp.flags[1] | (lp.nbins[1] << kBinsShift));
       } else if (wd == 1) {
         v = make_uint4(__float_as_uint(lp.z[0]), __float_as_uint(lp.z[1]), ybits0, ybits1);
       } else if (wd == 2) {
@@ -975,7 +984,7 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
     uint32_t gk = 0, fl = 0;
     for (int c = 0; c < static_cast<int>(ncta); ++c) {
       const uint32_t pf = ibx[c].flags[r];
-      fl |= pf;
+      fl |= pf & ((1u << kBinsShift) - 1u);
       if (pf & kFlagFinite) gk = max(gk, ibx[c].maxkey[r]);
     }
     const uint32_t g16 = key16_of<TIn>(gk);
@@ -989,9 +998,10 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       uint32_t cs = 0;
       if (fl & kFlagFinite) {
         for (int c = 0; c < static_cast<int>(ncta); ++c) {
-          if (!(ibx[c].flags[r] & kFlagFinite)) continue;
+          const uint32_t pf = ibx[c].flags[r];
+          if (!(pf & kFlagFinite)) continue;
           const int dl = d - static_cast<int>(g16 - key16_of<TIn>(ibx[c].maxkey[r]));
-          if (dl >= 0) cs += ibx[c].cnt[r][dl];
+          if (dl >= 0 && dl < static_cast<int>(pf >> kBinsShift)) cs += ibx[c].cnt[r][dl];  // (others not sent)
         }
       }
       ns.cnt[r][d] = cs;

@@ -307,3 +307,15 @@ def test_draft_rows_in_place_and_resident_agree(name, kw, production):
     compare_logits(g_in_place, o, w, production=production, max_exempt_frac=0.05)
     compare_logits(g_res, o, w, production=production, max_exempt_frac=0.05)
     np.testing.assert_array_equal(g_in_place["num_accepted"], g_res["num_accepted"])
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 16])
+@pytest.mark.parametrize("resident", [False, True])
+def test_explicit_cluster_sizes(cluster, resident):
+    """Every cluster size in both forms; V=12008 leaves a ragged last chunk
+    (16-byte aligned rows, chunks of 12008 / C rounded up to 8 elements)."""
+    import speculative_decoding_token_rejection_gb300 as sv
+    w = workloads.make("fused", N=20, V=12008, seed=15)
+    o = oracle.verify(w)
+    g = H().run_gpu(w, cluster_ctas=cluster, flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0)
+    compare_logits(g, o, w, max_exempt_frac=0.1)
