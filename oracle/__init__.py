@@ -97,7 +97,8 @@ def _lib():
                                                _P, _P]
         lib.oracle_sample_rows.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int64,
                                            _P, _P, _P, _P, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
-                                           ctypes.c_uint32, _P, _P, _P, _P]
+                                           ctypes.c_uint32, _P, _P, _P, _P,
+                                           _P, _P, _P, ctypes.c_int64, _P, _P, ctypes.c_int64]
         lib.oracle_ngram_propose.argtypes = [ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                              ctypes.c_int32, ctypes.c_int64, _P, _P]
         assert lib.oracle_sizeof_args() == ctypes.sizeof(_Args), "oracle_args layout mismatch"
@@ -215,11 +216,13 @@ def verify(w: dict, *, production: bool = False, seed: int = 0, offset: int = 0,
 
 
 def sample_rows(logits, *, temperature=None, top_k=None, top_p=None, exponentials=None, seed=0, offset=0,
-                rng_row_base=0, with_probs=True):
+                rng_row_base=0, with_probs=True, repetition_penalty=None, penalty_cu=None, penalty_ids=None,
+                banned_cu=None, banned_ids=None):
     """Draft-side sampler: one token per logits row (fp32 array [R, V] or bf16
-    bits uint16 [R, V]).  Test mode when ``exponentials`` is given.  Returns
-    dict(tokens [R], probs [R, V] or None, status, diag [R, 2] = race flip
-    index, top-p edge flag)."""
+    bits uint16 [R, V]).  Test mode when ``exponentials`` is given.  Optional
+    logits processors per row (lists as in ``verify``).  Returns dict(tokens
+    [R], probs [R, V] or None, status, diag [R, 2] = race flip index, top-p
+    edge flag)."""
     lib = _lib()
     bf16 = logits.dtype == np.uint16
     l = _c(logits, np.uint16 if bf16 else np.float32)
@@ -232,8 +235,13 @@ def sample_rows(logits, *, temperature=None, top_k=None, top_p=None, exponential
     probs = np.zeros((R, V), np.float32) if with_probs else None
     status = np.zeros(1, np.int32)
     diag = np.zeros((R, 2), np.float64)
+    theta = _c(repetition_penalty, np.float32)
+    pcu, pids = _c(penalty_cu, np.int64), _c(penalty_ids, np.int32)
+    bcu, bids = _c(banned_cu, np.int64), _c(banned_ids, np.int32)
     rc = lib.oracle_sample_rows(R, V, 1 if bf16 else 0, _ptr(l), V, _ptr(temp), _ptr(tk), _ptr(tp), _ptr(E), V,
-                                seed, offset, rng_row_base, _ptr(tokens), _ptr(probs), _ptr(status), _ptr(diag))
+                                seed, offset, rng_row_base, _ptr(tokens), _ptr(probs), _ptr(status), _ptr(diag),
+                                _ptr(theta), _ptr(pcu), _ptr(pids), 0 if pids is None else int(pids.shape[0]),
+                                _ptr(bcu), _ptr(bids), 0 if bids is None else int(bids.shape[0]))
     if rc != 0:
         raise RuntimeError(f"oracle_sample_rows failed with {rc}")
     return dict(tokens=tokens, probs=probs, status=int(status[0]), diag=diag)

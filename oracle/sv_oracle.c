@@ -418,37 +418,45 @@ static int has_processors(const oracle_args *a) {
   return a->entry == ORC_ENTRY_LOGITS && (a->banned_cu || a->repetition_penalty);
 }
 
-static void process_row(const oracle_args *a, int i, int64_t s, int j, float *row) {
-  if (!has_processors(a)) return;
-  const int V = a->vocab_size;
+/* The processors on one row, from explicit lists: banned ids ban[bb..be),
+ * penalised ids pen[pb..pe) plus extra[0..nextra) when theta is given. */
+static void process_lists(float *row, int V, int dtype, const float *theta, const int32_t *ban, int64_t bb,
+                          int64_t be, const int32_t *pen, int64_t pb, int64_t pe, const int32_t *extra,
+                          int nextra) {
   unsigned char *mark = calloc((size_t)V, 1); /* 1 banned, 2 penalised */
-  int64_t b, e;
-  if (a->banned_cu && list_range(a->banned_cu, a->banned_total, i, &b, &e))
-    for (int64_t k = b; k < e; ++k) {
-      int32_t x = a->banned_ids[k];
-      if (x >= 0 && x < V) mark[x] = 1;
+  for (int64_t k = bb; k < be; ++k) {
+    int32_t x = ban[k];
+    if (x >= 0 && x < V) mark[x] = 1;
+  }
+  if (theta) {
+    for (int64_t k = pb; k < pe; ++k) {
+      int32_t x = pen[k];
+      if (x >= 0 && x < V && !mark[x]) mark[x] = 2;
     }
-  if (a->repetition_penalty) {
-    if (a->penalty_cu && list_range(a->penalty_cu, a->penalty_total, i, &b, &e))
-      for (int64_t k = b; k < e; ++k) {
-        int32_t x = a->penalty_ids[k];
-        if (x >= 0 && x < V && !mark[x]) mark[x] = 2;
-      }
-    for (int k = 0; k < j; ++k) {
-      int32_t x = a->draft_ids[s + k];
+    for (int k = 0; k < nextra; ++k) {
+      int32_t x = extra[k];
       if (x >= 0 && x < V && !mark[x]) mark[x] = 2;
     }
   }
-  const float theta = a->repetition_penalty ? a->repetition_penalty[i] : 1.0f;
   for (int x = 0; x < V; ++x) {
     if (mark[x] == 1) {
       row[x] = -INFINITY;
     } else if (mark[x] == 2) {
-      float v = row[x] > 0.0f ? row[x] / theta : row[x] * theta;
-      row[x] = a->dtype == ORC_BF16 ? round_to_bf16(v) : v;
+      float v = row[x] > 0.0f ? row[x] / *theta : row[x] * *theta;
+      row[x] = dtype == ORC_BF16 ? round_to_bf16(v) : v;
     }
   }
   free(mark);
+}
+
+/* Position j of request i: its context list plus the drafts y_0 .. y_{j-1}. */
+static void process_row(const oracle_args *a, int i, int64_t s, int j, float *row) {
+  if (!has_processors(a)) return;
+  int64_t bb = 0, be = 0, pb = 0, pe = 0;
+  if (a->banned_cu) list_range(a->banned_cu, a->banned_total, i, &bb, &be);
+  if (a->penalty_cu) list_range(a->penalty_cu, a->penalty_total, i, &pb, &pe);
+  process_lists(row, a->vocab_size, a->dtype, a->repetition_penalty ? &a->repetition_penalty[i] : NULL,
+                a->banned_ids, bb, be, a->penalty_ids, pb, pe, a->draft_ids + s, j);
 }
 
 static void emit_invalid(const oracle_args *a, int i) {
@@ -749,7 +757,11 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
                        const float *temperature, const int32_t *top_k, const float *top_p,
                        const float *exponentials, int64_t exp_stride, uint64_t seed, uint64_t offset,
                        uint32_t rng_row_base, int32_t *tokens, float *probs_out, int32_t *status,
-                       double *diag /* [rows, 2]: race flip index, top-p edge */) {
+                       double *diag /* [rows, 2]: race flip index, top-p edge */,
+                       /* logits processors per row (lists as in oracle_args, row r = request r) */
+                       const float *repetition_penalty, const int64_t *penalty_cu, const int32_t *penalty_ids,
+                       int64_t penalty_total, const int64_t *banned_cu, const int32_t *banned_ids,
+                       int64_t banned_total) {
   float *l = (float *)malloc(sizeof(float) * (size_t)V);
   float *p = (float *)malloc(sizeof(float) * (size_t)V);
   float *E = (float *)malloc(sizeof(float) * (size_t)V);
@@ -770,7 +782,24 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
       tokens[r] = -1;
       continue;
     }
-    if (temp == 0.0f) { /* greedy drafting: argmax of the raw logits */
+    {
+      int64_t pb = 0, pe = 0, bb = 0, be = 0;
+      if ((penalty_cu && !list_range(penalty_cu, penalty_total, r, &pb, &pe)) ||
+          (banned_cu && !list_range(banned_cu, banned_total, r, &bb, &be))) {
+        *status |= ORC_BAD_LIST;
+        tokens[r] = -1;
+        continue;
+      }
+      if (repetition_penalty && !(repetition_penalty[r] > 0.0f && !isinf(repetition_penalty[r]))) {
+        *status |= ORC_BAD_PARAM;
+        tokens[r] = -1;
+        continue;
+      }
+      if (banned_cu || repetition_penalty)
+        process_lists(l, V, dtype, repetition_penalty ? &repetition_penalty[r] : NULL, banned_ids, bb, be,
+                      penalty_ids, pb, pe, NULL, 0);
+    }
+    if (temp == 0.0f) { /* greedy drafting: argmax of the (processed) logits */
       int g = argmax_row(l, V);
       if (g < 0) *status |= ORC_BAD_VALUES;
       tokens[r] = g;

@@ -145,12 +145,12 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
              test_stop_token_truncates_commit_and_rollback,
              test_identical_processing_of_target_and_draft, test_bf16_rounding_of_penalised_logits)
     mutants = {
-        "drafts not in the set": ("for (int k = 0; k < j; ++k) {", "for (int k = 0; k < j - 1; ++k) {"),
-        "penalty overrides ban": ("        if (x >= 0 && x < V && !mark[x]) mark[x] = 2;\n      }\n    for (int k = 0; k < j",
-                                  "        if (x >= 0 && x < V) mark[x] = 2;\n      }\n    for (int k = 0; k < j"),
-        "drafts only with a context list": ("  if (a->repetition_penalty) {\n    if (a->penalty_cu",
-                                            "  if (a->repetition_penalty && a->penalty_cu) {\n    if (a->penalty_cu"),
-        "no bf16 rounding": ("row[x] = a->dtype == ORC_BF16 ? round_to_bf16(v) : v;", "row[x] = v;"),
+        "drafts not in the set": ("for (int k = 0; k < nextra; ++k) {", "for (int k = 0; k < nextra - 1; ++k) {"),
+        "penalty overrides ban": ("      if (x >= 0 && x < V && !mark[x]) mark[x] = 2;\n    }\n    for (int k = 0; k < nextra",
+                                  "      if (x >= 0 && x < V) mark[x] = 2;\n    }\n    for (int k = 0; k < nextra"),
+        "drafts only with a context list": ("a->penalty_ids, pb, pe, a->draft_ids + s, j);",
+                                            "a->penalty_ids, pb, pe, a->draft_ids + s, a->penalty_cu ? j : 0);"),
+        "no bf16 rounding": ("row[x] = dtype == ORC_BF16 ? round_to_bf16(v) : v;", "row[x] = v;"),
         "stop off by one": ("        A = m;\n        break;", "        A = m > 0 ? m - 1 : 0;\n        break;"),
         "draft side unprocessed": ("load_row(base, a->dtype, row, stride, a->vocab_size, tmp);\n  process_row(a, i, s, j, tmp);",
                                    "load_row(base, a->dtype, row, stride, a->vocab_size, tmp);\n"
@@ -177,3 +177,33 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
         finally:
             oracle_mod.build, oracle_mod._LIB = orig_build, saved
         assert caught, name
+
+
+def test_sampler_applies_the_same_processors():
+    """The draft-side sampler's probability row under processors equals the
+    verifier's q row at the same position (identical transforms on q), and a
+    banned argmax is never drafted greedily."""
+    rng = np.random.default_rng(3)
+    V = 40
+    d = rng.standard_normal((1, V)).astype(np.float32) * 2
+    t = rng.standard_normal((2, V)).astype(np.float32) * 2
+    ctx = np.array([int(np.argmax(d[0])), 7, 7, 3], np.int32)
+    ban = np.array([11, 12], np.int32)
+    s = oracle.sample_rows(d, temperature=[0.9], top_k=[10], top_p=[0.95], exponentials=np.ones((1, V)),
+                           repetition_penalty=[1.7], penalty_cu=[len(ctx)], penalty_ids=ctx, banned_cu=[2],
+                           banned_ids=ban)
+    assert s["status"] == 0
+    y = int(s["tokens"][0])
+    w = hand_workload(t, d, [y], entry="logits", u=[0.999999], E=np.ones((1, V)), temperature=[0.9],
+                      top_k=[10], top_p=[0.95])
+    w["repetition_penalty"] = np.array([1.7], np.float32)
+    w["penalty_cu"], w["penalty_ids"] = np.array([len(ctx)], np.int64), ctx
+    w["banned_cu"], w["banned_ids"] = np.array([2], np.int64), ban
+    o = oracle.verify(w)
+    assert o["dbg_qy"][0] == s["probs"][0, y]
+    assert np.all(s["probs"][0, ban] == 0)
+    g = oracle.sample_rows(d, temperature=[0.0], banned_cu=[1], banned_ids=np.array([int(np.argmax(d[0]))],
+                                                                                     np.int32))
+    assert g["tokens"][0] != int(np.argmax(d[0]))
+    bad = oracle.sample_rows(d, temperature=[0.9], banned_cu=[5], banned_ids=ban)
+    assert bad["status"] == oracle.BAD_LIST and bad["tokens"][0] == -1
