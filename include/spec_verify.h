@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 4u
+#define SPEC_VERIFY_ABI_VERSION 5u
 #define SV_PLACEHOLDER_TOKEN_ID (-1)
 #define SV_PADDING_SLOT_ID (-1)
 #define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
@@ -220,6 +220,18 @@ typedef struct spec_verify_sample_args {
   float *probs;          /* [R rows, probs_row_stride] out or NULL: the transformed row (random rows only) */
   int64_t probs_row_stride;
   int32_t *status;       /* [1] or NULL: SV_DATA_* bits OR-ed in */
+
+  /* Logits processors per row, as in spec_verify_args (row r = request r;
+   * no drafts are added implicitly: a row's penalty list holds its whole
+   * context, drafts sampled before it included), so that the sampled q is the
+   * q the verifier rebuilds. */
+  const float *repetition_penalty;    /* [R] theta, or NULL */
+  const int64_t *penalty_cu;          /* [R] or NULL */
+  const int32_t *penalty_token_ids;
+  int64_t penalty_total;
+  const int64_t *banned_cu;           /* [R] or NULL */
+  const int32_t *banned_token_ids;
+  int64_t banned_total;
 } spec_verify_sample_args;
 
 sv_status spec_verify_sample(spec_verify_t handle, const spec_verify_sample_args *args, void *stream);

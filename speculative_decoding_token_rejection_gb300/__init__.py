@@ -73,6 +73,8 @@ class SpecVerifySampleArgs(ctypes.Structure):
         ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
         ("rng_row_base", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
         ("tokens", _P), ("probs", _P), ("probs_row_stride", ctypes.c_int64), ("status", _P),
+        ("repetition_penalty", _P), ("penalty_cu", _P), ("penalty_token_ids", _P), ("penalty_total", ctypes.c_int64),
+        ("banned_cu", _P), ("banned_token_ids", _P), ("banned_total", ctypes.c_int64),
     ]
 
 
@@ -305,8 +307,11 @@ def spec_verify_run(handle: int, stream=None, **kw) -> None:
 
 
 def build_sample_args(*, logits, tokens, probs=None, temperature=None, top_k=None, top_p=None, exponentials=None,
-                      seed: int = 0, offset: int = 0, rng_row_base: int = 0, status=None) -> SpecVerifySampleArgs:
-    """Validate tensors and fill a SpecVerifySampleArgs (no device work)."""
+                      seed: int = 0, offset: int = 0, rng_row_base: int = 0, status=None, repetition_penalty=None,
+                      penalty_cu=None, penalty_token_ids=None, banned_cu=None,
+                      banned_token_ids=None) -> SpecVerifySampleArgs:
+    """Validate tensors and fill a SpecVerifySampleArgs (no device work).
+    Logits processors per row as in ``build_args``."""
     import torch
     device = logits.device
     R, V = logits.shape
@@ -330,6 +335,13 @@ def build_sample_args(*, logits, tokens, probs=None, temperature=None, top_k=Non
     if probs is not None:
         a.probs, a.probs_row_stride = _rows(probs, "probs", device, V, R, (torch.float32,))
     a.status = _ptr(status, torch.int32, "status", device, numel=1)
+    a.repetition_penalty = _ptr(repetition_penalty, torch.float32, "repetition_penalty", device, numel=R)
+    for name, cu_l, ids_l in (("penalty", penalty_cu, penalty_token_ids), ("banned", banned_cu, banned_token_ids)):
+        setattr(a, f"{name}_cu", _ptr(cu_l, torch.int64, f"{name}_cu", device, numel=R))
+        has_ids = ids_l is not None and ids_l.numel() > 0
+        setattr(a, f"{name}_token_ids", _ptr(ids_l, torch.int32, f"{name}_token_ids", device, ndim=1)
+                if has_ids else None)
+        setattr(a, f"{name}_total", int(ids_l.numel()) if ids_l is not None else 0)
     return a
 
 

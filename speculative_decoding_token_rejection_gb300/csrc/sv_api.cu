@@ -305,6 +305,10 @@ sv_status spec_verify_check_sample_args(const spec_verify_config *c, const spec_
   if (a->probs && a->probs_row_stride < a->vocab_size)
     return fail(SV_ERR_INVALID_ARG, "probs_row_stride < vocab_size");
   if (!a->tokens) return fail(SV_ERR_INVALID_ARG, "tokens is NULL");
+  if (a->penalty_cu && (a->penalty_total < 0 || (a->penalty_total > 0 && !a->penalty_token_ids)))
+    return fail(SV_ERR_INVALID_ARG, "bad penalty list");
+  if (a->banned_cu && (a->banned_total < 0 || (a->banned_total > 0 && !a->banned_token_ids)))
+    return fail(SV_ERR_INVALID_ARG, "bad banned list");
   return SV_OK;
 }
 
@@ -332,10 +336,17 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   p.probs = a->probs;
   p.probs_stride = a->probs_row_stride;
   p.status = a->status;
+  p.rep_penalty = a->repetition_penalty;
+  p.pen_cu = a->penalty_cu;
+  p.pen_ids = a->penalty_token_ids;
+  p.pen_total = a->penalty_total;
+  p.ban_cu = a->banned_cu;
+  p.ban_ids = a->banned_token_ids;
+  p.ban_total = a->banned_total;
   const bool bf16 = a->dtype == SV_BF16;
   const int eb = bf16 ? 2 : 4;
   int cluster = 0, chunk = 0;
-  if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk, false, true))
+  if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk, p.rep_penalty || p.ban_cu, true))
     return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for a row to fit in the cluster's shared memory", p.V);
   const bool vec = sv::aligned16(a->logits) && (a->row_stride % (16 / eb) == 0);
   const cudaError_t e = sv::launch_sample(p, bf16, cluster, chunk, vec, static_cast<cudaStream_t>(stream));

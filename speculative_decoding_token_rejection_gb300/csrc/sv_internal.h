@@ -71,6 +71,13 @@ struct SampleParams {
   float *probs;
   int64_t probs_stride;
   int32_t *status;
+  const float *rep_penalty;
+  const int64_t *pen_cu;
+  const int32_t *pen_ids;
+  int64_t pen_total;
+  const int64_t *ban_cu;
+  const int32_t *ban_ids;
+  int64_t ban_total;
 };
 
 // The n-gram proposer's parameters (device pointers, sizes).

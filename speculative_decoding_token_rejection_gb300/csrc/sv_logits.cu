@@ -1633,6 +1633,11 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
   int32_t token = -1;
   int step = 0;
   uint32_t phase = 0;
+  // processor bitmaps (present only when the call has processors)
+  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
+  const int words = (chunk + 31) / 32;
+  uint32_t *const pen_bits = reinterpret_cast<uint32_t *>(inbox + 2 * ncta);
+  uint32_t *const ban_bits = pen_bits + words;
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     fence_mbar_init();
@@ -1640,14 +1645,52 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
   __syncthreads();
   cluster_sync();  // every CTA of the cluster runs before any store into a peer
   const float temp = P.temperature ? P.temperature[r] : 1.0f;
+  bool ok = true;
   if (!(temp >= 0.0f) || isinf(temp)) {
     bits |= SV_DATA_BAD_PARAM;
+    ok = false;
+  }
+  int64_t pen_b = 0, pen_e = 0, ban_b = 0, ban_e = 0;
+  if (ok && ((P.pen_cu && !list_range(P.pen_cu, P.pen_total, r, pen_b, pen_e)) ||
+             (P.ban_cu && !list_range(P.ban_cu, P.ban_total, r, ban_b, ban_e)))) {
+    bits |= SV_DATA_BAD_LIST;
+    ok = false;
+  }
+  float theta = 1.0f;
+  if (ok && P.rep_penalty) {
+    theta = P.rep_penalty[r];
+    if (!(theta > 0.0f) || isinf(theta)) {
+      bits |= SV_DATA_BAD_PARAM;
+      ok = false;
+    }
+  }
+  if (ok && procs) {  // this chunk's banned and penalised keys
+    auto mark = [&](uint32_t *bm, int32_t x) {
+      if (x >= x0 && x < x0 + n) atomicOr(&bm[(x - x0) >> 5], 1u << ((x - x0) & 31));
+    };
+    for (int w = tid; w < 2 * words; w += kThreads) pen_bits[w] = 0u;
+    __syncthreads();
+    if (P.ban_cu)
+      for (int64_t k = ban_b + tid; k < ban_e; k += kThreads) mark(ban_bits, P.ban_ids[k]);
+    if (P.rep_penalty && P.pen_cu)
+      for (int64_t k = pen_b + tid; k < pen_e; k += kThreads) mark(pen_bits, P.pen_ids[k]);
+    __syncthreads();
+  }
+  if (!ok) {
+    // nothing sampled
   } else if (temp == 0.0f) {
     unsigned long long best = 0;
     uint32_t fl = 0;
-    argmax_logits<TIn, kVec>(row + x0, x0, n, best, fl);
+    if (procs) {  // the row goes through shared memory to be processed
+      const TIn *grow[2] = {row + x0, nullptr};
+      if (load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase) & kFlagTimeout) fl |= SV_DATA_COPY_TIMEOUT;
+      apply_processors(srow, 1, n, pen_bits, ban_bits, words, theta);
+      argmax_smem(srow[0], x0, n, best, fl);
+    } else {
+      argmax_logits<TIn, kVec>(row + x0, x0, n, best, fl);
+    }
     const KeyFlags kr = cluster_reduce(KeyFlags{best, fl}, sm.red, step++, ncta);
-    if (kr.flags & SV_DATA_BAD_VALUES) bits |= SV_DATA_BAD_VALUES;
+    if (kr.flags & (SV_DATA_BAD_VALUES | SV_DATA_COPY_TIMEOUT)) bits |= kr.flags & (SV_DATA_BAD_VALUES | SV_DATA_COPY_TIMEOUT);
     else token = static_cast<int32_t>(key_index(kr.key));
   } else {
     int topk = P.top_k ? P.top_k[r] : 0;
@@ -1658,6 +1701,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
     } else {
       const TIn *grow[2] = {row + x0, nullptr};
       const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase);
+      if (procs) apply_processors(srow, 1, n, pen_bits, ban_bits, words, theta);
       RowStats st[2];
       if (!position_stats<TIn>(sm, inbox, srow, 1, n, __fdiv_rn(kLog2e, temp), topk, topp, lf, st, &bits, step,
                                ncta, rank)) {
@@ -1798,7 +1842,8 @@ cudaError_t enable_sample_kernels(int max_cluster, int max_dyn) {
 
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
   const bool test = p.exponentials != nullptr;
-  const size_t dyn = static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster);
+  const size_t dyn = static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster) +
+                     ((p.rep_penalty || p.ban_cu) ? logits_bitmap_bytes(chunk) : 0);
   if (bf16) {
     if (test) return vec ? launch_sample_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
                          : launch_sample_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);

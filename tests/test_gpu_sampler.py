@@ -117,3 +117,61 @@ def test_sampler_production_chi_square():
     assert np.all(cnt[e == 0] == 0)
     nz = e > 0
     assert scipy.stats.chisquare(cnt[nz], R * e[nz] / e[nz].sum()).pvalue > 0.01
+
+
+def _proc_lists(R, V, rng):
+    ctx = [rng.integers(-2, V + 2, size=int(rng.integers(0, 60))) for _ in range(R)]
+    ban = [rng.integers(0, V, size=int(rng.integers(0, 8))) for _ in range(R)]
+    out = {"repetition_penalty": rng.uniform(0.6, 2.0, size=R).astype(np.float32)}
+    for name, lists in (("penalty", ctx), ("banned", ban)):
+        out[f"{name}_cu"] = np.cumsum([len(x) for x in lists]).astype(np.int64)
+        out[f"{name}_ids"] = np.concatenate(lists).astype(np.int32)
+    return out
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("temp", [0.0, 0.8])
+def test_sampler_with_processors(bf16, temp):
+    """Banned tokens and the repetition penalty per row, against the oracle:
+    tokens exact (outside the tolerance band of the race) and the written q
+    rows within 1e-6."""
+    import torch
+    import speculative_decoding_token_rejection_gb300 as sv
+    rng = np.random.default_rng(int(bf16) + 2)
+    R, V = 24, 20000
+    rows = rng.standard_normal((R, V)).astype(np.float32) * 2.5
+    if bf16:
+        rows = workloads._to_bf16_bits(rows)
+    lists = _proc_lists(R, V, rng)
+    # the argmax of a few rows is banned outright
+    E = rng.exponential(size=(R, V)).astype(np.float32)
+    kw = dict(temperature=np.full(R, temp, np.float32), top_k=np.full(R, 50, np.int32),
+              top_p=np.full(R, 0.9, np.float32))
+    o = oracle.sample_rows(rows, exponentials=E, **kw, repetition_penalty=lists["repetition_penalty"],
+                           penalty_cu=lists["penalty_cu"], penalty_ids=lists["penalty_ids"],
+                           banned_cu=lists["banned_cu"], banned_ids=lists["banned_ids"])
+    dev = torch.device("cuda:0")
+    t = (torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16) if bf16 else torch.from_numpy(rows)).to(dev)
+    tok = torch.full((R,), -7, dtype=torch.int32, device=dev)
+    probs = torch.zeros((R, V), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    h = sv.spec_verify_create(R, 1, V, device=0)
+    try:
+        T = lambda x, dt: torch.as_tensor(x).to(dev)
+        sv.spec_verify_sample(h, logits=t, tokens=tok, probs=probs, exponentials=torch.from_numpy(E).to(dev),
+                              temperature=T(kw["temperature"], None), top_k=T(kw["top_k"], None),
+                              top_p=T(kw["top_p"], None), status=st,
+                              repetition_penalty=T(lists["repetition_penalty"], None),
+                              penalty_cu=T(lists["penalty_cu"], None), penalty_token_ids=T(lists["penalty_ids"], None),
+                              banned_cu=T(lists["banned_cu"], None), banned_token_ids=T(lists["banned_ids"], None))
+        torch.cuda.synchronize()
+    finally:
+        sv.spec_verify_destroy(h)
+    assert int(st.item()) == o["status"]
+    g = tok.cpu().numpy()
+    exempt = o["diag"][:, 0] < 1
+    np.testing.assert_array_equal(g[~exempt], o["tokens"][~exempt])
+    assert exempt.mean() <= 0.1
+    if temp > 0:
+        d = np.abs(probs.cpu().numpy() - o["probs"])
+        assert d.max() <= 1e-6

@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_description(lib):
-    assert lib.spec_verify_abi_version() == 4
+    assert lib.spec_verify_abi_version() == 5
     assert lib.spec_verify_sizeof_args() == ctypes.sizeof(sv.SpecVerifyArgs)
     assert lib.spec_verify_sizeof_config() == ctypes.sizeof(sv.SpecVerifyConfig)
 
