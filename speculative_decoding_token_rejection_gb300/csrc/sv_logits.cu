@@ -196,7 +196,6 @@ struct Inbox {
   unsigned long long tot[2];
   uint16_t cnt[2][kNearBins];
 };
-constexpr int kInboxWords = sizeof(Inbox) / 16;  // 16-byte stores per sender per peer
 static_assert(sizeof(Inbox) % 16 == 0, "inbox slots are written with 16-byte stores");
 
 struct LogitsSmem {
@@ -845,20 +844,6 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       const int nw = n >> 1;
       const int ng = nw >> 2;  // 16-byte groups
       const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
-      // Counting one candidate: the warp walks the set bits of per-lane masks
-      // in step, one candidate per lane per trip.
-      auto count_group = [&](int v, uint32_t em) {
-        while (__any_sync(0xFFFFFFFFu, em != 0u)) {
-          if (em != 0u) {
-            const int pos = __ffs(em) - 1;
-            em &= em - 1u;
-            const int x = 8 * v + 2 * (pos & 3) + (pos >> 2);
-            const uint32_t b = bits_at(row, x);
-            const uint32_t d = lk16 - E::key(b);
-            if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
-          }
-        }
-      };
       // 8-bit candidate mask of one 16-byte group: bit t is the low half of
       // word t, bit 4 + t its high half
       auto group_mask = [&](const uint4 &dv) {
@@ -869,7 +854,8 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       };
       if (reg_groups) {
         // groups whose largest value reaches the window, two per compare; only
-        // those are read again
+        // those are read again, and the warp walks the set bits of their
+        // candidate masks in step (one candidate per lane per trip)
         uint32_t cg = 0u;
 #pragma unroll
         for (int i = 0; i < kGroupWords; ++i) {
@@ -877,15 +863,25 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
           cg |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * i);
         }
         while (__any_sync(0xFFFFFFFFu, cg != 0u)) {
-          int v = 0;
+          uint4 dv = make_uint4(0u, 0u, 0u, 0u);
           uint32_t em = 0u;
           if (cg != 0u) {
             const int pos = __ffs(cg) - 1;
             cg &= cg - 1u;
-            v = tid + pos * kThreads;
-            em = group_mask(s4[v]);
+            dv = s4[tid + pos * kThreads];
+            em = group_mask(dv);
           }
-          count_group(v, em);
+          // the candidates come out of the group already in registers
+          while (__any_sync(0xFFFFFFFFu, em != 0u)) {
+            if (em != 0u) {
+              const int pos = __ffs(em) - 1;
+              em &= em - 1u;
+              const uint32_t wv = (pos & 2) ? ((pos & 1) ? dv.w : dv.z) : ((pos & 1) ? dv.y : dv.x);
+              const uint32_t b = (pos & 4) ? (wv >> 16) : (wv & 0xFFFFu);
+              const uint32_t d = lk16 - E::key(b);
+              if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
+            }
+          }
         }
       }
       // Otherwise a lane tests eight 16-byte groups at once (packed compares,
