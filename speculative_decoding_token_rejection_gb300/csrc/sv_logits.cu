@@ -1120,11 +1120,23 @@ __device__ __forceinline__ void race_quad_l(const float w[4], int xg, const floa
   }
 }
 
+// A race weight: the probability with the normaliser applied as a product
+// with its reciprocal (within an ulp of the quotient prob_of gives; race keys
+// that close are inside the tolerance band anyway), which spares a division
+// per entry of a dense row.
+template <typename TIn>
+__device__ __forceinline__ float weight_of(uint32_t b, const RowStats &st, float rz) {
+  using E = Elem<TIn>;
+  if (E::key(b) < st.cut) return 0.0f;
+  return __fmul_rn(exp2f(__fmul_rn(__fsub_rn(E::val(b), st.vmax), st.c2)), rz);
+}
+
 template <typename TIn, bool kResidual>
-__device__ __forceinline__ float race_w(uint32_t bp, uint32_t bq, const RowStats &ps, const RowStats &qs) {
-  const float p = prob_of<TIn>(bp, ps);
+__device__ __forceinline__ float race_w(uint32_t bp, uint32_t bq, const RowStats &ps, const RowStats &qs, float rp,
+                                        float rq) {
+  const float p = weight_of<TIn>(bp, ps, rp);
   if (kResidual) {
-    const float d = __fsub_rn(p, prob_of<TIn>(bq, qs));
+    const float d = __fsub_rn(p, weight_of<TIn>(bq, qs, rq));
     return d > 0.0f ? d : 0.0f;
   }
   return p > 0.0f ? p : 0.0f;
@@ -1146,6 +1158,7 @@ __device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const Ro
   const uint32_t cpb = bf16_bits_of_key(ps.cut), cqb = bf16_bits_of_key(qs.cut);
   const uint32_t cp2 = cpb | (cpb << 16), cq2 = cqb | (cqb << 16);
   const bool packed_test = sizeof(TIn) == 2 && (ps.cut > 0x007Fu) && (!kResidual || qs.cut > 0x007Fu);
+  const float rp = __frcp_rn(ps.zp), rq = __frcp_rn(qs.zp);
   for (int v = threadIdx.x; v < nv; v += kThreads) {
     const uint4 dp = p4[v];
     const uint4 dq = kResidual ? q4[v] : dp;
@@ -1163,10 +1176,10 @@ __device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const Ro
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       if (sizeof(TIn) == 2) {
-        w[2 * t] = race_w<TIn, kResidual>(wp[t] & 0xFFFFu, wq[t] & 0xFFFFu, ps, qs);
-        w[2 * t + 1] = race_w<TIn, kResidual>(wp[t] >> 16, wq[t] >> 16, ps, qs);
+        w[2 * t] = race_w<TIn, kResidual>(wp[t] & 0xFFFFu, wq[t] & 0xFFFFu, ps, qs, rp, rq);
+        w[2 * t + 1] = race_w<TIn, kResidual>(wp[t] >> 16, wq[t] >> 16, ps, qs, rp, rq);
       } else {
-        w[t] = race_w<TIn, kResidual>(wp[t], wq[t], ps, qs);
+        w[t] = race_w<TIn, kResidual>(wp[t], wq[t], ps, qs, rp, rq);
       }
     }
 #pragma unroll
@@ -1178,7 +1191,7 @@ __device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const Ro
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int x = 4 * q + t;
-      w[t] = x < n ? race_w<TIn, kResidual>(bits_at(sp, x), kResidual ? bits_at(sq, x) : 0u, ps, qs) : 0.0f;
+      w[t] = x < n ? race_w<TIn, kResidual>(bits_at(sp, x), kResidual ? bits_at(sq, x) : 0u, ps, qs, rp, rq) : 0.0f;
     }
     race_quad_l<kTest>(w, x0 + 4 * q, Erow, rk, rs, bk, bx, flags);
   }
