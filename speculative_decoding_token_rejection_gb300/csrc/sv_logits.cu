@@ -198,8 +198,19 @@ struct Inbox {
 };
 static_assert(sizeof(Inbox) % 16 == 0, "inbox slots are written with 16-byte stores");
 
+// Windows below the first: running totals and results per row.
+struct Bands {
+  unsigned long long cnt_above[2];   // keys above the current window
+  unsigned long long mass_above[2];  // their fixed-point mass
+  unsigned long long kept[2];        // mass of the kept set once resolved
+  uint32_t cut[2];                   // resolved cut (16-bit key)
+  int done[2];                       // resolved (or needs no further window)
+  int fallback;                      // give the rows to the multi-pass selection
+};
+
 struct LogitsSmem {
   ReduceSmem red;
+  Bands bands;
   StatPart part[2];
   StatSum sum;
   NearSum near;
@@ -681,6 +692,267 @@ __device__ __forceinline__ bool near_select(const unsigned long long *cnt, const
   return true;
 }
 
+// One warp resolves a row in a window below the first one.  cnt_above and
+// mass_above are the count and fixed-point mass of every key above the
+// window; the choices are those of near_select continued across windows.
+// Returns 1 when resolved (*out), 0 when the threshold or cut lies further
+// down (*cnt_tot, *mass_tot: this window's totals), 2 when the top-p cut of a
+// top-k row lies above this window (the multi-pass selection takes over).
+__device__ __forceinline__ int band_select(const unsigned long long *cnt, const unsigned long long *mass, int topk,
+                                           bool use_p, float topp, unsigned long long total,
+                                           unsigned long long cnt_above, unsigned long long mass_above,
+                                           NearChoice *out, unsigned long long *cnt_tot,
+                                           unsigned long long *mass_tot) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long c[kBinsPerLane], m[kBinsPerLane], cs = 0, ms = 0;
+#pragma unroll
+  for (int t = 0; t < kBinsPerLane; ++t) {
+    c[t] = cnt[kBinsPerLane * lane + t];
+    m[t] = mass[kBinsPerLane * lane + t];
+    cs += c[t];
+    ms += m[t];
+  }
+  unsigned long long ci = cs, mi = ms;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long vc = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+    const unsigned long long vm = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+    if (lane >= o) {
+      ci += vc;
+      mi += vm;
+    }
+  }
+  *cnt_tot = __shfl_sync(0xFFFFFFFFu, ci, 31);
+  *mass_tot = __shfl_sync(0xFFFFFFFFu, mi, 31);
+  const unsigned long long cb = cnt_above + ci - cs, mb = mass_above + mi - ms;  // totals before this lane's bins
+  int last = kNearBins - 1;
+  unsigned long long kept = 0;
+  if (topk > 0) {
+    const unsigned long long k = static_cast<unsigned long long>(topk);
+    int found = -1;
+    unsigned long long kin = 0;
+    if (cb < k && cnt_above + ci >= k) {
+      unsigned long long acc = cb, macc = mb;
+#pragma unroll
+      for (int t = 0; t < kBinsPerLane; ++t) {
+        acc += c[t];
+        macc += m[t];
+        if (found < 0 && acc >= k) {
+          found = kBinsPerLane * lane + t;
+          kin = macc;
+        }
+      }
+    }
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0);
+    if (!ball) return 0;
+    const int src = __ffs(ball) - 1;
+    last = __shfl_sync(0xFFFFFFFFu, found, src);
+    kept = __shfl_sync(0xFFFFFFFFu, kin, src);
+    if (!use_p) {
+      out->last = last;
+      out->kept = kept;
+      return 1;
+    }
+  } else {
+    kept = total;
+  }
+  unsigned long long need = static_cast<unsigned long long>(static_cast<double>(topp) * static_cast<double>(kept));
+  if (need == 0ull) need = 1ull;
+  if (topk > 0 && need <= mass_above) return 2;
+  int found = -1;
+  unsigned long long in = 0;
+  if (mb < need && mass_above + mi >= need) {
+    unsigned long long acc = mb;
+#pragma unroll
+    for (int t = 0; t < kBinsPerLane; ++t) {
+      acc += m[t];
+      if (found < 0 && acc >= need) {
+        found = kBinsPerLane * lane + t;
+        in = acc;
+      }
+    }
+  }
+  const unsigned ball = __ballot_sync(0xFFFFFFFFu, found >= 0 && found <= last);
+  if (!ball) return 0;
+  const int src = __ffs(ball) - 1;
+  out->last = __shfl_sync(0xFFFFFFFFu, found, src);
+  out->kept = __shfl_sync(0xFFFFFFFFu, in, src);
+  return 1;
+}
+
+constexpr int kMaxBands = 24;  // windows below the first before the multi-pass selection takes over
+
+// Windows 1, 2, ... below the first: window b holds the keys
+// [g - kNearBins (b + 1) + 1, g - kNearBins b] of the row's global maximum g.
+// Rows the first window resolved keep its result.  Returns false when a row
+// needs the multi-pass selection (the cut of a top-k row above its threshold's
+// window, or more than kMaxBands windows).
+template <typename TIn>
+__device__ bool window_rounds(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], int nr, int n, float c2, int topk,
+                              bool use_p, float topp, RowStats st[2], int &step, uint32_t ncta, uint32_t rank) {
+  using E = Elem<TIn>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  NearSum &ns = sm.near;
+  Bands &bd = sm.bands;
+  if (warp < nr) {  // the first window's totals (complete whenever it failed)
+    const int r = warp;
+    unsigned long long c = 0, m = 0;
+#pragma unroll
+    for (int t = 0; t < kBinsPerLane; ++t) {
+      c += ns.cnt[r][kBinsPerLane * lane + t];
+      m += ns.mass[r][kBinsPerLane * lane + t];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+      m += __shfl_xor_sync(0xFFFFFFFFu, m, o);
+    }
+    if (lane == 0) {
+      bd.done[r] = sm.sel.ok[r];
+      bd.cnt_above[r] = c;
+      bd.mass_above[r] = m;
+    }
+  }
+  if (tid == 0) bd.fallback = 0;
+  __syncthreads();
+  uint32_t g16[2] = {0u, 0u};
+  float gv[2] = {0.0f, 0.0f};
+  for (int r = 0; r < nr; ++r) {
+    g16[r] = ns.gmax[r];
+    gv[r] = E::val_of_key(ns.gmax[r]);
+  }
+  const int ng = n >> 3;
+  for (int band = 1;; ++band) {
+    bool active = false;
+    for (int r = 0; r < nr; ++r) active |= !bd.done[r];
+    if (!active || bd.fallback) break;
+    const int par = step & 1;
+    StatPart &bp = sm.part[par];
+    zero_part(bp, kRCnt, nr);
+    __syncthreads();
+    for (int r = 0; r < nr; ++r) {
+      if (bd.done[r]) continue;
+      const int hi = static_cast<int>(g16[r]) - kNearBins * band;  // this window's largest key
+      if (hi < 0x80) continue;  // below every finite key: nothing to count
+      const int lo = max(hi - (kNearBins - 1), 0x80);
+      const uint32_t lob = bf16_bits_of_key(static_cast<uint32_t>(lo)),
+                     hib = bf16_bits_of_key(static_cast<uint32_t>(hi + 1));
+      const uint32_t lo2 = lob | (lob << 16), hi2 = hib | (hib << 16);
+      uint32_t *cnt = bp.cnt[r];
+      const TIn *row = srow[r];
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
+      auto band_mask = [&](const uint4 &dv) {  // bit t: low half of word t in the window, bit 4 + t: high half
+        uint32_t g = ((bf16x2_ge_mask(dv.x, lo2) & ~bf16x2_ge_mask(dv.x, hi2)) & 0x00010001u) |
+                     (((bf16x2_ge_mask(dv.y, lo2) & ~bf16x2_ge_mask(dv.y, hi2)) & 0x00010001u) << 1) |
+                     (((bf16x2_ge_mask(dv.z, lo2) & ~bf16x2_ge_mask(dv.z, hi2)) & 0x00010001u) << 2) |
+                     (((bf16x2_ge_mask(dv.w, lo2) & ~bf16x2_ge_mask(dv.w, hi2)) & 0x00010001u) << 3);
+        return (g | (g >> 12)) & 0xFFu;
+      };
+      auto count = [&](uint32_t b) {
+        const uint32_t d = static_cast<uint32_t>(hi) - E::key(b);
+        if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
+      };
+      // every group of this thread is read (these windows are rare; keeping
+      // the group maxima live through the reduction would cost registers on
+      // the common path), 32 groups per mask word
+      const int per_thread = (ng + kThreads - 1) / kThreads;
+      for (int i0 = 0; i0 < per_thread; i0 += 32) {
+        uint32_t cg = 0u;
+        for (int i = i0; i < min(per_thread, i0 + 32); ++i)
+          if (tid + i * kThreads < ng) cg |= 1u << (i - i0);
+        while (__any_sync(0xFFFFFFFFu, cg != 0u)) {
+          uint4 dv = make_uint4(0u, 0u, 0u, 0u);
+          uint32_t em = 0u;
+          if (cg != 0u) {
+            const int pos = __ffs(cg) - 1;
+            cg &= cg - 1u;
+            dv = s4[tid + (i0 + pos) * kThreads];
+            em = band_mask(dv);
+          }
+          while (__any_sync(0xFFFFFFFFu, em != 0u)) {
+            if (em != 0u) {
+              const int pos = __ffs(em) - 1;
+              em &= em - 1u;
+              const uint32_t wv = (pos & 2) ? ((pos & 1) ? dv.w : dv.z) : ((pos & 1) ? dv.y : dv.x);
+              count((pos & 4) ? (wv >> 16) : (wv & 0xFFFFu));
+            }
+          }
+        }
+      }
+      for (int x = (ng << 3) + tid; x < n; x += kThreads) count(bits_at(row, x));
+    }
+    __syncthreads();
+    // every CTA stores its window counts (16-bit) into its slot of every peer's
+    // inbox; after the barrier the sums need no shift (one anchor for all)
+    Inbox *const ibx = inbox + par * static_cast<int>(ncta);
+    {
+      const int words = kNearBins / 8;
+      for (int t = tid; t < nr * words * static_cast<int>(ncta); t += kThreads) {
+        const int c = t / (nr * words), k = t % (nr * words);
+        const int r = k / words, d0 = (k % words) * 8;
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
+        if (!bd.done[r]) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) h[q] = bp.cnt[r][d0 + 2 * q] | (bp.cnt[r][d0 + 2 * q + 1] << 16);
+        }
+        st_dsmem_v4(map_to_rank(smem_addr(reinterpret_cast<uint4 *>(&ibx[rank]) + 3 + r * words + d0 / 8),
+                                static_cast<uint32_t>(c)),
+                    make_uint4(h[0], h[1], h[2], h[3]));
+      }
+    }
+    cluster_sync();
+    ++step;
+    if (tid < nr * kNearBins) {
+      const int r = tid / kNearBins, d = tid % kNearBins;
+      unsigned long long cs = 0;
+      const int key = static_cast<int>(g16[r]) - kNearBins * band - d;
+      if (!bd.done[r] && key >= 0x80) {
+        for (int c = 0; c < static_cast<int>(ncta); ++c) cs += ibx[c].cnt[r][d];
+      }
+      ns.cnt[r][d] = cs;
+      ns.mass[r][d] = cs ? cs * to_fixed(exp2f(__fmul_rn(__fsub_rn(E::val_of_key(static_cast<uint32_t>(key)), gv[r]),
+                                                       c2)))
+                         : 0ull;
+    }
+    __syncthreads();
+    if (warp < nr && !bd.done[warp]) {
+      const int r = warp;
+      NearChoice ch;
+      unsigned long long ct = 0, mt = 0;
+      const int res = band_select(ns.cnt[r], ns.mass[r], topk, use_p, topp, ns.tot[r], bd.cnt_above[r],
+                                  bd.mass_above[r], &ch, &ct, &mt);
+      if (lane == 0) {
+        const int hi = static_cast<int>(g16[r]) - kNearBins * band;
+        if (res == 1) {
+          bd.done[r] = 1;
+          bd.cut[r] = static_cast<uint32_t>(hi - ch.last);
+          bd.kept[r] = ch.kept;
+        } else if (res == 2 || band >= kMaxBands || hi - (kNearBins - 1) <= 0x80) {
+          bd.fallback = 1;  // (keys exhausted without a cut: rounding between the totals)
+        } else {
+          bd.cnt_above[r] += ct;
+          bd.mass_above[r] += mt;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (bd.fallback) {
+    __syncthreads();
+    return false;
+  }
+  for (int r = 0; r < nr; ++r) {
+    if (sm.sel.ok[r]) {  // resolved by the first window
+      st[r].cut = sm.sel.prefix[r];
+      st[r].zp = ns.z[r];
+    } else {
+      st[r].cut = bd.cut[r];
+      st[r].zp = static_cast<float>(static_cast<double>(bd.kept[r]) * (1.0 / static_cast<double>(kMassScale)));
+    }
+  }
+  return true;
+}
+
 template <typename TIn>
 __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], int nr, int n, float c2, int topk,
                                float topp, uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step,
@@ -911,12 +1183,17 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
         if (E::finite(b) && E::key(b) >= lo && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
       }
       if (use_p && !use_k) {  // top-p alone: the whole row is kept before the cut
+        // a compensated fp32 sum per thread, converted once to fixed point
         const float lv = E::val_of_key(lp.maxkey[r]);
-        unsigned long long tot = 0;
+        float sum = 0.0f, comp = 0.0f;
         for_each_elem(srow[r], n, [&](uint32_t b, int) {
-          if (E::finite(b)) tot += to_fixed(exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2)));
+          if (!E::finite(b)) return;
+          const float y = exp2f(__fmul_rn(__fsub_rn(E::val(b), lv), c2)) - comp;  // Kahan
+          const float t = sum + y;
+          comp = (t - sum) - y;
+          sum = t;
         });
-        tt[r] = tot;
+        tt[r] = to_fixed(sum);
       }
     }
     if (use_p && !use_k) block_sum_tot(sm, lp, tt, nr);
@@ -1060,6 +1337,14 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
     }
     return true;
   }
+  // bf16 rows whose top-k threshold or top-p cut lies below the first window:
+  // count the next windows of kNearBins keys, anchored on the global maximum
+  // (the first window's bins are complete when it fails: with top-p alone no
+  // floor applies, and a top-k threshold below the window puts every CTA's
+  // floor below it too), one reduction per window
+  if (kB == 16 && window_rounds<TIn>(sm, inbox, srow, nr, n, c2, use_k ? topk : 0, use_p, topp, st, step, ncta,
+                                     rank))
+    return true;
   uint32_t maxk16[2] = {0u, 0u};
   for (int r = 0; r < nr; ++r) maxk16[r] = key16_of<TIn>(ns.gmax[r]);
   __syncthreads();
