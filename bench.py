@@ -58,6 +58,7 @@ def parse_args():
     ap.add_argument("--requests", type=int, default=0, help="override the batch size (profiling runs only)")
     ap.add_argument("--logits-steps", type=int, default=300)
     ap.add_argument("--no-logits", action="store_true")
+    ap.add_argument("--logits-variant-steps", type=int, default=30)
     ap.add_argument("--ngram-steps", type=int, default=200)
     ap.add_argument("--logits-resident", action="store_true",
                     help="keep both row chunks of the logits entry in shared memory (comparison runs)")
@@ -191,19 +192,22 @@ def logits_algorithmic_bytes(nacc, gammas, temps, V, G, elem=2):
     return int(per.sum())
 
 
-def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
+def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, top_p=0.9, steps=None, w=None):
     """The logits entry on the same batch shape: bf16 target/draft logits with
-    T=0.8, top-k 50, top-p 0.9 per request (production Philox)."""
+    T=0.8, top-k 50, top-p 0.9 per request (production Philox); other
+    sampling settings on the same rows with ``top_k`` / ``top_p``."""
     import numpy as np
     import torch
     import workloads
-    w = workloads.make("fused", seed=3 + 1000 * rank, test_mode=False, N=args.requests or None)
+    if w is None:
+        w = workloads.make("fused", seed=3 + 1000 * rank, test_mode=False, N=args.requests or None)
     N, G, V, T = w["N"], w["gamma"], w["V"], w["T"]
+    w = dict(w, top_k=np.full(N, top_k, np.int32), top_p=np.full(N, top_p, np.float32))
     gam = workloads.gammas_of(w)
     t = workloads.as_torch(w, dev)
     ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster,
                       flags=sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0)
-    K = max(3, min(args.steps, args.logits_steps))
+    K = max(3, min(args.steps, steps or args.logits_steps))
     W = args.warmup
     nacc = torch.empty((K + W, N), dtype=torch.int32, device=dev)
     out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
@@ -247,8 +251,8 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
     traffic, traffic_sha = stored_traffic("verify_logits_fused", LOGITS_KERNEL_SOURCES)
     ver.close()
     return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
-            "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k 50, top-p 0.9, "
-                                   "production Philox", "entry": "logits",
+            "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k {top_k if top_k > 0 else 'off'}, "
+                                   f"top-p {top_p if top_p < 1 else 'off'}, production Philox", "entry": "logits",
                        "draft_rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
@@ -258,7 +262,7 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream):
                          "traffic_source_sha": traffic_sha},
             "acceptance": {"mean_accepted": float(na.mean()),
                            "A_hist": np.bincount(na.reshape(-1), minlength=G + 1).tolist()},
-            "gpu_launches": K}
+            "gpu_launches": K, "_w": w}
 
 
 def time_ngram(args, sv, dev, world, rank, dist, stream):
@@ -406,6 +410,17 @@ def run_ours(args, world, rank, local_rank):
     t1 = time.time()
     barrier()
     logits = None if args.no_logits else time_logits_entry(args, sv, lib, dev, world, rank, dist, stream)
+    if logits:
+        # the same rows under two other common settings (fewer launches)
+        wl = logits.pop("_w")
+        logits["other_settings"] = {}
+        for name, kk, pp in (("top_p_0.9_alone", 0, 0.9), ("temperature_alone", 0, 1.0)):
+            o = time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=kk, top_p=pp,
+                                  steps=args.logits_variant_steps, w=wl)
+            o.pop("_w")
+            logits["other_settings"][name] = {k: o[k] for k in ("value", "ms_per_step", "steps", "config")}
+            logits["other_settings"][name]["roofline_frac"] = o["roofline"]["frac"]
+            logits["gpu_launches"] += o["gpu_launches"]
     ngram = None if args.no_ngram else time_ngram(args, sv, dev, world, rank, dist, stream)
     clocks.stop()
     total_ms = ev[0].elapsed_time(ev[K])
