@@ -981,27 +981,86 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   const int ng_all = n >> 3;
   const bool reg_groups = kB == 16 && ng_all <= 2 * kGroupWords * kThreads;
   uint32_t gw[2][kGroupWords];
+  // dense rows with register-held group maxima also sum their weights in this
+  // pass: each thread keeps a compensated sum relative to its running maximum
+  // and rescales it when the maximum rises (once per rising group)
+  const bool fuse_z = !near && reg_groups;
+  float omax[2] = {-INFINITY, -INFINITY}, osum[2] = {0.0f, 0.0f};
   for (int r = 0; r < nr; ++r) {
     if (kB == 16 && reg_groups) {
       const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
       uint32_t acc = 0xFF80FF80u;  // (-inf, -inf)
-#pragma unroll
-      for (int i = 0; i < kGroupWords; ++i) {
-        uint32_t half[2] = {0x7FFFu, 0x7FFFu};  // NaN: never a window candidate
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int v = tid + (2 * i + h) * kThreads;
-          if (v < ng_all) {
-            const uint4 d = s4[v];
-            uint32_t p2 = bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w));
-            p2 = bf16x2_max_nan(p2, (p2 >> 16) | (p2 << 16));
-            acc = bf16x2_max_nan(acc, p2);
-            half[h] = p2 & 0xFFFFu;
+      float om = -INFINITY, oz = 0.0f, oc = 0.0f;
+      auto raise_to = [&](float m) {  // a larger running maximum: rescale the sum
+        if (m > om) {
+          if (om != -INFINITY) {
+            const float f = exp2f(__fmul_rn(__fsub_rn(om, m), c2));
+            oz = __fmul_rn(oz, f);
+            oc = __fmul_rn(oc, f);
           }
+          om = m;
         }
-        gw[r][i] = half[0] | (half[1] << 16);
+      };
+      auto add = [&](uint32_t b) {  // (-inf adds 0; NaN/+inf rows are rejected anyway)
+        const float y = exp2f(__fmul_rn(__fsub_rn(E::val(b), om), c2)) - oc;  // Kahan
+        const float t = oz + y;
+        oc = (t - oz) - y;
+        oz = t;
+      };
+      if (fuse_z) {  // (its own copy of the loop: the common one stays as it is)
+#pragma unroll
+        for (int i = 0; i < kGroupWords; ++i) {
+          uint32_t half[2] = {0x7FFFu, 0x7FFFu};  // NaN: never a window candidate
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int v = tid + (2 * i + h) * kThreads;
+            if (v < ng_all) {
+              const uint4 d = s4[v];
+              uint32_t p2 = bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w));
+              p2 = bf16x2_max_nan(p2, (p2 >> 16) | (p2 << 16));
+              acc = bf16x2_max_nan(acc, p2);
+              half[h] = p2 & 0xFFFFu;
+              raise_to(E::val(p2 & 0xFFFFu));
+              if (om != -INFINITY) {
+                const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  add(w[t] & 0xFFFFu);
+                  add(w[t] >> 16);
+                }
+              }
+            }
+          }
+          gw[r][i] = half[0] | (half[1] << 16);
+        }
+        for (int x = (ng_all << 3) + tid; x < n; x += kThreads) {
+          const uint32_t b = bits_at(srow[r], x);
+          acc = bf16x2_max_nan(acc, b | 0xFF800000u);
+          raise_to(E::val(b));
+          if (om != -INFINITY) add(b);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kGroupWords; ++i) {
+          uint32_t half[2] = {0x7FFFu, 0x7FFFu};  // NaN: never a window candidate
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int v = tid + (2 * i + h) * kThreads;
+            if (v < ng_all) {
+              const uint4 d = s4[v];
+              uint32_t p2 = bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w));
+              p2 = bf16x2_max_nan(p2, (p2 >> 16) | (p2 << 16));
+              acc = bf16x2_max_nan(acc, p2);
+              half[h] = p2 & 0xFFFFu;
+            }
+          }
+          gw[r][i] = half[0] | (half[1] << 16);
+        }
+        for (int x = (ng_all << 3) + tid; x < n; x += kThreads)
+          acc = bf16x2_max_nan(acc, bits_at(srow[r], x) | 0xFF800000u);
       }
-      for (int x = (ng_all << 3) + tid; x < n; x += kThreads) acc = bf16x2_max_nan(acc, bits_at(srow[r], x) | 0xFF800000u);
+      omax[r] = om;
+      osum[r] = oz;
       acc = bf16x2_max_nan(acc, (acc >> 16) | (acc << 16));
       const uint32_t mb = acc & 0xFFFFu;  // this thread's largest value, NaN if it saw one
       if (E::is_nan(mb) || E::is_pinf(mb)) fl[r] |= kFlagBad;
@@ -1202,6 +1261,10 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
     for (int r = 0; r < nr; ++r) {
       if (!(lp.flags[r] & kFlagFinite)) continue;
       const float lv = E::val_of_key(lp.maxkey[r]);
+      if (fuse_z) {  // the max pass summed already: rescale onto the CTA's maximum
+        zt[r] = omax[r] != -INFINITY ? __fmul_rn(osum[r], exp2f(__fmul_rn(__fsub_rn(omax[r], lv), c2))) : 0.0f;
+        continue;
+      }
       float sum = 0.0f, comp = 0.0f;
       for_each_elem(srow[r], n, [&](uint32_t b, int) {
         if (!E::finite(b)) return;  // -inf adds nothing (NaN/+inf already flagged)
