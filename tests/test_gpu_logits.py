@@ -319,3 +319,31 @@ def test_explicit_cluster_sizes(cluster, resident):
     o = oracle.verify(w)
     g = H().run_gpu(w, cluster_ctas=cluster, flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0)
     compare_logits(g, o, w, max_exempt_frac=0.1)
+
+
+@pytest.mark.parametrize("top_k,top_p,temp,budget", [
+    (2000, 1.0, 0.8, 0.5),     # top-k threshold several windows below the maximum
+    (2000, 0.9, 0.8, 0.5),     # ... with a cut inside its window or above it (the multi-pass selection)
+    (600, 0.3, 1.0, 0.5),
+    (0, 0.9, 0.8, 0.5),        # top-p alone, cut below the first window
+    (0, 0.95, 0.8, 0.5),       # a wider nucleus: more windows
+    (0, 0.98, 0.6, 0.5),
+    # close to 1 on a flat row: each key near the cut carries < 1e-6 of mass, so
+    # every cut lies in the 1e-6 edge band; outputs are checked for validity
+    (0, 0.9999, 2.5, 1.0),
+    (5000, 0.97, 1.2, 0.5)])
+def test_thresholds_below_the_first_window(top_k, top_p, temp, budget):
+    """Rows whose threshold or cut lies below the first 128-key window, on a
+    vocabulary large enough for several windows."""
+    w = workloads.make("fused", N=12, V=40000, seed=37)
+    w["top_k"] = np.full(12, top_k, np.int32)
+    w["top_p"] = np.full(12, top_p, np.float32)
+    w["temperature"] = np.full(12, temp, np.float32)
+    o = oracle.verify(w)
+    g = H().run_gpu(w)
+    compare_logits(g, o, w, max_exempt_frac=budget)
+    A = g["num_accepted"]
+    assert np.all((A >= 0) & (A <= w["gamma"]))
+    for i in range(12):
+        assert np.all((g["out_tokens"][i, :A[i] + 1] >= 0) & (g["out_tokens"][i, :A[i] + 1] < w["V"]))
+        assert np.all(g["out_tokens"][i, A[i] + 1:] == -1)
