@@ -984,7 +984,7 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   // dense rows with register-held group maxima also sum their weights in this
   // pass: each thread keeps a compensated sum relative to its running maximum
   // and rescales it when the maximum rises (once per rising group)
-  const bool fuse_z = !near && reg_groups;
+  const bool fuse_z = reg_groups && (!near || (use_p && !use_k));  // dense rows, or top-p alone (its total)
   float omax[2] = {-INFINITY, -INFINITY}, osum[2] = {0.0f, 0.0f};
   for (int r = 0; r < nr; ++r) {
     if (kB == 16 && reg_groups) {
@@ -1241,7 +1241,12 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
         const uint32_t d = lk16 - E::key(b);
         if (E::finite(b) && E::key(b) >= lo && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
       }
-      if (use_p && !use_k) {  // top-p alone: the whole row is kept before the cut
+      if (use_p && !use_k && fuse_z) {  // top-p alone: the max pass summed the whole row already
+        const float lv = E::val_of_key(lp.maxkey[r]);
+        tt[r] = omax[r] != -INFINITY
+                    ? to_fixed(__fmul_rn(osum[r], exp2f(__fmul_rn(__fsub_rn(omax[r], lv), c2))))
+                    : 0ull;
+      } else if (use_p && !use_k) {  // top-p alone: the whole row is kept before the cut
         // a compensated fp32 sum per thread, converted once to fixed point
         const float lv = E::val_of_key(lp.maxkey[r]);
         float sum = 0.0f, comp = 0.0f;
