@@ -253,7 +253,7 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, t
     return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
             "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k {top_k if top_k > 0 else 'off'}, "
                                    f"top-p {top_p if top_p < 1 else 'off'}, production Philox", "entry": "logits",
-                       "draft_rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)"},
+                       "rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
                          "algorithmic_bytes_per_launch": alg, "full_tensor_bytes": full,

@@ -82,11 +82,11 @@ enum sv_data_status {
   SV_DATA_BAD_LIST = 256          /* a penalty, banned or stop list range of the request is invalid */
 };
 
-/* Handle flags.  SV_FLAG_RESIDENT_ROWS: the logits entry keeps both the target
- * and the draft row chunk of a position in shared memory (two CTAs per SM).
- * By default only the target chunk is copied and the draft chunk is read in
- * place after an L2 prefetch (three CTAs per SM); calls with logits
- * processors or unaligned rows always keep both.  Results are identical. */
+/* Handle flags.  SV_FLAG_RESIDENT_ROWS: the logits entry copies both the
+ * target and the draft row chunk of a position into shared memory (two CTAs
+ * per SM).  By default both chunks are read in place after an L2 prefetch
+ * (four CTAs per SM); calls with logits processors or unaligned rows always
+ * copy them.  Results are identical. */
 #define SV_FLAG_RESIDENT_ROWS 1u
 
 typedef struct spec_verify_ctx *spec_verify_t;

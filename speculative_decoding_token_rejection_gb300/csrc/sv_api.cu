@@ -46,18 +46,26 @@ int choose_cluster(const spec_verify_ctx *ctx, int N, int V) {
 
 bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk,
                           bool bitmaps, bool resident) {
-  // The rows of the current position live in the cluster's shared memory (the
-  // target chunk, and the draft chunk too when resident).  Start from the
-  // CTA count of the probability entry and grow it until a CTA is small
-  // enough for two (resident) or three CTAs to share an SM.
+  // Resident rows live in the cluster's shared memory: start from the CTA
+  // count of the probability entry and grow it until a CTA is small enough
+  // for two to share an SM.  Rows read in place need no shared memory for
+  // themselves (four CTAs share an SM): grow the cluster, up to the portable
+  // 8, until a CTA's chunk is small enough for its group maxima to stay in
+  // registers.
   auto chunk_for = [&](int c) { return ((V + c - 1) / c + 7) & ~7; };
   auto bytes_for = [&](int c) {
     return static_cast<long long>(logits_dyn_bytes(c, chunk_for(c), elem_bytes, resident, bitmaps));
   };
-  const long long per_cta = ctx->smem_per_sm / (resident ? 2 : 3) - 1024 - static_cast<long long>(logits_static_smem());
   int c = ctx->cfg.cluster_ctas > 0 ? ctx->cfg.cluster_ctas : choose_cluster(ctx, N, V);
-  if (ctx->cfg.cluster_ctas == 0)
-    while (c < ctx->max_cluster && bytes_for(c) > per_cta) c *= 2;
+  if (ctx->cfg.cluster_ctas == 0) {
+    if (resident) {
+      const long long per_cta = ctx->smem_per_sm / 2 - 1024 - static_cast<long long>(logits_static_smem());
+      while (c < ctx->max_cluster && bytes_for(c) > per_cta) c *= 2;
+    } else {
+      const int cap = ctx->max_cluster < 8 ? ctx->max_cluster : 8;
+      while (c < cap && chunk_for(c) > logits_reg_group_chunk()) c *= 2;
+    }
+  }
   // (window bins are 16-bit counts of one CTA's chunk)
   if (bytes_for(c) > ctx->max_dyn_smem || chunk_for(c) > 65535) return false;
   *cluster = c;

@@ -99,6 +99,7 @@ cudaError_t enable_probs_kernels(int max_cluster);
 cudaError_t launch_probs(const VerifyParams &p, int cluster, bool vec, cudaStream_t stream);
 
 size_t logits_static_smem();
+int logits_reg_group_chunk();  // largest bf16 chunk whose group maxima stay in registers
 // Dynamic shared memory a logits-entry CTA needs besides its row chunks: the
 // double-buffered inboxes of the one-barrier row-statistics reduction.
 size_t logits_inbox_bytes(int cluster);

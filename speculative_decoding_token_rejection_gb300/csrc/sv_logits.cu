@@ -136,7 +136,9 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kNearBins = 128;         // near-max bins: distances 0..127 from the row's largest key
 constexpr int kMaxCluster = 16;
 constexpr int kWalkGroups = 8;  // 16-byte groups a lane tests per window-scan step
-constexpr int kGroupWords = 8;  // registers of packed group maxima per row and thread (2 groups each)
+constexpr int kGroupWords = 5;  // registers of packed group maxima per row and thread (2 groups each)
+// largest bf16 chunk whose 16-byte groups all have their maxima in registers
+constexpr int kRegGroupChunk = 2 * kGroupWords * 8 * kThreads;
 
 struct StatPart {  // one CTA's partials of one reduction round, for up to 2 rows
   uint32_t maxkey[2];
@@ -1553,13 +1555,21 @@ __device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const Ro
 // Load this CTA's chunk of nr rows into shared memory.  Aligned rows arrive
 // through one bulk copy per row (TMA, completing on the CTA's mbarrier), with
 // plain loads only for a last partial 16-byte group; other rows use plain
-// loads.  With kRes false only the target row is copied: the draft row stays
-// in global memory and is only prefetched into L2 here.  Returns
-// kFlagTimeout if the copy did not complete in time.
+// loads.  With kRes false (aligned rows only) nothing is copied: the rows are
+// read where they lie, and their chunks are only prefetched into L2 here.
+// Returns kFlagTimeout if the copy did not complete in time.
 template <typename TIn, bool kVec, bool kRes = true>
 __device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *const srow[2], int nr, int n,
                               uint32_t &phase) {
   const int tid = threadIdx.x;
+  if (kVec && !kRes) {  // both chunks are read in place: warm L2 with them
+    if (tid == 0) {
+      const uint32_t body = (static_cast<uint32_t>(n) * sizeof(TIn)) & ~15u;
+      if (body)
+        for (int r = 0; r < nr; ++r) prefetch_l2(grow[r], body);
+    }
+    return 0u;
+  }
   const int nc = kRes ? nr : 1;  // rows copied into shared memory
   fence_proxy_async_smem();  // earlier reads of the rows before the async overwrite
   __syncthreads();
@@ -1682,18 +1692,18 @@ __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsig
 }
 
 // kRes: both row chunks of a position live in shared memory (two CTAs per
-// SM).  Otherwise only the target chunk does; the draft chunk is read where
-// it lies (prefetched into L2 next to the target copy), which leaves room for
-// three CTAs per SM.  Calls with logits processors, which rewrite both rows,
-// always take the resident form.
+// SM).  Otherwise (aligned rows) both chunks are read where they lie after a
+// bulk L2 prefetch: a CTA then holds only its statistics and inbox in shared
+// memory, and four share an SM.  Calls with logits processors, which rewrite
+// both rows, always take the resident form.
 template <typename TIn, bool kTest, bool kVec, bool kRes>
-__global__ void __launch_bounds__(kThreads, kRes ? 2 : 3) logits_kernel(const VerifyParams P, int chunk) {
+__global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const VerifyParams P, int chunk) {
+  static_assert(kRes || kVec, "rows read in place must be 16-byte aligned");
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ LogitsSmem sm;
   TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem) + (kRes ? chunk : 0)};
-  Inbox *const inbox =
-      reinterpret_cast<Inbox *>(dyn_smem + (kRes ? 2 : 1) * static_cast<size_t>(chunk) * sizeof(TIn));
+  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + (kRes ? 2 : 0) * static_cast<size_t>(chunk) * sizeof(TIn));
 
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int i = static_cast<int>(blockIdx.x / ncta);
@@ -1886,8 +1896,8 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 3) logits_kernel(const Ve
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
         if (procs) add_drafts(j);
         const uint32_t lf = load_rows<TIn, kVec, kRes>(sm, grow, srow, nr, n, phase);
-        // this position's rows: the draft chunk in shared memory, or where it lies
-        TIn *const rows[2] = {srow[0], kRes ? srow[1] : const_cast<TIn *>(grow[1])};
+        // this position's rows: in shared memory, or where they lie
+        TIn *const rows[2] = {kRes ? srow[0] : const_cast<TIn *>(grow[0]), kRes ? srow[1] : const_cast<TIn *>(grow[1])};
         join();
         int y_owner = -1;
         uint32_t yb0 = 0u, yb1 = 0u;
@@ -2154,8 +2164,7 @@ cudaError_t enable_one(int max_cluster, int max_dyn) {
 }
 
 // Forms built per element type and randomness: unaligned rows (resident),
-// aligned rows with both chunks resident, aligned rows with the draft chunk
-// read in place.
+// aligned rows with both chunks resident, aligned rows read in place.
 template <typename TIn, bool kTest>
 cudaError_t enable_forms(int max_cluster, int max_dyn) {
   cudaError_t e;
@@ -2175,10 +2184,11 @@ cudaError_t launch_form(const VerifyParams &p, int cluster, int chunk, size_t dy
 }  // namespace
 
 size_t logits_static_smem() { return sizeof(LogitsSmem); }
+int logits_reg_group_chunk() { return kRegGroupChunk; }
 size_t logits_inbox_bytes(int cluster) { return 2 * static_cast<size_t>(cluster) * sizeof(Inbox); }
 size_t logits_bitmap_bytes(int chunk) { return ((2 * static_cast<size_t>((chunk + 31) / 32) * 4) + 15) & ~size_t{15}; }
 size_t logits_dyn_bytes(int cluster, int chunk, int elem_bytes, bool resident, bool bitmaps) {
-  return (resident ? 2 : 1) * static_cast<size_t>(chunk) * elem_bytes + logits_inbox_bytes(cluster) +
+  return (resident ? 2 : 0) * static_cast<size_t>(chunk) * elem_bytes + logits_inbox_bytes(cluster) +
          (bitmaps ? logits_bitmap_bytes(chunk) : 0);
 }
 

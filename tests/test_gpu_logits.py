@@ -148,6 +148,21 @@ def test_fp32_logits_fused():
     compare_logits(H().run_gpu(w), oracle.verify(w), w)
 
 
+@pytest.mark.parametrize("cluster,V", [(1, 40000), (2, 40000), (1, 20480), (1, 20488)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_in_place_chunks_beyond_register_groups(cluster, V, dtype):
+    """Rows read in place whose chunk is larger than the 20480 bf16 elements
+    whose group maxima stay in registers take the group-walk scan instead;
+    20480 itself is the last chunk on the register path."""
+    w = workloads.make("fused", N=12, V=V, seed=16)
+    if dtype == "fp32":
+        w = dict(w, dtype="f32", target=workloads.bf16_bits_to_f32(w["target"]),
+                 draft=workloads.bf16_bits_to_f32(w["draft"]))
+    o = oracle.verify(w)
+    g = H().run_gpu(w, cluster_ctas=cluster)
+    compare_logits(g, o, w, max_exempt_frac=0.1)
+
+
 @pytest.mark.parametrize("top_k,top_p,temp,budget", [
     (1, 1.0, 1.0, 0.2), (5, 1.0, 0.5, 0.2), (0, 0.5, 1.0, 0.2), (7, 0.3, 0.9, 0.2), (4095, 0.95, 1.3, 0.2),
     (20, 1e-4, 1.0, 0.2),
@@ -296,7 +311,7 @@ def test_top_k_threshold_bound_cases(shape, top_k):
                                                 ("fused", dict(N=24, V=12000), True),
                                                 ("ragged", dict(N=48, V=9000), False)])
 def test_draft_rows_in_place_and_resident_agree(name, kw, production):
-    """The two forms of the logits kernel -- draft row chunk read in place
+    """The two forms of the logits kernel -- row chunks read in place
     (default) or copied into shared memory -- against the oracle and against
     each other (identical except inside the tolerance band)."""
     import speculative_decoding_token_rejection_gb300 as sv
