@@ -782,6 +782,32 @@ __device__ __forceinline__ int band_select(const unsigned long long *cnt, const 
   return 1;
 }
 
+// Every 16-byte group of a bf16 chunk, kWalkGroups per lane with their loads
+// in flight together: mask(group) gives 8 candidate bits (bit t: the low half
+// of word t, bit 4 + t: its high half), the lanes' masks form one 64-bit word
+// each, and the warp walks the set bits in step (one candidate per lane per
+// trip), handing each candidate's bits to take.
+template <typename TIn, typename MaskF, typename TakeF>
+__device__ __forceinline__ void walk_groups(const TIn *row, int ng, MaskF mask, TakeF take) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
+  for (int vb = warp * 32; vb < ng; vb += kWalkGroups * kThreads) {
+    unsigned long long M = 0ull;
+#pragma unroll
+    for (int h = 0; h < kWalkGroups; ++h) {
+      const int v = vb + h * kThreads + lane;
+      if (v < ng) M |= static_cast<unsigned long long>(mask(s4[v])) << (8 * h);
+    }
+    while (__any_sync(0xFFFFFFFFu, M != 0ull)) {
+      if (M != 0ull) {
+        const int pos = __ffsll(static_cast<long long>(M)) - 1;
+        M &= M - 1ull;
+        take(bits_at(row, 8 * (vb + (pos >> 3) * kThreads + lane) + 2 * (pos & 3) + ((pos >> 2) & 1)));
+      }
+    }
+  }
+}
+
 constexpr int kMaxBands = 24;  // windows below the first before the multi-pass selection takes over
 
 // Windows 1, 2, ... below the first: window b holds the keys
@@ -842,7 +868,6 @@ __device__ bool window_rounds(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], 
       const uint32_t lo2 = lob | (lob << 16), hi2 = hib | (hib << 16);
       uint32_t *cnt = bp.cnt[r];
       const TIn *row = srow[r];
-      const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
       auto band_mask = [&](const uint4 &dv) {  // bit t: low half of word t in the window, bit 4 + t: high half
         uint32_t g = ((bf16x2_ge_mask(dv.x, lo2) & ~bf16x2_ge_mask(dv.x, hi2)) & 0x00010001u) |
                      (((bf16x2_ge_mask(dv.y, lo2) & ~bf16x2_ge_mask(dv.y, hi2)) & 0x00010001u) << 1) |
@@ -854,33 +879,9 @@ __device__ bool window_rounds(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], 
         const uint32_t d = static_cast<uint32_t>(hi) - E::key(b);
         if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
       };
-      // every group of this thread is read (these windows are rare; keeping
-      // the group maxima live through the reduction would cost registers on
-      // the common path), 32 groups per mask word
-      const int per_thread = (ng + kThreads - 1) / kThreads;
-      for (int i0 = 0; i0 < per_thread; i0 += 32) {
-        uint32_t cg = 0u;
-        for (int i = i0; i < min(per_thread, i0 + 32); ++i)
-          if (tid + i * kThreads < ng) cg |= 1u << (i - i0);
-        while (__any_sync(0xFFFFFFFFu, cg != 0u)) {
-          uint4 dv = make_uint4(0u, 0u, 0u, 0u);
-          uint32_t em = 0u;
-          if (cg != 0u) {
-            const int pos = __ffs(cg) - 1;
-            cg &= cg - 1u;
-            dv = s4[tid + (i0 + pos) * kThreads];
-            em = band_mask(dv);
-          }
-          while (__any_sync(0xFFFFFFFFu, em != 0u)) {
-            if (em != 0u) {
-              const int pos = __ffs(em) - 1;
-              em &= em - 1u;
-              const uint32_t wv = (pos & 2) ? ((pos & 1) ? dv.w : dv.z) : ((pos & 1) ? dv.y : dv.x);
-              count((pos & 4) ? (wv >> 16) : (wv & 0xFFFFu));
-            }
-          }
-        }
-      }
+      // every group is read again (keeping the group maxima live through the
+      // reduction would cost registers on the common path)
+      walk_groups(row, ng, band_mask, count);
       for (int x = (ng << 3) + tid; x < n; x += kThreads) count(bits_at(row, x));
     }
     __syncthreads();
@@ -1161,7 +1162,6 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   // top-k/top-p rows are left to the multi-pass path.
   if (kB == 16 && near) {
     unsigned long long tt[2] = {0ull, 0ull};
-    const int lane = tid & 31, warp = tid >> 5;
     for (int r = 0; r < nr; ++r) {
       if (!(lp.flags[r] & kFlagFinite)) continue;  // empty or no finite value: contributes nothing
       const uint32_t lk16 = key16_of<TIn>(lp.maxkey[r]);
@@ -1217,27 +1217,12 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
           }
         }
       }
-      // Otherwise a lane tests eight 16-byte groups at once (packed compares,
-      // every load in flight together) into one 64-bit candidate mask and the
-      // warp walks its set bits.
-      for (int vb = warp * 32; !reg_groups && vb < ng; vb += kWalkGroups * kThreads) {
-        unsigned long long M = 0ull;
-#pragma unroll
-        for (int h = 0; h < kWalkGroups; ++h) {
-          const int v = vb + h * kThreads + lane;
-          if (v < ng) M |= static_cast<unsigned long long>(group_mask(s4[v])) << (8 * h);
-        }
-        while (__any_sync(0xFFFFFFFFu, M != 0ull)) {
-          if (M != 0ull) {
-            const int pos = __ffsll(static_cast<long long>(M)) - 1;
-            M &= M - 1ull;
-            const int x = 8 * (vb + (pos >> 3) * kThreads + lane) + 2 * (pos & 3) + ((pos >> 2) & 1);
-            const uint32_t b = bits_at(row, x);
-            const uint32_t d = lk16 - E::key(b);
-            if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
-          }
-        }
-      }
+      // Otherwise every group is tested, kWalkGroups per lane at once.
+      if (!reg_groups)
+        walk_groups(row, ng, group_mask, [&](uint32_t b) {
+          const uint32_t d = lk16 - E::key(b);
+          if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
+        });
       for (int x = ((nw >> 2) << 3) + tid; x < n; x += kThreads) {
         const uint32_t b = bits_at(srow[r], x);
         const uint32_t d = lk16 - E::key(b);
