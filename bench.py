@@ -63,6 +63,11 @@ def parse_args():
     ap.add_argument("--logits-resident", action="store_true",
                     help="keep both row chunks of the logits entry in shared memory (comparison runs)")
     ap.add_argument("--no-ngram", action="store_true")
+    ap.add_argument("--sampler-steps", type=int, default=100)
+    ap.add_argument("--processor-steps", type=int, default=100)
+    ap.add_argument("--synthetic-steps", type=int, default=1000)
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the draft-side sampler, processors and synthetic-acceptance objects")
     return ap.parse_args()
 
 
@@ -265,6 +270,189 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, t
             "gpu_launches": K, "_w": w}
 
 
+def _timed_launches(step, K, W, stream, dev, dist):
+    """W untimed launches, then K launches between CUDA events on ``stream``;
+    the mean milliseconds per launch (max over ranks)."""
+    import torch
+    for k in range(W):
+        step(k)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(K):
+        step(W + k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return ms
+
+
+def time_sampler(args, sv, dev, world, rank, dist, stream, w, write_q):
+    """The draft-side sampler on one draft step of the fused batch: one bf16
+    row of V=151936 per request (N=512 rows), T=0.8, top-k 50, top-p 0.9,
+    production Philox.  Launch k samples draft position k mod gamma, so
+    consecutive launches read different rows (155.6 MB per launch, above the
+    L2 size).  With ``write_q`` the transformed fp32 row of every request is
+    written out too, in the probability entry's q layout."""
+    import numpy as np
+    import torch
+    N, G, V = w["N"], w["gamma"], w["V"]
+    draft = torch.from_numpy(w["draft"].view(np.int16)).view(torch.bfloat16).to(dev).view(N, G, V)
+    temp = torch.from_numpy(np.asarray(w["temperature"], np.float32)).to(dev)
+    top_k = torch.full((N,), 50, dtype=torch.int32, device=dev)
+    top_p = torch.full((N,), 0.9, dtype=torch.float32, device=dev)
+    tokens = torch.empty((N,), dtype=torch.int32, device=dev)
+    probs = torch.empty((N, V), dtype=torch.float32, device=dev) if write_q else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    h = sv.spec_verify_create(N, 1, V, device=dev.index, cluster_ctas=args.cluster)
+    lib = sv.load_library()
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    built = [sv.build_sample_args(logits=draft[:, j, :], tokens=tokens, probs=probs, temperature=temp,
+                                  top_k=top_k, top_p=top_p, seed=20240603, rng_row_base=rank * N, status=status)
+             for j in range(G)]
+
+    def step(k):
+        a = built[k % G]
+        a.offset = k
+        if lib.spec_verify_sample(ctypes.c_void_p(h), ctypes.byref(a), sptr) != 0:
+            raise RuntimeError(lib.spec_verify_last_error().decode())
+
+    K = max(3, min(args.steps, args.sampler_steps))
+    ms = _timed_launches(step, K, args.warmup, stream, dev, dist)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    sv.spec_verify_destroy(h)
+    alg = N * V * 2 + N * (4 + 4 + 4 + 4) + (N * V * 4 if write_q else 0)
+    peak, src = measured_peak()
+    return {"value": world * N / (ms / 1e3), "unit": "sampled tokens/s", "ms_per_step": ms, "steps": K,
+            "config": {"workload": f"draft step of the fused batch: {N} bf16 rows of V={V}, T=0.8, top-k 50, "
+                                   "top-p 0.9, production Philox" + (", fp32 q rows written" if write_q else ""),
+                       "l2": "no flush: launch k reads draft position k mod 7 (155.6 MB per launch, > 126 MB L2)"},
+            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg},
+            "gpu_launches": K}
+
+
+def processor_lists(N, V, seed, context=512, banned=16, stop=2):
+    """Per-request logits processors of a serving batch: a repetition penalty
+    of 1.2 over the last ``context`` tokens of each request's context, ``banned``
+    banned ids and ``stop`` stop ids (uniform over the vocabulary), as
+    inclusive int64 prefix sums and int32 ids."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    out = {"repetition_penalty": np.full(N, 1.2, np.float32)}
+    for name, n in (("penalty", context), ("banned", banned), ("stop", stop)):
+        out[f"{name}_cu"] = np.arange(1, N + 1, dtype=np.int64) * n
+        out[f"{name}_ids"] = rng.integers(0, V, size=N * n).astype(np.int32)
+    return out
+
+
+def time_processors(args, sv, lib, dev, world, rank, dist, stream, w):
+    """The logits entry on the fused batch with logits processors and stop
+    tokens: repetition penalty 1.2 over a 512-token context per request (the
+    request's drafts join it as they are committed), 16 banned ids and 2 stop
+    ids per request; both row chunks of a position are copied into shared
+    memory and rewritten there."""
+    import numpy as np
+    import torch
+    import workloads
+    N, G, V, T = w["N"], w["gamma"], w["V"], w["T"]
+    w = dict(w, top_k=np.full(N, 50, np.int32), top_p=np.full(N, 0.9, np.float32))
+    gam = workloads.gammas_of(w)
+    t = workloads.as_torch(w, dev)
+    pl = {k: torch.from_numpy(v).to(dev) for k, v in processor_lists(N, V, seed=11 + 1000 * rank).items()}
+    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster)
+    K = max(3, min(args.steps, args.processor_steps))
+    nacc = torch.empty((K + args.warmup, N), dtype=torch.int32, device=dev)
+    out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = sv.build_args(entry="logits", draft_ids=t["draft_ids"], target=t["target"], draft=t["draft"],
+                      temperature=t["temperature"], top_k=t["top_k"], top_p=t["top_p"], out_tokens=out,
+                      num_accepted=nacc[0], status=status, seed=20240604, rng_request_base=rank * N,
+                      repetition_penalty=pl["repetition_penalty"], penalty_cu=pl["penalty_cu"],
+                      penalty_token_ids=pl["penalty_ids"], banned_cu=pl["banned_cu"],
+                      banned_token_ids=pl["banned_ids"], stop_cu=pl["stop_cu"], stop_token_ids=pl["stop_ids"])
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    h = ctypes.c_void_p(ver.handle)
+
+    def step(k):
+        a.offset = k
+        a.num_accepted = nacc.data_ptr() + 4 * N * k
+        if lib.spec_verify_run(h, ctypes.byref(a), sptr) != 0:
+            raise RuntimeError(lib.spec_verify_last_error().decode())
+
+    ms = _timed_launches(step, K, args.warmup, stream, dev, dist)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    na = nacc[args.warmup:].cpu().numpy()
+    lists = sum(int(v.numel()) * v.element_size() for v in pl.values())
+    alg = float(np.mean([logits_algorithmic_bytes(na[k], gam, w["temperature"], V, G) for k in range(K)])) + lists
+    peak, src = measured_peak()
+    ver.close()
+    return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
+            "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k 50, top-p 0.9, "
+                                   "repetition penalty 1.2 over 512 context ids, 16 banned ids, 2 stop ids per "
+                                   "request, production Philox", "entry": "logits", "rows": "shared memory"},
+            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg},
+            "acceptance": {"mean_accepted": float(na.mean())}, "gpu_launches": K}
+
+
+SYNTHETIC_RATES = [0.8, 0.7, 0.6, 0.5, 0.4, 0.3, 0.2]
+
+
+def time_synthetic(args, sv, lib, dev, world, rank, dist, stream, t, gammas, N, G, V, T):
+    """The probability entry on the headline batch in synthetic acceptance
+    mode: position j is accepted with the preset rate r_j (non-increasing), so
+    no p(y), q(y) are gathered; the race still streams the row pair of the
+    stopping position (or the bonus row)."""
+    import numpy as np
+    import torch
+    rates = torch.tensor(SYNTHETIC_RATES[:G] + [0.0] * max(0, G - len(SYNTHETIC_RATES)), dtype=torch.float32,
+                         device=dev)
+    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster)
+    K = max(3, min(args.steps, args.synthetic_steps))
+    nacc = torch.empty((K + args.warmup, N), dtype=torch.int32, device=dev)
+    out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = sv.build_args(entry="probs", draft_ids=t["draft_ids"], target=t["target"], draft=t["draft"],
+                      temperature=t["temperature"], out_tokens=out, num_accepted=nacc[0], status=status,
+                      seed=20240605, rng_request_base=rank * N, synthetic_acceptance_rates=rates)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    h = ctypes.c_void_p(ver.handle)
+
+    def step(k):
+        a.offset = k
+        a.num_accepted = nacc.data_ptr() + 4 * N * k
+        if lib.spec_verify_run(h, ctypes.byref(a), sptr) != 0:
+            raise RuntimeError(lib.spec_verify_last_error().decode())
+
+    ms = _timed_launches(step, K, args.warmup, stream, dev, dist)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    na = nacc[args.warmup:].cpu().numpy().astype(np.int64)
+    g = gammas.astype(np.int64)
+    # the probability entry's bytes without the gathers: ids, the raced row(s), outputs
+    alg = float(np.mean([int((4 * g + np.where(na[k] < g, 8 * V, 4 * V) + 4 + 4 * (G + 1) + 4).sum())
+                         for k in range(K)])) + 4 * G
+    peak, src = measured_peak()
+    ver.close()
+    return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
+            "config": {"workload": f"fused_probs: N={N} gamma={G} V={V} fp32 rows, synthetic rates "
+                                   f"{SYNTHETIC_RATES[:G]}, production Philox", "entry": "probs"},
+            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg},
+            "acceptance": {"mean_accepted": float(na.mean()),
+                           "A_hist": np.bincount(na.reshape(-1), minlength=G + 1).tolist()},
+            "gpu_launches": K}
+
+
 def time_ngram(args, sv, dev, world, rank, dist, stream):
     """The batched n-gram proposer on its default batch (512 repetitive
     histories of 1024..16384 tokens, min/max n-gram 5, k = 7).  The histories
@@ -422,6 +610,15 @@ def run_ours(args, world, rank, local_rank):
             logits["other_settings"][name]["roofline_frac"] = o["roofline"]["frac"]
             logits["gpu_launches"] += o["gpu_launches"]
     ngram = None if args.no_ngram else time_ngram(args, sv, dev, world, rank, dist, stream)
+    nxt = {}
+    if not args.no_next:
+        nxt["synthetic_acceptance"] = time_synthetic(args, sv, lib, dev, world, rank, dist, stream, t, gammas,
+                                                     N, G, V, T)
+        if logits:
+            nxt["logits_processors"] = time_processors(args, sv, lib, dev, world, rank, dist, stream, wl)
+            nxt["draft_sampler"] = time_sampler(args, sv, dev, world, rank, dist, stream, wl, write_q=False)
+            nxt["draft_sampler_with_q_rows"] = time_sampler(args, sv, dev, world, rank, dist, stream, wl,
+                                                            write_q=True)
     clocks.stop()
     total_ms = ev[0].elapsed_time(ev[K])
     per_launch = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
@@ -474,6 +671,7 @@ def run_ours(args, world, rank, local_rank):
         line["logits_entry"] = logits
     if ngram:
         line["ngram_proposer"] = ngram
+    line.update(nxt)
     if e2e:
         line["e2e"] = e2e
         line["e2e_full_copy"] = e2e_fc

@@ -104,7 +104,8 @@ int logits_reg_group_chunk();  // largest bf16 chunk whose group maxima stay in 
 // double-buffered inboxes of the one-barrier row-statistics reduction.
 size_t logits_inbox_bytes(int cluster);
 cudaError_t enable_sample_kernels(int max_cluster, int max_dyn);
-cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream);
+cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
+                          cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);
 // resident: both row chunks of a position in shared memory (needed by the
 // processors and by unaligned rows); otherwise the draft chunk is read in place.
@@ -116,9 +117,10 @@ size_t logits_bitmap_bytes(int chunk);
 size_t logits_dyn_bytes(int cluster, int chunk, int elem_bytes, bool resident, bool bitmaps);
 
 // Cluster size and per-CTA row chunk (elements, a multiple of 8) for the
-// logits entry; returns false if no cluster size fits the rows in shared memory.
+// logits entry (chained: positions one after another) and the sampler;
+// returns false if no cluster size fits the rows in shared memory.
 bool choose_logits_layout(const spec_verify_ctx *ctx, int N, int V, int elem_bytes, int *cluster, int *chunk,
-                          bool bitmaps, bool resident);
+                          bool bitmaps, bool resident, bool chained);
 
 void set_last_error(const char *fmt, ...);
 

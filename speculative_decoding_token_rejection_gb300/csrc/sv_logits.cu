@@ -1973,12 +1973,11 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
 // exponential race (argmax at temperature 0), and the fp32 probability row can
 // be written out for the probability entry.
 // ---------------------------------------------------------------------------
-template <typename TIn, bool kTest, bool kVec>
-__global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams P, int chunk) {
+template <typename TIn, bool kTest, bool kVec, bool kRes>
+__global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const SampleParams P, int chunk) {
+  static_assert(kRes || kVec, "rows read in place must be 16-byte aligned");
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ LogitsSmem sm;
-  TIn *const srow[2] = {reinterpret_cast<TIn *>(dyn_smem), reinterpret_cast<TIn *>(dyn_smem)};
-  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + static_cast<size_t>(chunk) * sizeof(TIn));
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int r = static_cast<int>(blockIdx.x / ncta);
   const int tid = threadIdx.x;
@@ -1986,12 +1985,17 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
   const TIn *row = static_cast<const TIn *>(P.logits) + static_cast<int64_t>(r) * P.row_stride;
   const int x0 = min(V, static_cast<int>(rank) * chunk);
   const int n = min(V, x0 + chunk) - x0;
+  // the row chunk: in shared memory, or read where it lies
+  TIn *const rc = kRes ? reinterpret_cast<TIn *>(dyn_smem) : const_cast<TIn *>(row + x0);
+  TIn *const srow[2] = {rc, rc};
+  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + (kRes ? static_cast<size_t>(chunk) * sizeof(TIn) : 0));
   uint32_t bits = 0;
   int32_t token = -1;
   int step = 0;
   uint32_t phase = 0;
-  // processor bitmaps (present only when the call has processors)
-  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
+  // processor bitmaps (present only when the call has processors, which
+  // always take the form with the row in shared memory)
+  const bool procs = kRes && (P.rep_penalty != nullptr || P.ban_cu != nullptr);
   const int words = (chunk + 31) / 32;
   uint32_t *const pen_bits = reinterpret_cast<uint32_t *>(inbox + 2 * ncta);
   uint32_t *const ban_bits = pen_bits + words;
@@ -2057,7 +2061,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
       bits |= SV_DATA_BAD_PARAM;
     } else {
       const TIn *grow[2] = {row + x0, nullptr};
-      const uint32_t lf = load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase);
+      const uint32_t lf = load_rows<TIn, kVec, kRes>(sm, grow, srow, 1, n, phase);
       if (procs) apply_processors(srow, 1, n, pen_bits, ban_bits, words, theta);
       RowStats st[2];
       if (!position_stats<TIn>(sm, inbox, srow, 1, n, __fdiv_rn(kLog2e, temp), topk, topp, lf, st, &bits, step,
@@ -2081,7 +2085,27 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
         }
         if (P.probs) {  // this CTA's chunk of the transformed row
           float *prow = P.probs + static_cast<int64_t>(r) * P.probs_stride + x0;
-          for (int x = tid; x < n; x += kThreads) prow[x] = prob_of<TIn>(bits_at(srow[0], x), st[0]);
+          int xs = 0;
+          if (kVec && sizeof(TIn) == 2 && (reinterpret_cast<uintptr_t>(prow) & 15u) == 0) {
+            // eight bf16 logits in, two float4 probabilities out
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[0]);
+            float4 *p4 = reinterpret_cast<float4 *>(prow);
+            const int ng = n >> 3;
+            for (int v = tid; v < ng; v += kThreads) {
+              const uint4 d = s4[v];
+              const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+              float o[8];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                o[2 * t] = prob_of<TIn>(w[t] & 0xFFFFu, st[0]);
+                o[2 * t + 1] = prob_of<TIn>(w[t] >> 16, st[0]);
+              }
+              p4[2 * v] = make_float4(o[0], o[1], o[2], o[3]);
+              p4[2 * v + 1] = make_float4(o[4], o[5], o[6], o[7]);
+            }
+            xs = ng << 3;
+          }
+          for (int x = xs + tid; x < n; x += kThreads) prow[x] = prob_of<TIn>(bits_at(srow[0], x), st[0]);
         }
       }
     }
@@ -2093,7 +2117,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
   cluster_sync();
 }
 
-template <typename TIn, bool kTest, bool kVec>
+template <typename TIn, bool kTest, bool kVec, bool kRes>
 cudaError_t launch_sample_one(const SampleParams &p, int cluster, int chunk, size_t dyn, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.R) * static_cast<unsigned>(cluster), 1, 1);
@@ -2107,17 +2131,36 @@ cudaError_t launch_sample_one(const SampleParams &p, int cluster, int chunk, siz
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sample_kernel<TIn, kTest, kVec>, p, chunk);
+  return cudaLaunchKernelEx(&cfg, sample_kernel<TIn, kTest, kVec, kRes>, p, chunk);
 }
 
-template <typename TIn, bool kTest, bool kVec>
+template <typename TIn, bool kTest, bool kVec, bool kRes>
 cudaError_t enable_sample_one(int max_cluster, int max_dyn) {
-  cudaError_t e = cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec>,
+  cudaError_t e = cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec, kRes>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
   if (e != cudaSuccess) return e;
   if (max_cluster > 8)
-    return cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec, kRes>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return cudaSuccess;
+}
+
+// Sampler forms per element type and randomness: unaligned rows (in shared
+// memory), aligned rows in shared memory (processors), aligned rows in place.
+template <typename TIn, bool kTest>
+cudaError_t enable_sample_forms(int max_cluster, int max_dyn) {
+  cudaError_t e;
+  if ((e = enable_sample_one<TIn, kTest, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<TIn, kTest, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_sample_one<TIn, kTest, true, false>(max_cluster, max_dyn);
+}
+
+template <typename TIn, bool kTest>
+cudaError_t launch_sample_form(const SampleParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
+                               cudaStream_t stream) {
+  if (!vec) return launch_sample_one<TIn, kTest, false, true>(p, cluster, chunk, dyn, stream);
+  return resident ? launch_sample_one<TIn, kTest, true, true>(p, cluster, chunk, dyn, stream)
+                  : launch_sample_one<TIn, kTest, true, false>(p, cluster, chunk, dyn, stream);
 }
 
 template <typename TIn, bool kTest, bool kVec, bool kRes>
@@ -2187,30 +2230,22 @@ cudaError_t enable_logits_kernels(int max_cluster, int max_dyn) {
 
 cudaError_t enable_sample_kernels(int max_cluster, int max_dyn) {
   cudaError_t e;
-  if ((e = enable_sample_one<uint16_t, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_sample_one<uint16_t, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_sample_one<uint16_t, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_sample_one<uint16_t, false, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_sample_one<float, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_sample_one<float, true, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_sample_one<float, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  return enable_sample_one<float, false, false>(max_cluster, max_dyn);
+  if ((e = enable_sample_forms<uint16_t, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_forms<uint16_t, false>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_forms<float, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_sample_forms<float, false>(max_cluster, max_dyn);
 }
 
-cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, cudaStream_t stream) {
+cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
+                          cudaStream_t stream) {
   const bool test = p.exponentials != nullptr;
-  const size_t dyn = static_cast<size_t>(chunk) * (bf16 ? 2 : 4) + logits_inbox_bytes(cluster) +
+  resident = resident || !vec;
+  const size_t dyn = (resident ? static_cast<size_t>(chunk) * (bf16 ? 2 : 4) : 0) + logits_inbox_bytes(cluster) +
                      ((p.rep_penalty || p.ban_cu) ? logits_bitmap_bytes(chunk) : 0);
-  if (bf16) {
-    if (test) return vec ? launch_sample_one<uint16_t, true, true>(p, cluster, chunk, dyn, stream)
-                         : launch_sample_one<uint16_t, true, false>(p, cluster, chunk, dyn, stream);
-    return vec ? launch_sample_one<uint16_t, false, true>(p, cluster, chunk, dyn, stream)
-               : launch_sample_one<uint16_t, false, false>(p, cluster, chunk, dyn, stream);
-  }
-  if (test) return vec ? launch_sample_one<float, true, true>(p, cluster, chunk, dyn, stream)
-                       : launch_sample_one<float, true, false>(p, cluster, chunk, dyn, stream);
-  return vec ? launch_sample_one<float, false, true>(p, cluster, chunk, dyn, stream)
-             : launch_sample_one<float, false, false>(p, cluster, chunk, dyn, stream);
+  if (bf16) return test ? launch_sample_form<uint16_t, true>(p, cluster, chunk, dyn, vec, resident, stream)
+                        : launch_sample_form<uint16_t, false>(p, cluster, chunk, dyn, vec, resident, stream);
+  return test ? launch_sample_form<float, true>(p, cluster, chunk, dyn, vec, resident, stream)
+              : launch_sample_form<float, false>(p, cluster, chunk, dyn, vec, resident, stream);
 }
 
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,

@@ -26,7 +26,7 @@ def _gpu():
     oracle.build()
 
 
-def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=False):
+def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=False, cluster=0, flags=0):
     import torch
     import gpu_harness
     import speculative_decoding_token_rejection_gb300 as sv
@@ -40,7 +40,7 @@ def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=Fals
     probs = torch.zeros((R, V), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     t = lambda a, dt: None if a is None else torch.as_tensor(np.asarray(a), dtype=dt).to(dev)
-    sv.spec_verify_sample(gpu_harness.verifier().handle, logits=logits, tokens=tokens, probs=probs,
+    sv.spec_verify_sample(gpu_harness.verifier(cluster, flags).handle, logits=logits, tokens=tokens, probs=probs,
                           temperature=t(temp, torch.float32), top_k=t(k, torch.int32), top_p=t(p, torch.float32),
                           exponentials=t(E, torch.float32), seed=seed, offset=offset, rng_row_base=base,
                           status=status)
@@ -48,10 +48,12 @@ def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=Fals
     return tokens.cpu().numpy(), probs.cpu().numpy(), int(status.item())
 
 
-def check(rows, temp, k, p, E=None, production=False, bf16=False, budget=0.02, seed=0, offset=0, base=0):
+def check(rows, temp, k, p, E=None, production=False, bf16=False, budget=0.02, seed=0, offset=0, base=0, cluster=0,
+          flags=0):
     o = oracle.sample_rows(rows, temperature=temp, top_k=k, top_p=p, exponentials=E, seed=seed, offset=offset,
                            rng_row_base=base)
-    tok, pr, st = run_sampler(rows, temp, k, p, E, bf16=bf16, seed=seed, offset=offset, base=base)
+    tok, pr, st = run_sampler(rows, temp, k, p, E, bf16=bf16, seed=seed, offset=offset, base=base, cluster=cluster,
+                              flags=flags)
     assert st == o["status"]
     temp = np.asarray(temp)
     rnd = temp > 0
@@ -67,6 +69,21 @@ def check(rows, temp, k, p, E=None, production=False, bf16=False, budget=0.02, s
 def fused_rows(R=64, V=151936):
     w = workloads.make("fused", N=max(1, R // 7), V=V, test_mode=False)
     return w["draft"][:R]
+
+
+@pytest.mark.parametrize("cluster", [0, 4, 8, 16])
+@pytest.mark.parametrize("resident", [False, True])
+def test_sampler_forms_and_cluster_sizes(cluster, resident):
+    """Rows read in place (default) or copied into shared memory, at the
+    automatic cluster size and explicit ones: 4 CTAs give chunks of 37984
+    keys (beyond the register-held group maxima), 8 and 16 stay within."""
+    import speculative_decoding_token_rejection_gb300 as sv
+    rows = fused_rows(24, 151936)
+    R, V = rows.shape
+    E = np.random.default_rng(2).standard_exponential((R, V), dtype=np.float32)
+    temp = np.where(np.arange(R) % 6 == 5, 0.0, 0.8).astype(np.float32)
+    check(rows, temp, np.full(R, 50), np.full(R, 0.9, np.float32), E, bf16=True, cluster=cluster,
+          flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0, budget=0.1)
 
 
 @pytest.mark.parametrize("V", [151936, 5000, 4097])
