@@ -254,6 +254,8 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, t
     peak, src = measured_peak()
     full = (2 * T + N) * V * 2
     traffic, traffic_sha = stored_traffic("verify_logits_fused", LOGITS_KERNEL_SOURCES)
+    if traffic is not None and (N != 512 or top_k != 50 or top_p != 0.9):
+        traffic = None  # the stored counters are scaled to a 512-request launch of this setting
     ver.close()
     return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
             "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k {top_k if top_k > 0 else 'off'}, "
@@ -329,13 +331,20 @@ def time_sampler(args, sv, dev, world, rank, dist, stream, w, write_q):
     sv.spec_verify_destroy(h)
     alg = N * V * 2 + N * (4 + 4 + 4 + 4) + (N * V * 4 if write_q else 0)
     peak, src = measured_peak()
+    traffic, traffic_sha = (None, None) if write_q else stored_traffic("draft_sampler_fused_rows",
+                                                                      LOGITS_KERNEL_SOURCES)
+    if traffic is not None and N != 512:
+        traffic = None  # the stored counters are scaled to a 512-row launch
     return {"value": world * N / (ms / 1e3), "unit": "sampled tokens/s", "ms_per_step": ms, "steps": K,
             "config": {"workload": f"draft step of the fused batch: {N} bf16 rows of V={V}, T=0.8, top-k 50, "
                                    "top-p 0.9, production Philox" + (", fp32 q rows written" if write_q else ""),
-                       "l2": "no flush: launch k reads draft position k mod 7 (155.6 MB per launch, > 126 MB L2)"},
+                       "l2": f"no flush: launch k reads draft position k mod {G} ({N * V * 2 / 1e6:.1f} MB per "
+                             f"launch; {N * G * V * 2 / 1e6:.0f} MB over {G} launches, > 126 MB L2)"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
-                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
-                         "algorithmic_bytes_per_launch": alg},
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg,
+                         "kernel_source_sha": kernel_source_hash(LOGITS_KERNEL_SOURCES),
+                         "traffic_source_sha": traffic_sha},
             "gpu_launches": K}
 
 
@@ -638,6 +647,8 @@ def run_ours(args, world, rank, local_rank):
     peak, peak_src = measured_peak()
     full_bytes = (T + N) * V * 4 + T * V * 4
     traffic, traffic_sha = stored_traffic()
+    if traffic is not None and N != 512:
+        traffic = None  # the stored counters are scaled to a 512-request launch
     acc = nacc_np.astype(np.int64)
     e2e, e2e_fc = (None, None) if args.no_e2e else run_e2e(args, w, t, ver, sv, dev, world, dist)
     cpu = None
