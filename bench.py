@@ -82,7 +82,8 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s earlier GB300 copy measurement)"
 
 
-LOGITS_KERNEL_SOURCES = ["sv_logits.cu", "sv_device.cuh"]
+LOGITS_KERNEL_SOURCES = ["sv_logits.cuh", "sv_logits.cu", "sv_logits_bf16.cu", "sv_logits_f32.cu", "sv_sample_bf16.cu",
+                         "sv_sample_f32.cu", "sv_device.cuh"]
 
 
 def kernel_source_hash(sources=None) -> str:
