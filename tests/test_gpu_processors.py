@@ -79,6 +79,27 @@ def test_ragged_production_with_processors():
     compare(g, o, w, production=True, max_exempt_frac=0.1)
 
 
+@pytest.mark.parametrize("top_k,top_p,temp,V,cluster", [
+    (50, 0.9, 0.8, 151936, 0),     # the fused setting at its vocabulary: 8 CTAs, register-held group maxima
+    (0, 0.9, 0.8, 151936, 0),      # top-p alone: cuts in windows below the first
+    (0, 1.0, 0.8, 151936, 0),      # temperature alone: dense sums and race
+    (2000, 1.0, 0.8, 30000, 0),    # a deep top-k threshold
+    (50, 0.9, 0.8, 40000, 1),      # one CTA per request over a 40000-key chunk
+])
+def test_processors_statistics_paths(top_k, top_p, temp, V, cluster):
+    """Every statistics path with processors (rows copied into shared memory
+    and rewritten there) against the oracle: the fused setting at its
+    vocabulary, cuts in windows below the first, dense rows, a deep top-k
+    threshold, and one CTA per request over a 40000-key chunk."""
+    w = workloads.make("fused", N=16, V=V, seed=23)
+    w["top_k"] = np.full(16, top_k, np.int32)
+    w["top_p"] = np.full(16, top_p, np.float32)
+    w["temperature"] = np.full(16, temp, np.float32)
+    add_lists(w, np.random.default_rng(9), theta=1.5, n_ctx=400, n_ban=20)
+    o = oracle.verify(w)
+    compare(H().run_gpu(w, cluster_ctas=cluster), o, w, max_exempt_frac=0.5)
+
+
 def test_synthetic_mode_with_processors():
     w = workloads.make("fused", N=20, V=8192, seed=9)
     add_lists(w, np.random.default_rng(7))
