@@ -122,7 +122,7 @@ cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chu
                           cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);
 // resident: both row chunks of a position in shared memory (needed by the
-// processors and by unaligned rows); otherwise the draft chunk is read in place.
+// processors and by unaligned rows); otherwise both are read in place.
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
                           cudaStream_t stream);
 // Dynamic shared memory of the processor bitmaps (banned and penalised keys of a chunk).

@@ -15,14 +15,15 @@
 // mass reaches top_p (ties at the cut kept), and Z' sums the kept terms.
 //
 // One thread-block cluster per request.  A random request walks its positions
-// in order, as a sequential verifier reads them: position j loads the target
-// and draft row chunks once from HBM into the CTAs' shared memory, computes
-// the row statistics there (max, exact radix-select threshold for top-k,
-// fixed-point mass radix-select for the top-p cut, normaliser), tests
-// fl32(u * q(y)) < p(y), and either moves on or runs the exponential race of
-// the residual max(p - q, 0) over the rows already in shared memory.  When all
-// drafts pass, the bonus row is raced over p.  Rows after the first rejection
-// are never read.  Greedy requests stream target rows from HBM and take the
+// in order, as a sequential verifier reads them: position j brings each CTA's
+// chunk of the target and draft rows from HBM once (into L2 by a bulk
+// prefetch and read in place, or copied into shared memory where the logits
+// processors rewrite them), computes the row statistics (max, the top-k
+// threshold and top-p cut from exact per-key window counts, normaliser),
+// tests fl32(u * q(y)) < p(y), and either moves on or runs the exponential
+// race of the residual max(p - q, 0) over the same chunks.  When all drafts
+// pass, the bonus row is raced over p.  Rows after the first rejection are
+// never read.  Greedy requests stream target rows from HBM and take the
 // cluster argmax of the raw logits, stopping at the first mismatch.
 //
 // All sums are deterministic: integer histograms and fixed-point (2^-40)
