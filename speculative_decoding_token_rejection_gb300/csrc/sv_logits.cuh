@@ -1423,7 +1423,7 @@ __device__ __forceinline__ float prob_of(uint32_t b, const RowStats &st) {
 }
 
 // ---------------------------------------------------------------------------
-// race over the rows in shared memory
+// race over the row chunks (in shared memory or read in place)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void consider_drawn_l(float w, uint32_t word, int x, float &bk, int &bx) {
   const float U = e_word_to_open_uniform(word);
@@ -1493,7 +1493,7 @@ __device__ __forceinline__ float race_w(uint32_t bp, uint32_t bq, const RowStats
 // groups in increasing order (then the tail quads), so its strict '>' keeps
 // its lowest index on ties.
 template <typename TIn, bool kTest, bool kResidual>
-__device__ __forceinline__ void race_smem(const TIn *sp, const TIn *sq, const RowStats &ps, const RowStats &qs,
+__device__ __forceinline__ void race_chunks(const TIn *sp, const TIn *sq, const RowStats &ps, const RowStats &qs,
                                           int x0, int n, const float *Erow, const RngKey &rk, uint32_t rs, float &bk,
                                           int &bx, uint32_t &flags) {
   constexpr int kPer = 16 / sizeof(TIn);  // 8 bf16 or 4 fp32 = 2 or 1 quads
@@ -1934,16 +1934,16 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
             continue;  // accepted: next position
           }
           residual = true;
-          race_smem<TIn, kTest, true>(rows[0], rows[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl);
+          race_chunks<TIn, kTest, true>(rows[0], rows[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl);
         } else {
-          race_smem<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
+          race_chunks<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
         }
         KeyFlags r = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
         if (r.key == 0ull && residual) {  // no positive residual key: race over p with the same E
           bk = 0.0f;
           bx = -1;
           fl = 0;
-          race_smem<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
+          race_chunks<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
           const KeyFlags r2 = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
           r.key = r2.key;
           r.flags |= r2.flags;
@@ -2080,7 +2080,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
         float bk = 0.0f;
         int bx = -1;
         uint32_t fl = 0;
-        race_smem<TIn, kTest, false>(srow[0], srow[0], st[0], st[0], x0, n, Erow, rk,
+        race_chunks<TIn, kTest, false>(srow[0], srow[0], st[0], st[0], x0, n, Erow, rk,
                                      P.row_base + static_cast<uint32_t>(r), bk, bx, fl);
         const KeyFlags kr = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
         bits |= kr.flags;
