@@ -100,6 +100,19 @@ def test_processors_statistics_paths(top_k, top_p, temp, V, cluster):
     compare(H().run_gpu(w, cluster_ctas=cluster), o, w, max_exempt_frac=0.5)
 
 
+@pytest.mark.parametrize("top_k,top_p", [(50, 0.9), (0, 0.9)])
+def test_processed_keys_win_races_and_windows(top_k, top_p):
+    """Processors that move keys into the kept set and onto the race's top
+    (theta < 1 raises every penalised logit), so processed keys decide group
+    maxima, window counts and race winners; against the oracle."""
+    w = workloads.make("fused", N=24, V=20000, seed=29)
+    w["top_k"] = np.full(24, top_k, np.int32)
+    w["top_p"] = np.full(24, top_p, np.float32)
+    add_lists(w, np.random.default_rng(10), theta=0.5, n_ctx=2000, n_ban=40)
+    o = oracle.verify(w)
+    compare(H().run_gpu(w), o, w, max_exempt_frac=0.3)
+
+
 def test_synthetic_mode_with_processors():
     w = workloads.make("fused", N=20, V=8192, seed=9)
     add_lists(w, np.random.default_rng(7))
