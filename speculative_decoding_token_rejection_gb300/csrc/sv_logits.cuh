@@ -1169,64 +1169,91 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   // top-k/top-p rows are left to the multi-pass path.
   if (kB == 16 && near) {
     unsigned long long tt[2] = {0ull, 0ull};
+    // each row's window: at most kNearBins - 1 keys below the CTA's largest,
+    // and not below the threshold's floor; at or below key(-inf): every
+    // finite key
+    uint32_t lk16s[2] = {0u, 0u}, los[2] = {0u, 0u};
     for (int r = 0; r < nr; ++r) {
       if (!(lp.flags[r] & kFlagFinite)) continue;  // empty or no finite value: contributes nothing
       const uint32_t lk16 = key16_of<TIn>(lp.maxkey[r]);
-      // window's smallest key (at most kNearBins - 1 below the largest, and not
-      // below the threshold's floor); at or below key(-inf): every finite key
       uint32_t lo = lk16 >= static_cast<uint32_t>(kNearBins - 1) ? lk16 - (kNearBins - 1) : 0u;
       if (use_floor) lo = max(lo, lp.floor[r]);
       if (tid == 0) lp.nbins[r] = min(static_cast<uint32_t>(kNearBins), lk16 - lo + 1u);
-      const uint32_t lob = lo > 0x007Fu ? bf16_bits_of_key(lo) : 0xFF80u;
-      const uint32_t lo2 = lob | (lob << 16);
-      uint32_t *cnt = lp.cnt[r];
-      const TIn *row = srow[r];
-      const int nw = n >> 1;
-      const int ng = nw >> 2;  // 16-byte groups
-      const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
-      // 8-bit candidate mask of one 16-byte group: bit t is the low half of
-      // word t, bit 4 + t its high half
-      auto group_mask = [&](const uint4 &dv) {
-        uint32_t g = (bf16x2_ge_mask(dv.x, lo2) & 0x00010001u) | ((bf16x2_ge_mask(dv.y, lo2) & 0x00010001u) << 1) |
-                     ((bf16x2_ge_mask(dv.z, lo2) & 0x00010001u) << 2) |
-                     ((bf16x2_ge_mask(dv.w, lo2) & 0x00010001u) << 3);
-        return (g | (g >> 12)) & 0xFFu;
-      };
-      if (reg_groups) {
-        // groups whose largest value reaches the window, two per compare; only
-        // those are read again, and the warp walks the set bits of their
-        // candidate masks in step (one candidate per lane per trip)
-        uint32_t cg = 0u;
+      lk16s[r] = lk16;
+      los[r] = lo;
+    }
+    auto lo_pair = [&](int r) {
+      const uint32_t lob = los[r] > 0x007Fu ? bf16_bits_of_key(los[r]) : 0xFF80u;
+      return lob | (lob << 16);
+    };
+    // 8-bit candidate mask of one 16-byte group: bit t is the low half of
+    // word t, bit 4 + t its high half
+    auto group_mask = [](const uint4 &dv, uint32_t lo2) {
+      uint32_t g = (bf16x2_ge_mask(dv.x, lo2) & 0x00010001u) | ((bf16x2_ge_mask(dv.y, lo2) & 0x00010001u) << 1) |
+                   ((bf16x2_ge_mask(dv.z, lo2) & 0x00010001u) << 2) |
+                   ((bf16x2_ge_mask(dv.w, lo2) & 0x00010001u) << 3);
+      return (g | (g >> 12)) & 0xFFu;
+    };
+    if (reg_groups) {
+      // groups whose largest value reaches the window, two per compare; only
+      // those are read again.  Each trip a lane reloads its next candidate
+      // group of both rows (the two loads in flight together), and the warp
+      // walks the set bits of their candidate masks in step (one candidate
+      // per lane per trip)
+      uint32_t cg[2] = {0u, 0u}, lo2s[2];
 #pragma unroll
-        for (int i = 0; i < kGroupWords; ++i) {
-          const uint32_t m = bf16x2_ge_mask(gw[r][i], lo2);
-          cg |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * i);
-        }
-        while (__any_sync(0xFFFFFFFFu, cg != 0u)) {
-          uint4 dv = make_uint4(0u, 0u, 0u, 0u);
-          uint32_t em = 0u;
-          if (cg != 0u) {
-            const int pos = __ffs(cg) - 1;
-            cg &= cg - 1u;
-            dv = s4[tid + pos * kThreads];
-            em = group_mask(dv);
+      for (int r = 0; r < 2; ++r) {
+        lo2s[r] = lo_pair(r);
+        if (r < nr && (lp.flags[r] & kFlagFinite)) {
+#pragma unroll
+          for (int i = 0; i < kGroupWords; ++i) {
+            const uint32_t m = bf16x2_ge_mask(gw[r][i], lo2s[r]);
+            cg[r] |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * i);
           }
-          // the candidates come out of the group already in registers
-          while (__any_sync(0xFFFFFFFFu, em != 0u)) {
-            if (em != 0u) {
-              const int pos = __ffs(em) - 1;
-              em &= em - 1u;
-              const uint32_t wv = (pos & 2) ? ((pos & 1) ? dv.w : dv.z) : ((pos & 1) ? dv.y : dv.x);
+        }
+      }
+      while (__any_sync(0xFFFFFFFFu, (cg[0] | cg[1]) != 0u)) {
+        uint4 dv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+        uint32_t em[2] = {0u, 0u};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          if (cg[r] != 0u) {
+            const int pos = __ffs(cg[r]) - 1;
+            cg[r] &= cg[r] - 1u;
+            dv[r] = reinterpret_cast<const uint4 *>(srow[r])[tid + pos * kThreads];
+            em[r] = 0x100u;  // loaded: the mask follows once both loads are issued
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          if (em[r]) em[r] = group_mask(dv[r], lo2s[r]);
+        // the candidates come out of the groups already in registers
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          uint32_t *cnt = lp.cnt[r];
+          while (__any_sync(0xFFFFFFFFu, em[r] != 0u)) {
+            if (em[r] != 0u) {
+              const int pos = __ffs(em[r]) - 1;
+              em[r] &= em[r] - 1u;
+              const uint32_t wv = (pos & 2) ? ((pos & 1) ? dv[r].w : dv[r].z) : ((pos & 1) ? dv[r].y : dv[r].x);
               const uint32_t b = (pos & 4) ? (wv >> 16) : (wv & 0xFFFFu);
-              const uint32_t d = lk16 - E::key(b);
+              const uint32_t d = lk16s[r] - E::key(b);
               if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
             }
           }
         }
       }
+    }
+    for (int r = 0; r < nr; ++r) {
+      if (!(lp.flags[r] & kFlagFinite)) continue;  // empty or no finite value: contributes nothing
+      const uint32_t lk16 = lk16s[r], lo = los[r], lo2 = lo_pair(r);
+      uint32_t *cnt = lp.cnt[r];
+      const TIn *row = srow[r];
+      const int nw = n >> 1;
+      const int ng = nw >> 2;  // 16-byte groups
       // Otherwise every group is tested, kWalkGroups per lane at once.
       if (!reg_groups)
-        walk_groups(row, ng, group_mask, [&](uint32_t b) {
+        walk_groups(row, ng, [&](const uint4 &dv) { return group_mask(dv, lo2); }, [&](uint32_t b) {
           const uint32_t d = lk16 - E::key(b);
           if (E::finite(b) && d < static_cast<uint32_t>(kNearBins)) atomicAdd(&cnt[d], 1u);
         });
