@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -996,89 +997,91 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   // and rescales it when the maximum rises (once per rising group)
   const bool fuse_z = reg_groups && (!near || (use_p && !use_k));  // dense rows, or top-p alone (its total)
   float omax[2] = {-INFINITY, -INFINITY}, osum[2] = {0.0f, 0.0f};
-  for (int r = 0; r < nr; ++r) {
-    if (kB == 16 && reg_groups) {
-      const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
-      uint32_t acc = 0xFF80FF80u;  // (-inf, -inf)
-      float om = -INFINITY, oz = 0.0f, oc = 0.0f;
-      auto raise_to = [&](float m) {  // a larger running maximum: rescale the sum
-        if (m > om) {
-          if (om != -INFINITY) {
-            const float f = exp2f(__fmul_rn(__fsub_rn(om, m), c2));
-            oz = __fmul_rn(oz, f);
-            oc = __fmul_rn(oc, f);
-          }
-          om = m;
+  // rows with register-held group maxima: both rows in one unrolled loop, so
+  // their group loads are in flight together (dense and top-p-alone rows also
+  // sum their weights, as in the per-row loop below)
+  const bool both_rows = kB == 16 && reg_groups;
+  // (one copy of the loop per kind of row, so the top-k / top-p copy keeps no
+  // branch between its loads)
+  auto both_rows_pass = [&](auto sums) {
+    constexpr bool kSums = decltype(sums)::value;
+    uint32_t acc[2] = {0xFF80FF80u, 0xFF80FF80u};  // (-inf, -inf)
+    float om2[2] = {-INFINITY, -INFINITY}, oz2[2] = {0.0f, 0.0f}, oc2[2] = {0.0f, 0.0f};
+    auto raise2 = [&](int r, float m) {  // a larger running maximum: rescale the sum
+      if (m > om2[r]) {
+        if (om2[r] != -INFINITY) {
+          const float f = exp2f(__fmul_rn(__fsub_rn(om2[r], m), c2));
+          oz2[r] = __fmul_rn(oz2[r], f);
+          oc2[r] = __fmul_rn(oc2[r], f);
         }
-      };
-      auto add = [&](uint32_t b) {  // (-inf adds 0; NaN/+inf rows are rejected anyway)
-        const float y = exp2f(__fmul_rn(__fsub_rn(E::val(b), om), c2)) - oc;  // Kahan
-        const float t = oz + y;
-        oc = (t - oz) - y;
-        oz = t;
-      };
-      if (fuse_z) {  // (its own copy of the loop: the common one stays as it is)
+        om2[r] = m;
+      }
+    };
+    auto add2 = [&](int r, uint32_t b) {  // (-inf adds 0; NaN/+inf rows are rejected anyway)
+      const float y = exp2f(__fmul_rn(__fsub_rn(E::val(b), om2[r]), c2)) - oc2[r];  // Kahan
+      const float t = oz2[r] + y;
+      oc2[r] = (t - oz2[r]) - y;
+      oz2[r] = t;
+    };
 #pragma unroll
-        for (int i = 0; i < kGroupWords; ++i) {
-          uint32_t half[2] = {0x7FFFu, 0x7FFFu};  // NaN: never a window candidate
+    for (int i = 0; i < kGroupWords; ++i) {
+      uint32_t half[2][2] = {{0x7FFFu, 0x7FFFu}, {0x7FFFu, 0x7FFFu}};  // NaN: never a window candidate
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int v = tid + (2 * i + h) * kThreads;
-            if (v < ng_all) {
-              const uint4 d = s4[v];
-              uint32_t p2 = bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w));
-              p2 = bf16x2_max_nan(p2, (p2 >> 16) | (p2 << 16));
-              acc = bf16x2_max_nan(acc, p2);
-              half[h] = p2 & 0xFFFFu;
-              raise_to(E::val(p2 & 0xFFFFu));
-              if (om != -INFINITY) {
+      for (int h = 0; h < 2; ++h) {
+        const int v = tid + (2 * i + h) * kThreads;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          if (r < nr && v < ng_all) {
+            const uint4 d = reinterpret_cast<const uint4 *>(srow[r])[v];
+            uint32_t p2 = bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w));
+            p2 = bf16x2_max_nan(p2, (p2 >> 16) | (p2 << 16));
+            acc[r] = bf16x2_max_nan(acc[r], p2);
+            half[r][h] = p2 & 0xFFFFu;
+            if (kSums) {
+              raise2(r, E::val(p2 & 0xFFFFu));
+              if (om2[r] != -INFINITY) {
                 const uint32_t w[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                  add(w[t] & 0xFFFFu);
-                  add(w[t] >> 16);
+                  add2(r, w[t] & 0xFFFFu);
+                  add2(r, w[t] >> 16);
                 }
               }
             }
           }
-          gw[r][i] = half[0] | (half[1] << 16);
         }
-        for (int x = (ng_all << 3) + tid; x < n; x += kThreads) {
-          const uint32_t b = bits_at(srow[r], x);
-          acc = bf16x2_max_nan(acc, b | 0xFF800000u);
-          raise_to(E::val(b));
-          if (om != -INFINITY) add(b);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < kGroupWords; ++i) {
-          uint32_t half[2] = {0x7FFFu, 0x7FFFu};  // NaN: never a window candidate
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int v = tid + (2 * i + h) * kThreads;
-            if (v < ng_all) {
-              const uint4 d = s4[v];
-              uint32_t p2 = bf16x2_max_nan(bf16x2_max_nan(d.x, d.y), bf16x2_max_nan(d.z, d.w));
-              p2 = bf16x2_max_nan(p2, (p2 >> 16) | (p2 << 16));
-              acc = bf16x2_max_nan(acc, p2);
-              half[h] = p2 & 0xFFFFu;
-            }
-          }
-          gw[r][i] = half[0] | (half[1] << 16);
-        }
-        for (int x = (ng_all << 3) + tid; x < n; x += kThreads)
-          acc = bf16x2_max_nan(acc, bits_at(srow[r], x) | 0xFF800000u);
       }
-      omax[r] = om;
-      osum[r] = oz;
-      acc = bf16x2_max_nan(acc, (acc >> 16) | (acc << 16));
-      const uint32_t mb = acc & 0xFFFFu;  // this thread's largest value, NaN if it saw one
+#pragma unroll
+      for (int r = 0; r < 2; ++r) gw[r][i] = half[r][0] | (half[r][1] << 16);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nr) continue;
+      for (int x = (ng_all << 3) + tid; x < n; x += kThreads) {
+        const uint32_t b = bits_at(srow[r], x);
+        acc[r] = bf16x2_max_nan(acc[r], b | 0xFF800000u);
+        if (kSums) {
+          raise2(r, E::val(b));
+          if (om2[r] != -INFINITY) add2(r, b);
+        }
+      }
+      omax[r] = om2[r];
+      osum[r] = oz2[r];
+      const uint32_t a2 = bf16x2_max_nan(acc[r], (acc[r] >> 16) | (acc[r] << 16));
+      const uint32_t mb = a2 & 0xFFFFu;  // this thread's largest value, NaN if it saw one
       if (E::is_nan(mb) || E::is_pinf(mb)) fl[r] |= kFlagBad;
       if (E::finite(mb)) {
         fl[r] |= kFlagFinite;
         mk[r] = E::key(mb);
       }
-    } else if (kB == 16) {
+    }
+  };
+  if (both_rows) {
+    if (fuse_z) both_rows_pass(std::true_type{});
+    else both_rows_pass(std::false_type{});
+  }
+  for (int r = 0; !both_rows && r < nr; ++r) {
+    if (kB == 16) {
       // pairs of bf16 through one NaN-propagating bf16x2 max per pair
       const int nw = n >> 1;
       const uint4 *s4 = reinterpret_cast<const uint4 *>(srow[r]);
