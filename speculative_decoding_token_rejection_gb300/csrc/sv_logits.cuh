@@ -998,11 +998,11 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
   const bool fuse_z = reg_groups && (!near || (use_p && !use_k));  // dense rows, or top-p alone (its total)
   float omax[2] = {-INFINITY, -INFINITY}, osum[2] = {0.0f, 0.0f};
   // rows with register-held group maxima: both rows in one unrolled loop, so
-  // their group loads are in flight together (dense and top-p-alone rows also
-  // sum their weights, as in the per-row loop below)
+  // their group loads are in flight together; one copy of the loop for
+  // summing rows and one for top-k / top-p rows, which so keeps no branch
+  // between its loads.  Wider bf16 chunks and fp32 rows take the per-row loop
+  // after it.
   const bool both_rows = kB == 16 && reg_groups;
-  // (one copy of the loop per kind of row, so the top-k / top-p copy keeps no
-  // branch between its loads)
   auto both_rows_pass = [&](auto sums) {
     constexpr bool kSums = decltype(sums)::value;
     uint32_t acc[2] = {0xFF80FF80u, 0xFF80FF80u};  // (-inf, -inf)
