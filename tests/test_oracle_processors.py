@@ -26,7 +26,7 @@ def _lists(ids):
 
 def test_greedy_golden_cases():
     g = load_golden("processors_examples.txt")
-    for c in ("g1", "g2", "g3"):
+    for c in ("g1", "g2", "g3", "g5"):
         rows = _rows(g[f"{c}_rows"])
         drafts = [int(x) for x in g[f"{c}_drafts"]]
         proc = {"repetition_penalty": np.array([float(g[f"{c}_theta"][0])], np.float32)}
@@ -151,6 +151,10 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
         "drafts only with a context list": ("a->penalty_ids, pb, pe, a->draft_ids + s, j);",
                                             "a->penalty_ids, pb, pe, a->draft_ids + s, a->penalty_cu ? j : 0);"),
         "no bf16 rounding": ("row[x] = dtype == ORC_BF16 ? round_to_bf16(v) : v;", "row[x] = v;"),
+        "penalty branches swapped": ("float v = row[x] > 0.0f ? row[x] / *theta : row[x] * *theta;",
+                                     "float v = row[x] > 0.0f ? row[x] * *theta : row[x] / *theta;"),
+        "penalty always divides": ("float v = row[x] > 0.0f ? row[x] / *theta : row[x] * *theta;",
+                                   "float v = row[x] / *theta;"),
         "stop off by one": ("        A = m;\n        break;", "        A = m > 0 ? m - 1 : 0;\n        break;"),
         "draft side unprocessed": ("load_row(base, a->dtype, row, stride, a->vocab_size, tmp);\n  process_row(a, i, s, j, tmp);",
                                    "load_row(base, a->dtype, row, stride, a->vocab_size, tmp);\n"
