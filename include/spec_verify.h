@@ -84,9 +84,9 @@ enum sv_data_status {
 
 /* Handle flags.  SV_FLAG_RESIDENT_ROWS: the logits entry copies both the
  * target and the draft row chunk of a position into shared memory (two CTAs
- * per SM).  By default both chunks are read in place after an L2 prefetch
- * (four CTAs per SM); calls with logits processors or unaligned rows always
- * copy them.  Results are identical. */
+ * per SM), and the sampler its row chunk.  By default aligned rows are read
+ * in place after an L2 prefetch (four CTAs per SM); calls with logits
+ * processors or unaligned rows always copy them.  Results are identical. */
 #define SV_FLAG_RESIDENT_ROWS 1u
 
 typedef struct spec_verify_ctx *spec_verify_t;
