@@ -11,10 +11,14 @@ inserted.
 
 Prints one JSON line: verified draft tokens/s for the whole job, the roofline
 of the verifier kernel against the measured HBM copy bandwidth, the logits
-entry on the same batch shape, the n-gram proposer on its own batch,
-end-to-end figures through the C ABI with
-inputs in pinned host memory (zero-copy rows, and full copies), the CPU oracle
-as a reported baseline, and the SM clocks sampled during the timed region.
+entry on the same batch shape (and two other sampling settings on its rows),
+the n-gram proposer on its own batch, the other next-step calls (synthetic
+acceptance, the logits entry with processors, the draft-side sampler with and
+without q rows), end-to-end figures through the C ABI with inputs in pinned
+host memory (zero-copy rows, and full copies), the CPU oracle on all host
+cores and on one as a reported baseline, and the SM clocks sampled during the
+timed region.  --impl reference times the CPU oracle itself on the same
+batch (all host cores).
 
   python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--gpus N]
 """
