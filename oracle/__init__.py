@@ -95,6 +95,8 @@ def _lib():
         lib.oracle_exponential.restype = ctypes.c_float
         lib.oracle_logits_to_probs.argtypes = [_P, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float,
                                                _P, _P]
+        lib.oracle_transform_row.argtypes = [_P, _P, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float,
+                                             _P, _P]
         lib.oracle_sample_rows.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int64,
                                            _P, _P, _P, _P, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
                                            ctypes.c_uint32, _P, _P, _P, _P,
@@ -138,6 +140,20 @@ def logits_to_probs(logits, temperature: float, top_k: int = 0, top_p: float = 1
     out = np.zeros_like(l)
     edge = np.zeros(1, dtype=np.int32)
     rc = _lib().oracle_logits_to_probs(_ptr(l), l.shape[0], temperature, int(top_k), top_p, _ptr(out), _ptr(edge))
+    return out, int(edge[0]), int(rc)
+
+
+def transform_row(logits, processed, temperature: float, top_k: int = 0, top_p: float = 1.0):
+    """The transform in the pages' order: temperature, top-k and top-p placed
+    on the raw row ``logits``, then the processed values ``processed`` (the same
+    row after banned ids and repetition penalty, or None) on the kept entries,
+    renormalised.  Returns (fp32 probabilities, top-p edge flag, status code)."""
+    l = _c(logits, np.float32)
+    lp = _c(processed, np.float32)
+    out = np.zeros_like(l)
+    edge = np.zeros(1, dtype=np.int32)
+    rc = _lib().oracle_transform_row(_ptr(l), _ptr(lp), l.shape[0], temperature, int(top_k), top_p, _ptr(out),
+                                     _ptr(edge))
     return out, int(edge[0]), int(rc)
 
 

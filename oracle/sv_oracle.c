@@ -39,10 +39,14 @@
  *    p; if that is all 0 as well the token is 0 (the lowest index) and the
  *    EMPTY_DISTRIBUTION status bit is raised;
  *  - temperature 0 selects the greedy path; argmax keeps the lowest index;
+ *    negative, NaN, infinite and subnormal (0 < T < FLT_MIN) temperatures are
+ *    invalid;
  *  - logits entry: value/T, top-k keeps every x with l(x) >= the k-th largest
  *    value (ties kept), softmax over the kept set (double), top-p keeps the
  *    shortest descending prefix whose cumulative probability reaches top_p
- *    plus every entry tied with its last element, renormalised, rounded to fp32;
+ *    plus every entry tied with its last element, then the logits processors
+ *    (banned ids, repetition penalty) act on the kept logits, renormalised,
+ *    rounded to fp32;
  *  - the rows a request reads are the rows a sequential verifier reads: rows
  *    after the first rejection are never examined, so their contents can not
  *    raise a status bit;
@@ -72,6 +76,7 @@
  *          E = fl32(-ln U), ln evaluated in double
  *   key (seed_lo, seed_hi); r = rng_request_base + request index.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -228,10 +233,29 @@ static int cmp_desc_double(const void *a, const void *b) {
   return (x < y) - (x > y);
 }
 
-/* Returns 0 on success, ORC_BAD_VALUES for NaN / +inf / no finite logit.
- * *edge is set to 1 if a top-p cumulative sum lands within 1e-6 of top_p. */
-int oracle_logits_to_probs(const float *l, int V, float temperature, int top_k, float top_p,
-                           float *out, int *edge) {
+/* The transform of one logits row, in the order of "vLLM source walk-through
+ * (10)", section "Rejection sampling: the two branches of RejectionSampler",
+ * step 2 (sampling constraints -- temperature, top-k, top-p -- first, then the
+ * logits processors such as penalties) and of "Speculative Decoding: propose,
+ * verify, accept", section 06 (temperature, top-k, top-p, banned tokens,
+ * repetition penalty):
+ *   1. value / T;
+ *   2. top-k on the raw row: keep x with l(x) >= tau, tau the k-th largest
+ *      logit counted with multiplicity;
+ *   3. softmax over the top-k set (double);
+ *   4. top-p: keep the shortest descending prefix whose cumulative
+ *      probability reaches top_p, plus every entry tied with its last one;
+ *   5. the logits processors act on the surviving logits: lp[x] replaces l(x)
+ *      for every kept x (a banned id's lp is -inf, a penalised id's lp is its
+ *      rewritten logit); lp == NULL means the request has no processors;
+ *   6. renormalise exp(v/T) over the kept x whose value v is finite, and round
+ *      to fp32.
+ * Returns 0 on success, ORC_BAD_VALUES for NaN / +inf / no finite logit in the
+ * raw row, NaN / +inf among the kept processed values, or a kept set whose
+ * every entry is banned (no distribution is left).  *edge is set to 1 if a
+ * top-p cumulative sum lands within 1e-6 of top_p. */
+int oracle_transform_row(const float *l, const float *lp, int V, float temperature, int top_k, float top_p,
+                         float *out, int *edge) {
   int n_finite = 0;
   for (int x = 0; x < V; ++x) {
     if (isnan(l[x]) || (isinf(l[x]) && l[x] > 0)) return ORC_BAD_VALUES;
@@ -249,20 +273,15 @@ int oracle_logits_to_probs(const float *l, int V, float temperature, int top_k, 
     tau = sorted[top_k - 1];
     free(sorted);
   }
-  /* softmax of l/T over the kept set, in double */
+  /* softmax of l/T over the top-k set, in double (it only places the top-p cut) */
   double T = (double)temperature;
   double m = -INFINITY;
   for (int x = 0; x < V; ++x)
     if ((double)l[x] >= tau && (double)l[x] / T > m) m = (double)l[x] / T;
-  double *e = (double *)calloc((size_t)V, sizeof(double));
   double Z = 0.0;
-  for (int x = 0; x < V; ++x) {
-    if ((double)l[x] >= tau) {
-      e[x] = exp((double)l[x] / T - m);
-      Z += e[x];
-    }
-  }
-  /* top-p over the kept set: walk the kept logits in descending order */
+  for (int x = 0; x < V; ++x)
+    if ((double)l[x] >= tau) Z += exp((double)l[x] / T - m);
+  /* top-p over the top-k set: walk the kept logits in descending order */
   double cut = tau;
   if (top_p < 1.0f) {
     int nk = 0;
@@ -288,14 +307,28 @@ int oracle_logits_to_probs(const float *l, int V, float temperature, int top_k, 
       *edge = 1;
     free(kept);
   }
-  /* renormalise over the final kept set */
+  /* the processors' values on the kept set, then the renormalisation */
+  const float *v = lp ? lp : l;
+  double m2 = -INFINITY;
+  for (int x = 0; x < V; ++x) {
+    if (!((double)l[x] >= tau && (double)l[x] >= cut)) continue;
+    if (isnan(v[x]) || (isinf(v[x]) && v[x] > 0)) return ORC_BAD_VALUES;
+    if (isfinite(v[x]) && (double)v[x] / T > m2) m2 = (double)v[x] / T;
+  }
+  if (m2 == -INFINITY) return ORC_BAD_VALUES; /* every kept logit was banned */
   double Z2 = 0.0;
   for (int x = 0; x < V; ++x)
-    if ((double)l[x] >= tau && (double)l[x] >= cut) Z2 += e[x];
+    if ((double)l[x] >= tau && (double)l[x] >= cut && isfinite(v[x])) Z2 += exp((double)v[x] / T - m2);
   for (int x = 0; x < V; ++x)
-    out[x] = ((double)l[x] >= tau && (double)l[x] >= cut) ? (float)(e[x] / Z2) : 0.0f;
-  free(e);
+    out[x] = ((double)l[x] >= tau && (double)l[x] >= cut && isfinite(v[x])) ? (float)(exp((double)v[x] / T - m2) / Z2)
+                                                                            : 0.0f;
   return 0;
+}
+
+/* The transform without logits processors. */
+int oracle_logits_to_probs(const float *l, int V, float temperature, int top_k, float top_p, float *out,
+                           int *edge) {
+  return oracle_transform_row(l, NULL, V, temperature, top_k, top_p, out, edge);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -384,16 +417,20 @@ static void race_diag(race_ctx *c, const float *w, const float *pa, const float 
 
 /* ------------------------------------------------------------------------
  * Logits processors ("Speculative Decoding: propose, verify, accept", section
- * 06: the same banned tokens and repetition penalty on p and q at a position;
- * "vLLM source walk-through (10)", section "Rejection sampling: the two
- * branches of RejectionSampler": processors such as penalties applied to the
- * verified logits).  Readings: a banned token's logit becomes -inf; the
- * repetition penalty (Keskar et al., CTRL, 2019) divides a positive logit by
- * theta and multiplies a non-positive one by it, once per distinct token of
- * the request's context list plus the drafts y_0 .. y_{j-1} already committed
- * when position j is verified; the result is rounded to the input type (bf16
+ * 06: the same banned tokens and repetition penalty on p and q at a position,
+ * listed after temperature, top-k and top-p; "vLLM source walk-through (10)",
+ * section "Rejection sampling: the two branches of RejectionSampler", step 2:
+ * the sampling constraints first, then the logits processors such as
+ * penalties).  Readings: a banned token's logit becomes -inf; the repetition
+ * penalty (Keskar et al., CTRL, 2019) divides a positive logit by theta and
+ * multiplies a non-positive one by it, once per distinct token of the
+ * request's context list plus the drafts y_0 .. y_{j-1} already committed when
+ * position j is verified; the result is rounded to the input type (bf16
  * round-to-nearest-even).  Ids outside [0, V) are ignored; a banned token is
- * not penalised.
+ * not penalised.  On a random row the processed values replace the logits of
+ * the entries that temperature, top-k and top-p kept (oracle_transform_row);
+ * a greedy row (temperature 0) draws nothing, so no sampling constraint
+ * applies to it: the processors act on the whole row and its argmax is taken.
  * ------------------------------------------------------------------------ */
 static int list_range(const int64_t *cu, int64_t total, int i, int64_t *b, int64_t *e) {
   *b = i ? cu[i - 1] : 0;
@@ -459,6 +496,11 @@ static void process_row(const oracle_args *a, int i, int64_t s, int j, float *ro
                 a->banned_ids, bb, be, a->penalty_ids, pb, pe, a->draft_ids + s, j);
 }
 
+/* A usable temperature: 0 (greedy) or a finite value of at least FLT_MIN.
+ * Reading: negative, NaN and infinite temperatures are invalid, and so are the
+ * subnormal ones in (0, FLT_MIN), whose reciprocal exceeds the fp32 range. */
+static int temperature_ok(float t) { return t == 0.0f || (t >= FLT_MIN && !isinf(t)); }
+
 static void emit_invalid(const oracle_args *a, int i) {
   int G = a->max_spec_len;
   for (int k = 0; k <= G; ++k) a->out_tokens[(int64_t)i * (G + 1) + k] = -1;
@@ -495,7 +537,7 @@ static void emit(const oracle_args *a, int i, int64_t s, int64_t tb, int g, int 
 
 /* fetch probability row j of the target (is_target) or draft side */
 static int prob_row(const oracle_args *a, int is_target, int64_t row, float T, int top_k, float top_p,
-                    float *tmp, float *out, int *edge, int i, int64_t s, int j) {
+                    float *tmp, float *proc, float *out, int *edge, int i, int64_t s, int j) {
   const void *base = is_target ? a->target : a->draft;
   int64_t stride = is_target ? a->target_row_stride : a->draft_row_stride;
   if (a->entry == ORC_ENTRY_PROBS) {
@@ -503,15 +545,20 @@ static int prob_row(const oracle_args *a, int is_target, int64_t row, float T, i
     return 0;
   }
   load_row(base, a->dtype, row, stride, a->vocab_size, tmp);
-  process_row(a, i, s, j, tmp);
+  const float *lp = NULL; /* the processed row, when the request has processors */
+  if (has_processors(a)) {
+    memcpy(proc, tmp, sizeof(float) * (size_t)a->vocab_size);
+    process_row(a, i, s, j, proc);
+    lp = proc;
+  }
   int e = 0;
-  int rc = oracle_logits_to_probs(tmp, a->vocab_size, T, top_k, top_p, out, &e);
+  int rc = oracle_transform_row(tmp, lp, a->vocab_size, T, top_k, top_p, out, &e);
   if (edge && e) *edge = 1;
   return rc;
 }
 
 static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB, float *bufC, float *bufD,
-                           int32_t *toks, race_ctx *rc) {
+                           float *bufE, int32_t *toks, race_ctx *rc) {
   const int G = a->max_spec_len, V = a->vocab_size;
   double *dg = a->diag ? a->diag + (int64_t)i * ORC_NDIAG : NULL;
   if (dg) {
@@ -540,7 +587,7 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
   const int64_t tb = s + i; /* first target row of request i */
 
   float temp = a->temperature ? a->temperature[i] : 1.0f;
-  if (!(temp >= 0.0f) || isinf(temp)) {
+  if (!temperature_ok(temp)) {
     *a->status |= ORC_BAD_PARAM;
     emit_invalid(a, i);
     return;
@@ -642,8 +689,8 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
       return;
     }
     float *p = bufA, *q = bufB;
-    int bad = prob_row(a, 1, tb + j, temp, top_k, top_p, bufC, p, &edge, i, s, j);
-    bad |= prob_row(a, 0, s + j, temp, top_k, top_p, bufD, q, &edge, i, s, j);
+    int bad = prob_row(a, 1, tb + j, temp, top_k, top_p, bufC, bufE, p, &edge, i, s, j);
+    bad |= prob_row(a, 0, s + j, temp, top_k, top_p, bufD, bufE, q, &edge, i, s, j);
     if (bad) {
       *a->status |= ORC_BAD_VALUES;
       emit_invalid(a, i);
@@ -694,7 +741,7 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
   }
   /* every draft accepted: bonus token from the last target row [P1; P2 s06] */
   float *p = bufA;
-  if (prob_row(a, 1, tb + g, temp, top_k, top_p, bufC, p, &edge, i, s, g)) {
+  if (prob_row(a, 1, tb + g, temp, top_k, top_p, bufC, bufE, p, &edge, i, s, g)) {
     *a->status |= ORC_BAD_VALUES;
     emit_invalid(a, i);
     return;
@@ -714,7 +761,7 @@ static void verify_request(const oracle_args *a, int i, float *bufA, float *bufB
 int oracle_verify_range(const oracle_args *a, int req_begin, int req_end) {
   const int V = a->vocab_size;
   if (V <= 0 || a->max_spec_len < 0) return -1;
-  float *buf = (float *)malloc(sizeof(float) * (size_t)V * 4);
+  float *buf = (float *)malloc(sizeof(float) * (size_t)V * 5);
   int32_t *toks = (int32_t *)malloc(sizeof(int32_t) * (size_t)(a->max_spec_len + 1));
   float *E_cache = (float *)malloc(sizeof(float) * (size_t)V);
   unsigned char *E_have = (unsigned char *)malloc((size_t)V);
@@ -731,7 +778,7 @@ int oracle_verify_range(const oracle_args *a, int req_begin, int req_end) {
   rc.E_cache = E_cache;
   rc.E_have = E_have;
   for (int i = req_begin; i < req_end; ++i)
-    verify_request(a, i, buf, buf + V, buf + 2 * (size_t)V, buf + 3 * (size_t)V, toks, &rc);
+    verify_request(a, i, buf, buf + V, buf + 2 * (size_t)V, buf + 3 * (size_t)V, buf + 4 * (size_t)V, toks, &rc);
   free(buf);
   free(toks);
   free(E_cache);
@@ -763,10 +810,11 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
                        int64_t penalty_total, const int64_t *banned_cu, const int32_t *banned_ids,
                        int64_t banned_total) {
   float *l = (float *)malloc(sizeof(float) * (size_t)V);
+  float *lp = (float *)malloc(sizeof(float) * (size_t)V);
   float *p = (float *)malloc(sizeof(float) * (size_t)V);
   float *E = (float *)malloc(sizeof(float) * (size_t)V);
-  if (!l || !p || !E) {
-    free(l); free(p); free(E);
+  if (!l || !lp || !p || !E) {
+    free(l); free(lp); free(p); free(E);
     return -2;
   }
   const uint64_t skey = seed ^ ((uint64_t)0x53414D50u << 32);
@@ -777,7 +825,7 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
       diag[2 * r] = INFINITY;
       diag[2 * r + 1] = 0;
     }
-    if (!(temp >= 0.0f) || isinf(temp)) {
+    if (!temperature_ok(temp)) {
       *status |= ORC_BAD_PARAM;
       tokens[r] = -1;
       continue;
@@ -795,12 +843,14 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
         tokens[r] = -1;
         continue;
       }
+      /* the processed copy of the row (the raw row still places the cuts) */
+      memcpy(lp, l, sizeof(float) * (size_t)V);
       if (banned_cu || repetition_penalty)
-        process_lists(l, V, dtype, repetition_penalty ? &repetition_penalty[r] : NULL, banned_ids, bb, be,
+        process_lists(lp, V, dtype, repetition_penalty ? &repetition_penalty[r] : NULL, banned_ids, bb, be,
                       penalty_ids, pb, pe, NULL, 0);
     }
-    if (temp == 0.0f) { /* greedy drafting: argmax of the (processed) logits */
-      int g = argmax_row(l, V);
+    if (temp == 0.0f) { /* greedy drafting: argmax of the processed logits */
+      int g = argmax_row(lp, V);
       if (g < 0) *status |= ORC_BAD_VALUES;
       tokens[r] = g;
       continue;
@@ -813,7 +863,7 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
       continue;
     }
     int edge = 0;
-    if (oracle_logits_to_probs(l, V, temp, k, tp, p, &edge)) {
+    if (oracle_transform_row(l, (banned_cu || repetition_penalty) ? lp : NULL, V, temp, k, tp, p, &edge)) {
       *status |= ORC_BAD_VALUES;
       tokens[r] = -1;
       continue;
@@ -856,6 +906,7 @@ int oracle_sample_rows(int32_t rows, int32_t V, int32_t dtype, const void *logit
     }
   }
   free(l);
+  free(lp);
   free(p);
   free(E);
   return 0;

@@ -427,6 +427,24 @@ def test_status_bits_and_invalid_requests(oracle_mod):
     assert r["status"] == 0 and r["out_tokens"].tolist() == [[0, -1, -1]]
 
 
+def test_subnormal_temperature_is_a_bad_parameter(oracle_mod):
+    """Reading: a temperature in (0, FLT_MIN) is invalid (its reciprocal leaves
+    the fp32 range); FLT_MIN itself is valid and behaves as a sharp softmax."""
+    p = [[0.5, 0.5], [0.5, 0.5]]
+    q = [[0.25, 0.75]]
+    for t, bad in ((1e-40, True), (float(np.float32(1.1754944e-38) / 2), True), (1.1754944e-38, False)):
+        r = oracle_mod.verify(hand_workload(p, q, [1], u=[0.9], E=[[1.0, 2.0]], temperature=[t]))
+        assert (r["status"] == oracle_mod.BAD_PARAM) == bad, t
+        if bad:
+            assert r["out_tokens"].tolist() == [[-1, -1]] and r["num_accepted"][0] == 0
+    l = np.array([[1.0, 0.5, -2.0]], np.float32)
+    s = oracle_mod.sample_rows(l, temperature=[1e-40], exponentials=np.ones((1, 3)))
+    assert s["status"] == oracle_mod.BAD_PARAM and s["tokens"][0] == -1
+    s = oracle_mod.sample_rows(l, temperature=[1.1754944e-38], exponentials=np.ones((1, 3)))
+    assert s["status"] == 0 and s["tokens"][0] == 0
+    np.testing.assert_array_equal(s["probs"][0], np.array([1.0, 0.0, 0.0], np.float32))
+
+
 # ----------------------------------------------------------------------------
 # logits -> probabilities (page 1 "Rejection sampling": temperature, top-k,
 # top-p applied identically; page 2 sections 06 and 14)

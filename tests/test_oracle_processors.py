@@ -137,13 +137,108 @@ def test_bad_lists_and_theta():
     assert oracle.verify(w, with_diag=False)["status"] == oracle.BAD_PARAM
 
 
+# ----------------------------------------------------------------------------
+# the order: temperature, top-k, top-p on the raw row, then the processors
+# ----------------------------------------------------------------------------
+def _case_lists(g, c):
+    kw = {}
+    if f"{c}_banned" in g:
+        kw["banned_cu"], kw["banned_ids"] = _lists([int(x) for x in g[f"{c}_banned"]])
+    if f"{c}_theta" in g:
+        kw["repetition_penalty"] = np.array([float(g[f"{c}_theta"][0])], np.float32)
+        kw["penalty_cu"], kw["penalty_ids"] = _lists([int(x) for x in g[f"{c}_context"]])
+    return kw
+
+
+def test_order_golden_sampler_rows():
+    """The draft-side sampler's transformed rows on the hand-worked cases t1-t5
+    (each separates the pages' order from processors-first)."""
+    g = load_golden("processors_order_examples.txt")
+    for c in ("t1", "t2", "t3", "t4", "t5"):
+        row = np.array([[float(x) for x in g[f"{c}_row"]]], np.float32)
+        V = row.shape[1]
+        s = oracle.sample_rows(row, temperature=[float(g[f"{c}_temp"][0])], top_k=[int(g[f"{c}_topk"][0])],
+                               top_p=[float(g[f"{c}_topp"][0])], exponentials=np.ones((1, V)), **_case_lists(g, c))
+        if f"{c}_status" in g:
+            assert s["status"] == int(g[f"{c}_status"][0]) and s["tokens"][0] == -1, c
+            continue
+        assert s["status"] == 0, c
+        expect = np.array([float(x) for x in g[f"{c}_expect"]], np.float32)
+        np.testing.assert_allclose(s["probs"][0], expect, rtol=0, atol=1e-7, err_msg=c)
+
+
+def test_order_golden_verifier_rows():
+    """The same cases through the verifier: the target and draft rows of one
+    position are the case's row, and the draft id walks over the vocabulary,
+    so dbg_py/dbg_qy read the whole transformed row back."""
+    g = load_golden("processors_order_examples.txt")
+    for c in ("t1", "t2", "t3", "t4", "t5"):
+        row = np.array([float(x) for x in g[f"{c}_row"]], np.float32)
+        V = row.shape[0]
+        for y in range(V):
+            t = np.stack([row, np.zeros(V, np.float32)])
+            w = hand_workload(t, row[None, :], [y], entry="logits", u=[0.5], E=np.ones((1, V)),
+                              temperature=[float(g[f"{c}_temp"][0])], top_k=[int(g[f"{c}_topk"][0])],
+                              top_p=[float(g[f"{c}_topp"][0])])
+            w.update(_case_lists(g, c))
+            o = oracle.verify(w, with_diag=False)
+            if f"{c}_status" in g:
+                assert o["status"] == int(g[f"{c}_status"][0]) and o["num_accepted"][0] == 0, c
+                assert list(o["out_tokens"][0]) == [-1, -1], c
+                continue
+            exp_y = float(g[f"{c}_expect"][y])
+            assert abs(o["dbg_py"][0] - exp_y) <= 1e-7 and abs(o["dbg_qy"][0] - exp_y) <= 1e-7, (c, y)
+
+
+def test_order_golden_commit():
+    """v1: the commit itself differs between the two orders."""
+    g = load_golden("processors_order_examples.txt")
+    t = _rows(g["v1_target"])
+    d = _rows(g["v1_draft"])
+    w = hand_workload(t, d, [int(x) for x in g["v1_drafts"]], entry="logits", u=[float(g["v1_u"][0])],
+                      E=np.ones((1, t.shape[1])), temperature=[1.0], top_k=[int(g["v1_topk"][0])], top_p=[1.0])
+    w["banned_cu"], w["banned_ids"] = _lists([int(x) for x in g["v1_banned"]])
+    o = oracle.verify(w, with_diag=False)
+    assert o["status"] == 0
+    assert o["num_accepted"][0] == int(g["v1_A"][0])
+    assert list(o["out_tokens"][0]) == [int(x) for x in g["v1_expect"]]
+    assert o["dbg_py"][0] == float(g["v1_py"][0]) and o["dbg_qy"][0] == float(g["v1_qy"][0])
+
+
+def test_order_golden_sampler_token():
+    g = load_golden("processors_order_examples.txt")
+    row = np.array([[float(x) for x in g["s1_row"]]], np.float32)
+    for E in (np.ones((1, 4)), np.array([[1.0, 5.0, 0.01, 1.0]])):
+        s = oracle.sample_rows(row, temperature=[1.0], top_k=[2], exponentials=E, banned_cu=[1],
+                               banned_ids=np.array([0], np.int32))
+        assert s["tokens"][0] == int(g["s1_token"][0]) and s["status"] == 0
+        np.testing.assert_array_equal(s["probs"][0], np.array([float(x) for x in g["s1_expect"]], np.float32))
+
+
+def test_transform_row_without_processors_matches_plain_transform():
+    """The processed-row entry with no processed row is the plain transform,
+    and a processed row equal to the raw row changes nothing."""
+    rng = np.random.default_rng(4)
+    for _ in range(20):
+        l = (rng.standard_normal(300) * 2).astype(np.float32)
+        k, tp, T = int(rng.integers(0, 60)), float(rng.uniform(0.2, 1.0)), float(rng.uniform(0.3, 2))
+        a, ea, ra = oracle.logits_to_probs(l, T, k, tp)
+        b, eb, rb = oracle.transform_row(l, None, T, k, tp)
+        c, ec, rc = oracle.transform_row(l, l.copy(), T, k, tp)
+        np.testing.assert_array_equal(a, b)
+        np.testing.assert_array_equal(a, c)
+        assert ra == rb == rc == 0 and ea == eb == ec
+
+
 def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
     import ctypes  # noqa: F401
     import subprocess
     src = oracle_mod._SRC.read_text()
     tests = (test_greedy_golden_cases, test_golden_g1_commit_length, test_penalty_without_context_list,
              test_stop_token_truncates_commit_and_rollback,
-             test_identical_processing_of_target_and_draft, test_bf16_rounding_of_penalised_logits)
+             test_identical_processing_of_target_and_draft, test_bf16_rounding_of_penalised_logits,
+             test_order_golden_sampler_rows, test_order_golden_verifier_rows, test_order_golden_commit,
+             test_order_golden_sampler_token)
     mutants = {
         "drafts not in the set": ("for (int k = 0; k < nextra; ++k) {", "for (int k = 0; k < nextra - 1; ++k) {"),
         "penalty overrides ban": ("      if (x >= 0 && x < V && !mark[x]) mark[x] = 2;\n    }\n    for (int k = 0; k < nextra",
@@ -156,9 +251,15 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
         "penalty always divides": ("float v = row[x] > 0.0f ? row[x] / *theta : row[x] * *theta;",
                                    "float v = row[x] / *theta;"),
         "stop off by one": ("        A = m;\n        break;", "        A = m > 0 ? m - 1 : 0;\n        break;"),
-        "draft side unprocessed": ("load_row(base, a->dtype, row, stride, a->vocab_size, tmp);\n  process_row(a, i, s, j, tmp);",
-                                   "load_row(base, a->dtype, row, stride, a->vocab_size, tmp);\n"
-                                   "  if (is_target) process_row(a, i, s, j, tmp);"),
+        "draft side unprocessed": ("  if (has_processors(a)) {\n    memcpy(proc",
+                                   "  if (has_processors(a) && is_target) {\n    memcpy(proc"),
+        "verifier: processors before the cuts": ("int rc = oracle_transform_row(tmp, lp, a->vocab_size",
+                                                 "int rc = oracle_transform_row(lp ? lp : tmp, lp, a->vocab_size"),
+        "sampler: processors before the cuts": (
+            "oracle_transform_row(l, (banned_cu || repetition_penalty) ? lp : NULL,",
+            "oracle_transform_row((banned_cu || repetition_penalty) ? lp : l, (banned_cu || repetition_penalty) ? lp : NULL,"),
+        "processed values ignored": ("const float *v = lp ? lp : l;", "const float *v = l;"),
+        "all-banned kept set not flagged": ("if (m2 == -INFINITY) return ORC_BAD_VALUES;", "if (m2 == -INFINITY) m2 = 0;"),
     }
     for name, (old, new) in mutants.items():
         assert src.count(old) == 1, name

@@ -178,8 +178,9 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
         "bonus row g-1": ("if (prob_row(a, 1, tb + g, temp,", "if (prob_row(a, 1, tb + g - 1, temp,"),
         "u times p": ("float uq = u * qy;", "float uq = u * py;"),
         "greedy keeps y": ("toks[j] = gj;", "toks[j] = (j < g) ? a->draft_ids[s + j] : gj;"),
-        "topk strict": ("if ((double)l[x] >= tau && (double)l[x] / T > m)",
-                        "if ((double)l[x] > tau && (double)l[x] / T > m)"),
+        "topk strict": ("(double)l[x] >= tau && (double)l[x] >= cut", "(double)l[x] > tau && (double)l[x] >= cut"),
+        "subnormal temperature accepted": ("return t == 0.0f || (t >= FLT_MIN && !isinf(t));",
+                                           "return t == 0.0f || (t > 0.0f && !isinf(t));"),
     }
     failures = {}
     for name, (old, new) in mutants.items():
