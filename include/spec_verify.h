@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 5u
+#define SPEC_VERIFY_ABI_VERSION 6u
 #define SV_PLACEHOLDER_TOKEN_ID (-1)
 #define SV_PADDING_SLOT_ID (-1)
 #define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
@@ -74,8 +74,9 @@ enum sv_data_status {
   SV_DATA_BAD_DRAFT_ID = 2,       /* draft id outside [0, V) at an examined position */
   SV_DATA_BAD_EXPONENTIAL = 4,    /* test-mode E <= 0 or NaN where a key needed it (key taken as 0) */
   SV_DATA_EMPTY_DISTRIBUTION = 8, /* a draw found no positive key; token 0 emitted */
-  SV_DATA_BAD_VALUES = 16,        /* NaN (greedy) or NaN/+inf/no finite logit (random logits) in a read row */
-  SV_DATA_BAD_PARAM = 32,         /* temperature < 0/NaN/inf, or top_p <= 0/NaN */
+  SV_DATA_BAD_VALUES = 16,        /* NaN (greedy) or NaN/+inf/no finite logit (random logits) in a read row,
+                                     or a kept set left empty by banned tokens */
+  SV_DATA_BAD_PARAM = 32,         /* temperature < 0/NaN/inf/subnormal, or top_p <= 0/NaN */
   SV_DATA_MISSING_DRAFT = 64,     /* draft == NULL but a random request needs draft rows */
   SV_DATA_COPY_TIMEOUT = 128,     /* a bulk row copy did not complete within its wait limit (request
                                      emits nothing); never expected on a healthy GPU */
@@ -85,9 +86,18 @@ enum sv_data_status {
 /* Handle flags.  SV_FLAG_RESIDENT_ROWS: the logits entry copies both the
  * target and the draft row chunk of a position into shared memory (two CTAs
  * per SM), and the sampler its row chunk.  By default aligned rows are read
- * in place after an L2 prefetch (four CTAs per SM); calls with logits
- * processors or unaligned rows always copy them.  Results are identical. */
+ * in place after an L2 prefetch (four CTAs per SM); unaligned rows are always
+ * copied.  Results are identical. */
 #define SV_FLAG_RESIDENT_ROWS 1u
+
+/* Call flags for tests (the test_flags field of the argument structs; 0 in
+ * normal use).  SV_TEST_EXPIRE_COPY_WAIT: the first wait for every bulk row
+ * copy into shared memory gives up at once, as if the copy had not completed
+ * within its limit; the copy still gets the ordinary second wait, so it lands
+ * before the CTA moves on.  The requests that copied rows then report
+ * SV_DATA_COPY_TIMEOUT and emit nothing.  Only calls whose rows are copied
+ * (SV_FLAG_RESIDENT_ROWS, or unaligned rows) are affected. */
+#define SV_TEST_EXPIRE_COPY_WAIT 1u
 
 typedef struct spec_verify_ctx *spec_verify_t;
 
@@ -137,7 +147,7 @@ typedef struct spec_verify_args {
   uint64_t seed;
   uint64_t offset;
   uint32_t rng_request_base;
-  uint32_t reserved1; /* must be 0 */
+  uint32_t test_flags; /* 0, or SV_TEST_EXPIRE_COPY_WAIT (tests only) */
 
   /* Outputs. */
   int32_t *out_tokens;          /* [N, G+1] committed tokens, -1 after the last one */
@@ -159,18 +169,24 @@ typedef struct spec_verify_args {
 
   /* Logits processors, logits entry only ("Speculative Decoding: propose,
    * verify, accept", section 06: the same banned tokens and repetition penalty
-   * on p and q at a position; "vLLM source walk-through (10)", section
-   * "Rejection sampling: the two branches of RejectionSampler").  Lists are
-   * per request, like cu_num_draft_tokens: request i owns entries
-   * [cu[i-1], cu[i]) (cu[-1] = 0) of the id array; ids outside [0, V) are
-   * ignored and repeats count once.  A banned token's logit becomes -inf on
-   * every row of the request.  With repetition_penalty, every distinct token
-   * of the request's penalty list, plus the drafts y_0 .. y_{j-1} when
-   * position j is verified, has its logit l replaced by l / theta if l > 0,
-   * else l * theta (fp32 arithmetic, rounded to the logits' type), on the
-   * target and the draft row alike; banned tokens are not penalised.  Theta
-   * must be > 0 and finite (else SV_DATA_BAD_PARAM).  The probability entry
-   * rejects these fields (its rows are already transformed). */
+   * on p and q at a position, after temperature, top-k and top-p; "vLLM
+   * source walk-through (10)", section "Rejection sampling: the two branches
+   * of RejectionSampler", step 2: the sampling constraints first, then the
+   * processors).  Lists are per request, like cu_num_draft_tokens: request i
+   * owns entries [cu[i-1], cu[i]) (cu[-1] = 0) of the id array; ids outside
+   * [0, V) are ignored and repeats count once.  A banned token's logit
+   * becomes -inf.  With repetition_penalty, every distinct token of the
+   * request's penalty list, plus the drafts y_0 .. y_{j-1} when position j is
+   * verified, has its logit l replaced by l / theta if l > 0, else l * theta
+   * (fp32 arithmetic, rounded to the logits' type), on the target and the
+   * draft row alike; banned tokens are not penalised.  On a random row the
+   * kept set is placed on the raw logits (temperature, top-k, top-p); the
+   * processed values then replace the kept logits and the kept set is
+   * renormalised (an entry the cuts dropped stays dropped; a kept set whose
+   * every entry is banned is SV_DATA_BAD_VALUES).  A greedy row takes the
+   * argmax of the whole processed row.  Theta must be > 0 and finite (else
+   * SV_DATA_BAD_PARAM).  The probability entry rejects these fields (its rows
+   * are already transformed). */
   const float *repetition_penalty;    /* [N] theta, or NULL: no penalty */
   const int64_t *penalty_cu;          /* [N] or NULL */
   const int32_t *penalty_token_ids;   /* [penalty_total] */
@@ -215,7 +231,7 @@ typedef struct spec_verify_sample_args {
   uint64_t seed;
   uint64_t offset;
   uint32_t rng_row_base; /* stream of row r: rng_row_base + r */
-  uint32_t reserved1;    /* must be 0 */
+  uint32_t test_flags;   /* 0, or SV_TEST_EXPIRE_COPY_WAIT (tests only) */
   int32_t *tokens;       /* [R] out: sampled token, -1 for an invalid row */
   float *probs;          /* [R rows, probs_row_stride] out or NULL: the transformed row (random rows only) */
   int64_t probs_row_stride;

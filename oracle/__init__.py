@@ -231,6 +231,43 @@ def verify(w: dict, *, production: bool = False, seed: int = 0, offset: int = 0,
                 dbg_py=dpy[:T], dbg_qy=dqy[:T], status=int(status[0]), diag=diag)
 
 
+def _threads(threads):
+    return max(1, threads if threads else (os.cpu_count() or 1))
+
+
+def verify_parallel(w: dict, *, threads: int = 0, **kw) -> dict:
+    """``verify`` over every request of ``w``, the requests split into
+    contiguous ranges run on host threads (ctypes releases the GIL during each
+    call; the C oracle keeps no global state), then merged.  Each range is the
+    oracle as it stands; the result is the one ``verify`` gives."""
+    from concurrent.futures import ThreadPoolExecutor
+    N = int(w["N"])
+    cuts = np.linspace(0, N, min(_threads(threads), max(N, 1)) + 1).astype(int)
+    ranges = [(int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+    if len(ranges) <= 1:
+        return verify(w, **kw)
+    with ThreadPoolExecutor(len(ranges)) as ex:
+        parts = list(ex.map(lambda r: verify(w, req_range=r, **kw), ranges))
+    if w.get("cu_num_draft_tokens") is not None:
+        cu = np.asarray(w["cu_num_draft_tokens"], np.int64)
+    else:
+        cu = (np.arange(1, N + 1) * int(w["gamma"])).astype(np.int64)
+    start = lambda i: int(cu[i - 1]) if i > 0 else 0
+    out = {k: (None if v is None else np.array(v, copy=True)) for k, v in parts[0].items() if k != "status"}
+    status = 0
+    for (a, b), r in zip(ranges, parts):
+        status |= r["status"]
+        for k in ("out_tokens", "num_accepted", "num_computed_tokens", "diag"):
+            if out.get(k) is not None:
+                out[k][a:b] = r[k][a:b]
+        for k in ("dbg_py", "dbg_qy"):
+            out[k][start(a):start(b)] = r[k][start(a):start(b)]
+        if out.get("slot_mapping") is not None:  # verify-token layout: request i at s_i + i .. s_i + i + gamma_i
+            out["slot_mapping"][start(a) + a:start(b) + b] = r["slot_mapping"][start(a) + a:start(b) + b]
+    out["status"] = status
+    return out
+
+
 def sample_rows(logits, *, temperature=None, top_k=None, top_p=None, exponentials=None, seed=0, offset=0,
                 rng_row_base=0, with_probs=True, repetition_penalty=None, penalty_cu=None, penalty_ids=None,
                 banned_cu=None, banned_ids=None):
@@ -261,6 +298,34 @@ def sample_rows(logits, *, temperature=None, top_k=None, top_p=None, exponential
     if rc != 0:
         raise RuntimeError(f"oracle_sample_rows failed with {rc}")
     return dict(tokens=tokens, probs=probs, status=int(status[0]), diag=diag)
+
+
+def sample_rows_parallel(logits, *, threads: int = 0, **kw):
+    """``sample_rows`` with the rows split into contiguous ranges run on host
+    threads, then concatenated (per-row arguments are sliced; production
+    draws keep their stream by offsetting ``rng_row_base``)."""
+    from concurrent.futures import ThreadPoolExecutor
+    R = logits.shape[0]
+    cuts = np.linspace(0, R, min(_threads(threads), max(R, 1)) + 1).astype(int)
+    ranges = [(int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+    per_row = ("temperature", "top_k", "top_p", "exponentials", "repetition_penalty")
+    if any(kw.get(k) is not None for k in ("penalty_cu", "banned_cu")):
+        raise ValueError("sample_rows_parallel takes no processor lists")
+
+    def run(r):
+        a, b = r
+        sub = {k: (None if v is None else np.asarray(v)[a:b]) if k in per_row else v for k, v in kw.items()}
+        sub["rng_row_base"] = int(kw.get("rng_row_base", 0)) + a
+        return sample_rows(logits[a:b], **sub)
+
+    with ThreadPoolExecutor(max(1, len(ranges))) as ex:
+        parts = list(ex.map(run, ranges))
+    probs = None if parts[0]["probs"] is None else np.concatenate([p["probs"] for p in parts])
+    status = 0
+    for p in parts:
+        status |= p["status"]
+    return dict(tokens=np.concatenate([p["tokens"] for p in parts]), probs=probs, status=status,
+                diag=np.concatenate([p["diag"] for p in parts]))
 
 
 def ngram_propose(tokens, cu_num_tokens, *, min_ngram: int, max_ngram: int, k: int, max_model_len: int):

@@ -252,8 +252,10 @@ static int cmp_desc_double(const void *a, const void *b) {
  *      to fp32.
  * Returns 0 on success, ORC_BAD_VALUES for NaN / +inf / no finite logit in the
  * raw row, NaN / +inf among the kept processed values, or a kept set whose
- * every entry is banned (no distribution is left).  *edge is set to 1 if a
- * top-p cumulative sum lands within 1e-6 of top_p. */
+ * every entry is banned (no distribution is left).  *edge is set to 1 if the
+ * cumulative probability of the values above the top-p cut value, or of the
+ * values through it, lies within 1e-6 of top_p (a perturbation of that size
+ * could move the cut to another value). */
 int oracle_transform_row(const float *l, const float *lp, int V, float temperature, int top_k, float top_p,
                          float *out, int *edge) {
   int n_finite = 0;
@@ -292,10 +294,9 @@ int oracle_transform_row(const float *l, const float *lp, int V, float temperatu
     for (int x = 0; x < V; ++x)
       if ((double)l[x] >= tau) kept[t++] = (double)l[x];
     qsort(kept, (size_t)nk, sizeof(double), cmp_desc_double);
-    double cum = 0.0, prev = 0.0;
+    double cum = 0.0;
     int found = 0;
     for (int r = 0; r < nk; ++r) {
-      prev = cum;
       cum += exp(kept[r] / T - m) / Z;
       if (cum >= (double)top_p) {
         cut = kept[r];
@@ -303,8 +304,18 @@ int oracle_transform_row(const float *l, const float *lp, int V, float temperatu
         break;
       }
     }
-    if (edge && (fabs(cum - (double)top_p) < 1e-6 || fabs(prev - (double)top_p) < 1e-6 || !found))
-      *edge = 1;
+    if (edge) {
+      /* Entries tied with the cut value are all kept, so the kept set changes
+       * only when a value-group boundary moves across top_p: the cumulative
+       * mass of the values above the cut value, and of those through it. */
+      double above = 0.0, through = 0.0;
+      for (int r = 0; r < nk; ++r) {
+        double e = exp(kept[r] / T - m) / Z;
+        if (kept[r] > cut) above += e;
+        if (kept[r] >= cut) through += e;
+      }
+      if (!found || fabs(above - (double)top_p) < 1e-6 || fabs(through - (double)top_p) < 1e-6) *edge = 1;
+    }
     free(kept);
   }
   /* the processors' values on the kept set, then the renormalisation */

@@ -35,6 +35,7 @@ _P = ctypes.c_void_p
 
 
 SV_FLAG_RESIDENT_ROWS = 1
+SV_TEST_EXPIRE_COPY_WAIT = 1
 
 
 class SpecVerifyConfig(ctypes.Structure):
@@ -54,7 +55,7 @@ class SpecVerifyArgs(ctypes.Structure):
         ("temperature", _P), ("top_k", _P), ("top_p", _P),
         ("uniforms", _P), ("exponentials", _P), ("exponentials_row_stride", ctypes.c_int64),
         ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
-        ("rng_request_base", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
+        ("rng_request_base", ctypes.c_uint32), ("test_flags", ctypes.c_uint32),
         ("out_tokens", _P), ("num_accepted", _P), ("num_computed_tokens", _P), ("slot_mapping", _P),
         ("dbg_py", _P), ("dbg_qy", _P), ("status", _P), ("synthetic_acceptance_rates", _P),
         ("repetition_penalty", _P), ("penalty_cu", _P), ("penalty_token_ids", _P), ("penalty_total", ctypes.c_int64),
@@ -71,7 +72,7 @@ class SpecVerifySampleArgs(ctypes.Structure):
         ("temperature", _P), ("top_k", _P), ("top_p", _P),
         ("exponentials", _P), ("exponentials_row_stride", ctypes.c_int64),
         ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
-        ("rng_row_base", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
+        ("rng_row_base", ctypes.c_uint32), ("test_flags", ctypes.c_uint32),
         ("tokens", _P), ("probs", _P), ("probs_row_stride", ctypes.c_int64), ("status", _P),
         ("repetition_penalty", _P), ("penalty_cu", _P), ("penalty_token_ids", _P), ("penalty_total", ctypes.c_int64),
         ("banned_cu", _P), ("banned_token_ids", _P), ("banned_total", ctypes.c_int64),
@@ -226,7 +227,7 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
                dbg_py=None, dbg_qy=None, status=None, device=None,
                host_rows: bool = False, synthetic_acceptance_rates=None, repetition_penalty=None,
                penalty_cu=None, penalty_token_ids=None, banned_cu=None, banned_token_ids=None, stop_cu=None,
-               stop_token_ids=None) -> SpecVerifyArgs:
+               stop_token_ids=None, test_flags: int = 0) -> SpecVerifyArgs:
     """Validate tensors and fill a SpecVerifyArgs (no device work).
 
     Logits processors (logits entry) and stop tokens (both entries) come as
@@ -275,6 +276,7 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
         a.exponentials, a.exponentials_row_stride = _rows(exponentials, "exponentials", device, V, N,
                                                           (torch.float32,), host_rows)
     a.seed, a.offset, a.rng_request_base = int(seed), int(offset), int(rng_request_base)
+    a.test_flags = int(test_flags)
     a.out_tokens = _ptr(out_tokens, torch.int32, "out_tokens", device, ndim=2)
     a.num_accepted = _ptr(num_accepted, torch.int32, "num_accepted", device, numel=N)
     a.num_computed_tokens = _ptr(num_computed_tokens, torch.int32, "num_computed_tokens", device, numel=N)
@@ -309,7 +311,7 @@ def spec_verify_run(handle: int, stream=None, **kw) -> None:
 def build_sample_args(*, logits, tokens, probs=None, temperature=None, top_k=None, top_p=None, exponentials=None,
                       seed: int = 0, offset: int = 0, rng_row_base: int = 0, status=None, repetition_penalty=None,
                       penalty_cu=None, penalty_token_ids=None, banned_cu=None,
-                      banned_token_ids=None) -> SpecVerifySampleArgs:
+                      banned_token_ids=None, test_flags: int = 0) -> SpecVerifySampleArgs:
     """Validate tensors and fill a SpecVerifySampleArgs (no device work).
     Logits processors per row as in ``build_args``."""
     import torch
@@ -331,6 +333,7 @@ def build_sample_args(*, logits, tokens, probs=None, temperature=None, top_k=Non
         a.exponentials, a.exponentials_row_stride = _rows(exponentials, "exponentials", device, V, R,
                                                           (torch.float32,))
     a.seed, a.offset, a.rng_row_base = int(seed), int(offset), int(rng_row_base)
+    a.test_flags = int(test_flags)
     a.tokens = _ptr(tokens, torch.int32, "tokens", device, numel=R)
     if probs is not None:
         a.probs, a.probs_row_stride = _rows(probs, "probs", device, V, R, (torch.float32,))

@@ -136,7 +136,8 @@ sv_status spec_verify_check_args(const spec_verify_config *c, const spec_verify_
   if (a->dtype != SV_F32 && a->dtype != SV_BF16) return fail(SV_ERR_INVALID_ARG, "bad dtype");
   if (a->entry == SV_ENTRY_PROBS && a->dtype != SV_F32)
     return fail(SV_ERR_UNSUPPORTED, "the probability entry takes fp32 rows");
-  if (a->reserved0 != 0 || a->reserved1 != 0) return fail(SV_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (a->reserved0 != 0) return fail(SV_ERR_INVALID_ARG, "reserved0 must be 0");
+  if (a->test_flags & ~SV_TEST_EXPIRE_COPY_WAIT) return fail(SV_ERR_INVALID_ARG, "unknown test_flags 0x%x", a->test_flags);
   if (a->num_draft_tokens_total < 0) return fail(SV_ERR_INVALID_ARG, "num_draft_tokens_total < 0");
   if (!a->cu_num_draft_tokens &&
       a->num_draft_tokens_total != static_cast<int64_t>(a->num_reqs) * a->max_spec_len)
@@ -273,6 +274,7 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
   p.stop_cu = a->stop_cu;
   p.stop_ids = a->stop_token_ids;
   p.stop_total = a->stop_total;
+  p.first_wait = (a->test_flags & SV_TEST_EXPIRE_COPY_WAIT) ? 0u : sv::kCopyWaitPolls;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (a->entry == SV_ENTRY_PROBS) {
@@ -288,7 +290,7 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
     const bool procs = a->repetition_penalty || a->banned_cu;
     const bool vec = sv::aligned16(a->target) && (a->target_row_stride % per16 == 0) &&
                      (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % per16 == 0));
-    const bool resident = procs || !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
+    const bool resident = !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
     if (!sv::choose_logits_layout(h, p.N, p.V, eb, &cluster, &chunk, procs, resident, true))
       return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for the rows to fit in the cluster's shared memory",
                   p.V);
@@ -309,7 +311,8 @@ sv_status spec_verify_check_sample_args(const spec_verify_config *c, const spec_
   if (a->vocab_size > c->vocab_size)
     return fail(SV_ERR_CAPACITY, "vocab_size %d > handle max %d", a->vocab_size, c->vocab_size);
   if (a->dtype != SV_F32 && a->dtype != SV_BF16) return fail(SV_ERR_INVALID_ARG, "bad dtype");
-  if (a->reserved0 != 0 || a->reserved1 != 0) return fail(SV_ERR_INVALID_ARG, "reserved fields must be 0");
+  if (a->reserved0 != 0) return fail(SV_ERR_INVALID_ARG, "reserved0 must be 0");
+  if (a->test_flags & ~SV_TEST_EXPIRE_COPY_WAIT) return fail(SV_ERR_INVALID_ARG, "unknown test_flags 0x%x", a->test_flags);
   if (a->num_rows == 0) return SV_OK;
   if (!a->logits) return fail(SV_ERR_INVALID_ARG, "logits is NULL");
   if (a->row_stride < a->vocab_size) return fail(SV_ERR_INVALID_ARG, "row_stride < vocab_size");
@@ -356,14 +359,15 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   p.ban_cu = a->banned_cu;
   p.ban_ids = a->banned_token_ids;
   p.ban_total = a->banned_total;
+  p.first_wait = (a->test_flags & SV_TEST_EXPIRE_COPY_WAIT) ? 0u : sv::kCopyWaitPolls;
   const bool bf16 = a->dtype == SV_BF16;
   const int eb = bf16 ? 2 : 4;
   int cluster = 0, chunk = 0;
   const bool procs = p.rep_penalty || p.ban_cu;
   const bool vec = sv::aligned16(a->logits) && (a->row_stride % (16 / eb) == 0);
-  // rows with processors (rewritten in place), unaligned rows, or the handle
-  // flag go through shared memory; other rows are read where they lie
-  const bool resident = procs || !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
+  // unaligned rows, or the handle flag, go through shared memory; other rows
+  // are read where they lie
+  const bool resident = !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
   if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk, procs, resident, false))
     return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for a row to fit in the cluster's shared memory", p.V);
   const cudaError_t e = sv::launch_sample(p, bf16, cluster, chunk, vec, resident, static_cast<cudaStream_t>(stream));

@@ -235,6 +235,13 @@ __device__ __forceinline__ int stop_commit(int A, TokFn tok, const int32_t *ids,
   return *first;
 }
 
+// A usable temperature: 0 (the greedy path) or a finite value of at least
+// FLT_MIN; negative, NaN, infinite and subnormal ones are bad parameters (the
+// reciprocal of a subnormal temperature leaves the fp32 range).
+__device__ __forceinline__ bool temperature_ok(float t) {
+  return t == 0.0f || (t >= __uint_as_float(0x00800000u) && !isinf(t));
+}
+
 // A per-request list range [b, e) (inclusive prefix sums, like
 // cu_num_draft_tokens); false if it is not inside [0, total].
 __device__ __forceinline__ bool list_range(const int64_t *cu, int64_t total, int i, int64_t &b, int64_t &e) {

@@ -53,6 +53,7 @@ struct VerifyParams {
   const int64_t *stop_cu;
   const int32_t *stop_ids;
   int64_t stop_total;
+  uint32_t first_wait;  // polls of the first wait for a bulk row copy (0 under SV_TEST_EXPIRE_COPY_WAIT)
 };
 
 // The draft-side sampler's parameters (device pointers, sizes).
@@ -78,6 +79,7 @@ struct SampleParams {
   const int64_t *ban_cu;
   const int32_t *ban_ids;
   int64_t ban_total;
+  uint32_t first_wait;  // polls of the first wait for a bulk row copy (0 under SV_TEST_EXPIRE_COPY_WAIT)
 };
 
 // The n-gram proposer's parameters (device pointers, sizes).
@@ -91,6 +93,9 @@ struct NgramParams {
   int32_t *status;
 };
 cudaError_t launch_ngram(const NgramParams &p, cudaStream_t stream);
+
+// Polls of the ordinary wait for a bulk row copy (each poll may suspend for a while).
+constexpr uint32_t kCopyWaitPolls = 1u << 20;
 
 // Picks the CTAs-per-request for a call (power of two, <= ctx->max_cluster).
 int choose_cluster(const spec_verify_ctx *ctx, int N, int V);
@@ -121,8 +126,8 @@ cudaError_t launch_sample_f32(const SampleParams &p, int cluster, int chunk, siz
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
                           cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);
-// resident: both row chunks of a position in shared memory (needed by the
-// processors and by unaligned rows); otherwise both are read in place.
+// resident: both row chunks of a position in shared memory (needed by
+// unaligned rows); otherwise both are read in place.
 cudaError_t launch_logits(const VerifyParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
                           cudaStream_t stream);
 // Dynamic shared memory of the processor bitmaps (banned and penalised keys of a chunk).

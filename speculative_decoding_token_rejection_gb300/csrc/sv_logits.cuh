@@ -140,7 +140,6 @@ __device__ __forceinline__ uint32_t bf16_bits_of_key(uint32_t k) {
 constexpr uint32_t kFlagBad = 1u;      // NaN or +inf in a random row
 constexpr uint32_t kFlagFinite = 2u;   // at least one finite logit
 constexpr uint32_t kFlagTimeout = 4u;  // the row's bulk copy did not complete in time
-constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kNearBins = 128;         // near-max bins: distances 0..127 from the row's largest key
 constexpr int kMaxCluster = 16;
 constexpr int kWalkGroups = 8;  // 16-byte groups a lane tests per window-scan step
@@ -229,7 +228,10 @@ struct LogitsSmem {
   Select sel;
   uint64_t bar;
   int stop_first;      // first committed stop token
-  uint32_t yproc[2];   // processed logits of the draft token (target, draft row), from its owner
+  uint4 xw[kMaxCluster];  // every CTA's word of the last cluster exchange, by rank
+  float pz[2];            // block totals of the processors' correction
+  uint32_t pmark;         // marks of the draft token, from the CTA holding it
+  uint32_t xmax[2];       // block maxima (ordered bits) of the processors' rescue pass
   int32_t tok[SV_MAX_SPEC_LEN + 1];
 };
 
@@ -967,8 +969,7 @@ __device__ bool window_rounds(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], 
 template <typename TIn>
 __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2], int nr, int n, float c2, int topk,
                                float topp, uint32_t load_flags, RowStats st[2], uint32_t *req_bits, int &step,
-                               uint32_t ncta, uint32_t rank, uint32_t ybits0 = 0u, uint32_t ybits1 = 0u,
-                               int y_owner = -1) {
+                               uint32_t ncta, uint32_t rank) {
   using E = Elem<TIn>;
   constexpr int kB = E::kBits;
   const int tid = threadIdx.x;
@@ -1325,7 +1326,7 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
         v = make_uint4(lp.maxkey[0], lp.maxkey[1], lp.flags[0] | (lp.nbins[0] << kBinsShift),
                        lp.flags[1] | (lp.nbins[1] << kBinsShift));
       } else if (wd == 1) {
-        v = make_uint4(__float_as_uint(lp.z[0]), __float_as_uint(lp.z[1]), ybits0, ybits1);
+        v = make_uint4(__float_as_uint(lp.z[0]), __float_as_uint(lp.z[1]), 0u, 0u);
       } else if (wd == 2) {
         v = make_uint4(static_cast<uint32_t>(lp.tot[0]), static_cast<uint32_t>(lp.tot[0] >> 32),
                        static_cast<uint32_t>(lp.tot[1]), static_cast<uint32_t>(lp.tot[1] >> 32));
@@ -1390,16 +1391,18 @@ __device__ bool position_stats(LogitsSmem &sm, Inbox *inbox, TIn *const srow[2],
       ns.tot[r] = tot;
     }
   }
-  if (tid == 0 && y_owner >= 0) {  // the draft token's processed logits travel in its owner's header
-    sm.yproc[0] = ibx[y_owner].pad[0];
-    sm.yproc[1] = ibx[y_owner].pad[1];
-  }
   __syncthreads();
 
   for (int r = 0; r < nr; ++r) {
     const uint32_t f = ns.flags[r];
-    if (f & kFlagTimeout) *req_bits |= SV_DATA_COPY_TIMEOUT;
-    if ((f & (kFlagBad | kFlagTimeout)) || !(f & kFlagFinite)) return false;
+    if (f & kFlagTimeout) {
+      *req_bits |= SV_DATA_COPY_TIMEOUT;
+      return false;
+    }
+    if ((f & kFlagBad) || !(f & kFlagFinite)) {
+      *req_bits |= SV_DATA_BAD_VALUES;
+      return false;
+    }
     st[r].vmax = E::val_of_key(ns.gmax[r]);
     st[r].c2 = c2;
     st[r].cut = 0u;
@@ -1450,6 +1453,66 @@ __device__ __forceinline__ float prob_of(uint32_t b, const RowStats &st) {
   if (E::key(b) < st.cut) return 0.0f;
   const float e = exp2f(__fmul_rn(__fsub_rn(E::val(b), st.vmax), st.c2));
   return __fdiv_rn(e, st.zp);
+}
+
+// ---------------------------------------------------------------------------
+// logits processors ("Speculative Decoding: propose, verify, accept", section
+// 06: the same banned tokens and repetition penalty on p and q at a position,
+// listed after temperature, top-k and top-p; "vLLM source walk-through (10)",
+// section "Rejection sampling: the two branches of RejectionSampler", step 2:
+// the sampling constraints first, then the logits processors).  The kept set
+// is placed on the raw rows by the ordinary statistics; the processors then
+// change only the marked entries it contains: a banned one drops out, a
+// penalised one takes the weight of l / theta (l > 0) or l * theta (fp32,
+// rounded to the row's type; Keskar et al., CTRL, 2019).  Each CTA marks its
+// chunk in two bitmaps (banned, penalised); the rows themselves are never
+// rewritten.  A greedy row (temperature 0) draws nothing, so no sampling
+// constraint applies to it: its argmax is taken over the processed row.
+// ---------------------------------------------------------------------------
+struct Procs {
+  const uint32_t *pen;  // penalised keys of this CTA's chunk, one bit each
+  const uint32_t *ban;  // banned keys (a banned key is never penalised)
+  float theta;
+};
+
+// 0: unmarked, 1: banned, 2: penalised (chunk-relative index xl)
+__device__ __forceinline__ uint32_t mark_at(const Procs &pr, int xl) {
+  const int w = xl >> 5, b = xl & 31;
+  if ((pr.ban[w] >> b) & 1u) return 1u;
+  return (pr.pen[w] >> b) & 1u ? 2u : 0u;
+}
+// Bit t set if entry xl + t is marked, for kPer entries from xl (a multiple of kPer).
+template <int kPer>
+__device__ __forceinline__ uint32_t group_marks(const Procs &pr, int xl) {
+  const int w = xl >> 5;
+  return ((pr.pen[w] | pr.ban[w]) >> (xl & 31)) & ((1u << kPer) - 1u);
+}
+
+// The value an entry takes under the processors, as bits of the row's type.
+template <typename TIn>
+__device__ __forceinline__ uint32_t processed_bits(uint32_t b, uint32_t mark, float theta) {
+  if (mark == 1u) return sizeof(TIn) == 2 ? 0xFF80u : 0xFF800000u;  // -inf
+  if (mark != 2u) return b;
+  const float v = Elem<TIn>::val(b);
+  const float f = v > 0.0f ? __fdiv_rn(v, theta) : __fmul_rn(v, theta);
+  if constexpr (sizeof(TIn) == 2) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  } else {
+    return __float_as_uint(f);
+  }
+}
+
+// Weight of value bits pb relative to the row's reference maximum (0 for -inf).
+template <typename TIn>
+__device__ __forceinline__ float kept_weight(uint32_t pb, const RowStats &st) {
+  return exp2f(__fmul_rn(__fsub_rn(Elem<TIn>::val(pb), st.vmax), st.c2));
+}
+
+// Probability of raw logit bits b with marks `mark` (prob_of when unmarked).
+template <typename TIn>
+__device__ __forceinline__ float prob_of_m(uint32_t b, uint32_t mark, const RowStats &st, float theta) {
+  if (Elem<TIn>::key(b) < st.cut) return 0.0f;  // kept sets are placed on the raw logits
+  return __fdiv_rn(kept_weight<TIn>(processed_bits<TIn>(b, mark, theta), st), st.zp);
 }
 
 // ---------------------------------------------------------------------------
@@ -1519,13 +1582,30 @@ __device__ __forceinline__ float race_w(uint32_t bp, uint32_t bq, const RowStats
   return p > 0.0f ? p : 0.0f;
 }
 
-// The race over this CTA's rows in shared memory.  Each thread takes 16-byte
-// groups in increasing order (then the tail quads), so its strict '>' keeps
-// its lowest index on ties.
-template <typename TIn, bool kTest, bool kResidual>
+// race_w for an entry with processor marks: the kept tests on the raw logits,
+// the weights from the processed ones.
+template <typename TIn, bool kResidual>
+__device__ __forceinline__ float race_w_m(uint32_t bp, uint32_t bq, uint32_t mark, const RowStats &ps,
+                                          const RowStats &qs, float rp, float rq, float theta) {
+  using E = Elem<TIn>;
+  const float p =
+      E::key(bp) < ps.cut ? 0.0f : __fmul_rn(kept_weight<TIn>(processed_bits<TIn>(bp, mark, theta), ps), rp);
+  if (kResidual) {
+    const float q =
+        E::key(bq) < qs.cut ? 0.0f : __fmul_rn(kept_weight<TIn>(processed_bits<TIn>(bq, mark, theta), qs), rq);
+    const float d = __fsub_rn(p, q);
+    return d > 0.0f ? d : 0.0f;
+  }
+  return p > 0.0f ? p : 0.0f;
+}
+
+// The race over this CTA's row chunks.  Each thread takes 16-byte groups in
+// increasing order (then the tail quads), so its strict '>' keeps its lowest
+// index on ties.  kProc: marked entries take their processed weights.
+template <typename TIn, bool kTest, bool kResidual, bool kProc = false>
 __device__ __forceinline__ void race_chunks(const TIn *sp, const TIn *sq, const RowStats &ps, const RowStats &qs,
                                           int x0, int n, const float *Erow, const RngKey &rk, uint32_t rs, float &bk,
-                                          int &bx, uint32_t &flags) {
+                                          int &bx, uint32_t &flags, const Procs &pr = Procs{nullptr, nullptr, 1.0f}) {
   constexpr int kPer = 16 / sizeof(TIn);  // 8 bf16 or 4 fp32 = 2 or 1 quads
   const int nv = n / kPer;
   const uint4 *p4 = reinterpret_cast<const uint4 *>(sp);
@@ -1559,6 +1639,17 @@ __device__ __forceinline__ void race_chunks(const TIn *sp, const TIn *sq, const 
         w[t] = race_w<TIn, kResidual>(wp[t], wq[t], ps, qs, rp, rq);
       }
     }
+    if (kProc) {  // marked entries of the group: processed weights
+      uint32_t mk = group_marks<kPer>(pr, v * kPer);
+      while (mk) {
+        const int t = __ffs(mk) - 1;
+        mk &= mk - 1u;
+        const int wi = sizeof(TIn) == 2 ? t >> 1 : t, sh = sizeof(TIn) == 2 ? 16 * (t & 1) : 0;
+        const uint32_t msk = sizeof(TIn) == 2 ? 0xFFFFu : 0xFFFFFFFFu;
+        w[t] = race_w_m<TIn, kResidual>((wp[wi] >> sh) & msk, (wq[wi] >> sh) & msk, mark_at(pr, v * kPer + t), ps,
+                                        qs, rp, rq, pr.theta);
+      }
+    }
 #pragma unroll
     for (int qd = 0; qd < kPer / 4; ++qd)
       race_quad_l<kTest>(&w[4 * qd], x0 + v * kPer + 4 * qd, Erow, rk, rs, bk, bx, flags);
@@ -1568,7 +1659,14 @@ __device__ __forceinline__ void race_chunks(const TIn *sp, const TIn *sq, const 
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int x = 4 * q + t;
-      w[t] = x < n ? race_w<TIn, kResidual>(bits_at(sp, x), kResidual ? bits_at(sq, x) : 0u, ps, qs, rp, rq) : 0.0f;
+      if (x >= n) {
+        w[t] = 0.0f;
+      } else if (kProc) {
+        w[t] = race_w_m<TIn, kResidual>(bits_at(sp, x), kResidual ? bits_at(sq, x) : 0u, mark_at(pr, x), ps, qs, rp,
+                                        rq, pr.theta);
+      } else {
+        w[t] = race_w<TIn, kResidual>(bits_at(sp, x), kResidual ? bits_at(sq, x) : 0u, ps, qs, rp, rq);
+      }
     }
     race_quad_l<kTest>(w, x0 + 4 * q, Erow, rk, rs, bk, bx, flags);
   }
@@ -1579,10 +1677,12 @@ __device__ __forceinline__ void race_chunks(const TIn *sp, const TIn *sq, const 
 // plain loads only for a last partial 16-byte group; other rows use plain
 // loads.  With kRes false (aligned rows only) nothing is copied: the rows are
 // read where they lie, and their chunks are only prefetched into L2 here.
-// Returns kFlagTimeout if the copy did not complete in time.
+// Returns kFlagTimeout if the copy did not complete within `first_limit`
+// polls; the copies in flight then get one more wait of the ordinary limit
+// (a test sets first_limit to 0 to take this path while every copy lands).
 template <typename TIn, bool kVec, bool kRes = true>
 __device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *const srow[2], int nr, int n,
-                              uint32_t &phase) {
+                              uint32_t &phase, uint32_t first_limit) {
   const int tid = threadIdx.x;
   if (kVec && !kRes) {  // both chunks are read in place: warm L2 with them
     if (tid == 0) {
@@ -1608,9 +1708,9 @@ __device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *con
     for (int r = 0; r < nc; ++r)
       for (int x = nb + tid; x < n; x += kThreads) srow[r][x] = grow[r][x];
     __syncthreads();
-    if (!mbar_wait_bounded(&sm.bar, phase, kWaitLimit)) {
+    if (!mbar_wait_bounded(&sm.bar, phase, first_limit)) {
       flags = kFlagTimeout;
-      mbar_wait_bounded(&sm.bar, phase, kWaitLimit);  // give the copies in flight one more bound
+      mbar_wait_bounded(&sm.bar, phase, kCopyWaitPolls);  // give the copies in flight one more bound
     }
     phase ^= 1u;
   } else {
@@ -1622,48 +1722,178 @@ __device__ uint32_t load_rows(LogitsSmem &sm, const TIn *const grow[2], TIn *con
 }
 
 // ---------------------------------------------------------------------------
-// logits processors on the rows in shared memory ("Speculative Decoding:
-// propose, verify, accept", section 06: the same banned tokens and repetition
-// penalty on the target and draft rows of a position).  Two bitmaps over this
-// CTA's chunk mark banned and penalised keys; after every row copy the marked
-// entries are rewritten: banned -> -inf, penalised -> l / theta if l > 0 else
-// l * theta (fp32, rounded to the row's type; Keskar et al., CTRL, 2019).
+// the processors' correction of a position's statistics
 // ---------------------------------------------------------------------------
-template <typename TIn>
-__device__ __forceinline__ void store_processed(TIn *row, int x, bool banned, float theta) {
-  using E = Elem<TIn>;
-  const float v = E::val(bits_at(row, x));
-  const float f = banned ? -INFINITY : (v > 0.0f ? __fdiv_rn(v, theta) : __fmul_rn(v, theta));
-  if constexpr (sizeof(TIn) == 2) {
-    row[x] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-  } else {
-    row[x] = f;
-  }
+// One cluster exchange of a 16-byte word per CTA: threads 0 .. ncta-1 store
+// `v` into this CTA's slot of every peer's inbox (the slots of the parity of
+// `step`), one cluster barrier, then sm.xw[c] holds CTA c's word in every CTA.
+__device__ __forceinline__ void cluster_exchange(LogitsSmem &sm, Inbox *inbox, const uint4 &v, int &step,
+                                                 uint32_t ncta, uint32_t rank) {
+  Inbox *const ibx = inbox + (step & 1) * static_cast<int>(ncta);
+  if (threadIdx.x < ncta) st_dsmem_v4(map_to_rank(smem_addr(&ibx[rank]), threadIdx.x), v);
+  cluster_sync();
+  ++step;
+  if (threadIdx.x < ncta) sm.xw[threadIdx.x] = *reinterpret_cast<const uint4 *>(&ibx[threadIdx.x]);
+  __syncthreads();
 }
 
-template <typename TIn>
-__device__ __forceinline__ void apply_processors(TIn *const srow[2], int nr, int n, const uint32_t *pen,
-                                                 const uint32_t *ban, int words, float theta) {
-  for (int w = threadIdx.x; w < words; w += kThreads) {
-    uint32_t bits = pen[w] | ban[w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      const int x = 32 * w + b;
-      if (x >= n) break;
-      const bool banned = (ban[w] >> b) & 1u;
-      for (int r = 0; r < nr; ++r) store_processed(srow[r], x, banned, theta);
-    }
+// Fixed-tree block sums of two floats into sm.pz (valid after the barrier).
+__device__ __forceinline__ void block_sum_pz(LogitsSmem &sm, const float v[2]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int r = 0; r < 2; ++r) {
+    float x = v[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    if (lane == 0) sm.wz[r][warp] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2) {
+    float x = 0.0f;
+    for (int w = 0; w < kWarps; ++w) x += sm.wz[threadIdx.x][w];
+    sm.pz[threadIdx.x] = x;
   }
   __syncthreads();
 }
 
-// Greedy with processors: thread-local argmax of a row chunk in shared memory.
+// Exact statistics of rows whose corrected normaliser cancelled (below half
+// of the raw one) or overflowed: the reference maximum becomes the largest
+// processed value among the kept, unbanned entries, and the normaliser is
+// summed afresh against it.  Two cluster exchanges; every CTA takes this path
+// alike (the condition is computed from cluster-wide totals).  Returns false
+// if a row keeps no unbanned entry (no distribution is left).
 template <typename TIn>
-__device__ __forceinline__ void argmax_smem(const TIn *row, int x0, int n, unsigned long long &best,
+__device__ bool proc_rescue(LogitsSmem &sm, Inbox *inbox, TIn *const rows[2], int nr, int n, const Procs &pr,
+                            RowStats st[2], const bool need[2], int &step, uint32_t ncta, uint32_t rank) {
+  using E = Elem<TIn>;
+  const int tid = threadIdx.x;
+  if (tid < 2) sm.xmax[tid] = 0u;
+  __syncthreads();
+  auto visit = [&](int r, auto f) {  // f(processed bits) over the kept, unbanned entries of row r
+    for_each_elem(rows[r], n, [&](uint32_t b, int x) {
+      if (E::key(b) < st[r].cut) return;
+      const uint32_t m = mark_at(pr, x);
+      if (m == 1u) return;
+      const uint32_t pb = processed_bits<TIn>(b, m, pr.theta);
+      if (E::finite(pb)) f(pb);  // (-inf adds nothing; NaN and +inf were rejected before)
+    });
+  };
+  for (int r = 0; r < nr; ++r) {
+    if (!need[r]) continue;
+    uint32_t mx = 0u;
+    visit(r, [&](uint32_t pb) { mx = max(mx, ordered_bits(E::val(pb))); });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if ((tid & 31) == 0 && mx) atomicMax(&sm.xmax[r], mx);
+  }
+  __syncthreads();
+  cluster_exchange(sm, inbox, make_uint4(sm.xmax[0], sm.xmax[1], 0u, 0u), step, ncta, rank);
+  float ref[2] = {0.0f, 0.0f};
+  for (int r = 0; r < nr; ++r) {
+    if (!need[r]) continue;
+    uint32_t mx = 0u;
+    for (int c = 0; c < static_cast<int>(ncta); ++c) mx = max(mx, r ? sm.xw[c].y : sm.xw[c].x);
+    if (mx == 0u) return false;
+    const uint32_t b = (mx & 0x80000000u) ? (mx & 0x7FFFFFFFu) : ~mx;  // inverse of ordered_bits
+    ref[r] = __uint_as_float(b);
+  }
+  float z[2] = {0.0f, 0.0f};
+  for (int r = 0; r < nr; ++r) {
+    if (!need[r]) continue;
+    float comp = 0.0f;
+    visit(r, [&](uint32_t pb) {  // compensated sum against the new reference
+      const float y = exp2f(__fmul_rn(__fsub_rn(E::val(pb), ref[r]), st[r].c2)) - comp;
+      const float t = z[r] + y;
+      comp = (t - z[r]) - y;
+      z[r] = t;
+    });
+  }
+  block_sum_pz(sm, z);
+  cluster_exchange(sm, inbox, make_uint4(__float_as_uint(sm.pz[0]), __float_as_uint(sm.pz[1]), 0u, 0u), step, ncta,
+                   rank);
+  for (int r = 0; r < nr; ++r) {
+    if (!need[r]) continue;
+    float t = 0.0f;
+    for (int c = 0; c < static_cast<int>(ncta); ++c) t += __uint_as_float(r ? sm.xw[c].y : sm.xw[c].x);
+    st[r].vmax = ref[r];
+    st[r].zp = t;
+  }
+  return true;
+}
+
+// After the raw statistics of a position: every marked entry of this CTA's
+// chunk that the kept set holds trades its raw weight for its processed one
+// (0 when banned), for the normaliser of each row.  Fixed summation order
+// (bitmap words by thread, bits ascending, a fixed block tree, then ranks in
+// order), so every CTA of the cluster gets the same totals.  The CTA holding
+// the draft token (y_local >= 0) publishes its marks in the same exchange.
+// Sets SV_DATA_BAD_VALUES and returns false if a kept processed value is NaN
+// or +inf or no unbanned entry is kept.
+template <typename TIn>
+__device__ bool proc_correct(LogitsSmem &sm, Inbox *inbox, TIn *const rows[2], int nr, int n, int words,
+                             const Procs &pr, RowStats st[2], int y_local, uint32_t &ymark, uint32_t *req_bits,
+                             int &step, uint32_t ncta, uint32_t rank) {
+  using E = Elem<TIn>;
+  const int tid = threadIdx.x;
+  float d[2] = {0.0f, 0.0f};
+  uint32_t bad = 0u;
+  for (int w = tid; w < words; w += kThreads) {
+    uint32_t bits = pr.pen[w] | pr.ban[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int xl = 32 * w + b;
+      if (xl >= n) break;
+      const uint32_t m = ((pr.ban[w] >> b) & 1u) ? 1u : 2u;
+      for (int r = 0; r < nr; ++r) {
+        const uint32_t rb = bits_at(rows[r], xl);
+        if (E::key(rb) < st[r].cut) continue;  // outside the kept set: the processors cannot bring it in
+        const uint32_t pb = processed_bits<TIn>(rb, m, pr.theta);
+        if (E::is_nan(pb) || E::is_pinf(pb)) bad = 1u;
+        d[r] += kept_weight<TIn>(pb, st[r]) - kept_weight<TIn>(rb, st[r]);
+      }
+    }
+  }
+  bad = __syncthreads_or(bad) ? 1u : 0u;
+  if (tid == 0) sm.pmark = y_local >= 0 ? 0x100u | mark_at(pr, y_local) : 0u;
+  block_sum_pz(sm, d);
+  cluster_exchange(sm, inbox, make_uint4(__float_as_uint(sm.pz[0]), __float_as_uint(sm.pz[1]), sm.pmark, bad), step,
+                   ncta, rank);
+  float z[2] = {st[0].zp, st[1].zp};
+  uint32_t ym = 0u, fb = 0u;
+  for (int c = 0; c < static_cast<int>(ncta); ++c) {
+    z[0] += __uint_as_float(sm.xw[c].x);
+    z[1] += __uint_as_float(sm.xw[c].y);
+    ym |= sm.xw[c].z;
+    fb |= sm.xw[c].w;
+  }
+  ymark = ym & 3u;
+  if (fb) {
+    *req_bits |= SV_DATA_BAD_VALUES;
+    return false;
+  }
+  bool need[2] = {false, false}, any = false;
+  for (int r = 0; r < nr; ++r) {
+    need[r] = !(z[r] >= 0.5f * st[r].zp && z[r] < INFINITY);
+    if (!need[r]) st[r].zp = z[r];
+    any |= need[r];
+  }
+  if (any && !proc_rescue<TIn>(sm, inbox, rows, nr, n, pr, st, need, step, ncta, rank)) {
+    *req_bits |= SV_DATA_BAD_VALUES;
+    return false;
+  }
+  return true;
+}
+
+// Greedy with processors: thread-local argmax of a row chunk (in shared memory
+// or read in place), every marked entry taking its processed value (-inf when
+// banned; a banned NaN is no longer a NaN).
+template <typename TIn>
+__device__ __forceinline__ void argmax_proc(const TIn *row, int x0, int n, const Procs &pr, unsigned long long &best,
                                             uint32_t &flags) {
   using E = Elem<TIn>;
   for_each_elem(row, n, [&](uint32_t b, int x) {
+    const uint32_t m = mark_at(pr, x);
+    if (m) b = processed_bits<TIn>(b, m, pr.theta);
     if (E::is_nan(b)) {
       flags |= SV_DATA_BAD_VALUES;
       return;
@@ -1716,8 +1946,8 @@ __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsig
 // kRes: both row chunks of a position live in shared memory (two CTAs per
 // SM).  Otherwise (aligned rows) both chunks are read where they lie after a
 // bulk L2 prefetch: a CTA then holds only its statistics and inbox in shared
-// memory, and four share an SM.  Calls with logits processors, which rewrite
-// both rows, always take the resident form.
+// memory, and four share an SM.  Logits processors work in either form (the
+// rows are never rewritten).
 template <typename TIn, bool kTest, bool kVec, bool kRes>
 __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const VerifyParams P, int chunk) {
   static_assert(kRes || kVec, "rows read in place must be 16-byte aligned");
@@ -1759,7 +1989,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
   const int g = valid ? static_cast<int>(e - s) : 0;
   const int64_t tb = s + i;
   const float temp = P.temperature ? P.temperature[i] : 1.0f;
-  if (valid && (!(temp >= 0.0f) || isinf(temp))) {
+  if (valid && !temperature_ok(temp)) {
     req_bits |= SV_DATA_BAD_PARAM;
     valid = false;
   }
@@ -1778,7 +2008,8 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
       valid = false;
     }
   }
-  const bool procs = kRes && (P.rep_penalty != nullptr || P.ban_cu != nullptr);
+  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
+  const Procs pr{pen_bits, ban_bits, theta};
   const bool greedy = valid && temp == 0.0f;
   int A = 0;
   int32_t last_tok = -1;
@@ -1824,12 +2055,17 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
     for (int j = 0;; ++j) {
       unsigned long long best = 0;
       uint32_t fl = 0;
-      if (procs) {  // the row goes through shared memory to be processed
+      if (procs) {  // the argmax of the processed row
         add_drafts(j);
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nullptr};
-        if (load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase) & kFlagTimeout) fl |= SV_DATA_COPY_TIMEOUT;
-        apply_processors(srow, 1, n, pen_bits, ban_bits, words, theta);
-        argmax_smem(srow[0], x0, n, best, fl);
+        const TIn *row = grow[0];
+        if (kRes) {
+          if (load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase, P.first_wait) & kFlagTimeout)
+            fl |= SV_DATA_COPY_TIMEOUT;
+          row = srow[0];
+        }
+        __syncthreads();  // the drafts' marks
+        argmax_proc<TIn>(row, x0, n, pr, best, fl);
       } else {
         argmax_logits<TIn, kVec>(tgt + (tb + j) * ts + x0, x0, n, best, fl);
       }
@@ -1917,27 +2153,23 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
         }
         const TIn *grow[2] = {tgt + (tb + j) * ts + x0, nr == 2 ? drf + (s + j) * ds + x0 : nullptr};
         if (procs) add_drafts(j);
-        const uint32_t lf = load_rows<TIn, kVec, kRes>(sm, grow, srow, nr, n, phase);
+        const uint32_t lf = load_rows<TIn, kVec, kRes>(sm, grow, srow, nr, n, phase, P.first_wait);
         // this position's rows: in shared memory, or where they lie
         TIn *const rows[2] = {kRes ? srow[0] : const_cast<TIn *>(grow[0]), kRes ? srow[1] : const_cast<TIn *>(grow[1])};
         join();
-        int y_owner = -1;
-        uint32_t yb0 = 0u, yb1 = 0u;
-        if (procs) {
-          apply_processors(rows, nr, n, pen_bits, ban_bits, words, theta);
-          if (j < g && y >= 0 && y < V) {  // the CTA holding y publishes its processed logits
-            y_owner = y / chunk;
-            if (static_cast<int>(rank) == y_owner) {
-              yb0 = bits_at(rows[0], y - x0);
-              yb1 = bits_at(rows[1], y - x0);
-            }
-          }
-        }
-        if (!position_stats<TIn>(sm, inbox, rows, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta, rank, yb0,
-                                 yb1, y_owner)) {
-          req_bits |= SV_DATA_BAD_VALUES;
+        if (!position_stats<TIn>(sm, inbox, rows, nr, n, c2, topk, topp, lf, st, &req_bits, step, ncta, rank)) {
           valid = false;
           break;
+        }
+        // the processors on the kept sets: corrected normalisers, the draft token's marks
+        uint32_t ymark = 0u;
+        if (procs) {
+          const int y_local = (j < g && y >= x0 && y < x0 + n) ? y - x0 : -1;
+          if (!proc_correct<TIn>(sm, inbox, rows, nr, n, words, pr, st, y_local, ymark, &req_bits, step, ncta,
+                                 rank)) {
+            valid = false;
+            break;
+          }
         }
         float bk = 0.0f;
         int bx = -1;
@@ -1949,12 +2181,8 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
             valid = false;
             break;
           }
-          if (procs) {
-            bty = sm.yproc[0];
-            bdy = sm.yproc[1];
-          }
-          const float py = prob_of<TIn>(bty, st[0]);
-          const float qy = prob_of<TIn>(bdy, st[1]);
+          const float py = prob_of_m<TIn>(bty, ymark, st[0], theta);
+          const float qy = prob_of_m<TIn>(bdy, ymark, st[1], theta);
           if (rank == 0 && tid == 0 && !P.rates) {
             if (P.dbg_py) P.dbg_py[s + j] = py;
             if (P.dbg_qy) P.dbg_qy[s + j] = qy;
@@ -1964,7 +2192,12 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
             continue;  // accepted: next position
           }
           residual = true;
-          race_chunks<TIn, kTest, true>(rows[0], rows[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl);
+          if (procs)
+            race_chunks<TIn, kTest, true, true>(rows[0], rows[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl, pr);
+          else
+            race_chunks<TIn, kTest, true>(rows[0], rows[1], st[0], st[1], x0, n, Erow, rk, rs, bk, bx, fl);
+        } else if (procs) {
+          race_chunks<TIn, kTest, false, true>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl, pr);
         } else {
           race_chunks<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
         }
@@ -1973,7 +2206,10 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
           bk = 0.0f;
           bx = -1;
           fl = 0;
-          race_chunks<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
+          if (procs)
+            race_chunks<TIn, kTest, false, true>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl, pr);
+          else
+            race_chunks<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], x0, n, Erow, rk, rs, bk, bx, fl);
           const KeyFlags r2 = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
           r.key = r2.key;
           r.flags |= r2.flags;
@@ -2030,9 +2266,8 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
   int32_t token = -1;
   int step = 0;
   uint32_t phase = 0;
-  // processor bitmaps (present only when the call has processors, which
-  // always take the form with the row in shared memory)
-  const bool procs = kRes && (P.rep_penalty != nullptr || P.ban_cu != nullptr);
+  // processor bitmaps (present only when the call has processors)
+  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
   const int words = (chunk + 31) / 32;
   uint32_t *const pen_bits = reinterpret_cast<uint32_t *>(inbox + 2 * ncta);
   uint32_t *const ban_bits = pen_bits + words;
@@ -2044,7 +2279,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
   cluster_sync();  // every CTA of the cluster runs before any store into a peer
   const float temp = P.temperature ? P.temperature[r] : 1.0f;
   bool ok = true;
-  if (!(temp >= 0.0f) || isinf(temp)) {
+  if (!temperature_ok(temp)) {
     bits |= SV_DATA_BAD_PARAM;
     ok = false;
   }
@@ -2074,16 +2309,21 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
       for (int64_t k = pen_b + tid; k < pen_e; k += kThreads) mark(pen_bits, P.pen_ids[k]);
     __syncthreads();
   }
+  const Procs pr{pen_bits, ban_bits, theta};
   if (!ok) {
     // nothing sampled
   } else if (temp == 0.0f) {
     unsigned long long best = 0;
     uint32_t fl = 0;
-    if (procs) {  // the row goes through shared memory to be processed
+    if (procs) {  // the argmax of the processed row
       const TIn *grow[2] = {row + x0, nullptr};
-      if (load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase) & kFlagTimeout) fl |= SV_DATA_COPY_TIMEOUT;
-      apply_processors(srow, 1, n, pen_bits, ban_bits, words, theta);
-      argmax_smem(srow[0], x0, n, best, fl);
+      const TIn *src = grow[0];
+      if (kRes) {
+        if (load_rows<TIn, kVec>(sm, grow, srow, 1, n, phase, P.first_wait) & kFlagTimeout)
+          fl |= SV_DATA_COPY_TIMEOUT;
+        src = srow[0];
+      }
+      argmax_proc<TIn>(src, x0, n, pr, best, fl);
     } else {
       argmax_logits<TIn, kVec>(row + x0, x0, n, best, fl);
     }
@@ -2098,20 +2338,25 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
       bits |= SV_DATA_BAD_PARAM;
     } else {
       const TIn *grow[2] = {row + x0, nullptr};
-      const uint32_t lf = load_rows<TIn, kVec, kRes>(sm, grow, srow, 1, n, phase);
-      if (procs) apply_processors(srow, 1, n, pen_bits, ban_bits, words, theta);
+      const uint32_t lf = load_rows<TIn, kVec, kRes>(sm, grow, srow, 1, n, phase, P.first_wait);
       RowStats st[2];
+      uint32_t ymark = 0u;
       if (!position_stats<TIn>(sm, inbox, srow, 1, n, __fdiv_rn(kLog2e, temp), topk, topp, lf, st, &bits, step,
-                               ncta, rank)) {
-        bits |= SV_DATA_BAD_VALUES;
+                               ncta, rank) ||
+          (procs && !proc_correct<TIn>(sm, inbox, srow, 1, n, words, pr, st, -1, ymark, &bits, step, ncta, rank))) {
+        // nothing sampled (the status bit is set)
       } else {
         const RngKey rk{P.seed_lo, P.seed_hi ^ 0x53414D50u, P.off_lo, P.off_hi};  // the sampler's own streams
         const float *Erow = kTest ? P.exponentials + static_cast<int64_t>(r) * P.exp_stride : nullptr;
         float bk = 0.0f;
         int bx = -1;
         uint32_t fl = 0;
-        race_chunks<TIn, kTest, false>(srow[0], srow[0], st[0], st[0], x0, n, Erow, rk,
-                                     P.row_base + static_cast<uint32_t>(r), bk, bx, fl);
+        if (procs)
+          race_chunks<TIn, kTest, false, true>(srow[0], srow[0], st[0], st[0], x0, n, Erow, rk,
+                                               P.row_base + static_cast<uint32_t>(r), bk, bx, fl, pr);
+        else
+          race_chunks<TIn, kTest, false>(srow[0], srow[0], st[0], st[0], x0, n, Erow, rk,
+                                         P.row_base + static_cast<uint32_t>(r), bk, bx, fl);
         const KeyFlags kr = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, sm.red, step++, ncta);
         bits |= kr.flags;
         if (kr.key == 0ull) {
@@ -2137,12 +2382,21 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
                 o[2 * t] = prob_of<TIn>(w[t] & 0xFFFFu, st[0]);
                 o[2 * t + 1] = prob_of<TIn>(w[t] >> 16, st[0]);
               }
+              if (procs) {  // marked entries: their processed probabilities
+                uint32_t mk = group_marks<8>(pr, 8 * v);
+                while (mk) {
+                  const int t = __ffs(mk) - 1;
+                  mk &= mk - 1u;
+                  o[t] = prob_of_m<TIn>((w[t >> 1] >> (16 * (t & 1))) & 0xFFFFu, mark_at(pr, 8 * v + t), st[0], theta);
+                }
+              }
               p4[2 * v] = make_float4(o[0], o[1], o[2], o[3]);
               p4[2 * v + 1] = make_float4(o[4], o[5], o[6], o[7]);
             }
             xs = ng << 3;
           }
-          for (int x = xs + tid; x < n; x += kThreads) prow[x] = prob_of<TIn>(bits_at(srow[0], x), st[0]);
+          for (int x = xs + tid; x < n; x += kThreads)
+            prow[x] = prob_of_m<TIn>(bits_at(srow[0], x), procs ? mark_at(pr, x) : 0u, st[0], theta);
         }
       }
     }

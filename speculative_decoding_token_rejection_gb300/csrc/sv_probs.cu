@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 4) probs_kernel(const VerifyParams P
   const int g = valid ? static_cast<int>(e - s) : 0;
   const int64_t tb = s + i;  // first target row of request i
   const float temp = P.temperature ? P.temperature[i] : 1.0f;
-  if (valid && (!(temp >= 0.0f) || isinf(temp))) {
+  if (valid && !temperature_ok(temp)) {
     req_bits |= SV_DATA_BAD_PARAM;
     valid = false;
   }

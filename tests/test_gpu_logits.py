@@ -4,12 +4,19 @@ Greedy rows compare raw logits, so their outputs are exact.  Random rows go
 through temperature, top-k, softmax and top-p on both sides; the oracle does it
 in double and rounds to fp32, the kernel in fp32.  The contract: p(y) and q(y)
 agree within 1e-6 absolute; committed tokens, num_accepted and the KV rollback
-agree exactly except for requests where the oracle reports a decision within
-tolerance of flipping: a perturbation of p and q inside both 1e-6 absolute and
-1e-5 relative could change an examined acceptance test (|u*q - p| below both
-bounds) or swap the two leading race keys, or a top-p cumulative sum lies
-within 1e-6 of top_p.  This is narrower than exempting every |u*q - p| < 1e-6.
-Exempted requests are counted and must stay rare.
+agree exactly except where the oracle reports a decision within tolerance of
+flipping.  The exemptions are narrow and each one frees only what it can
+change:
+  * an acceptance test that a perturbation of p and q inside both 1e-6
+    absolute and 1e-5 relative could flip (|u*q - p| below both bounds): the
+    acceptance count, the tokens and the rollback of that request are free,
+    and p(y), q(y) are still compared on the positions both sides examined;
+  * a race whose two leading keys such a perturbation could swap: only the
+    drawn token (the last committed one) is free; the acceptance count, the
+    accepted tokens, the rollback and every p(y), q(y) must match;
+  * a top-p cut whose value-group sum lies within 1e-6 of top_p (the kept set
+    itself may differ): the request's outputs are free.
+Exempted requests are counted, printed, and never more than 5% of a batch.
 """
 import numpy as np
 import pytest
@@ -38,39 +45,57 @@ def H():
     return gpu_harness
 
 
-def exempt_mask(o, production=False):
+def exempt_classes(o, production=False):
+    """Per request: (acceptance within the band, race within the band, top-p
+    edge), from the oracle's diagnostics."""
     d = o["diag"]
-    m = (d[:, oracle.DIAG_ACCEPT_MARGIN] < 1) | (d[:, oracle.DIAG_RACE_FLIP] < 1) | \
-        (d[:, oracle.DIAG_TOPP_EDGE] > 0)
-    if production:
-        m |= d[:, oracle.DIAG_RACE_RELGAP] < TOL
-    return m
+    accept = d[:, oracle.DIAG_ACCEPT_MARGIN] < 1
+    race = d[:, oracle.DIAG_RACE_FLIP] < 1
+    if production:  # production E can differ by an ulp of log: relative key gaps below 1e-6 too
+        race |= d[:, oracle.DIAG_RACE_RELGAP] < TOL
+    edge = d[:, oracle.DIAG_TOPP_EDGE] > 0
+    return accept, race, edge
 
 
-def compare_logits(g, o, w, production=False, max_exempt_frac=0.02):
-    ex = exempt_mask(o, production)
-    keep = ~ex
+def exempt_mask(o, production=False):
+    accept, race, edge = exempt_classes(o, production)
+    return accept | race | edge
+
+
+def compare_logits(g, o, w, production=False, max_exempt_frac=0.05):
+    assert max_exempt_frac <= 0.05
+    accept, race, edge = exempt_classes(o, production)
+    free = accept | edge  # the acceptance count itself may differ
+    ex = free | race
     gam = workloads.gammas_of(w)
-    np.testing.assert_array_equal(g["num_accepted"][keep], o["num_accepted"][keep])
-    np.testing.assert_array_equal(g["out_tokens"][keep], o["out_tokens"][keep])
+    A_g, A_o = g["num_accepted"], o["num_accepted"]
+    np.testing.assert_array_equal(A_g[~free], A_o[~free])
+    np.testing.assert_array_equal(g["out_tokens"][~ex], o["out_tokens"][~ex])
     assert g["status"] == o["status"]
     s = 0
     for i in range(w["N"]):
         gi = int(gam[i])
-        if keep[i]:
+        if not free[i]:
+            if race[i]:  # only the drawn token may differ
+                a = int(A_o[i])
+                np.testing.assert_array_equal(g["out_tokens"][i, :a], o["out_tokens"][i, :a])
+                np.testing.assert_array_equal(g["out_tokens"][i, a + 1:], o["out_tokens"][i, a + 1:])
             if o["num_computed_tokens"] is not None:
                 assert g["num_computed_tokens"][i] == o["num_computed_tokens"][i]
             if o["slot_mapping"] is not None:
                 np.testing.assert_array_equal(g["slot_mapping"][s + i:s + i + gi + 1],
                                               o["slot_mapping"][s + i:s + i + gi + 1])
-            og, gg = o["dbg_py"][s:s + gi], g["dbg_py"][s:s + gi]
-            np.testing.assert_array_equal(np.isnan(og), np.isnan(gg))
-            m = ~np.isnan(og)
-            assert np.all(np.abs(gg[m] - og[m]) <= TOL), (i, gg[m], og[m])
-            og, gg = o["dbg_qy"][s:s + gi], g["dbg_qy"][s:s + gi]
-            m = ~np.isnan(og)
-            assert np.all(np.abs(gg[m] - og[m]) <= TOL), (i, gg[m], og[m])
+        if not edge[i]:
+            for key in ("dbg_py", "dbg_qy"):
+                og, gg = o[key][s:s + gi], g[key][s:s + gi]
+                if not free[i]:  # the same positions were examined
+                    np.testing.assert_array_equal(np.isnan(og), np.isnan(gg))
+                m = ~np.isnan(og) & ~np.isnan(gg)  # positions both sides examined
+                assert np.all(np.abs(gg[m] - og[m]) <= TOL), (i, key, gg[m], og[m])
         s += gi
+    if ex.any():
+        print(f"exempt: {int(accept.sum())} acceptance, {int(race.sum())} race, {int(edge.sum())} top-p edge "
+              f"of {w['N']} requests")
     assert ex.mean() <= max_exempt_frac, f"{ex.sum()} of {w['N']} requests exempted"
     return int(ex.sum())
 
@@ -117,25 +142,14 @@ def test_random_logits_test_mode(name, kw):
     compare_logits(g, o, w)
 
 
-def test_fused_full_size_sampled():
-    """N=512, gamma=7, V=151936 bf16 logits: the GPU runs the whole batch, the
-    oracle checks the first 48 requests one by one."""
+def test_fused_full_size_test_mode():
+    """N=512, gamma=7, V=151936 bf16 logits in test mode (explicit u and E):
+    every request against the oracle (threaded over the host's cores)."""
     w = workloads.make("fused")
     g = H().run_gpu(w)
-    n = 48
-    o = oracle.verify(w, req_range=(0, n))
-    sub = lambda r: {k: (v[:n] if k in ("out_tokens", "num_accepted", "num_computed_tokens", "diag") and v is not None
-                         else v) for k, v in r.items()}
-    T = n * w["gamma"]
-    gs, os_ = sub(g), sub(o)
-    for r in (gs, os_):
-        r["dbg_py"], r["dbg_qy"] = r["dbg_py"][:T], r["dbg_qy"][:T]
-        r["slot_mapping"] = r["slot_mapping"][:T + n]
-    gs["status"] = os_["status"]  # status of the other requests is not computed by the oracle here
-    ws = dict(w, N=n)
-    compare_logits(gs, os_, ws, max_exempt_frac=0.05)
+    o = oracle.verify_parallel(w)
+    compare_logits(g, o, w)
     assert g["status"] == 0
-    # every request obeys the invariants
     A = g["num_accepted"]
     assert np.all((A >= 0) & (A <= w["gamma"]))
     assert np.all((g["out_tokens"] >= 0).sum(axis=1) == A + 1)
@@ -160,37 +174,41 @@ def test_in_place_chunks_beyond_register_groups(cluster, V, dtype):
                  draft=workloads.bf16_bits_to_f32(w["draft"]))
     o = oracle.verify(w)
     g = H().run_gpu(w, cluster_ctas=cluster)
-    compare_logits(g, o, w, max_exempt_frac=0.1)
+    compare_logits(g, o, w)
 
 
-@pytest.mark.parametrize("top_k,top_p,temp,budget", [
-    (1, 1.0, 1.0, 0.2), (5, 1.0, 0.5, 0.2), (0, 0.5, 1.0, 0.2), (7, 0.3, 0.9, 0.2), (4095, 0.95, 1.3, 0.2),
-    (20, 1e-4, 1.0, 0.2),
-    # a flattened row cut at 0.999: tail entries near the cut carry ~1e-6 each, so most cuts sit
-    # inside the 1e-6 band and are exempted; the rest must still match exactly
-    (0, 0.999, 2.0, 0.8)])
-def test_sampling_parameter_grid(top_k, top_p, temp, budget):
-    w = workloads.make("fused", N=10, V=4096, seed=31)
-    w["top_k"] = np.full(10, top_k, np.int32)
-    w["top_p"] = np.full(10, top_p, np.float32)
-    w["temperature"] = np.full(10, temp, np.float32)
-    compare_logits(H().run_gpu(w), oracle.verify(w), w, max_exempt_frac=budget)
+@pytest.mark.parametrize("top_k,top_p,temp,N", [
+    (1, 1.0, 1.0, 10), (5, 1.0, 0.5, 10), (0, 0.5, 1.0, 10), (7, 0.3, 0.9, 10), (4095, 0.95, 1.3, 10),
+    (20, 1e-4, 1.0, 10),
+    # a flattened row (T = 2) with a wide nucleus: 2 of the 40 cuts lie within 1e-6 of a value-group sum
+    (0, 0.95, 2.0, 40)])
+def test_sampling_parameter_grid(top_k, top_p, temp, N):
+    w = workloads.make("fused", N=N, V=4096, seed=31)
+    w["top_k"] = np.full(N, top_k, np.int32)
+    w["top_p"] = np.full(N, top_p, np.float32)
+    w["temperature"] = np.full(N, temp, np.float32)
+    compare_logits(H().run_gpu(w), oracle.verify(w), w)
 
 
 def test_top_k_ties_at_threshold():
-    V = 64
+    """Sixteen requests whose rows hold a ten-way tie at the top-k threshold
+    (top_k 4 keeps the maximum and all ten tied keys), drafts among the tied
+    ids; the oracle exempts none of them."""
+    V, N, G = 64, 16, 5
     rng = np.random.default_rng(2)
-    rows = []
-    for _ in range(6):
-        l = rng.standard_normal(V).astype(np.float32)
-        l[5:15] = 2.0  # ten-way tie
-        l[3] = 3.0
-        rows.append(l)
-    rows = np.array(rows, np.float32)
-    ids = [5, 9, 3, 14, 0]
-    w = hand_workload(rows, rows[:5] + np.float32(0.01), ids, entry="logits", u=rng.random(5),
-                      E=rng.exponential(size=(1, V)), top_k=[4], top_p=[1.0], temperature=[1.0])
-    compare_logits(H().run_gpu(w), oracle.verify(w), w, max_exempt_frac=1.0)
+    t, d, ids = [], [], []
+    for _ in range(N):
+        rows = rng.standard_normal((G + 1, V)).astype(np.float32)
+        rows[:, 5:15] = 2.0  # ten-way tie
+        rows[:, 3] = 3.0
+        t.append(rows)
+        d.append(rows[:G] + np.float32(0.01))
+        ids += list(rng.choice([5, 9, 3, 14, 0, 20], size=G))
+    w = hand_workload(np.concatenate(t), np.concatenate(d), ids, entry="logits", u=rng.random(N * G),
+                      E=rng.exponential(size=(N, V)), top_k=[4] * N, top_p=[1.0] * N, temperature=[1.0] * N)
+    o = oracle.verify(w)
+    assert compare_logits(H().run_gpu(w), o, w) == 0
+    assert len(set(o["num_accepted"].tolist())) > 2
 
 
 def test_logits_status_cases():
@@ -304,7 +322,7 @@ def test_top_k_threshold_bound_cases(shape, top_k):
     w["draft"] = bits[N * (G + 1):]
     w["top_k"] = np.full(N, top_k, np.int32)
     w["top_p"] = np.full(N, 0.95 if top_k > 8 else 1.0, np.float32)
-    compare_logits(H().run_gpu(w), oracle.verify(w), w, max_exempt_frac=0.5)
+    compare_logits(H().run_gpu(w), oracle.verify(w), w)
 
 
 @pytest.mark.parametrize("name,kw,production", [("fused", dict(N=40, V=151936), False),
@@ -333,32 +351,52 @@ def test_explicit_cluster_sizes(cluster, resident):
     w = workloads.make("fused", N=20, V=12008, seed=15)
     o = oracle.verify(w)
     g = H().run_gpu(w, cluster_ctas=cluster, flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0)
-    compare_logits(g, o, w, max_exempt_frac=0.1)
+    compare_logits(g, o, w)
 
 
-@pytest.mark.parametrize("top_k,top_p,temp,budget", [
-    (2000, 1.0, 0.8, 0.5),     # top-k threshold several windows below the maximum
-    (2000, 0.9, 0.8, 0.5),     # ... with a cut inside its window or above it (the multi-pass selection)
-    (600, 0.3, 1.0, 0.5),
-    (0, 0.9, 0.8, 0.5),        # top-p alone, cut below the first window
-    (0, 0.95, 0.8, 0.5),       # a wider nucleus: more windows
-    (0, 0.98, 0.6, 0.5),
-    # close to 1 on a flat row: each key near the cut carries < 1e-6 of mass, so
-    # every cut lies in the 1e-6 edge band; outputs are checked for validity
-    (0, 0.9999, 2.5, 1.0),
-    (5000, 0.97, 1.2, 0.5)])
-def test_thresholds_below_the_first_window(top_k, top_p, temp, budget):
+@pytest.mark.parametrize("top_k,top_p,temp,N", [
+    (2000, 1.0, 0.8, 12),      # top-k threshold several windows below the maximum
+    (2000, 0.9, 0.8, 12),      # ... with a cut inside its window or above it (the multi-pass selection)
+    (600, 0.3, 1.0, 12),
+    (0, 0.9, 0.8, 24),         # top-p alone, cut below the first window
+    (0, 0.95, 0.8, 12),        # a wider nucleus: more windows
+    (0, 0.98, 0.6, 12),
+    (5000, 0.97, 1.2, 12)])
+def test_thresholds_below_the_first_window(top_k, top_p, temp, N):
     """Rows whose threshold or cut lies below the first 128-key window, on a
     vocabulary large enough for several windows."""
-    w = workloads.make("fused", N=12, V=40000, seed=37)
-    w["top_k"] = np.full(12, top_k, np.int32)
-    w["top_p"] = np.full(12, top_p, np.float32)
-    w["temperature"] = np.full(12, temp, np.float32)
+    w = workloads.make("fused", N=N, V=40000, seed=37)
+    w["top_k"] = np.full(N, top_k, np.int32)
+    w["top_p"] = np.full(N, top_p, np.float32)
+    w["temperature"] = np.full(N, temp, np.float32)
     o = oracle.verify(w)
     g = H().run_gpu(w)
-    compare_logits(g, o, w, max_exempt_frac=budget)
+    compare_logits(g, o, w)
+    _valid_outputs(g, w)
+
+
+def _valid_outputs(g, w):
     A = g["num_accepted"]
     assert np.all((A >= 0) & (A <= w["gamma"]))
-    for i in range(12):
+    for i in range(w["N"]):
         assert np.all((g["out_tokens"][i, :A[i] + 1] >= 0) & (g["out_tokens"][i, :A[i] + 1] < w["V"]))
         assert np.all(g["out_tokens"][i, A[i] + 1:] == -1)
+
+
+def test_flat_rows_cut_near_one_are_valid():
+    """A nucleus of 0.9999 on flat rows (T = 2.5): every key near the cut
+    carries less than 1e-6 of mass, so every cut lies inside the tolerance band
+    and the kept set may legitimately differ from the oracle's.  Not a parity
+    case: the outputs must be valid (counts in range, committed tokens in the
+    vocabulary, -1 after them, accepted tokens equal to the drafts)."""
+    w = workloads.make("fused", N=12, V=40000, seed=37)
+    w["top_k"] = np.zeros(12, np.int32)
+    w["top_p"] = np.full(12, 0.9999, np.float32)
+    w["temperature"] = np.full(12, 2.5, np.float32)
+    g = H().run_gpu(w)
+    assert g["status"] == 0
+    _valid_outputs(g, w)
+    G = w["gamma"]
+    for i in range(12):
+        a = int(g["num_accepted"][i])
+        assert list(g["out_tokens"][i, :a]) == list(w["draft_ids"][i * G:i * G + a])

@@ -58,7 +58,7 @@ def test_random_logits_with_processors(dtype, theta):
                  draft=workloads.bf16_bits_to_f32(w["draft"]))
     add_lists(w, np.random.default_rng(4), theta=theta)
     o = oracle.verify(w)
-    compare(H().run_gpu(w), o, w, max_exempt_frac=0.1)
+    compare(H().run_gpu(w), o, w)
     assert (o["num_accepted"] < workloads.gammas_of(w)).any()
 
 
@@ -76,7 +76,7 @@ def test_ragged_production_with_processors():
     add_lists(w, np.random.default_rng(6), theta=1.8)
     o = oracle.verify(w, production=True, seed=3, offset=5)
     g = H().run_gpu(w, production=True, seed=3, offset=5)
-    compare(g, o, w, production=True, max_exempt_frac=0.1)
+    compare(g, o, w, production=True)
 
 
 @pytest.mark.parametrize("top_k,top_p,temp,V,cluster", [
@@ -87,17 +87,16 @@ def test_ragged_production_with_processors():
     (50, 0.9, 0.8, 40000, 1),      # one CTA per request over a 40000-key chunk
 ])
 def test_processors_statistics_paths(top_k, top_p, temp, V, cluster):
-    """Every statistics path with processors (rows copied into shared memory
-    and rewritten there) against the oracle: the fused setting at its
-    vocabulary, cuts in windows below the first, dense rows, a deep top-k
-    threshold, and one CTA per request over a 40000-key chunk."""
+    """Every statistics path with processors against the oracle: the fused
+    setting at its vocabulary, cuts in windows below the first, dense rows, a
+    deep top-k threshold, and one CTA per request over a 40000-key chunk."""
     w = workloads.make("fused", N=16, V=V, seed=23)
     w["top_k"] = np.full(16, top_k, np.int32)
     w["top_p"] = np.full(16, top_p, np.float32)
     w["temperature"] = np.full(16, temp, np.float32)
     add_lists(w, np.random.default_rng(9), theta=1.5, n_ctx=400, n_ban=20)
     o = oracle.verify(w)
-    compare(H().run_gpu(w, cluster_ctas=cluster), o, w, max_exempt_frac=0.5)
+    compare(H().run_gpu(w, cluster_ctas=cluster), o, w)
 
 
 @pytest.mark.parametrize("top_k,top_p", [(50, 0.9), (0, 0.9)])
@@ -110,7 +109,7 @@ def test_processed_keys_win_races_and_windows(top_k, top_p):
     w["top_p"] = np.full(24, top_p, np.float32)
     add_lists(w, np.random.default_rng(10), theta=0.5, n_ctx=2000, n_ban=40)
     o = oracle.verify(w)
-    compare(H().run_gpu(w), o, w, max_exempt_frac=0.3)
+    compare(H().run_gpu(w), o, w)
 
 
 def test_synthetic_mode_with_processors():
@@ -118,7 +117,7 @@ def test_synthetic_mode_with_processors():
     add_lists(w, np.random.default_rng(7))
     rates = np.array([0.9, 0.8, 0.8, 0.5, 0.4, 0.2, 0.1], np.float32)
     o = oracle.verify(w, synthetic_rates=rates)
-    compare(H().run_gpu(w, synthetic_rates=rates), o, w, max_exempt_frac=0.1)
+    compare(H().run_gpu(w, synthetic_rates=rates), o, w)
 
 
 def test_stop_tokens_probability_entry_exact():
@@ -165,3 +164,141 @@ def test_everything_banned_is_bad_values():
     o = oracle.verify(w)
     assert o["status"] == oracle.BAD_VALUES
     H().assert_same(H().run_gpu(w), o, check_dbg=False)
+
+
+# ----------------------------------------------------------------------------
+# the order: temperature, top-k, top-p on the raw rows, then the processors
+# ----------------------------------------------------------------------------
+def _golden_lists(g, c):
+    kw = {}
+    if f"{c}_banned" in g:
+        ids = np.array([int(x) for x in g[f"{c}_banned"]], np.int32)
+        kw["banned_cu"], kw["banned_ids"] = np.array([len(ids)], np.int64), ids
+    if f"{c}_theta" in g:
+        ids = np.array([int(x) for x in g[f"{c}_context"]], np.int32)
+        kw["repetition_penalty"] = np.array([float(g[f"{c}_theta"][0])], np.float32)
+        kw["penalty_cu"], kw["penalty_ids"] = np.array([len(ids)], np.int64), ids
+    return kw
+
+
+@pytest.mark.parametrize("resident", [False, True])
+def test_order_golden_cases(resident):
+    """The hand-worked cases that separate the pages' order from
+    processors-first, through the GPU: every transformed probability of each
+    case row (the draft id walks over the vocabulary), and the commit that
+    differs between the two orders, exactly as the oracle and the fixture."""
+    import speculative_decoding_token_rejection_gb300 as sv
+    from conftest import load_golden
+    g = load_golden("processors_order_examples.txt")
+    flags = sv.SV_FLAG_RESIDENT_ROWS if resident else 0
+    for c in ("t1", "t2", "t3", "t4", "t5"):
+        row = np.array([float(x) for x in g[f"{c}_row"]], np.float32)
+        V = row.shape[0]
+        N = V  # one request per draft id
+        t = np.concatenate([np.stack([row, np.zeros(V, np.float32)]) for _ in range(N)])
+        d = np.tile(row, (N, 1))
+        E = np.tile(np.arange(1, V + 1, dtype=np.float32), (N, 1))  # distinct keys: no race ties
+        w = hand_workload(t, d, list(range(V)), entry="logits", u=[0.5] * N, E=E,
+                          temperature=[float(g[f"{c}_temp"][0])] * N, top_k=[int(g[f"{c}_topk"][0])] * N,
+                          top_p=[float(g[f"{c}_topp"][0])] * N)
+        for k, v in _golden_lists(g, c).items():
+            if k.endswith("_cu"):
+                v = v[0] * np.arange(1, N + 1, dtype=np.int64)
+            elif k.endswith("_ids"):
+                v = np.tile(v, N)
+            else:
+                v = np.full(N, v[0], np.float32)
+            w[k] = v
+        o = oracle.verify(w)
+        r = H().run_gpu(w, flags=flags)
+        if f"{c}_status" in g:
+            assert o["status"] == r["status"] == int(g[f"{c}_status"][0]), c
+            assert np.all(r["out_tokens"] == -1) and np.all(r["num_accepted"] == 0), c
+            continue
+        compare(r, o, w)
+        expect = np.array([float(x) for x in g[f"{c}_expect"]], np.float32)
+        assert np.all(np.abs(r["dbg_py"] - expect) <= 1e-6) and np.all(np.abs(r["dbg_qy"] - expect) <= 1e-6), c
+    tg = np.array([[float(x) for x in r.split()] for r in " ".join(g["v1_target"]).split("|")], np.float32)
+    dr = np.array([[float(x) for x in g["v1_draft"]]], np.float32)
+    w = hand_workload(tg, dr, [int(x) for x in g["v1_drafts"]], entry="logits", u=[float(g["v1_u"][0])],
+                      E=np.ones((1, tg.shape[1])), temperature=[1.0], top_k=[int(g["v1_topk"][0])], top_p=[1.0])
+    w.update(_golden_lists(g, "v1"))
+    r = H().run_gpu(w, flags=flags)
+    assert r["status"] == 0 and r["num_accepted"][0] == int(g["v1_A"][0])
+    assert list(r["out_tokens"][0]) == [int(x) for x in g["v1_expect"]]
+    assert r["dbg_py"][0] == float(g["v1_py"][0]) and r["dbg_qy"][0] == float(g["v1_qy"][0])
+
+
+def _spiked(N, V, seed, top, gap_rest):
+    """bf16 logits rows N(0, 1) whose maximum is `top` at index 7 (every row),
+    with the rest `gap_rest` lower on average."""
+    rng = np.random.default_rng(seed)
+    G = 3
+    rows = (rng.standard_normal((N * (G + 1) + N * G, V)) + (top - gap_rest)).astype(np.float32)
+    rows[:, 7] = top
+    bits = workloads._to_bf16_bits(rows)
+    w = hand_workload(bits[:N * (G + 1)], bits[N * (G + 1):], rng.integers(0, V, size=N * G), entry="logits",
+                      dtype="bf16", u=rng.random(N * G), E=rng.exponential(size=(N, V)),
+                      temperature=np.full(N, 0.8, np.float32), top_k=np.full(N, 50, np.int32),
+                      top_p=np.full(N, 0.9, np.float32))
+    w["draft_ids"][::G] = 7  # position 0 drafts the spiked id
+    return w
+
+
+@pytest.mark.parametrize("resident", [False, True])
+def test_banned_maximum_far_above_the_rest(resident):
+    """The row maximum is banned and every other kept key lies ~40 nats below
+    it: the corrected normaliser cancels to nothing relative to the raw
+    maximum, so the kernel recomputes the kept set's statistics against its
+    largest unbanned value (the oracle renormalises in double)."""
+    import speculative_decoding_token_rejection_gb300 as sv
+    w = _spiked(24, 3000, 5, top=40.0, gap_rest=40.0 * 0.8 + 3)
+    w["top_p"] = np.ones(24, np.float32)  # top-k 50 alone: the kept set is the maximum and 49 keys far below
+    w["banned_cu"] = np.arange(1, 25, dtype=np.int64)
+    w["banned_ids"] = np.full(24, 7, np.int32)
+    o = oracle.verify(w)
+    assert o["status"] == 0 and np.all(o["dbg_py"][::3] == 0)  # y = 7 is banned at position 0
+    compare(H().run_gpu(w, flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0), o, w)
+
+
+def test_penalty_raising_past_the_fp32_range():
+    """theta 1e-3 raises the maximum (l / theta, l > 0) so far that its weight
+    relative to the raw maximum overflows fp32: the kernel recomputes the
+    statistics against the processed maximum.  theta 2e-38 overflows the
+    processed logit itself to +inf: no distribution, the bad-values status."""
+    for theta, status in ((1e-3, 0), (2e-38, oracle.BAD_VALUES)):
+        w = _spiked(16, 3000, 6, top=10.0, gap_rest=4.0)
+        w["repetition_penalty"] = np.full(16, theta, np.float32)
+        w["penalty_cu"] = np.arange(1, 17, dtype=np.int64)
+        w["penalty_ids"] = np.full(16, 7, np.int32)
+        o = oracle.verify(w)
+        assert o["status"] == status
+        r = H().run_gpu(w)
+        if status:
+            H().assert_same(r, o, check_dbg=False)
+        else:
+            compare(r, o, w)
+
+
+def test_banned_nucleus_is_bad_values():
+    """top_p small enough that each row's nucleus is its maximum alone, and
+    the maximum banned: no distribution is left (oracle: bad values)."""
+    w = _spiked(16, 3000, 7, top=12.0, gap_rest=10.0)
+    w["top_k"] = np.zeros(16, np.int32)
+    w["top_p"] = np.full(16, 0.5, np.float32)
+    w["banned_cu"] = np.arange(1, 17, dtype=np.int64)
+    w["banned_ids"] = np.full(16, 7, np.int32)
+    o = oracle.verify(w)
+    assert o["status"] == oracle.BAD_VALUES and np.all(o["num_accepted"] == 0)
+    H().assert_same(H().run_gpu(w), o, check_dbg=False)
+
+
+@pytest.mark.parametrize("resident", [False, True])
+def test_processors_in_both_forms(resident):
+    """The fused setting with the bench's kind of lists, rows read in place
+    (the default) or copied into shared memory: both against the oracle."""
+    import speculative_decoding_token_rejection_gb300 as sv
+    w = workloads.make("fused", N=32, V=30000, seed=41)
+    add_lists(w, np.random.default_rng(12), theta=1.2, n_ctx=512, n_ban=16)
+    o = oracle.verify(w)
+    compare(H().run_gpu(w, flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0), o, w)

@@ -26,7 +26,7 @@ def _gpu():
     oracle.build()
 
 
-def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=False, cluster=0, flags=0):
+def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=False, cluster=0, flags=0, test_flags=0):
     import torch
     import gpu_harness
     import speculative_decoding_token_rejection_gb300 as sv
@@ -43,13 +43,14 @@ def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=Fals
     sv.spec_verify_sample(gpu_harness.verifier(cluster, flags).handle, logits=logits, tokens=tokens, probs=probs,
                           temperature=t(temp, torch.float32), top_k=t(k, torch.int32), top_p=t(p, torch.float32),
                           exponentials=t(E, torch.float32), seed=seed, offset=offset, rng_row_base=base,
-                          status=status)
+                          status=status, test_flags=test_flags)
     torch.cuda.synchronize()
     return tokens.cpu().numpy(), probs.cpu().numpy(), int(status.item())
 
 
-def check(rows, temp, k, p, E=None, production=False, bf16=False, budget=0.02, seed=0, offset=0, base=0, cluster=0,
+def check(rows, temp, k, p, E=None, production=False, bf16=False, budget=0.05, seed=0, offset=0, base=0, cluster=0,
           flags=0):
+    assert budget <= 0.05
     o = oracle.sample_rows(rows, temperature=temp, top_k=k, top_p=p, exponentials=E, seed=seed, offset=offset,
                            rng_row_base=base)
     tok, pr, st = run_sampler(rows, temp, k, p, E, bf16=bf16, seed=seed, offset=offset, base=base, cluster=cluster,
@@ -83,7 +84,7 @@ def test_sampler_forms_and_cluster_sizes(cluster, resident):
     E = np.random.default_rng(2).standard_exponential((R, V), dtype=np.float32)
     temp = np.where(np.arange(R) % 6 == 5, 0.0, 0.8).astype(np.float32)
     check(rows, temp, np.full(R, 50), np.full(R, 0.9, np.float32), E, bf16=True, cluster=cluster,
-          flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0, budget=0.1)
+          flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0)
 
 
 @pytest.mark.parametrize("V", [151936, 5000, 4097])
@@ -110,7 +111,7 @@ def test_sampler_greedy_rows_and_status():
     rows[4, 17] = np.nan
     temp = np.array([0, 1, 0, 0.5, 1, -2], np.float32)
     E = rng.standard_exponential((6, 300), dtype=np.float32)
-    tok = check(rows, temp, np.zeros(6), np.ones(6, np.float32), E, budget=1.0)
+    tok = check(rows, temp, np.zeros(6), np.ones(6, np.float32), E)
     assert tok[4] == -1 and tok[5] == -1
 
 
@@ -146,12 +147,14 @@ def _proc_lists(R, V, rng):
     return out
 
 
+@pytest.mark.parametrize("resident", [False, True])
 @pytest.mark.parametrize("bf16", [True, False])
 @pytest.mark.parametrize("temp", [0.0, 0.8])
-def test_sampler_with_processors(bf16, temp):
-    """Banned tokens and the repetition penalty per row, against the oracle:
-    tokens exact (outside the tolerance band of the race) and the written q
-    rows within 1e-6."""
+def test_sampler_with_processors(bf16, temp, resident):
+    """Banned tokens and the repetition penalty per row, against the oracle,
+    with the rows read in place or copied into shared memory: tokens exact
+    (outside the tolerance band of the race) and the written q rows within
+    1e-6."""
     import torch
     import speculative_decoding_token_rejection_gb300 as sv
     rng = np.random.default_rng(int(bf16) + 2)
@@ -172,7 +175,7 @@ def test_sampler_with_processors(bf16, temp):
     tok = torch.full((R,), -7, dtype=torch.int32, device=dev)
     probs = torch.zeros((R, V), dtype=torch.float32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    h = sv.spec_verify_create(R, 1, V, device=0)
+    h = sv.spec_verify_create(R, 1, V, device=0, flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0)
     try:
         T = lambda x, dt: torch.as_tensor(x).to(dev)
         sv.spec_verify_sample(h, logits=t, tokens=tok, probs=probs, exponentials=torch.from_numpy(E).to(dev),
@@ -186,9 +189,9 @@ def test_sampler_with_processors(bf16, temp):
         sv.spec_verify_destroy(h)
     assert int(st.item()) == o["status"]
     g = tok.cpu().numpy()
-    exempt = o["diag"][:, 0] < 1
+    exempt = (o["diag"][:, 0] < 1) | (o["diag"][:, 1] > 0)
     np.testing.assert_array_equal(g[~exempt], o["tokens"][~exempt])
-    assert exempt.mean() <= 0.1
+    assert exempt.mean() <= 0.05
     if temp > 0:
         d = np.abs(probs.cpu().numpy() - o["probs"])
         assert d.max() <= 1e-6

@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_description(lib):
-    assert lib.spec_verify_abi_version() == 5
+    assert lib.spec_verify_abi_version() == 6
     assert lib.spec_verify_sizeof_args() == ctypes.sizeof(sv.SpecVerifyArgs)
     assert lib.spec_verify_sizeof_config() == ctypes.sizeof(sv.SpecVerifyConfig)
 
@@ -199,7 +199,9 @@ def _sample_args(R=4, V=1000):
     (lambda a: setattr(a, "tokens", None), sv.SV_ERR_INVALID_ARG),
     (lambda a: (setattr(a, "probs", FAKE), setattr(a, "probs_row_stride", 10)), sv.SV_ERR_INVALID_ARG),
     (lambda a: (setattr(a, "exponentials", FAKE), setattr(a, "exponentials_row_stride", 1000)), sv.SV_OK),
-    (lambda a: setattr(a, "reserved1", 3), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "test_flags", 3), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "test_flags", 1), sv.SV_OK),
+    (lambda a: setattr(a, "reserved0", 2), sv.SV_ERR_INVALID_ARG),
     (lambda a: (setattr(a, "num_rows", 0), setattr(a, "logits", None)), sv.SV_OK),
 ])
 def test_check_sample_args(lib, mutate, code):

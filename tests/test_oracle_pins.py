@@ -558,3 +558,23 @@ def test_synthetic_rates_must_be_non_increasing(oracle_mod):
     assert r["status"] == oracle_mod.BAD_PARAM and np.all(r["out_tokens"] == -1)
     r = oracle_mod.verify(w, synthetic_rates=np.array([1.0, 1.0, 1.0, 1.0], np.float32))
     assert np.all(r["num_accepted"] == 4)  # u < 1 always: every draft kept, bonus drawn
+
+
+def test_threaded_oracle_is_the_oracle(oracle_mod):
+    """The threaded helpers that the full-size GPU tests use give exactly the
+    single-threaded oracle's results (every output, ragged batch, production
+    draws; sampler rows with their streams)."""
+    import workloads
+    w = workloads.make("ragged", N=40, V=3000, test_mode=False)
+    a = oracle_mod.verify(w, production=True, seed=3, offset=2)
+    b = oracle_mod.verify_parallel(w, production=True, seed=3, offset=2, threads=7)
+    assert a["status"] == b["status"]
+    for k in ("out_tokens", "num_accepted", "num_computed_tokens", "slot_mapping", "dbg_py", "dbg_qy", "diag"):
+        np.testing.assert_array_equal(np.nan_to_num(a[k], nan=-9), np.nan_to_num(b[k], nan=-9), err_msg=k)
+    rows = w["draft"][:30]
+    kw = dict(temperature=np.full(30, 0.9, np.float32), top_k=np.full(30, 20), seed=4, offset=1, rng_row_base=3)
+    x = oracle_mod.sample_rows(rows, **kw)
+    y = oracle_mod.sample_rows_parallel(rows, threads=4, **kw)
+    np.testing.assert_array_equal(x["tokens"], y["tokens"])
+    np.testing.assert_array_equal(x["probs"], y["probs"])
+    np.testing.assert_array_equal(x["diag"], y["diag"])

@@ -66,18 +66,19 @@ def test_race_flip_and_relgap_values():
 
 
 def test_top_p_edge_flags():
-    row = np.zeros(2, np.float32)
-    for tp, flag in zip(_f("edge_topp"), _g()["edge_flag"]):
-        tp32 = np.float32(tp)
-        assert float(tp32) == tp  # each listed top_p is an fp32 value
-        _, edge, rc = oracle.logits_to_probs(row, 1.0, 0, float(tp32))
-        assert rc == 0 and edge == int(flag), tp
-        # the same flag through the verifier's diagnostics (logits entry)
-        t = np.zeros((2, 2), np.float32)
-        w = hand_workload(t, np.zeros((1, 2), np.float32), [0], entry="logits", u=[0.25], E=np.ones((1, 2)),
-                          temperature=[1.0], top_p=[float(tp32)])
-        o = oracle.verify(w)
-        assert o["diag"][0, oracle.DIAG_TOPP_EDGE] == int(flag), tp
+    for rk, tk, fk in (("edge_row", "edge_topp", "edge_flag"), ("tie_row", "tie_topp", "tie_flag")):
+        row = np.array(_f(rk), np.float32)
+        V = row.shape[0]
+        for tp, flag in zip(_f(tk), _g()[fk]):
+            tp32 = float(np.float32(tp))
+            _, edge, rc = oracle.logits_to_probs(row, 1.0, 0, tp32)
+            assert rc == 0 and edge == int(flag), (rk, tp)
+            # the same flag through the verifier's diagnostics (logits entry)
+            t = np.stack([row, np.zeros(V, np.float32)])
+            w = hand_workload(t, row[None, :], [0], entry="logits", u=[0.25], E=np.ones((1, V)), temperature=[1.0],
+                              top_p=[tp32])
+            o = oracle.verify(w)
+            assert o["diag"][0, oracle.DIAG_TOPP_EDGE] == int(flag), (rk, tp)
 
 
 def test_sampler_race_flip_value():
@@ -104,11 +105,13 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
         "race flip drops q from the relative scale": (
             "double m1 = (double)pa[win] + (qa ? (double)qa[win] : 0.0);", "double m1 = (double)pa[win];"),
         "relgap not relative": ("double r = k1 > 0 ? d / k1 : 0.0;", "double r = k1 > 0 ? d : 0.0;"),
-        "top-p edge band 1e-5": ("if (edge && (fabs(cum - (double)top_p) < 1e-6 ||",
-                                 "if (edge && (fabs(cum - (double)top_p) < 1e-5 ||"),
-        "top-p edge ignores the sum before the cut": (
-            "fabs(cum - (double)top_p) < 1e-6 || fabs(prev - (double)top_p) < 1e-6 || !found",
-            "fabs(cum - (double)top_p) < 1e-6 || !found"),
+        "top-p edge band 1e-5": ("fabs(above - (double)top_p) < 1e-6 || fabs(through - (double)top_p) < 1e-6",
+                                 "fabs(above - (double)top_p) < 1e-5 || fabs(through - (double)top_p) < 1e-5"),
+        "top-p edge ignores the sum above the cut": (
+            "fabs(above - (double)top_p) < 1e-6 || fabs(through - (double)top_p) < 1e-6",
+            "fabs(through - (double)top_p) < 1e-6"),
+        "top-p edge on single entries, not value groups": ("if (kept[r] > cut) above += e;",
+                                                          "if (kept[r] > cut || (r == 0 && kept[1] >= cut)) above += e;"),
         "sampler flip drops the runner-up's draw": ("double f = flip_index(d / (1.0 / e1 + 1.0 / (double)E[x]),",
                                                     "double f = flip_index(d / (1.0 / e1),"),
     }
