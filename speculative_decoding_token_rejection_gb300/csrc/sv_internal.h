@@ -109,20 +109,21 @@ int logits_reg_group_chunk();  // largest bf16 chunk whose group maxima stay in 
 // double-buffered inboxes of the one-barrier row-statistics reduction.
 size_t logits_inbox_bytes(int cluster);
 cudaError_t enable_sample_kernels(int max_cluster, int max_dyn);
-// per kernel and element type (sv_logits_{bf16,f32}.cu, sv_sample_{bf16,f32}.cu); dyn = dynamic shared
-// memory per CTA
-cudaError_t enable_logits_kernels_bf16(int max_cluster, int max_dyn);
-cudaError_t enable_logits_kernels_f32(int max_cluster, int max_dyn);
-cudaError_t enable_sample_kernels_bf16(int max_cluster, int max_dyn);
-cudaError_t enable_sample_kernels_f32(int max_cluster, int max_dyn);
-cudaError_t launch_logits_bf16(const VerifyParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
-                               cudaStream_t stream);
-cudaError_t launch_logits_f32(const VerifyParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
-                              cudaStream_t stream);
-cudaError_t launch_sample_bf16(const SampleParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
-                               cudaStream_t stream);
-cudaError_t launch_sample_f32(const SampleParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
-                              cudaStream_t stream);
+// per kernel, element type and processor setting (sv_logits_{bf16,f32}[_proc].cu,
+// sv_sample_{bf16,f32}[_proc].cu); dyn = dynamic shared memory per CTA
+#define SV_KERNEL_SET(kind, P, suffix)                                                                          \
+  cudaError_t enable_##kind##_kernels_##suffix(int max_cluster, int max_dyn);                                  \
+  cudaError_t launch_##kind##_##suffix(const P &p, int cluster, int chunk, size_t dyn, bool vec, bool resident, \
+                                       cudaStream_t stream);
+SV_KERNEL_SET(logits, VerifyParams, bf16)
+SV_KERNEL_SET(logits, VerifyParams, f32)
+SV_KERNEL_SET(logits, VerifyParams, bf16_proc)
+SV_KERNEL_SET(logits, VerifyParams, f32_proc)
+SV_KERNEL_SET(sample, SampleParams, bf16)
+SV_KERNEL_SET(sample, SampleParams, f32)
+SV_KERNEL_SET(sample, SampleParams, bf16_proc)
+SV_KERNEL_SET(sample, SampleParams, f32_proc)
+#undef SV_KERNEL_SET
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
                           cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);

@@ -1948,7 +1948,7 @@ __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsig
 // bulk L2 prefetch: a CTA then holds only its statistics and inbox in shared
 // memory, and four share an SM.  Logits processors work in either form (the
 // rows are never rewritten).
-template <typename TIn, bool kTest, bool kVec, bool kRes>
+template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const VerifyParams P, int chunk) {
   static_assert(kRes || kVec, "rows read in place must be 16-byte aligned");
   using E = Elem<TIn>;
@@ -2008,7 +2008,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
       valid = false;
     }
   }
-  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
+  constexpr bool procs = kProc;  // the call has logits processors (P.rep_penalty or P.ban_cu)
   const Procs pr{pen_bits, ban_bits, theta};
   const bool greedy = valid && temp == 0.0f;
   int A = 0;
@@ -2246,7 +2246,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
 // exponential race (argmax at temperature 0), and the fp32 probability row can
 // be written out for the probability entry.
 // ---------------------------------------------------------------------------
-template <typename TIn, bool kTest, bool kVec, bool kRes>
+template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const SampleParams P, int chunk) {
   static_assert(kRes || kVec, "rows read in place must be 16-byte aligned");
   extern __shared__ __align__(16) unsigned char dyn_smem[];
@@ -2267,7 +2267,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
   int step = 0;
   uint32_t phase = 0;
   // processor bitmaps (present only when the call has processors)
-  const bool procs = P.rep_penalty != nullptr || P.ban_cu != nullptr;
+  constexpr bool procs = kProc;  // P.rep_penalty or P.ban_cu
   const int words = (chunk + 31) / 32;
   uint32_t *const pen_bits = reinterpret_cast<uint32_t *>(inbox + 2 * ncta);
   uint32_t *const ban_bits = pen_bits + words;
@@ -2408,7 +2408,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const Sa
   cluster_sync();
 }
 
-template <typename TIn, bool kTest, bool kVec, bool kRes>
+template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 cudaError_t launch_sample_one(const SampleParams &p, int cluster, int chunk, size_t dyn, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.R) * static_cast<unsigned>(cluster), 1, 1);
@@ -2422,39 +2422,39 @@ cudaError_t launch_sample_one(const SampleParams &p, int cluster, int chunk, siz
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sample_kernel<TIn, kTest, kVec, kRes>, p, chunk);
+  return cudaLaunchKernelEx(&cfg, sample_kernel<TIn, kTest, kVec, kRes, kProc>, p, chunk);
 }
 
-template <typename TIn, bool kTest, bool kVec, bool kRes>
+template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 cudaError_t enable_sample_one(int max_cluster, int max_dyn) {
-  cudaError_t e = cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec, kRes>,
+  cudaError_t e = cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec, kRes, kProc>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
   if (e != cudaSuccess) return e;
   if (max_cluster > 8)
-    return cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec, kRes>,
+    return cudaFuncSetAttribute(sample_kernel<TIn, kTest, kVec, kRes, kProc>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return cudaSuccess;
 }
 
-// Sampler forms per element type and randomness: unaligned rows (in shared
-// memory), aligned rows in shared memory (processors), aligned rows in place.
-template <typename TIn, bool kTest>
+// Sampler forms per element type, randomness and processors: unaligned rows
+// (in shared memory), aligned rows in shared memory, aligned rows in place.
+template <typename TIn, bool kTest, bool kProc>
 cudaError_t enable_sample_forms(int max_cluster, int max_dyn) {
   cudaError_t e;
-  if ((e = enable_sample_one<TIn, kTest, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_sample_one<TIn, kTest, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  return enable_sample_one<TIn, kTest, true, false>(max_cluster, max_dyn);
+  if ((e = enable_sample_one<TIn, kTest, false, true, kProc>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_sample_one<TIn, kTest, true, true, kProc>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_sample_one<TIn, kTest, true, false, kProc>(max_cluster, max_dyn);
 }
 
-template <typename TIn, bool kTest>
+template <typename TIn, bool kTest, bool kProc>
 cudaError_t launch_sample_form(const SampleParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
                                cudaStream_t stream) {
-  if (!vec) return launch_sample_one<TIn, kTest, false, true>(p, cluster, chunk, dyn, stream);
-  return resident ? launch_sample_one<TIn, kTest, true, true>(p, cluster, chunk, dyn, stream)
-                  : launch_sample_one<TIn, kTest, true, false>(p, cluster, chunk, dyn, stream);
+  if (!vec) return launch_sample_one<TIn, kTest, false, true, kProc>(p, cluster, chunk, dyn, stream);
+  return resident ? launch_sample_one<TIn, kTest, true, true, kProc>(p, cluster, chunk, dyn, stream)
+                  : launch_sample_one<TIn, kTest, true, false, kProc>(p, cluster, chunk, dyn, stream);
 }
 
-template <typename TIn, bool kTest, bool kVec, bool kRes>
+template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 cudaError_t launch_one(const VerifyParams &p, int cluster, int chunk, size_t dyn, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.N) * static_cast<unsigned>(cluster), 1, 1);
@@ -2468,67 +2468,69 @@ cudaError_t launch_one(const VerifyParams &p, int cluster, int chunk, size_t dyn
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, logits_kernel<TIn, kTest, kVec, kRes>, p, chunk);
+  return cudaLaunchKernelEx(&cfg, logits_kernel<TIn, kTest, kVec, kRes, kProc>, p, chunk);
 }
 
-template <typename TIn, bool kTest, bool kVec, bool kRes>
+template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 cudaError_t enable_one(int max_cluster, int max_dyn) {
-  cudaError_t e = cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec, kRes>,
+  cudaError_t e = cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec, kRes, kProc>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
   if (e != cudaSuccess) return e;
   if (max_cluster > 8)
-    return cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec, kRes>,
+    return cudaFuncSetAttribute(logits_kernel<TIn, kTest, kVec, kRes, kProc>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return cudaSuccess;
 }
 
-// Forms built per element type and randomness: unaligned rows (resident),
-// aligned rows with both chunks resident, aligned rows read in place.
-template <typename TIn, bool kTest>
+// Forms built per element type, randomness and processors: unaligned rows
+// (resident), aligned rows with both chunks resident, aligned rows read in
+// place.
+template <typename TIn, bool kTest, bool kProc>
 cudaError_t enable_forms(int max_cluster, int max_dyn) {
   cudaError_t e;
-  if ((e = enable_one<TIn, kTest, false, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  if ((e = enable_one<TIn, kTest, true, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  return enable_one<TIn, kTest, true, false>(max_cluster, max_dyn);
+  if ((e = enable_one<TIn, kTest, false, true, kProc>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  if ((e = enable_one<TIn, kTest, true, true, kProc>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_one<TIn, kTest, true, false, kProc>(max_cluster, max_dyn);
 }
 
-template <typename TIn, bool kTest>
+template <typename TIn, bool kTest, bool kProc>
 cudaError_t launch_form(const VerifyParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
                         cudaStream_t stream) {
-  if (!vec) return launch_one<TIn, kTest, false, true>(p, cluster, chunk, dyn, stream);
-  return resident ? launch_one<TIn, kTest, true, true>(p, cluster, chunk, dyn, stream)
-                  : launch_one<TIn, kTest, true, false>(p, cluster, chunk, dyn, stream);
+  if (!vec) return launch_one<TIn, kTest, false, true, kProc>(p, cluster, chunk, dyn, stream);
+  return resident ? launch_one<TIn, kTest, true, true, kProc>(p, cluster, chunk, dyn, stream)
+                  : launch_one<TIn, kTest, true, false, kProc>(p, cluster, chunk, dyn, stream);
 }
 
-// Every form of both kernels for one element type (test and production
-// randomness), and their launches; each element-type translation unit turns
-// these into its named entry points.
-template <typename TIn>
+// Every form of both kernels for one element type and processor setting
+// (test and production randomness), and their launches; each translation unit
+// turns these into its named entry points.
+template <typename TIn, bool kProc>
 cudaError_t enable_type_logits(int max_cluster, int max_dyn) {
   cudaError_t e;
-  if ((e = enable_forms<TIn, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  return enable_forms<TIn, false>(max_cluster, max_dyn);
+  if ((e = enable_forms<TIn, true, kProc>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_forms<TIn, false, kProc>(max_cluster, max_dyn);
 }
 
-template <typename TIn>
+template <typename TIn, bool kProc>
 cudaError_t enable_type_sample(int max_cluster, int max_dyn) {
   cudaError_t e;
-  if ((e = enable_sample_forms<TIn, true>(max_cluster, max_dyn)) != cudaSuccess) return e;
-  return enable_sample_forms<TIn, false>(max_cluster, max_dyn);
+  if ((e = enable_sample_forms<TIn, true, kProc>(max_cluster, max_dyn)) != cudaSuccess) return e;
+  return enable_sample_forms<TIn, false, kProc>(max_cluster, max_dyn);
 }
 
-template <typename TIn>
+template <typename TIn, bool kProc>
 cudaError_t launch_type_logits(const VerifyParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
                                cudaStream_t stream) {
-  return p.exponentials != nullptr ? launch_form<TIn, true>(p, cluster, chunk, dyn, vec, resident, stream)
-                                   : launch_form<TIn, false>(p, cluster, chunk, dyn, vec, resident, stream);
+  return p.exponentials != nullptr ? launch_form<TIn, true, kProc>(p, cluster, chunk, dyn, vec, resident, stream)
+                                   : launch_form<TIn, false, kProc>(p, cluster, chunk, dyn, vec, resident, stream);
 }
 
-template <typename TIn>
+template <typename TIn, bool kProc>
 cudaError_t launch_type_sample(const SampleParams &p, int cluster, int chunk, size_t dyn, bool vec, bool resident,
                                cudaStream_t stream) {
-  return p.exponentials != nullptr ? launch_sample_form<TIn, true>(p, cluster, chunk, dyn, vec, resident, stream)
-                                   : launch_sample_form<TIn, false>(p, cluster, chunk, dyn, vec, resident, stream);
+  return p.exponentials != nullptr
+             ? launch_sample_form<TIn, true, kProc>(p, cluster, chunk, dyn, vec, resident, stream)
+             : launch_sample_form<TIn, false, kProc>(p, cluster, chunk, dyn, vec, resident, stream);
 }
 
 }  // namespace

@@ -90,10 +90,11 @@ def test_processors_statistics_paths(top_k, top_p, temp, V, cluster):
     """Every statistics path with processors against the oracle: the fused
     setting at its vocabulary, cuts in windows below the first, dense rows, a
     deep top-k threshold, and one CTA per request over a 40000-key chunk."""
-    w = workloads.make("fused", N=16, V=V, seed=23)
-    w["top_k"] = np.full(16, top_k, np.int32)
-    w["top_p"] = np.full(16, top_p, np.float32)
-    w["temperature"] = np.full(16, temp, np.float32)
+    N = 32
+    w = workloads.make("fused", N=N, V=V, seed=23)
+    w["top_k"] = np.full(N, top_k, np.int32)
+    w["top_p"] = np.full(N, top_p, np.float32)
+    w["temperature"] = np.full(N, temp, np.float32)
     add_lists(w, np.random.default_rng(9), theta=1.5, n_ctx=400, n_ban=20)
     o = oracle.verify(w)
     compare(H().run_gpu(w, cluster_ctas=cluster), o, w)

@@ -4,8 +4,12 @@ This module only *makes inputs*: draft/target logits or probability rows, draft
 ids, uniforms ``u`` and exponentials ``E`` for test mode, the ragged
 ``cu_num_draft_tokens`` layout and the KV bookkeeping (``num_computed_tokens``,
 ``slot_mapping``).  It holds none of the verifier's arithmetic: no acceptance
-test, no residual, no race, no top-k/top-p thresholding and no rollback.  Both
-the CPU oracle and the CUDA path are fed from it with byte-identical arrays.
+test, no residual, no race and no rollback.  To *make* the fused workload's
+draft ids and probability rows it samples from the stated distribution
+(temperature 0.8, top-k 50, top-p 0.9) with a float32 recipe of its own
+(``_nucleus_rows``: library topk and softmax, a numpy cumulative sum); the
+verifier's transform itself lives in the oracle and the kernels.  Both the
+CPU oracle and the CUDA path are fed from it with byte-identical arrays.
 
 Shapes follow the tutorial page "Speculative Decoding: propose, verify, accept",
 section 02: draft ids ``[N, gamma]``, draft rows ``[N, gamma, V]`` and target rows
@@ -26,11 +30,13 @@ Recipes (one per named workload; sizes can be shrunk for parity tests):
 * ``random``  N=64, gamma=4, V=128256; as ``tiny`` with sigma 2 / 0.5.
 * ``fused``   N=512, gamma=7, V=151936; bf16 logits, target ~N(0, 2.5^2), draft
   = target + N(0, 0.7^2); temperature 0.8, top-k 50, top-p 0.9 per request.
-  Draft ids are drawn from the draft rows' 50 largest logits under a float32
-  softmax at T=0.8 (input synthesis; the nucleus cut is left to the verifier).
+  Draft ids are drawn from the transformed draft rows (``_nucleus_rows``), as
+  the draft-side sampler would draw them, so every draft lies in q's support.
 * ``fused_probs``  the same batch materialised as fp32 probability rows for the
-  probability entry: each row keeps its 50 largest logits, softmaxed at T=0.8,
-  zero elsewhere (sparse rows with the fused workload's support size).
+  probability entry: every target and draft row through ``_nucleus_rows``
+  (its 50 largest logits, a float32 softmax at T=0.8, cut to the shortest
+  descending prefix reaching 0.9 with ties at the cut kept, renormalised; zero
+  elsewhere), and the same draft ids.
 * ``ragged``  N=256, gamma_i ~ U{0..8} (ragged via ``cu_num_draft_tokens``),
   V=128256; bf16 logits, target ~N(0, 2^2), per-request draft noise sigma in
   {0.1, 1.0, 3.0}; a seeded half of the requests is greedy (T=0), the rest T=1
@@ -185,14 +191,32 @@ def _greedy(name, rng, N, G, V):
                 top_p=None, num_computed_tokens=ncomp, slot_mapping=slots)
 
 
-def _top_support_softmax(rows_f32: np.ndarray, temp: float, k: int):
-    """For each row: indices of its ``k`` largest values and a float32 softmax of
-    value/temp over them (input synthesis for the sparse fused workload)."""
+def _nucleus_rows(rows_f32: np.ndarray, temp: float, k: int, top_p: float):
+    """Input synthesis for the fused workload.  For each row: the indices of its
+    largest values -- the k largest and every value tied with the k-th -- and
+    their weights: a float32 softmax of value/temp over that set, cut to the
+    shortest descending prefix whose float64 cumulative sum reaches ``top_p``
+    (every entry equal to the last kept value kept too), renormalised in
+    float64 and rounded to float32; 0 for the entries the cut drops.  Returns
+    (indices [rows, m], weights [rows, m]) with m >= k."""
     import torch
     x = torch.from_numpy(np.ascontiguousarray(rows_f32))
-    vals, idx = torch.topk(x, k, dim=-1, largest=True, sorted=True)
-    w = torch.softmax(vals / temp, dim=-1, dtype=torch.float32)
-    return idx.numpy().astype(np.int64), w.numpy()
+    m = min(x.shape[-1], 4 * k)
+    while True:  # widen until no row's tie at the k-th value runs past the m taken
+        vals, idx = torch.topk(x, m, dim=-1, largest=True, sorted=True)
+        if m == x.shape[-1] or bool((vals[:, -1] < vals[:, k - 1]).all()):
+            break
+        m = min(x.shape[-1], 2 * m)
+    in_k = vals >= vals[:, k - 1:k]
+    z = torch.where(in_k, vals / temp, torch.tensor(float("-inf")))
+    w = torch.softmax(z, dim=-1, dtype=torch.float32).numpy().astype(np.float64)
+    v = vals.numpy()
+    first = (np.cumsum(w, axis=-1) < top_p).sum(axis=-1)  # first entry reaching top_p
+    first = np.minimum(first, in_k.numpy().sum(axis=-1) - 1)
+    keep = v >= v[np.arange(v.shape[0]), first][:, None]
+    w = np.where(keep, w, 0.0)
+    w /= w.sum(axis=-1, keepdims=True)
+    return idx.numpy().astype(np.int64), w.astype(np.float32)
 
 
 def _fused(name, rng, N, G, V):
@@ -225,13 +249,13 @@ def _fused(name, rng, N, G, V):
         d_bits[r0:r1] = _to_bf16_bits(dl)
         if G:
             d32 = bf16_bits_to_f32(d_bits[r0:r1]).reshape(-1, V)
-            d_idx, d_w = _top_support_softmax(d32, temp, kk)
+            d_idx, d_w = _nucleus_rows(d32, temp, kk, top_p)
             pick = _inverse_cdf(crng, d_w)
             ids[r0:r1] = d_idx[np.arange(d_idx.shape[0]), pick].reshape(r1 - r0, G)
             if probs:
                 np.put_along_axis(q[r0:r1].reshape(-1, V), d_idx, d_w, axis=-1)
         if probs:
-            t_idx, t_w = _top_support_softmax(bf16_bits_to_f32(t_bits[r0:r1]).reshape(-1, V), temp, kk)
+            t_idx, t_w = _nucleus_rows(bf16_bits_to_f32(t_bits[r0:r1]).reshape(-1, V), temp, kk, top_p)
             np.put_along_axis(p[r0:r1].reshape(-1, V), t_idx, t_w, axis=-1)
 
     nchunks = len(chunk_seeds)
@@ -244,7 +268,7 @@ def _fused(name, rng, N, G, V):
     if not probs:
         out.update(entry="logits", dtype="bf16", target=t_bits.reshape(T + N, V), draft=d_bits.reshape(T, V))
         return out
-    # fused_probs: sparse fp32 probability rows with the same support size
+    # fused_probs: sparse fp32 probability rows of the same distributions
     out.update(entry="probs", dtype="f32", target=p.reshape(T + N, V), draft=q.reshape(T, V), top_k=None,
                top_p=None)
     return out
