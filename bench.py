@@ -65,6 +65,8 @@ def parse_args():
     ap.add_argument("--no-logits", action="store_true")
     ap.add_argument("--logits-variant-steps", type=int, default=30)
     ap.add_argument("--ngram-steps", type=int, default=200)
+    ap.add_argument("--logits-form", choices=["auto", "cluster", "stream"], default="auto",
+                    help="logits entry: library choice with the small-top-k hint, clusters only, or one CTA per request")
     ap.add_argument("--logits-resident", action="store_true",
                     help="keep both row chunks of the logits entry in shared memory (comparison runs)")
     ap.add_argument("--no-ngram", action="store_true")
@@ -89,6 +91,7 @@ def measured_peak():
 
 LOGITS_KERNEL_SOURCES = ["sv_logits.cuh", "sv_logits.cu", "sv_logits_bf16.cu", "sv_logits_f32.cu", "sv_sample_bf16.cu",
                          "sv_sample_f32.cu", "sv_device.cuh"]  # (the processor units instantiate the same templates)
+STREAM_KERNEL_SOURCES = ["sv_stream.cuh", "sv_stream_bf16.cu", "sv_logits.cuh", "sv_device.cuh"]
 
 
 def kernel_source_hash(sources=None) -> str:
@@ -222,8 +225,12 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, t
     w = dict(w, top_k=np.full(N, top_k, np.int32), top_p=np.full(N, top_p, np.float32))
     gam = workloads.gammas_of(w)
     t = workloads.as_torch(w, dev)
-    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster,
-                      flags=sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0)
+    flags = sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0
+    if args.logits_form == "stream":
+        flags |= sv.SV_FLAG_ONE_CTA_PER_REQUEST
+    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster, flags=flags)
+    # the caller knows its sampling parameters: top-k 50 is a small top-k
+    hints = sv.SV_HINT_SMALL_TOP_K if (0 < top_k <= sv.SV_SMALL_TOP_K_MAX and args.logits_form != "cluster") else 0
     K = max(3, min(args.steps, steps or args.logits_steps))
     W = args.warmup
     nacc = torch.empty((K + W, N), dtype=torch.int32, device=dev)
@@ -233,7 +240,7 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, t
                       temperature=t["temperature"], top_k=t["top_k"], top_p=t["top_p"], out_tokens=out,
                       num_accepted=nacc[0], num_computed_tokens=t["num_computed_tokens"].clone(),
                       slot_mapping=t["slot_mapping"].clone(), status=status, seed=20240602,
-                      rng_request_base=rank * N)
+                      rng_request_base=rank * N, hints=hints)
     sptr = ctypes.c_void_p(stream.cuda_stream)
     h = ctypes.c_void_p(ver.handle)
 
@@ -265,20 +272,28 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, t
     ms = total_ms / K
     peak, src = measured_peak()
     full = (2 * T + N) * V * 2
-    traffic, traffic_sha = stored_traffic("verify_logits_fused", LOGITS_KERNEL_SOURCES)
+    # the form the library takes (include/spec_verify.h: the flag, or the hint on a batch of at least two
+    # requests per SM; never with resident rows)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    stream_form = not args.logits_resident and (args.logits_form == "stream" or (hints and N >= 2 * sms))
+    sources = STREAM_KERNEL_SOURCES if stream_form else LOGITS_KERNEL_SOURCES
+    traffic, traffic_sha = stored_traffic("verify_logits_fused_stream" if stream_form else "verify_logits_fused",
+                                          sources)
     if traffic is not None and (N != 512 or top_k != 50 or top_p != 0.9):
         traffic = None  # the stored counters are scaled to a 512-request launch of this setting
     ver.close()
     return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
             "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k {top_k if top_k > 0 else 'off'}, "
                                    f"top-p {top_p if top_p < 1 else 'off'}, production Philox", "entry": "logits",
-                       "rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)"},
+                       "rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)",
+                       "hints": "small top-k" if hints else "none",
+                       "form": "one CTA per request" if stream_form else "clusters"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
                          "algorithmic_bytes_per_launch": alg, "full_tensor_bytes": full,
                          "full_tensor_equiv_gbs": full / (ms / 1e3) / 1e9,
                          "full_tensor_equiv_of_peak": full / (ms / 1e3) / 1e9 / peak,
-                         "kernel_source_sha": kernel_source_hash(LOGITS_KERNEL_SOURCES),
+                         "kernel_source_sha": kernel_source_hash(sources),
                          "traffic_source_sha": traffic_sha},
             "acceptance": {"mean_accepted": float(na.mean()),
                            "A_hist": np.bincount(na.reshape(-1), minlength=G + 1).tolist()},

@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 6u
+#define SPEC_VERIFY_ABI_VERSION 7u
 #define SV_PLACEHOLDER_TOKEN_ID (-1)
 #define SV_PADDING_SLOT_ID (-1)
 #define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
@@ -89,6 +89,23 @@ enum sv_data_status {
  * in place after an L2 prefetch (four CTAs per SM); unaligned rows are always
  * copied.  Results are identical. */
 #define SV_FLAG_RESIDENT_ROWS 1u
+/* SV_FLAG_ONE_CTA_PER_REQUEST: logits-entry calls with aligned rows and no
+ * logits processors always take the one-CTA-per-request form (see
+ * SV_HINT_SMALL_TOP_K); by default the library takes it only for hinted
+ * calls whose batch fills the GPU.  Results are identical in both forms. */
+#define SV_FLAG_ONE_CTA_PER_REQUEST 2u
+
+/* Call hints (the hints field of spec_verify_args; they never change a
+ * result).  SV_HINT_SMALL_TOP_K: the caller states that every random request
+ * of the call has 1 <= top_k <= SV_SMALL_TOP_K_MAX.  For such a batch, large
+ * enough to give every request its own CTA at once, the logits entry verifies
+ * each request with one CTA that reads a position's two rows once (keeping
+ * the largest key of every 128-byte block), reads again the few blocks that
+ * can hold the top-k set, and derives the threshold, the top-p cut, the
+ * normaliser and the race from those candidates; a request outside the
+ * statement is still verified exactly, by a slower multi-pass path. */
+#define SV_HINT_SMALL_TOP_K 1u
+#define SV_SMALL_TOP_K_MAX 256
 
 /* Call flags for tests (the test_flags field of the argument structs; 0 in
  * normal use).  SV_TEST_EXPIRE_COPY_WAIT: the first wait for every bulk row
@@ -108,7 +125,7 @@ typedef struct spec_verify_config {
   int32_t vocab_size;   /* largest vocab_size of any call (>= 1) */
   int32_t device;       /* CUDA device ordinal the handle's calls run on */
   int32_t cluster_ctas; /* CTAs cooperating on one request: 0 = automatic, else 1, 2, 4, 8 or 16 */
-  uint32_t flags;       /* 0, or SV_FLAG_RESIDENT_ROWS */
+  uint32_t flags;       /* 0, or SV_FLAG_* bits */
 } spec_verify_config;
 
 /* One verification call.  N = num_reqs, G = max_spec_len, V = vocab_size,
@@ -121,7 +138,7 @@ typedef struct spec_verify_args {
   int32_t vocab_size;   /* V >= 1 */
   int32_t entry;        /* SV_ENTRY_PROBS or SV_ENTRY_LOGITS */
   int32_t dtype;        /* SV_F32 (both entries) or SV_BF16 (logits entry only) */
-  int32_t reserved0;    /* must be 0 */
+  uint32_t hints;       /* 0, or SV_HINT_* bits */
   int64_t num_draft_tokens_total; /* T = cu[N-1]; must equal N*G when cu == NULL */
 
   const int32_t *draft_ids;           /* [T] draft token ids, request-major */

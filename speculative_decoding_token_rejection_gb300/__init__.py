@@ -35,6 +35,9 @@ _P = ctypes.c_void_p
 
 
 SV_FLAG_RESIDENT_ROWS = 1
+SV_FLAG_ONE_CTA_PER_REQUEST = 2
+SV_HINT_SMALL_TOP_K = 1
+SV_SMALL_TOP_K_MAX = 256
 SV_TEST_EXPIRE_COPY_WAIT = 1
 
 
@@ -47,7 +50,7 @@ class SpecVerifyConfig(ctypes.Structure):
 class SpecVerifyArgs(ctypes.Structure):
     _fields_ = [
         ("num_reqs", ctypes.c_int32), ("max_spec_len", ctypes.c_int32), ("vocab_size", ctypes.c_int32),
-        ("entry", ctypes.c_int32), ("dtype", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("entry", ctypes.c_int32), ("dtype", ctypes.c_int32), ("hints", ctypes.c_uint32),
         ("num_draft_tokens_total", ctypes.c_int64),
         ("draft_ids", _P), ("cu_num_draft_tokens", _P),
         ("target", _P), ("target_row_stride", ctypes.c_int64),
@@ -227,7 +230,7 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
                dbg_py=None, dbg_qy=None, status=None, device=None,
                host_rows: bool = False, synthetic_acceptance_rates=None, repetition_penalty=None,
                penalty_cu=None, penalty_token_ids=None, banned_cu=None, banned_token_ids=None, stop_cu=None,
-               stop_token_ids=None, test_flags: int = 0) -> SpecVerifyArgs:
+               stop_token_ids=None, test_flags: int = 0, hints: int = 0) -> SpecVerifyArgs:
     """Validate tensors and fill a SpecVerifyArgs (no device work).
 
     Logits processors (logits entry) and stop tokens (both entries) come as
@@ -277,6 +280,7 @@ def build_args(*, entry: str, draft_ids, target, out_tokens, num_accepted, draft
                                                           (torch.float32,), host_rows)
     a.seed, a.offset, a.rng_request_base = int(seed), int(offset), int(rng_request_base)
     a.test_flags = int(test_flags)
+    a.hints = int(hints)
     a.out_tokens = _ptr(out_tokens, torch.int32, "out_tokens", device, ndim=2)
     a.num_accepted = _ptr(num_accepted, torch.int32, "num_accepted", device, numel=N)
     a.num_computed_tokens = _ptr(num_computed_tokens, torch.int32, "num_computed_tokens", device, numel=N)

@@ -113,7 +113,8 @@ static sv_status check_config(const spec_verify_config *c) {
   const int cc = c->cluster_ctas;
   if (!(cc == 0 || cc == 1 || cc == 2 || cc == 4 || cc == 8 || cc == 16))
     return fail(SV_ERR_INVALID_ARG, "cluster_ctas must be 0, 1, 2, 4, 8 or 16");
-  if (c->flags & ~SV_FLAG_RESIDENT_ROWS) return fail(SV_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
+  if (c->flags & ~(SV_FLAG_RESIDENT_ROWS | SV_FLAG_ONE_CTA_PER_REQUEST))
+    return fail(SV_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   if (static_cast<long long>(c->max_num_reqs) * (cc ? cc : 16) > INT_MAX)
     return fail(SV_ERR_INVALID_ARG, "max_num_reqs too large for one grid");
   return SV_OK;
@@ -136,7 +137,7 @@ sv_status spec_verify_check_args(const spec_verify_config *c, const spec_verify_
   if (a->dtype != SV_F32 && a->dtype != SV_BF16) return fail(SV_ERR_INVALID_ARG, "bad dtype");
   if (a->entry == SV_ENTRY_PROBS && a->dtype != SV_F32)
     return fail(SV_ERR_UNSUPPORTED, "the probability entry takes fp32 rows");
-  if (a->reserved0 != 0) return fail(SV_ERR_INVALID_ARG, "reserved0 must be 0");
+  if (a->hints & ~SV_HINT_SMALL_TOP_K) return fail(SV_ERR_INVALID_ARG, "unknown hints 0x%x", a->hints);
   if (a->test_flags & ~SV_TEST_EXPIRE_COPY_WAIT) return fail(SV_ERR_INVALID_ARG, "unknown test_flags 0x%x", a->test_flags);
   if (a->num_draft_tokens_total < 0) return fail(SV_ERR_INVALID_ARG, "num_draft_tokens_total < 0");
   if (!a->cu_num_draft_tokens &&
@@ -200,6 +201,8 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, config->device);
     max_dyn = optin - static_cast<int>(sv::logits_static_smem()) - 1024;
+    if ((e = sv::enable_stream_kernels_bf16()) != cudaSuccess || (e = sv::enable_stream_kernels_f32()) != cudaSuccess)
+      result = fail(SV_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(e));
     if (sv::enable_probs_kernels(16) != cudaSuccess || sv::enable_logits_kernels(16, max_dyn) != cudaSuccess ||
         sv::enable_sample_kernels(16, max_dyn) != cudaSuccess) {
       cudaGetLastError();
@@ -291,6 +294,17 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
     const bool vec = sv::aligned16(a->target) && (a->target_row_stride % per16 == 0) &&
                      (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % per16 == 0));
     const bool resident = !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
+    // one CTA per request: aligned rows read in place, no processors, and
+    // either the handle asks for it or the caller states small top-k values
+    // and the batch gives every SM at least two requests
+    const bool stream_form = vec && !procs && !(h->cfg.flags & SV_FLAG_RESIDENT_ROWS) &&
+                             ((h->cfg.flags & SV_FLAG_ONE_CTA_PER_REQUEST) ||
+                              ((a->hints & SV_HINT_SMALL_TOP_K) && p.N >= 2 * h->num_sms));
+    if (stream_form) {
+      e = bf16 ? sv::launch_stream_bf16(p, s) : sv::launch_stream_f32(p, s);
+      if (e != cudaSuccess) return fail(SV_ERR_CUDA, "verifier launch: %s", cudaGetErrorString(e));
+      return SV_OK;
+    }
     if (!sv::choose_logits_layout(h, p.N, p.V, eb, &cluster, &chunk, procs, resident, true))
       return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for the rows to fit in the cluster's shared memory",
                   p.V);

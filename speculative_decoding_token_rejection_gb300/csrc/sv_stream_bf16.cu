@@ -1,0 +1,11 @@
+// sv_stream_bf16.cu -- the one-CTA-per-request form of the logits entry for
+// bf16 logits (templates in sv_stream.cuh).
+#include "sv_stream.cuh"
+
+namespace sv {
+
+cudaError_t enable_stream_kernels_bf16() { return enable_type_stream<uint16_t>(); }
+
+cudaError_t launch_stream_bf16(const VerifyParams &p, cudaStream_t stream) { return launch_type_stream<uint16_t>(p, stream); }
+
+}  // namespace sv

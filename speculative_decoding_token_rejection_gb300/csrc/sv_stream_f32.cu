@@ -1,0 +1,11 @@
+// sv_stream_f32.cu -- the one-CTA-per-request form of the logits entry for
+// fp32 logits (templates in sv_stream.cuh).
+#include "sv_stream.cuh"
+
+namespace sv {
+
+cudaError_t enable_stream_kernels_f32() { return enable_type_stream<float>(); }
+
+cudaError_t launch_stream_f32(const VerifyParams &p, cudaStream_t stream) { return launch_type_stream<float>(p, stream); }
+
+}  // namespace sv

@@ -31,7 +31,7 @@ def processor_args(w, dev):
 
 
 def run_gpu(w, *, production=False, seed=0, offset=0, rng_request_base=0, cluster_ctas=0, stream=None,
-            synthetic_rates=None, flags=0, test_flags=0):
+            synthetic_rates=None, flags=0, test_flags=0, hints=0):
     """Run the CUDA path on workload ``w``; returns numpy results like oracle.verify."""
     dev = torch.device("cuda:0")
     t = workloads.as_torch(w, dev)
@@ -53,7 +53,7 @@ def run_gpu(w, *, production=False, seed=0, offset=0, rng_request_base=0, cluste
         seed=seed, offset=offset, rng_request_base=rng_request_base, out_tokens=out, num_accepted=nacc,
         num_computed_tokens=ncomp, slot_mapping=slots, dbg_py=dpy, dbg_qy=dqy, status=status,
         synthetic_acceptance_rates=None if synthetic_rates is None else
-        torch.as_tensor(np.asarray(synthetic_rates, np.float32)).to(dev), test_flags=test_flags,
+        torch.as_tensor(np.asarray(synthetic_rates, np.float32)).to(dev), test_flags=test_flags, hints=hints,
         **processor_args(w, dev))
     torch.cuda.synchronize()
     cpu = lambda x: None if x is None else x.cpu().numpy()

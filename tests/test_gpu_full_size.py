@@ -58,12 +58,16 @@ def test_synthetic_acceptance_bench_batch():
     compare(g, o, w, production=True, max_exempt_frac=0.01)
 
 
-def test_logits_entry_bench_batch():
-    """The fused logits batch (bf16, T=0.8, top-k 50, top-p 0.9) in the
-    default form (rows read in place, 8 CTAs per request): every one of the
-    512 requests against the oracle."""
+@pytest.mark.parametrize("form", ["cluster", "stream"])
+def test_logits_entry_bench_batch(form):
+    """The fused logits batch (bf16, T=0.8, top-k 50, top-p 0.9) in both
+    forms: clusters (rows read in place, 8 CTAs per request; no hint) and,
+    with the small-top-k hint the bench passes, one CTA per request: every
+    one of the 512 requests against the oracle."""
+    import speculative_decoding_token_rejection_gb300 as sv
     w = fused_logits()
-    g = H().run_gpu(w, production=True, seed=20240602, offset=5)
+    hints = sv.SV_HINT_SMALL_TOP_K if form == "stream" else 0
+    g = H().run_gpu(w, production=True, seed=20240602, offset=5, hints=hints)
     o = oracle.verify_parallel(w, production=True, seed=20240602, offset=5)
     n_ex = compare(g, o, w, production=True)
     print(f"logits batch: {n_ex} of {w['N']} requests exempted")

@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_description(lib):
-    assert lib.spec_verify_abi_version() == 6
+    assert lib.spec_verify_abi_version() == 7
     assert lib.spec_verify_sizeof_args() == ctypes.sizeof(sv.SpecVerifyArgs)
     assert lib.spec_verify_sizeof_config() == ctypes.sizeof(sv.SpecVerifyConfig)
 
@@ -76,7 +76,8 @@ def cfg(**kw):
     (lambda a: setattr(a, "dtype", sv.SV_BF16), sv.SV_ERR_UNSUPPORTED),  # probs entry is fp32 only
     (lambda a: (setattr(a, "entry", sv.SV_ENTRY_LOGITS), setattr(a, "dtype", sv.SV_BF16)), sv.SV_OK),
     (lambda a: setattr(a, "entry", sv.SV_ENTRY_LOGITS), sv.SV_OK),  # fp32 logits
-    (lambda a: setattr(a, "reserved0", 1), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "hints", 2), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "hints", 1), sv.SV_OK),
     (lambda a: setattr(a, "num_draft_tokens_total", 11), sv.SV_ERR_INVALID_ARG),  # != N*G without cu
     (lambda a: setattr(a, "draft_ids", None), sv.SV_ERR_INVALID_ARG),
     (lambda a: setattr(a, "target", None), sv.SV_ERR_INVALID_ARG),
@@ -126,7 +127,8 @@ def test_check_args(lib, mutate, code):
     (dict(cluster_ctas=3), sv.SV_ERR_INVALID_ARG),
     (dict(cluster_ctas=16), sv.SV_OK),
     (dict(flags=sv.SV_FLAG_RESIDENT_ROWS), sv.SV_OK),
-    (dict(flags=2), sv.SV_ERR_INVALID_ARG),
+    (dict(flags=sv.SV_FLAG_ONE_CTA_PER_REQUEST), sv.SV_OK),
+    (dict(flags=4), sv.SV_ERR_INVALID_ARG),
 ])
 def test_check_config(lib, kw, code):
     assert sv.spec_verify_check_args(cfg(**kw), good_args()) == code
