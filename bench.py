@@ -343,8 +343,17 @@ def time_sampler(args, sv, dev, world, rank, dist, stream, w, write_q):
     h = sv.spec_verify_create(N, 1, V, device=dev.index, cluster_ctas=args.cluster)
     lib = sv.load_library()
     sptr = ctypes.c_void_p(stream.cuda_stream)
+    # the caller knows its sampling parameters: top-k 50 is a small top-k (one CTA per row on a large batch)
+    hints = sv.SV_HINT_SMALL_TOP_K if args.logits_form != "cluster" else 0
+    flags_f = sv.SV_FLAG_ONE_CTA_PER_REQUEST if args.logits_form == "stream" else 0
+    if flags_f:
+        sv.spec_verify_destroy(h)
+        h = sv.spec_verify_create(N, 1, V, device=dev.index, cluster_ctas=args.cluster, flags=flags_f)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    stream_form = bool(flags_f) or (bool(hints) and N >= 2 * sms)
     built = [sv.build_sample_args(logits=draft[:, j, :], tokens=tokens, probs=probs, temperature=temp,
-                                  top_k=top_k, top_p=top_p, seed=20240603, rng_row_base=rank * N, status=status)
+                                  top_k=top_k, top_p=top_p, seed=20240603, rng_row_base=rank * N, status=status,
+                                  hints=hints)
              for j in range(G)]
 
     def step(k):
@@ -359,19 +368,21 @@ def time_sampler(args, sv, dev, world, rank, dist, stream, w, write_q):
     sv.spec_verify_destroy(h)
     alg = N * V * 2 + N * (4 + 4 + 4 + 4) + (N * V * 4 if write_q else 0)
     peak, src = measured_peak()
-    traffic, traffic_sha = (None, None) if write_q else stored_traffic("draft_sampler_fused_rows",
-                                                                      LOGITS_KERNEL_SOURCES)
+    sources = STREAM_KERNEL_SOURCES if stream_form else LOGITS_KERNEL_SOURCES
+    traffic, traffic_sha = (None, None) if write_q else stored_traffic(
+        "draft_sampler_fused_rows_per_row" if stream_form else "draft_sampler_fused_rows", sources)
     if traffic is not None and N != 512:
         traffic = None  # the stored counters are scaled to a 512-row launch
     return {"value": world * N / (ms / 1e3), "unit": "sampled tokens/s", "ms_per_step": ms, "steps": K,
             "config": {"workload": f"draft step of the fused batch: {N} bf16 rows of V={V}, T=0.8, top-k 50, "
                                    "top-p 0.9, production Philox" + (", fp32 q rows written" if write_q else ""),
+                       "form": "one CTA per row" if stream_form else "clusters",
                        "l2": f"no flush: launch k reads draft position k mod {G} ({N * V * 2 / 1e6:.1f} MB per "
                              f"launch; {N * G * V * 2 / 1e6:.0f} MB over {G} launches, > 126 MB L2)"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
                          "algorithmic_bytes_per_launch": alg,
-                         "kernel_source_sha": kernel_source_hash(LOGITS_KERNEL_SOURCES),
+                         "kernel_source_sha": kernel_source_hash(sources),
                          "traffic_source_sha": traffic_sha},
             "gpu_launches": K}
 

@@ -89,16 +89,18 @@ enum sv_data_status {
  * in place after an L2 prefetch (four CTAs per SM); unaligned rows are always
  * copied.  Results are identical. */
 #define SV_FLAG_RESIDENT_ROWS 1u
-/* SV_FLAG_ONE_CTA_PER_REQUEST: logits-entry calls with aligned rows and no
- * logits processors always take the one-CTA-per-request form (see
- * SV_HINT_SMALL_TOP_K); by default the library takes it only for hinted
- * calls whose batch fills the GPU.  Results are identical in both forms. */
+/* SV_FLAG_ONE_CTA_PER_REQUEST: logits-entry and sampler calls with aligned
+ * rows, no logits processors and no SV_FLAG_RESIDENT_ROWS always take the
+ * one-CTA-per-request (per-row) form (see SV_HINT_SMALL_TOP_K); by default
+ * the library takes it only for hinted calls with at least two requests
+ * (rows) per SM.  Results are identical in both forms. */
 #define SV_FLAG_ONE_CTA_PER_REQUEST 2u
 
-/* Call hints (the hints field of spec_verify_args; they never change a
- * result).  SV_HINT_SMALL_TOP_K: the caller states that every random request
- * of the call has 1 <= top_k <= SV_SMALL_TOP_K_MAX.  For such a batch, large
- * enough to give every request its own CTA at once, the logits entry verifies
+/* Call hints (the hints field of spec_verify_args and spec_verify_sample_args;
+ * they never change a result).  SV_HINT_SMALL_TOP_K: the caller states that
+ * every random request (row) of the call has 1 <= top_k <= SV_SMALL_TOP_K_MAX.
+ * For such a batch, large enough to give every request its own CTA at once,
+ * the sampler samples each row with one CTA the same way, and the logits entry verifies
  * each request with one CTA that reads a position's two rows once (keeping
  * the largest key of every 128-byte block), reads again the few blocks that
  * can hold the top-k set, and derives the threshold, the top-p cut, the
@@ -237,7 +239,7 @@ typedef struct spec_verify_sample_args {
   int32_t num_rows;   /* R >= 0 (0 is a no-op); at most the handle's max_num_reqs */
   int32_t vocab_size; /* V, at most the handle's vocab_size */
   int32_t dtype;      /* SV_F32 or SV_BF16 logits */
-  int32_t reserved0;  /* must be 0 */
+  uint32_t hints;     /* 0, or SV_HINT_* bits */
   const void *logits; /* [R rows, row_stride] */
   int64_t row_stride; /* elements between rows (>= V) */
   const float *temperature; /* [R] or NULL (= 1) */

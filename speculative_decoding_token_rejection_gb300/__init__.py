@@ -70,7 +70,7 @@ class SpecVerifyArgs(ctypes.Structure):
 class SpecVerifySampleArgs(ctypes.Structure):
     _fields_ = [
         ("num_rows", ctypes.c_int32), ("vocab_size", ctypes.c_int32), ("dtype", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("hints", ctypes.c_uint32),
         ("logits", _P), ("row_stride", ctypes.c_int64),
         ("temperature", _P), ("top_k", _P), ("top_p", _P),
         ("exponentials", _P), ("exponentials_row_stride", ctypes.c_int64),
@@ -315,7 +315,7 @@ def spec_verify_run(handle: int, stream=None, **kw) -> None:
 def build_sample_args(*, logits, tokens, probs=None, temperature=None, top_k=None, top_p=None, exponentials=None,
                       seed: int = 0, offset: int = 0, rng_row_base: int = 0, status=None, repetition_penalty=None,
                       penalty_cu=None, penalty_token_ids=None, banned_cu=None,
-                      banned_token_ids=None, test_flags: int = 0) -> SpecVerifySampleArgs:
+                      banned_token_ids=None, test_flags: int = 0, hints: int = 0) -> SpecVerifySampleArgs:
     """Validate tensors and fill a SpecVerifySampleArgs (no device work).
     Logits processors per row as in ``build_args``."""
     import torch
@@ -338,6 +338,7 @@ def build_sample_args(*, logits, tokens, probs=None, temperature=None, top_k=Non
                                                           (torch.float32,))
     a.seed, a.offset, a.rng_row_base = int(seed), int(offset), int(rng_row_base)
     a.test_flags = int(test_flags)
+    a.hints = int(hints)
     a.tokens = _ptr(tokens, torch.int32, "tokens", device, numel=R)
     if probs is not None:
         a.probs, a.probs_row_stride = _rows(probs, "probs", device, V, R, (torch.float32,))

@@ -325,7 +325,7 @@ sv_status spec_verify_check_sample_args(const spec_verify_config *c, const spec_
   if (a->vocab_size > c->vocab_size)
     return fail(SV_ERR_CAPACITY, "vocab_size %d > handle max %d", a->vocab_size, c->vocab_size);
   if (a->dtype != SV_F32 && a->dtype != SV_BF16) return fail(SV_ERR_INVALID_ARG, "bad dtype");
-  if (a->reserved0 != 0) return fail(SV_ERR_INVALID_ARG, "reserved0 must be 0");
+  if (a->hints & ~SV_HINT_SMALL_TOP_K) return fail(SV_ERR_INVALID_ARG, "unknown hints 0x%x", a->hints);
   if (a->test_flags & ~SV_TEST_EXPIRE_COPY_WAIT) return fail(SV_ERR_INVALID_ARG, "unknown test_flags 0x%x", a->test_flags);
   if (a->num_rows == 0) return SV_OK;
   if (!a->logits) return fail(SV_ERR_INVALID_ARG, "logits is NULL");
@@ -382,6 +382,14 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   // unaligned rows, or the handle flag, go through shared memory; other rows
   // are read where they lie
   const bool resident = !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
+  // one CTA per row: the handle flag, or the small-top-k hint on a batch of at least two rows per SM
+  if (vec && !procs && !(h->cfg.flags & SV_FLAG_RESIDENT_ROWS) &&
+      ((h->cfg.flags & SV_FLAG_ONE_CTA_PER_REQUEST) || ((a->hints & SV_HINT_SMALL_TOP_K) && p.R >= 2 * h->num_sms))) {
+    const cudaError_t e = bf16 ? sv::launch_stream_sample_bf16(p, static_cast<cudaStream_t>(stream))
+                               : sv::launch_stream_sample_f32(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SV_ERR_CUDA, "sampler launch: %s", cudaGetErrorString(e));
+    return SV_OK;
+  }
   if (!sv::choose_logits_layout(h, p.R, p.V, eb, &cluster, &chunk, procs, resident, false))
     return fail(SV_ERR_UNSUPPORTED, "vocab_size %d too large for a row to fit in the cluster's shared memory", p.V);
   const cudaError_t e = sv::launch_sample(p, bf16, cluster, chunk, vec, resident, static_cast<cudaStream_t>(stream));

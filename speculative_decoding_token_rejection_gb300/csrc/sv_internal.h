@@ -124,11 +124,14 @@ SV_KERNEL_SET(sample, SampleParams, f32)
 SV_KERNEL_SET(sample, SampleParams, bf16_proc)
 SV_KERNEL_SET(sample, SampleParams, f32_proc)
 #undef SV_KERNEL_SET
-// the one-CTA-per-request form of the logits entry (sv_stream_{bf16,f32}.cu)
+// the one-CTA-per-request form of the logits entry (sv_stream_{bf16,f32}.cu; enabling covers the sampler form too)
 cudaError_t enable_stream_kernels_bf16();
 cudaError_t enable_stream_kernels_f32();
 cudaError_t launch_stream_bf16(const VerifyParams &p, cudaStream_t stream);
 cudaError_t launch_stream_f32(const VerifyParams &p, cudaStream_t stream);
+// the one-CTA-per-row form of the draft-side sampler (the same translation units)
+cudaError_t launch_stream_sample_bf16(const SampleParams &p, cudaStream_t stream);
+cudaError_t launch_stream_sample_f32(const SampleParams &p, cudaStream_t stream);
 cudaError_t launch_sample(const SampleParams &p, bool bf16, int cluster, int chunk, bool vec, bool resident,
                           cudaStream_t stream);
 cudaError_t enable_logits_kernels(int max_cluster, int max_dyn);

@@ -924,18 +924,163 @@ cudaError_t launch_stream_one(const VerifyParams &p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, stream_kernel<TIn, kTest>, p);
 }
 
+// The draft-side sampler in the same form: one CTA per row ("vLLM source
+// walk-through (10)", section "propose() multi-step loop": each draft step
+// samples its token from the transformed draft row).  The row is read once
+// with its block maxima, the candidates give the threshold, cut and
+// normaliser, and the bonus-style race runs over the kept candidates; the
+// transformed fp32 row, if asked for, is written from a second read of the
+// row (from L2).  Rows outside the candidate path take the exact statistics
+// and the race over the whole row.  The same results as sample_kernel.
+template <typename TIn, bool kTest>
+__global__ void __launch_bounds__(kThreads, 4) stream_sample_kernel(const SampleParams P) {
+  using E = Elem<TIn>;
+  extern __shared__ __align__(16) unsigned char dyn_smem[];
+  StreamSmem &ss = *reinterpret_cast<StreamSmem *>(dyn_smem);
+  const int r = static_cast<int>(blockIdx.x);
+  const int tid = threadIdx.x;
+  const int V = P.V;
+  TIn *const row = const_cast<TIn *>(static_cast<const TIn *>(P.logits) + static_cast<int64_t>(r) * P.row_stride);
+  TIn *const rows[2] = {row, row};
+  uint32_t bits = 0;
+  int32_t token = -1;
+  int step = 0;
+  const float temp = P.temperature ? P.temperature[r] : 1.0f;
+  if (!temperature_ok(temp)) {
+    bits |= SV_DATA_BAD_PARAM;
+  } else if (temp == 0.0f) {
+    unsigned long long best = 0;
+    uint32_t fl = 0;
+    argmax_logits<TIn, true>(row, 0, V, best, fl);
+    const KeyFlags kr = cluster_reduce(KeyFlags{best, fl}, ss.red, step++, 1);
+    if (kr.flags & SV_DATA_BAD_VALUES) bits |= SV_DATA_BAD_VALUES;
+    else token = static_cast<int32_t>(key_index(kr.key));
+  } else {
+    int topk = P.top_k ? P.top_k[r] : 0;
+    if (topk >= V || topk < 0) topk = 0;
+    const float topp = P.top_p ? P.top_p[r] : 1.0f;
+    if (!(topp > 0.0f)) {
+      bits |= SV_DATA_BAD_PARAM;
+    } else {
+      const bool cand = topk > 0 && topk <= kStreamTopK &&
+                        (V / (16 / static_cast<int>(sizeof(TIn))) + kStep - 1) / kStep <=
+                            kBlockSteps * (kMaxBlocks / kThreads);
+      if (cand)
+        stream_pass<TIn, true>(ss, rows, 1, V, 0);
+      else
+        stream_pass<TIn, false>(ss, rows, 1, V, 0);
+      const uint32_t f = ss.flags[0];
+      if ((f & kFlagBad) || !(f & kFlagFinite)) {
+        bits |= SV_DATA_BAD_VALUES;
+      } else {
+        RowStats st[2];
+        for (int q = 0; q < 2; ++q) {
+          st[q].vmax = E::val_of_key(ss.maxkey[0]);
+          st[q].c2 = __fdiv_rn(kLog2e, temp);
+          st[q].cut = 0u;
+          st[q].zp = 0.0f;
+        }
+        if (cand) gather_candidates<TIn>(ss, rows, 1, V, topk);
+        const bool fast = cand && !ss.overflow;
+        if (fast) {
+          cand_stats<TIn>(ss, 1, topk, topp, st);
+        } else {
+          const uint32_t maxk16[2] = {key16_of<TIn>(ss.maxkey[0]), key16_of<TIn>(ss.maxkey[0])};
+          stats_slow<TIn>(ss.fb, rows, 1, V, st[0].c2, topk, topp, maxk16, st, step, 1);
+        }
+        const RngKey rk{P.seed_lo, P.seed_hi ^ 0x53414D50u, P.off_lo, P.off_hi};  // the sampler's own streams
+        const uint32_t rs = P.row_base + static_cast<uint32_t>(r);
+        const float *Erow = kTest ? P.exponentials + static_cast<int64_t>(r) * P.exp_stride : nullptr;
+        float bk = 0.0f;
+        int bx = -1;
+        uint32_t fl = 0;
+        if (fast)
+          cand_race<TIn, kTest, false>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl);
+        else
+          race_chunks<TIn, kTest, false>(row, row, st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl);
+        const KeyFlags kr = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, ss.red, step++, 1);
+        bits |= kr.flags;
+        if (kr.key == 0ull) {
+          bits |= SV_DATA_EMPTY_DISTRIBUTION;
+          token = 0;
+        } else {
+          token = static_cast<int32_t>(key_index(kr.key));
+        }
+        if (P.probs) {  // the transformed row
+          float *prow = P.probs + static_cast<int64_t>(r) * P.probs_stride;
+          int xs = 0;
+          if (sizeof(TIn) == 2 && (reinterpret_cast<uintptr_t>(prow) & 15u) == 0) {
+            // eight bf16 logits in, two float4 probabilities out
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
+            float4 *p4 = reinterpret_cast<float4 *>(prow);
+            const int ng = V >> 3;
+            for (int v = tid; v < ng; v += kThreads) {
+              const uint4 d = ld_stream_u4(s4 + v);
+              const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+              float o[8];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                o[2 * t] = prob_of<TIn>(w[t] & 0xFFFFu, st[0]);
+                o[2 * t + 1] = prob_of<TIn>(w[t] >> 16, st[0]);
+              }
+              p4[2 * v] = make_float4(o[0], o[1], o[2], o[3]);
+              p4[2 * v + 1] = make_float4(o[4], o[5], o[6], o[7]);
+            }
+            xs = ng << 3;
+          }
+          for (int x = xs + tid; x < V; x += kThreads) prow[x] = prob_of<TIn>(bits_at(row, x), st[0]);
+        }
+      }
+    }
+  }
+  if (tid == 0) {
+    P.tokens[r] = token;
+    if (bits && P.status) atomicOr(P.status, static_cast<int>(bits));
+  }
+}
+
+template <typename TIn, bool kTest>
+cudaError_t launch_stream_sample_one(const SampleParams &p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.R), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(StreamSmem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (the exact statistics use cluster barriers)
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stream_sample_kernel<TIn, kTest>, p);
+}
+
 template <typename TIn>
 cudaError_t enable_type_stream() {
-  cudaError_t e = cudaFuncSetAttribute(stream_kernel<TIn, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(sizeof(StreamSmem)));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(stream_kernel<TIn, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(StreamSmem)));
+  const int dyn = static_cast<int>(sizeof(StreamSmem));
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(stream_kernel<TIn, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(stream_kernel<TIn, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(stream_sample_kernel<TIn, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                dyn)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(stream_sample_kernel<TIn, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
 }
 
 template <typename TIn>
 cudaError_t launch_type_stream(const VerifyParams &p, cudaStream_t stream) {
   return p.exponentials != nullptr ? launch_stream_one<TIn, true>(p, stream) : launch_stream_one<TIn, false>(p, stream);
+}
+
+template <typename TIn>
+cudaError_t launch_type_stream_sample(const SampleParams &p, cudaStream_t stream) {
+  return p.exponentials != nullptr ? launch_stream_sample_one<TIn, true>(p, stream)
+                                   : launch_stream_sample_one<TIn, false>(p, stream);
 }
 
 }  // namespace

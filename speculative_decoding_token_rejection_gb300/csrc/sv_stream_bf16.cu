@@ -1,5 +1,6 @@
-// sv_stream_bf16.cu -- the one-CTA-per-request form of the logits entry for
-// bf16 logits (templates in sv_stream.cuh).
+// sv_stream_bf16.cu -- the one-CTA-per-request form of the logits entry and the
+// one-CTA-per-row form of the draft-side sampler for bf16 logits (templates in
+// sv_stream.cuh).
 #include "sv_stream.cuh"
 
 namespace sv {
@@ -7,5 +8,9 @@ namespace sv {
 cudaError_t enable_stream_kernels_bf16() { return enable_type_stream<uint16_t>(); }
 
 cudaError_t launch_stream_bf16(const VerifyParams &p, cudaStream_t stream) { return launch_type_stream<uint16_t>(p, stream); }
+
+cudaError_t launch_stream_sample_bf16(const SampleParams &p, cudaStream_t stream) {
+  return launch_type_stream_sample<uint16_t>(p, stream);
+}
 
 }  // namespace sv

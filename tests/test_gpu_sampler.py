@@ -26,7 +26,8 @@ def _gpu():
     oracle.build()
 
 
-def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=False, cluster=0, flags=0, test_flags=0):
+def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=False, cluster=0, flags=0, test_flags=0,
+                hints=0):
     import torch
     import gpu_harness
     import speculative_decoding_token_rejection_gb300 as sv
@@ -43,18 +44,18 @@ def run_sampler(rows_np, temp, k, p, E=None, seed=0, offset=0, base=0, bf16=Fals
     sv.spec_verify_sample(gpu_harness.verifier(cluster, flags).handle, logits=logits, tokens=tokens, probs=probs,
                           temperature=t(temp, torch.float32), top_k=t(k, torch.int32), top_p=t(p, torch.float32),
                           exponentials=t(E, torch.float32), seed=seed, offset=offset, rng_row_base=base,
-                          status=status, test_flags=test_flags)
+                          status=status, test_flags=test_flags, hints=hints)
     torch.cuda.synchronize()
     return tokens.cpu().numpy(), probs.cpu().numpy(), int(status.item())
 
 
 def check(rows, temp, k, p, E=None, production=False, bf16=False, budget=0.05, seed=0, offset=0, base=0, cluster=0,
-          flags=0):
+          flags=0, hints=0):
     assert budget <= 0.05
     o = oracle.sample_rows(rows, temperature=temp, top_k=k, top_p=p, exponentials=E, seed=seed, offset=offset,
                            rng_row_base=base)
     tok, pr, st = run_sampler(rows, temp, k, p, E, bf16=bf16, seed=seed, offset=offset, base=base, cluster=cluster,
-                              flags=flags)
+                              flags=flags, hints=hints)
     assert st == o["status"]
     temp = np.asarray(temp)
     rnd = temp > 0
@@ -195,3 +196,79 @@ def test_sampler_with_processors(bf16, temp, resident):
     if temp > 0:
         d = np.abs(probs.cpu().numpy() - o["probs"])
         assert d.max() <= 1e-6
+
+
+# ----------------------------------------------------------------------------
+# one CTA per row (SV_FLAG_ONE_CTA_PER_REQUEST, or the small-top-k hint on a
+# batch of at least two rows per SM): the same contract
+# ----------------------------------------------------------------------------
+def _one_cta():
+    import speculative_decoding_token_rejection_gb300 as sv
+    return sv.SV_FLAG_ONE_CTA_PER_REQUEST
+
+
+@pytest.mark.parametrize("V", [151936, 5000, 4097, 13])
+def test_sampler_one_cta_per_row_fused_rows(V):
+    rows = fused_rows(64, V)
+    R = rows.shape[0]
+    E = np.random.default_rng(6).standard_exponential((R, V), dtype=np.float32)
+    temp = np.where(np.arange(R) % 9 == 4, 0.0, 0.8).astype(np.float32)
+    check(rows, temp, np.full(R, min(50, V - 1)), np.full(R, 0.9, np.float32), E, bf16=True, flags=_one_cta())
+
+
+@pytest.mark.parametrize("k,p,temp", [(0, 1.0, 1.0), (0, 0.95, 0.7), (200, 1.0, 1.3), (1, 1.0, 1.0), (256, 0.9, 0.8),
+                                      (257, 0.9, 0.8)])
+def test_sampler_one_cta_per_row_grid_fp32(k, p, temp):
+    rng = np.random.default_rng(7)
+    R, V = 48, 6000
+    rows = (rng.standard_normal((R, V)) * 2.0).astype(np.float32)
+    E = rng.standard_exponential((R, V), dtype=np.float32)
+    check(rows, np.full(R, temp, np.float32), np.full(R, k), np.full(R, p, np.float32), E, flags=_one_cta())
+
+
+def test_sampler_one_cta_per_row_greedy_and_status():
+    rng = np.random.default_rng(8)
+    rows = (rng.standard_normal((6, 300)) * 2).astype(np.float32)
+    rows[4, 17] = np.nan
+    temp = np.array([0, 1, 0, 0.5, 1, -2], np.float32)
+    E = rng.standard_exponential((6, 300), dtype=np.float32)
+    tok = check(rows, temp, np.full(6, 3), np.ones(6, np.float32), E, flags=_one_cta())
+    assert tok[4] == -1 and tok[5] == -1
+
+
+def test_sampler_one_cta_per_row_production():
+    rows = fused_rows(48, 20000)
+    R = rows.shape[0]
+    check(rows, np.full(R, 0.8, np.float32), np.full(R, 50), np.full(R, 0.9, np.float32), None, bf16=True,
+          seed=5, offset=2, base=9, flags=_one_cta())
+
+
+def test_sampler_one_cta_per_row_chi_square():
+    """Production draws of the per-row form follow the transformed row."""
+    rng = np.random.default_rng(9)
+    V, R = 7, 1_000_000
+    l = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    probs, _, _ = oracle.logits_to_probs(l, 0.7, 4, 0.9)
+    tok, _, st = run_sampler(np.tile(l, (R, 1)), np.full(R, 0.7, np.float32), np.full(R, 4),
+                             np.full(R, 0.9, np.float32), None, seed=22, offset=3, flags=_one_cta())
+    assert st == 0
+    cnt = np.bincount(tok, minlength=V)
+    e = probs.astype(np.float64)
+    assert np.all(cnt[e == 0] == 0)
+    nz = e > 0
+    assert scipy.stats.chisquare(cnt[nz], R * e[nz] / e[nz].sum()).pvalue > 0.01
+
+
+def test_sampler_forms_agree_bitwise_with_hint():
+    """512 fused rows (the bench's draft step): the hinted call takes one CTA
+    per row; tokens and probability rows equal the cluster form's bit for bit."""
+    import speculative_decoding_token_rejection_gb300 as sv
+    w = workloads.make("fused", seed=3, test_mode=False)
+    rows = w["draft"][::7][:512]
+    R = rows.shape[0]
+    args = (rows, np.full(R, 0.8, np.float32), np.full(R, 50), np.full(R, 0.9, np.float32), None)
+    t0, p0, s0 = run_sampler(*args, bf16=True, seed=4, offset=1)
+    t1, p1, s1 = run_sampler(*args, bf16=True, seed=4, offset=1, hints=sv.SV_HINT_SMALL_TOP_K)
+    assert s0 == s1 == 0
+    np.testing.assert_array_equal(t0, t1)
+    np.testing.assert_array_equal(p0, p1)

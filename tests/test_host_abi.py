@@ -203,7 +203,8 @@ def _sample_args(R=4, V=1000):
     (lambda a: (setattr(a, "exponentials", FAKE), setattr(a, "exponentials_row_stride", 1000)), sv.SV_OK),
     (lambda a: setattr(a, "test_flags", 3), sv.SV_ERR_INVALID_ARG),
     (lambda a: setattr(a, "test_flags", 1), sv.SV_OK),
-    (lambda a: setattr(a, "reserved0", 2), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "hints", 2), sv.SV_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "hints", sv.SV_HINT_SMALL_TOP_K), sv.SV_OK),
     (lambda a: (setattr(a, "num_rows", 0), setattr(a, "logits", None)), sv.SV_OK),
 ])
 def test_check_sample_args(lib, mutate, code):
