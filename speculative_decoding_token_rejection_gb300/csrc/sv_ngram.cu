@@ -4,7 +4,8 @@
 // length in [min_ngram, max_ngram] proposing the tokens that followed it).
 //
 // One CTA per request.  The CTA streams the request's history from HBM with
-// 16-byte loads, up to kLoads per thread in flight, and compares each token
+// 16-byte loads, up to kLoads per thread in flight (a longer history is first
+// prefetched into L2 in one bulk request), and compares each token
 // with the last one; only the rare equal tokens E (E <= L - 2, so a token
 // follows) start the backward comparison t[E - j] == t[L - 1 - j] against the
 // tail held in shared memory.  The CTA keeps the largest (length, E) -- the
@@ -61,6 +62,12 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
         }
       }
     };
+    // a history longer than one round warms L2 in one bulk prefetch, so the
+    // later rounds find it there instead of waiting on HBM one after another
+    if (vec && tid == 0 && ngroups > static_cast<int64_t>(kLoads) * kThreads) {
+      const int64_t gend = min(g0 + 4 * ngroups, P.total & ~static_cast<int64_t>(3));
+      if (gend > g0) prefetch_l2(P.tokens + g0, static_cast<uint32_t>((gend - g0) * 4));
+    }
     load_round(0);  // in flight together with the tail
     const int span = static_cast<int>(min(static_cast<int64_t>(P.max_n), L));
     for (int j = tid; j < span; j += kThreads) tail[j] = t[L - 1 - j];
@@ -76,6 +83,7 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
       if (vb > 0) load_round(vb);
 #pragma unroll
       for (int u = 0; u < kLoads; ++u) {
+        if (d[u].x != last && d[u].y != last && d[u].z != last && d[u].w != last) continue;  // (almost every group)
         const int64_t E0 = g0 + 4 * (vb + u * kThreads + tid) - s;
         const int32_t w[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
 #pragma unroll

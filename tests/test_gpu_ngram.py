@@ -24,10 +24,12 @@ def handle(R, k):
     return _HANDLES[key]
 
 
-def run_gpu(tokens, cu, *, min_n, max_n, k, mml):
+def run_gpu(tokens, cu, *, min_n, max_n, k, mml, misalign=0):
     dev = torch.device("cuda:0")
     R = len(cu)
-    t = torch.as_tensor(np.asarray(tokens, np.int32)).to(dev)
+    # misalign: the token buffer starts `misalign` int32 past a 16-byte boundary (plain loads, no bulk copies)
+    t = torch.as_tensor(np.concatenate([np.zeros(misalign, np.int32), np.asarray(tokens, np.int32)])).to(dev)
+    t = t[misalign:]
     c = torch.as_tensor(np.asarray(cu, np.int64)).to(dev)
     out = torch.full((R, k), -7, dtype=torch.int32, device=dev)
     num = torch.full((R,), -7, dtype=torch.int32, device=dev)
@@ -39,8 +41,8 @@ def run_gpu(tokens, cu, *, min_n, max_n, k, mml):
     return dict(draft_token_ids=out.cpu().numpy(), num_draft_tokens=num.cpu().numpy(), status=int(st.item()))
 
 
-def check(tokens, cu, **kw):
-    g = run_gpu(tokens, cu, **kw)
+def check(tokens, cu, misalign=0, **kw):
+    g = run_gpu(tokens, cu, misalign=misalign, **kw)
     o = oracle.ngram_propose(tokens, cu, min_ngram=kw["min_n"], max_ngram=kw["max_n"], k=kw["k"],
                              max_model_len=kw["mml"])
     np.testing.assert_array_equal(g["num_draft_tokens"], o["num_draft_tokens"])
@@ -103,3 +105,22 @@ def test_full_batch_sampled():
         assert g["num_draft_tokens"][q] == o["num_draft_tokens"][0]
         np.testing.assert_array_equal(g["draft_token_ids"][q], o["draft_token_ids"][0])
     assert (g["num_draft_tokens"] > 0).mean() > 0.25  # half the segments repeat: many tails were seen before
+
+
+@pytest.mark.parametrize("misalign", [0, 1, 3])
+def test_histories_across_chunks(misalign):
+    """Histories longer than one shared-memory chunk (12284 tokens), with
+    matches on both sides of every chunk boundary (a three-token alphabet),
+    through bulk copies (aligned buffer) and plain loads (misaligned)."""
+    rng = np.random.default_rng(17 + misalign)
+    lens = np.array([12283, 12284, 12285, 12290, 24570, 30001, 5, 4097])
+    tokens = rng.integers(0, 3, size=int(lens.sum())).astype(np.int32)
+    cu = np.cumsum(lens)
+    for (min_n, max_n, k) in [(8, 8, 5), (1, 20, 7), (3, 5, 3)]:
+        check(tokens, cu, misalign=misalign, min_n=min_n, max_n=max_n, k=k, mml=1 << 20)
+
+
+@pytest.mark.parametrize("misalign", [1, 2])
+def test_repetitive_histories_misaligned_buffer(misalign):
+    tokens, cu = workloads.make_histories(24, min_len=300, max_len=20000, vocab=50, p_copy=0.6, seed=5)
+    check(tokens, cu, misalign=misalign, min_n=5, max_n=5, k=7, mml=1 << 20)
