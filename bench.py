@@ -406,8 +406,8 @@ def time_processors(args, sv, lib, dev, world, rank, dist, stream, w):
     tokens: repetition penalty 1.2 over a 512-token context per request (the
     request's drafts join it as they are committed), 16 banned ids and 2 stop
     ids per request.  The kept sets are placed on the raw rows (read in place
-    unless --logits-resident) and the processors then correct the marked
-    entries they contain."""
+    unless --logits-resident) and the processors then act on the kept entries;
+    with the small-top-k hint the call takes one CTA per request."""
     import numpy as np
     import torch
     import workloads
@@ -416,8 +416,14 @@ def time_processors(args, sv, lib, dev, world, rank, dist, stream, w):
     gam = workloads.gammas_of(w)
     t = workloads.as_torch(w, dev)
     pl = {k: torch.from_numpy(v).to(dev) for k, v in processor_lists(N, V, seed=11 + 1000 * rank).items()}
-    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster,
-                      flags=sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0)
+    flags = sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0
+    if args.logits_form == "stream":
+        flags |= sv.SV_FLAG_ONE_CTA_PER_REQUEST
+    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster, flags=flags)
+    # top-k 50 is a small top-k: with the hint a batch of two requests per SM takes one CTA per request
+    hints = sv.SV_HINT_SMALL_TOP_K if args.logits_form != "cluster" else 0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    stream_form = not args.logits_resident and (args.logits_form == "stream" or (hints and N >= 2 * sms))
     K = max(3, min(args.steps, args.processor_steps))
     nacc = torch.empty((K + args.warmup, N), dtype=torch.int32, device=dev)
     out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
@@ -427,7 +433,8 @@ def time_processors(args, sv, lib, dev, world, rank, dist, stream, w):
                       num_accepted=nacc[0], status=status, seed=20240604, rng_request_base=rank * N,
                       repetition_penalty=pl["repetition_penalty"], penalty_cu=pl["penalty_cu"],
                       penalty_token_ids=pl["penalty_ids"], banned_cu=pl["banned_cu"],
-                      banned_token_ids=pl["banned_ids"], stop_cu=pl["stop_cu"], stop_token_ids=pl["stop_ids"])
+                      banned_token_ids=pl["banned_ids"], stop_cu=pl["stop_cu"], stop_token_ids=pl["stop_ids"],
+                      hints=hints)
     sptr = ctypes.c_void_p(stream.cuda_stream)
     h = ctypes.c_void_p(ver.handle)
 
@@ -448,7 +455,8 @@ def time_processors(args, sv, lib, dev, world, rank, dist, stream, w):
             "config": {"workload": f"fused: N={N} gamma={G} V={V} bf16 logits, T=0.8, top-k 50, top-p 0.9, "
                                    "repetition penalty 1.2 over 512 context ids, 16 banned ids, 2 stop ids per "
                                    "request, production Philox", "entry": "logits",
-                       "rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)"},
+                       "rows": "shared memory" if args.logits_resident else "read in place (L2 prefetch)",
+                       "form": "one CTA per request" if stream_form else "clusters"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
                          "algorithmic_bytes_per_launch": alg},

@@ -89,11 +89,15 @@ enum sv_data_status {
  * in place after an L2 prefetch (four CTAs per SM); unaligned rows are always
  * copied.  Results are identical. */
 #define SV_FLAG_RESIDENT_ROWS 1u
-/* SV_FLAG_ONE_CTA_PER_REQUEST: logits-entry and sampler calls with aligned
- * rows, no logits processors and no SV_FLAG_RESIDENT_ROWS always take the
+/* SV_FLAG_ONE_CTA_PER_REQUEST: logits-entry calls with aligned rows (with or
+ * without logits processors) and sampler calls with aligned rows and no
+ * processors, in a handle without SV_FLAG_RESIDENT_ROWS, always take the
  * one-CTA-per-request (per-row) form (see SV_HINT_SMALL_TOP_K); by default
  * the library takes it only for hinted calls with at least two requests
- * (rows) per SM.  Results are identical in both forms. */
+ * (rows) per SM.  Without processors the two forms' results are identical;
+ * with processors both stay within the tolerance of the exact definition
+ * (the one-CTA form sums the processed kept set afresh, the cluster form
+ * corrects the raw sum). */
 #define SV_FLAG_ONE_CTA_PER_REQUEST 2u
 
 /* Call hints (the hints field of spec_verify_args and spec_verify_sample_args;

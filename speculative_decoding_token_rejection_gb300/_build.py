@@ -21,7 +21,8 @@ LIB_NAME = "libspec_verify.so"
 LIB_PATH = PKG / LIB_NAME
 SOURCES = ["sv_api.cu", "sv_probs.cu", "sv_logits.cu", "sv_logits_bf16.cu", "sv_logits_f32.cu", "sv_logits_bf16_proc.cu",
            "sv_logits_f32_proc.cu", "sv_sample_bf16.cu", "sv_sample_f32.cu", "sv_sample_bf16_proc.cu",
-           "sv_sample_f32_proc.cu", "sv_stream_bf16.cu", "sv_stream_f32.cu", "sv_ngram.cu"]
+           "sv_sample_f32_proc.cu", "sv_stream_bf16.cu", "sv_stream_f32.cu",
+           "sv_stream_bf16_proc.cu", "sv_stream_f32_proc.cu", "sv_ngram.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I", str(INCLUDE), "-I", str(CSRC)]

@@ -192,7 +192,7 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, config->device);
   sv_status result = SV_OK;
   int max_cluster = 16;
-  int max_dyn = 0;
+  int max_dyn = 0, optin_all = 0;
   if (e != cudaSuccess) {
     result = fail(SV_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
   } else if (major != 10 || minor != 3) {
@@ -201,7 +201,10 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, config->device);
     max_dyn = optin - static_cast<int>(sv::logits_static_smem()) - 1024;
-    if ((e = sv::enable_stream_kernels_bf16()) != cudaSuccess || (e = sv::enable_stream_kernels_f32()) != cudaSuccess)
+    optin_all = optin;
+    if ((e = sv::enable_stream_kernels_bf16()) != cudaSuccess || (e = sv::enable_stream_kernels_f32()) != cudaSuccess ||
+        (e = sv::enable_stream_kernels_bf16_proc(optin)) != cudaSuccess ||
+        (e = sv::enable_stream_kernels_f32_proc(optin)) != cudaSuccess)
       result = fail(SV_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(e));
     if (sv::enable_probs_kernels(16) != cudaSuccess || sv::enable_logits_kernels(16, max_dyn) != cudaSuccess ||
         sv::enable_sample_kernels(16, max_dyn) != cudaSuccess) {
@@ -222,6 +225,7 @@ sv_status spec_verify_create(const spec_verify_config *config, spec_verify_t *ou
   h->num_sms = sms;
   h->max_cluster = max_cluster;
   h->max_dyn_smem = max_dyn;
+  h->max_dyn_optin = optin_all;
   h->smem_per_sm = smem_sm;
   *out = h;
   return SV_OK;
@@ -294,14 +298,19 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
     const bool vec = sv::aligned16(a->target) && (a->target_row_stride % per16 == 0) &&
                      (!a->draft || (sv::aligned16(a->draft) && a->draft_row_stride % per16 == 0));
     const bool resident = !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
-    // one CTA per request: aligned rows read in place, no processors, and
-    // either the handle asks for it or the caller states small top-k values
-    // and the batch gives every SM at least two requests
-    const bool stream_form = vec && !procs && !(h->cfg.flags & SV_FLAG_RESIDENT_ROWS) &&
+    // one CTA per request: aligned rows read in place (with processors, the
+    // row bitmaps within the shared memory a CTA may take), and either the
+    // handle asks for it or the caller states small top-k values and the
+    // batch gives every SM at least two requests
+    const bool stream_form = vec && !(h->cfg.flags & SV_FLAG_RESIDENT_ROWS) &&
+                             (!procs || sv::stream_dyn_smem(p.V, true) <= static_cast<size_t>(h->max_dyn_optin)) &&
                              ((h->cfg.flags & SV_FLAG_ONE_CTA_PER_REQUEST) ||
                               ((a->hints & SV_HINT_SMALL_TOP_K) && p.N >= 2 * h->num_sms));
     if (stream_form) {
-      e = bf16 ? sv::launch_stream_bf16(p, s) : sv::launch_stream_f32(p, s);
+      if (procs)
+        e = bf16 ? sv::launch_stream_bf16_proc(p, s) : sv::launch_stream_f32_proc(p, s);
+      else
+        e = bf16 ? sv::launch_stream_bf16(p, s) : sv::launch_stream_f32(p, s);
       if (e != cudaSuccess) return fail(SV_ERR_CUDA, "verifier launch: %s", cudaGetErrorString(e));
       return SV_OK;
     }

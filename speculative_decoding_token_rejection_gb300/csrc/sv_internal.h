@@ -12,6 +12,7 @@ struct spec_verify_ctx {
   int max_cluster;  // largest cluster size the kernels were enabled for (8 or 16)
   int max_dyn_smem; // dynamic shared memory the logits kernels may request per CTA
   int smem_per_sm;  // shared memory of one SM (for the CTAs-per-SM target of the layout)
+  int max_dyn_optin;  // dynamic shared memory a CTA without static shared memory may request
 };
 
 namespace sv {
@@ -129,6 +130,13 @@ cudaError_t enable_stream_kernels_bf16();
 cudaError_t enable_stream_kernels_f32();
 cudaError_t launch_stream_bf16(const VerifyParams &p, cudaStream_t stream);
 cudaError_t launch_stream_f32(const VerifyParams &p, cudaStream_t stream);
+// with logits processors (sv_stream_{bf16,f32}_proc.cu); max_dyn bounds the dynamic shared memory
+cudaError_t enable_stream_kernels_bf16_proc(int max_dyn);
+cudaError_t enable_stream_kernels_f32_proc(int max_dyn);
+cudaError_t launch_stream_bf16_proc(const VerifyParams &p, cudaStream_t stream);
+cudaError_t launch_stream_f32_proc(const VerifyParams &p, cudaStream_t stream);
+// dynamic shared memory of one logits-entry CTA in that form (procs: with the row bitmaps)
+size_t stream_dyn_smem(int V, bool procs);
 // the one-CTA-per-row form of the draft-side sampler (the same translation units)
 cudaError_t launch_stream_sample_bf16(const SampleParams &p, cudaStream_t stream);
 cudaError_t launch_stream_sample_f32(const SampleParams &p, cudaStream_t stream);

@@ -647,22 +647,36 @@ __device__ __noinline__ void cand_stats(StreamSmem &ss, int nr, int topk, float 
 
 // The race over the kept candidates of the target row (kResidual: of
 // max(p - q, 0), with q looked up among the draft row's candidates).
-template <typename TIn, bool kTest, bool kResidual>
+// The value bits of an order key (the inverse of Elem<TIn>::key).
+template <typename TIn>
+__device__ __forceinline__ uint32_t bits_of_key(uint32_t k) {
+  const uint32_t f = __float_as_uint(Elem<TIn>::val_of_key(k));
+  return sizeof(TIn) == 2 ? (f >> 16) : f;  // (bf16 to fp32 is exact)
+}
+
+// Weight of a kept candidate (raw key k, index x) under a row's statistics;
+// with kProc, its processed value (0 when banned).
+template <typename TIn, bool kProc>
+__device__ __forceinline__ float cand_weight(uint32_t k, int x, const RowStats &st, const Procs &pr) {
+  if (kProc) return kept_weight<TIn>(processed_bits<TIn>(bits_of_key<TIn>(k), mark_at(pr, x), pr.theta), st);
+  return exp2f(__fmul_rn(__fsub_rn(Elem<TIn>::val_of_key(k), st.vmax), st.c2));
+}
+
+template <typename TIn, bool kTest, bool kResidual, bool kProc = false>
 __device__ __noinline__ void cand_race(const StreamSmem &ss, const RowStats &ps, const RowStats &qs, const float *Erow,
-                          const RngKey &rk, uint32_t rs, float &bk, int &bx, uint32_t &flags) {
-  using E = Elem<TIn>;
+                          const RngKey &rk, uint32_t rs, float &bk, int &bx, uint32_t &flags, const Procs &pr) {
   const float rp = __frcp_rn(ps.zp), rq = __frcp_rn(qs.zp);
   for (int i = threadIdx.x; i < ss.cnt[0]; i += kThreads) {
     const uint32_t key = ss.key[0][i];
     if (key < ps.cut) continue;
     const int x = ss.idx[0][i];
-    float w = __fmul_rn(exp2f(__fmul_rn(__fsub_rn(E::val_of_key(key), ps.vmax), ps.c2)), rp);
+    float w = __fmul_rn(cand_weight<TIn, kProc>(key, x, ps, pr), rp);
     if (kResidual) {
       float q = 0.0f;
       for (int j = 0; j < ss.cnt[1]; ++j) {
         if (ss.idx[1][j] != x) continue;
         const uint32_t kq = ss.key[1][j];
-        if (kq >= qs.cut) q = __fmul_rn(exp2f(__fmul_rn(__fsub_rn(E::val_of_key(kq), qs.vmax), qs.c2)), rq);
+        if (kq >= qs.cut) q = __fmul_rn(cand_weight<TIn, kProc>(kq, x, qs, pr), rq);
         break;
       }
       w = __fsub_rn(w, q);
@@ -692,16 +706,94 @@ __device__ __noinline__ void cand_race(const StreamSmem &ss, const RowStats &ps,
   }
 }
 
+// The logits processors on the kept candidates ("vLLM source walk-through
+// (10)", section "Rejection sampling: the two branches of RejectionSampler",
+// step 2; "Speculative Decoding: propose, verify, accept", section 06): the
+// kept set stays the one the raw statistics placed; each kept candidate takes
+// its processed value (a banned one drops out), and the normaliser is summed
+// afresh over them against the largest processed kept value, in 2^-40 fixed
+// point as integers.  st[r].vmax / zp are replaced.  Returns false (a status
+// bit is set) if a kept processed value is NaN or +inf, or no unbanned entry
+// is kept.
+template <typename TIn>
+__device__ __noinline__ bool cand_process(StreamSmem &ss, int nr, const Procs &pr, RowStats st[2], uint32_t *req_bits) {
+  using E = Elem<TIn>;
+  const int tid = threadIdx.x;
+  if (tid < 2) {
+    ss.maxkey[tid] = 0u;
+    ss.flags[tid] = 0u;
+    ss.kept[tid] = 0ull;
+  }
+  __syncthreads();
+  for (int r = 0; r < nr; ++r) {
+    uint32_t mk = 0u, fl = 0u;
+    for (int i = tid; i < ss.cnt[r]; i += kThreads) {
+      const uint32_t key = ss.key[r][i];
+      if (key < st[r].cut) continue;
+      const uint32_t m = mark_at(pr, ss.idx[r][i]);
+      if (m == 1u) continue;  // banned
+      const uint32_t pb = processed_bits<TIn>(bits_of_key<TIn>(key), m, pr.theta);
+      if (!E::finite(pb)) fl |= kFlagBad;  // (finite raw values only reach here)
+      else mk = max(mk, E::key(pb) + 1u);  // +1: 0 means none
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mk = max(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
+      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+    }
+    if ((tid & 31) == 0) {
+      atomicMax(&ss.maxkey[r], mk);
+      atomicOr(&ss.flags[r], fl);
+    }
+  }
+  __syncthreads();
+  for (int r = 0; r < nr; ++r)
+    if ((ss.flags[r] & kFlagBad) || ss.maxkey[r] == 0u) {
+      *req_bits |= SV_DATA_BAD_VALUES;
+      return false;
+    }
+  for (int r = 0; r < nr; ++r) {
+    st[r].vmax = E::val_of_key(ss.maxkey[r] - 1u);
+    unsigned long long z = 0;
+    for (int i = tid; i < ss.cnt[r]; i += kThreads) {
+      const uint32_t key = ss.key[r][i];
+      if (key < st[r].cut) continue;
+      const uint32_t m = mark_at(pr, ss.idx[r][i]);
+      if (m == 1u) continue;
+      z += to_fixed(kept_weight<TIn>(processed_bits<TIn>(bits_of_key<TIn>(key), m, pr.theta), st[r]));
+    }
+    block_add_u64(z, &ss.kept[r]);
+  }
+  __syncthreads();
+  for (int r = 0; r < nr; ++r)
+    st[r].zp = static_cast<float>(static_cast<double>(ss.kept[r]) * (1.0 / static_cast<double>(kMassScale)));
+  __syncthreads();
+  return true;
+}
+
+// Dynamic shared memory of the logits-entry form: the state, then with
+// processors the banned and penalised bitmaps of the whole row and the
+// inboxes the exact statistics' processor correction exchanges through.
+__host__ __device__ constexpr size_t stream_bitmap_words(int V) { return (static_cast<size_t>(V) + 31) / 32; }
+__host__ __device__ constexpr size_t stream_dyn_bytes(int V, bool procs) {
+  return sizeof(StreamSmem) + (procs ? ((2 * stream_bitmap_words(V) * 4 + 15) & ~size_t{15}) + 2 * sizeof(Inbox) : 0);
+}
+
 // CTAs per SM of the logits-entry form: three (85 registers) measure faster
 // than four on the fused batch (0.269 against 0.291 ms); the requests beyond
 // the first wave start as the shortest walks finish.
 constexpr int kStreamCtasPerSm = 3;
 
-template <typename TIn, bool kTest>
+template <typename TIn, bool kTest, bool kProc>
 __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(const VerifyParams P) {
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   StreamSmem &ss = *reinterpret_cast<StreamSmem *>(dyn_smem);
+  const int words = static_cast<int>(stream_bitmap_words(P.V));
+  uint32_t *const pen_bits = reinterpret_cast<uint32_t *>(dyn_smem + sizeof(StreamSmem));  // (kProc only)
+  uint32_t *const ban_bits = pen_bits + words;
+  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + sizeof(StreamSmem) +
+                                                 ((2 * static_cast<size_t>(words) * 4 + 15) & ~size_t{15}));
   const int i = static_cast<int>(blockIdx.x);
   const int tid = threadIdx.x;
   const int G = P.G, V = P.V;
@@ -731,10 +823,42 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     req_bits |= SV_DATA_BAD_PARAM;
     valid = false;
   }
-  int64_t stop_b = 0, stop_e = 0;
-  if (valid && P.stop_cu && !list_range(P.stop_cu, P.stop_total, i, stop_b, stop_e)) {
+  int64_t stop_b = 0, stop_e = 0, pen_b = 0, pen_e = 0, ban_b = 0, ban_e = 0;
+  if (valid && ((P.stop_cu && !list_range(P.stop_cu, P.stop_total, i, stop_b, stop_e)) ||
+                (kProc && P.pen_cu && !list_range(P.pen_cu, P.pen_total, i, pen_b, pen_e)) ||
+                (kProc && P.ban_cu && !list_range(P.ban_cu, P.ban_total, i, ban_b, ban_e)))) {
     req_bits |= SV_DATA_BAD_LIST;
     valid = false;
+  }
+  float theta = 1.0f;
+  if (kProc && valid && P.rep_penalty) {
+    theta = P.rep_penalty[i];
+    if (!(theta > 0.0f) || isinf(theta)) {
+      req_bits |= SV_DATA_BAD_PARAM;
+      valid = false;
+    }
+  }
+  const Procs pr{pen_bits, ban_bits, theta};
+  auto mark = [&](uint32_t *bm, int32_t x) {
+    if (x >= 0 && x < V) atomicOr(&bm[x >> 5], 1u << (x & 31));
+  };
+  int added = 0;  // drafts already in the penalty bitmap
+  // position j penalises the drafts y_0 .. y_{j-1} too (they are committed by then)
+  auto add_drafts = [&](int j) {
+    if (kProc && P.rep_penalty) {
+      for (; added < j; ++added)
+        if (tid == 0) mark(pen_bits, P.ids[s + added]);
+      __syncthreads();
+    }
+  };
+  if (kProc && valid) {  // the whole row's banned and penalised keys
+    for (int w = tid; w < 2 * words; w += kThreads) pen_bits[w] = 0u;
+    __syncthreads();
+    if (P.ban_cu)
+      for (int64_t k = ban_b + tid; k < ban_e; k += kThreads) mark(ban_bits, P.ban_ids[k]);
+    if (P.rep_penalty && P.pen_cu)
+      for (int64_t k = pen_b + tid; k < pen_e; k += kThreads) mark(pen_bits, P.pen_ids[k]);
+    __syncthreads();
   }
   const bool greedy = valid && temp == 0.0f;
   int A = 0;
@@ -745,7 +869,12 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
     for (int j = 0;; ++j) {
       unsigned long long best = 0;
       uint32_t fl = 0;
-      argmax_logits<TIn, true>(tgt + (tb + j) * ts, 0, V, best, fl);
+      if (kProc) {  // the argmax of the processed row
+        add_drafts(j);
+        argmax_proc<TIn>(tgt + (tb + j) * ts, 0, V, pr, best, fl);
+      } else {
+        argmax_logits<TIn, true>(tgt + (tb + j) * ts, 0, V, best, fl);
+      }
       const KeyFlags r = cluster_reduce(KeyFlags{best, fl}, ss.red, step++, 1);
       if (r.flags & SV_DATA_BAD_VALUES) {
         req_bits |= SV_DATA_BAD_VALUES;
@@ -826,6 +955,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
         }
         TIn *const rows[2] = {const_cast<TIn *>(tgt + (tb + j) * ts),
                               nr == 2 ? const_cast<TIn *>(drf + (s + j) * ds) : nullptr};
+        add_drafts(j);
         if (cand)
           stream_pass<TIn, true>(ss, rows, nr, V, j >= 1 ? 4 : 0);
         else
@@ -850,6 +980,21 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
           const uint32_t maxk16[2] = {key16_of<TIn>(ss.maxkey[0]), key16_of<TIn>(ss.maxkey[1])};
           stats_slow<TIn>(ss.fb, rows, nr, V, c2, topk, topp, maxk16, st, step, 1);
         }
+        // the processors on the kept sets: their weights and normalisers, the draft token's marks
+        uint32_t ymark = 0u;
+        if (kProc) {
+          if (fast) {
+            if (!cand_process<TIn>(ss, nr, pr, st, &req_bits)) {
+              valid = false;
+              break;
+            }
+          } else if (!proc_correct<TIn>(ss.fb, inbox, rows, nr, V, words, pr, st,
+                                        (j < g && y >= 0 && y < V) ? y : -1, ymark, &req_bits, step, 1, 0)) {
+            valid = false;
+            break;
+          }
+          ymark = (j < g && y >= 0 && y < V) ? mark_at(pr, y) : 0u;
+        }
         float bk = 0.0f;
         int bx = -1;
         uint32_t fl = 0;
@@ -860,8 +1005,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
             valid = false;
             break;
           }
-          const float py = prob_of<TIn>(bty, st[0]);
-          const float qy = prob_of<TIn>(bdy, st[1]);
+          const float py = kProc ? prob_of_m<TIn>(bty, ymark, st[0], theta) : prob_of<TIn>(bty, st[0]);
+          const float qy = kProc ? prob_of_m<TIn>(bdy, ymark, st[1], theta) : prob_of<TIn>(bdy, st[1]);
           if (tid == 0 && !P.rates) {
             if (P.dbg_py) P.dbg_py[s + j] = py;
             if (P.dbg_qy) P.dbg_qy[s + j] = qy;
@@ -872,13 +1017,13 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
           }
           residual = true;
           if (fast)
-            cand_race<TIn, kTest, true>(ss, st[0], st[1], Erow, rk, rs, bk, bx, fl);
+            cand_race<TIn, kTest, true, kProc>(ss, st[0], st[1], Erow, rk, rs, bk, bx, fl, pr);
           else
-            race_chunks<TIn, kTest, true>(rows[0], rows[1], st[0], st[1], 0, V, Erow, rk, rs, bk, bx, fl);
+            race_chunks<TIn, kTest, true, kProc>(rows[0], rows[1], st[0], st[1], 0, V, Erow, rk, rs, bk, bx, fl, pr);
         } else if (fast) {
-          cand_race<TIn, kTest, false>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl);
+          cand_race<TIn, kTest, false, kProc>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl, pr);
         } else {
-          race_chunks<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl);
+          race_chunks<TIn, kTest, false, kProc>(rows[0], rows[1], st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl, pr);
         }
         KeyFlags r = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, ss.red, step++, 1);
         if (r.key == 0ull && residual) {  // no positive residual key: race over p with the same E
@@ -886,9 +1031,9 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
           bx = -1;
           fl = 0;
           if (fast)
-            cand_race<TIn, kTest, false>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl);
+            cand_race<TIn, kTest, false, kProc>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl, pr);
           else
-            race_chunks<TIn, kTest, false>(rows[0], rows[1], st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl);
+            race_chunks<TIn, kTest, false, kProc>(rows[0], rows[1], st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl, pr);
           const KeyFlags r2 = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, ss.red, step++, 1);
           r.key = r2.key;
           r.flags |= r2.flags;
@@ -912,12 +1057,12 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(cons
   emit_request(i, G, g, A, valid, tb, req_bits, tok, P.out, P.nacc, P.ncomp, P.slots, P.status);
 }
 
-template <typename TIn, bool kTest>
+template <typename TIn, bool kTest, bool kProc>
 cudaError_t launch_stream_one(const VerifyParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.N), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = sizeof(StreamSmem);
+  cfg.dynamicSmemBytes = stream_dyn_bytes(p.V, kProc);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (the fallback paths use cluster barriers)
@@ -926,7 +1071,7 @@ cudaError_t launch_stream_one(const VerifyParams &p, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stream_kernel<TIn, kTest>, p);
+  return cudaLaunchKernelEx(&cfg, stream_kernel<TIn, kTest, kProc>, p);
 }
 
 // The draft-side sampler in the same form: one CTA per row ("vLLM source
@@ -1000,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_sample_kernel(const Sample
         int bx = -1;
         uint32_t fl = 0;
         if (fast)
-          cand_race<TIn, kTest, false>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl);
+          cand_race<TIn, kTest, false>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl, Procs{nullptr, nullptr, 1.0f});
         else
           race_chunks<TIn, kTest, false>(row, row, st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl);
         const KeyFlags kr = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, ss.red, step++, 1);
@@ -1061,25 +1206,28 @@ cudaError_t launch_stream_sample_one(const SampleParams &p, cudaStream_t stream)
   return cudaLaunchKernelEx(&cfg, stream_sample_kernel<TIn, kTest>, p);
 }
 
-template <typename TIn>
-cudaError_t enable_type_stream() {
-  const int dyn = static_cast<int>(sizeof(StreamSmem));
+// max_dyn: the dynamic shared memory the processor form may request (its row bitmaps grow with V)
+template <typename TIn, bool kProc>
+cudaError_t enable_type_stream(int max_dyn) {
+  const int dyn = kProc ? max_dyn : static_cast<int>(sizeof(StreamSmem));
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(stream_kernel<TIn, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
+  if ((e = cudaFuncSetAttribute(stream_kernel<TIn, true, kProc>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
       cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(stream_kernel<TIn, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) !=
-      cudaSuccess)
+  if ((e = cudaFuncSetAttribute(stream_kernel<TIn, false, kProc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                dyn)) != cudaSuccess)
     return e;
+  if (kProc) return cudaSuccess;
   if ((e = cudaFuncSetAttribute(stream_sample_kernel<TIn, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 dyn)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(stream_sample_kernel<TIn, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
 }
 
-template <typename TIn>
+template <typename TIn, bool kProc>
 cudaError_t launch_type_stream(const VerifyParams &p, cudaStream_t stream) {
-  return p.exponentials != nullptr ? launch_stream_one<TIn, true>(p, stream) : launch_stream_one<TIn, false>(p, stream);
+  return p.exponentials != nullptr ? launch_stream_one<TIn, true, kProc>(p, stream)
+                                   : launch_stream_one<TIn, false, kProc>(p, stream);
 }
 
 template <typename TIn>

@@ -1,0 +1,13 @@
+// sv_stream_bf16_proc.cu -- the one-CTA-per-request form of the logits entry
+// for bf16 logits, calls with logits processors (templates in sv_stream.cuh).
+#include "sv_stream.cuh"
+
+namespace sv {
+
+cudaError_t enable_stream_kernels_bf16_proc(int max_dyn) { return enable_type_stream<uint16_t, true>(max_dyn); }
+
+cudaError_t launch_stream_bf16_proc(const VerifyParams &p, cudaStream_t stream) {
+  return launch_type_stream<uint16_t, true>(p, stream);
+}
+
+}  // namespace sv

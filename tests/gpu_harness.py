@@ -30,9 +30,15 @@ def processor_args(w, dev):
     return out
 
 
+# handle flags OR-ed into every run_gpu call (a test module sets it to rerun
+# other modules' cases in another form of the kernels)
+EXTRA_FLAGS = 0
+
+
 def run_gpu(w, *, production=False, seed=0, offset=0, rng_request_base=0, cluster_ctas=0, stream=None,
             synthetic_rates=None, flags=0, test_flags=0, hints=0):
     """Run the CUDA path on workload ``w``; returns numpy results like oracle.verify."""
+    flags |= EXTRA_FLAGS
     dev = torch.device("cuda:0")
     t = workloads.as_torch(w, dev)
     N, G, T = w["N"], w["gamma"], w["T"]

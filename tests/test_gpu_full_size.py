@@ -75,14 +75,18 @@ def test_logits_entry_bench_batch(form):
     assert np.all((A >= 0) & (A <= w["gamma"]))
 
 
-def test_logits_processors_bench_batch():
+@pytest.mark.parametrize("form", ["cluster", "stream"])
+def test_logits_processors_bench_batch(form):
     """The fused logits batch with the bench's processors (repetition
-    penalty 1.2 over 512 context ids, 16 banned and 2 stop ids per request):
-    every one of the 512 requests against the oracle."""
+    penalty 1.2 over 512 context ids, 16 banned and 2 stop ids per request),
+    in both forms (the small-top-k hint the bench passes selects one CTA per
+    request): every one of the 512 requests against the oracle."""
     import bench
+    import speculative_decoding_token_rejection_gb300 as sv
     w = dict(fused_logits())
     w.update(bench.processor_lists(w["N"], w["V"], seed=11))
-    g = H().run_gpu(w, production=True, seed=20240604, offset=2)
+    hints = sv.SV_HINT_SMALL_TOP_K if form == "stream" else 0
+    g = H().run_gpu(w, production=True, seed=20240604, offset=2, hints=hints)
     o = oracle.verify_parallel(w, production=True, seed=20240604, offset=2)
     n_ex = compare(g, o, w, production=True)
     print(f"processors batch: {n_ex} of {w['N']} requests exempted")

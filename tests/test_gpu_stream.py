@@ -160,12 +160,49 @@ def test_stream_status_cases():
     H().assert_same(run(w), o, check_dbg=False)
 
 
-def test_stream_flag_with_processors_is_exact():
-    """Calls with logits processors take the cluster form under the flag."""
+def test_stream_processors_bench_lists():
+    """The bench's processors (repetition penalty over 512 context ids, 16
+    banned and 2 stop ids per request) in the one-CTA form."""
     import bench
     w = dict(workloads.make("fused", N=16, V=12000))
     w.update(bench.processor_lists(w["N"], w["V"], seed=5))
     compare(run(w), oracle.verify(w), w)
+
+
+@pytest.fixture
+def one_cta_everywhere():
+    import gpu_harness
+    import speculative_decoding_token_rejection_gb300 as sv
+    gpu_harness.EXTRA_FLAGS = sv.SV_FLAG_ONE_CTA_PER_REQUEST
+    yield
+    gpu_harness.EXTRA_FLAGS = 0
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("test_random_logits_with_processors", dict(dtype="bf16", theta=1.3)),
+    ("test_random_logits_with_processors", dict(dtype="f32", theta=0.7)),
+    ("test_greedy_with_processors_exact", {}),
+    ("test_ragged_production_with_processors", {}),
+    ("test_processors_statistics_paths", dict(top_k=50, top_p=0.9, temp=0.8, V=151936, cluster=0)),
+    ("test_processors_statistics_paths", dict(top_k=0, top_p=0.9, temp=0.8, V=151936, cluster=0)),
+    ("test_processors_statistics_paths", dict(top_k=2000, top_p=1.0, temp=0.8, V=30000, cluster=0)),
+    ("test_processed_keys_win_races_and_windows", dict(top_k=50, top_p=0.9)),
+    ("test_synthetic_mode_with_processors", {}),
+    ("test_list_and_theta_errors", {}),
+    ("test_everything_banned_is_bad_values", {}),
+    ("test_order_golden_cases", dict(resident=False)),
+    ("test_banned_maximum_far_above_the_rest", dict(resident=False)),
+    ("test_penalty_raising_past_the_fp32_range", {}),
+    ("test_banned_nucleus_is_bad_values", {}),
+])
+def test_stream_processor_cases(name, kw, one_cta_everywhere):
+    """The processor cases of test_gpu_processors.py, rerun with every call in
+    the one-CTA form: the kept set from the raw candidates, the processed kept
+    candidates summed afresh (or, off the candidate path, the exact statistics'
+    correction), the draft token's marks, the race over processed weights, and
+    greedy rows' argmax over the processed row."""
+    import test_gpu_processors
+    getattr(test_gpu_processors, name)(**kw)
 
 
 def test_stream_and_cluster_forms_agree_bitwise():
