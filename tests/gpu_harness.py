@@ -12,7 +12,7 @@ _VERIFIERS = {}
 def verifier(cluster_ctas=0, flags=0):
     key = (cluster_ctas, flags)
     if key not in _VERIFIERS:
-        _VERIFIERS[key] = sv.Verifier(1 << 20, sv.SV_MAX_SPEC_LEN, 1 << 18, device=0, cluster_ctas=cluster_ctas,
+        _VERIFIERS[key] = sv.Verifier(1 << 20, sv.SV_MAX_SPEC_LEN, 1 << 19, device=0, cluster_ctas=cluster_ctas,
                                       flags=flags)
     return _VERIFIERS[key]
 

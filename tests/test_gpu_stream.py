@@ -217,3 +217,21 @@ def test_stream_and_cluster_forms_agree_bitwise():
     np.testing.assert_array_equal(a["dbg_py"], b["dbg_py"])
     np.testing.assert_array_equal(a["dbg_qy"], b["dbg_qy"])
     assert a["status"] == b["status"] == 0
+
+
+@pytest.mark.parametrize("V", [262144, 262152])
+def test_stream_block_capacity_edge(V):
+    """bf16 rows of exactly the block maxima's room (32 steps, 4096 blocks per
+    row) take the candidate path; 8 logits more leave it for the exact
+    statistics."""
+    w = workloads.make("fused", N=4, V=V, seed=47)
+    compare(run(w), oracle.verify(w), w)
+
+
+def test_stream_processors_at_the_capacity_edge():
+    """Processors with row bitmaps of a 262144-logit vocabulary (64 KB per
+    CTA)."""
+    import bench
+    w = dict(workloads.make("fused", N=4, V=262144, seed=48))
+    w.update(bench.processor_lists(w["N"], w["V"], seed=6))
+    compare(run(w), oracle.verify(w), w)
