@@ -428,15 +428,25 @@ __device__ __forceinline__ void gather_candidates(StreamSmem &ss, const TIn *con
       em[k] = 0u;
       if (gg[k] < 0) continue;
       const int r = rr[k];
-      const uint32_t gm = word_top<TIn>(max_word<TIn>(max_word<TIn>(d[k].x, d[k].y), max_word<TIn>(d[k].z, d[k].w)));
-      if (key16_of_bits<TIn>(gm) < (r ? lim[1] : lim[0])) continue;
       const uint32_t tk = (r ? f16[1] : f16[0]) << (E::kBits - 16);
+      if constexpr (sizeof(TIn) == 2) {
+        // two elements per packed compare against the floor's value (NaN fails;
+        // a -0.0 may pass a +0.0 floor: an extra candidate below the floor,
+        // which the exact selection that follows ignores)
+        uint32_t t2 = bf16_bits_of_key(tk);
+        t2 |= t2 << 16;
+        const uint32_t m0 = bf16x2_ge_mask(d[k].x, t2), m1 = bf16x2_ge_mask(d[k].y, t2);
+        const uint32_t m2 = bf16x2_ge_mask(d[k].z, t2), m3 = bf16x2_ge_mask(d[k].w, t2);
+        em[k] = (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
+                ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
+      } else {
+        const uint32_t gm = word_top<TIn>(max_word<TIn>(max_word<TIn>(d[k].x, d[k].y), max_word<TIn>(d[k].z, d[k].w)));
+        if (key16_of_bits<TIn>(gm) < (r ? lim[1] : lim[0])) continue;
 #pragma unroll
-      for (int t = 0; t < kPer; ++t) {
-        const int wi = sizeof(TIn) == 2 ? t >> 1 : t;
-        const uint32_t wv = wi == 0 ? d[k].x : wi == 1 ? d[k].y : wi == 2 ? d[k].z : d[k].w;
-        const uint32_t bb = sizeof(TIn) == 2 ? ((t & 1) ? (wv >> 16) : (wv & 0xFFFFu)) : wv;
-        if (!E::is_nan(bb) && E::key(bb) >= tk) em[k] |= 1u << t;
+        for (int t = 0; t < kPer; ++t) {
+          const uint32_t bb = t == 0 ? d[k].x : t == 1 ? d[k].y : t == 2 ? d[k].z : d[k].w;
+          if (!E::is_nan(bb) && E::key(bb) >= tk) em[k] |= 1u << t;
+        }
       }
       cnt += static_cast<uint32_t>(__popc(em[k])) << (16 * r);
     }
