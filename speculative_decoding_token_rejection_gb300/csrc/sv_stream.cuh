@@ -329,11 +329,15 @@ __device__ __forceinline__ void gather_candidates(StreamSmem &ss, const TIn *con
   const uint32_t m16[2] = {ss.maxkey[0] >> (E::kBits - 16), ss.maxkey[1] >> (E::kBits - 16)};
   for (int t = tid; t < 512; t += kThreads) ss.hist[t >> 8][t & 255] = 0u;
   __syncthreads();
-  for (int r = 0; r < nr; ++r)
-    for (int b = tid; b < nb; b += kThreads) {
-      const uint32_t d = m16[r] - ss.bm[r][b];  // (every block maximum is at most the row's)
-      if (d < 256u) atomicAdd(&ss.hist[r][d], 1u);
+  for (int r = 0; r < nr; ++r) {
+    const uint32_t *const bm2 = reinterpret_cast<const uint32_t *>(ss.bm[r]);  // two block maxima per word
+    for (int b = tid; b < nb / 2; b += kThreads) {
+      const uint32_t two = bm2[b];
+      const uint32_t d0 = m16[r] - (two & 0xFFFFu), d1 = m16[r] - (two >> 16);  // (no block maximum exceeds the row's)
+      if (d0 < 256u) atomicAdd(&ss.hist[r][d0], 1u);
+      if (d1 < 256u) atomicAdd(&ss.hist[r][d1], 1u);
     }
+  }
   __syncthreads();
   if (warp < nr) {  // one warp per row walks the distances from 0
     const int r = warp;
