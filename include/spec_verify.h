@@ -89,9 +89,9 @@ enum sv_data_status {
  * in place after an L2 prefetch (four CTAs per SM); unaligned rows are always
  * copied.  Results are identical. */
 #define SV_FLAG_RESIDENT_ROWS 1u
-/* SV_FLAG_ONE_CTA_PER_REQUEST: logits-entry calls with aligned rows (with or
- * without logits processors) and sampler calls with aligned rows and no
- * processors, in a handle without SV_FLAG_RESIDENT_ROWS, always take the
+/* SV_FLAG_ONE_CTA_PER_REQUEST: logits-entry and sampler calls with aligned
+ * rows (with or without logits processors), in a handle without
+ * SV_FLAG_RESIDENT_ROWS, always take the
  * one-CTA-per-request (per-row) form (see SV_HINT_SMALL_TOP_K); by default
  * the library takes it only for hinted calls with at least two requests
  * (rows) per SM.  Without processors the two forms' results are identical;

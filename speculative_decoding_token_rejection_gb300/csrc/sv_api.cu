@@ -392,10 +392,13 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   // are read where they lie
   const bool resident = !vec || (h->cfg.flags & SV_FLAG_RESIDENT_ROWS);
   // one CTA per row: the handle flag, or the small-top-k hint on a batch of at least two rows per SM
-  if (vec && !procs && !(h->cfg.flags & SV_FLAG_RESIDENT_ROWS) &&
+  // (with processors, when the row bitmaps fit a CTA's shared memory)
+  if (vec && !(h->cfg.flags & SV_FLAG_RESIDENT_ROWS) &&
+      (!procs || sv::stream_dyn_smem(p.V, true) <= static_cast<size_t>(h->max_dyn_optin)) &&
       ((h->cfg.flags & SV_FLAG_ONE_CTA_PER_REQUEST) || ((a->hints & SV_HINT_SMALL_TOP_K) && p.R >= 2 * h->num_sms))) {
-    const cudaError_t e = bf16 ? sv::launch_stream_sample_bf16(p, static_cast<cudaStream_t>(stream))
-                               : sv::launch_stream_sample_f32(p, static_cast<cudaStream_t>(stream));
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = procs ? (bf16 ? sv::launch_stream_sample_bf16_proc(p, cs) : sv::launch_stream_sample_f32_proc(p, cs))
+                                : (bf16 ? sv::launch_stream_sample_bf16(p, cs) : sv::launch_stream_sample_f32(p, cs));
     if (e != cudaSuccess) return fail(SV_ERR_CUDA, "sampler launch: %s", cudaGetErrorString(e));
     return SV_OK;
   }

@@ -135,6 +135,8 @@ cudaError_t enable_stream_kernels_bf16_proc(int max_dyn);
 cudaError_t enable_stream_kernels_f32_proc(int max_dyn);
 cudaError_t launch_stream_bf16_proc(const VerifyParams &p, cudaStream_t stream);
 cudaError_t launch_stream_f32_proc(const VerifyParams &p, cudaStream_t stream);
+cudaError_t launch_stream_sample_bf16_proc(const SampleParams &p, cudaStream_t stream);
+cudaError_t launch_stream_sample_f32_proc(const SampleParams &p, cudaStream_t stream);
 // dynamic shared memory of one logits-entry CTA in that form (procs: with the row bitmaps)
 size_t stream_dyn_smem(int V, bool procs);
 // the one-CTA-per-row form of the draft-side sampler (the same translation units)

@@ -1096,7 +1096,7 @@ cudaError_t launch_stream_one(const VerifyParams &p, cudaStream_t stream) {
 // transformed fp32 row, if asked for, is written from a second read of the
 // row (from L2).  Rows outside the candidate path take the exact statistics
 // and the race over the whole row.  The same results as sample_kernel.
-template <typename TIn, bool kTest>
+template <typename TIn, bool kTest, bool kProc>
 __global__ void __launch_bounds__(kThreads, 4) stream_sample_kernel(const SampleParams P) {
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
@@ -1106,16 +1106,54 @@ __global__ void __launch_bounds__(kThreads, 4) stream_sample_kernel(const Sample
   const int V = P.V;
   TIn *const row = const_cast<TIn *>(static_cast<const TIn *>(P.logits) + static_cast<int64_t>(r) * P.row_stride);
   TIn *const rows[2] = {row, row};
+  // with processors: the row's banned and penalised bitmaps, then the inboxes (as the logits entry)
+  const int words = static_cast<int>(stream_bitmap_words(V));
+  uint32_t *const pen_bits = reinterpret_cast<uint32_t *>(dyn_smem + sizeof(StreamSmem));
+  uint32_t *const ban_bits = pen_bits + words;
+  Inbox *const inbox = reinterpret_cast<Inbox *>(dyn_smem + sizeof(StreamSmem) +
+                                                 ((2 * static_cast<size_t>(words) * 4 + 15) & ~size_t{15}));
   uint32_t bits = 0;
   int32_t token = -1;
   int step = 0;
   const float temp = P.temperature ? P.temperature[r] : 1.0f;
-  if (!temperature_ok(temp)) {
-    bits |= SV_DATA_BAD_PARAM;
+  bool ok = temperature_ok(temp);
+  if (!ok) bits |= SV_DATA_BAD_PARAM;
+  int64_t pen_b = 0, pen_e = 0, ban_b = 0, ban_e = 0;
+  if (kProc && ok && ((P.pen_cu && !list_range(P.pen_cu, P.pen_total, r, pen_b, pen_e)) ||
+                      (P.ban_cu && !list_range(P.ban_cu, P.ban_total, r, ban_b, ban_e)))) {
+    bits |= SV_DATA_BAD_LIST;
+    ok = false;
+  }
+  float theta = 1.0f;
+  if (kProc && ok && P.rep_penalty) {
+    theta = P.rep_penalty[r];
+    if (!(theta > 0.0f) || isinf(theta)) {
+      bits |= SV_DATA_BAD_PARAM;
+      ok = false;
+    }
+  }
+  const Procs pr{pen_bits, ban_bits, theta};
+  if (kProc && ok) {  // the row's banned and penalised keys
+    auto mark = [&](uint32_t *bm, int32_t x) {
+      if (x >= 0 && x < V) atomicOr(&bm[x >> 5], 1u << (x & 31));
+    };
+    for (int w = tid; w < 2 * words; w += kThreads) pen_bits[w] = 0u;
+    __syncthreads();
+    if (P.ban_cu)
+      for (int64_t k = ban_b + tid; k < ban_e; k += kThreads) mark(ban_bits, P.ban_ids[k]);
+    if (P.rep_penalty && P.pen_cu)
+      for (int64_t k = pen_b + tid; k < pen_e; k += kThreads) mark(pen_bits, P.pen_ids[k]);
+    __syncthreads();
+  }
+  if (!ok) {
+    // nothing sampled
   } else if (temp == 0.0f) {
     unsigned long long best = 0;
     uint32_t fl = 0;
-    argmax_logits<TIn, true>(row, 0, V, best, fl);
+    if (kProc)  // the argmax of the processed row
+      argmax_proc<TIn>(row, 0, V, pr, best, fl);
+    else
+      argmax_logits<TIn, true>(row, 0, V, best, fl);
     const KeyFlags kr = cluster_reduce(KeyFlags{best, fl}, ss.red, step++, 1);
     if (kr.flags & SV_DATA_BAD_VALUES) bits |= SV_DATA_BAD_VALUES;
     else token = static_cast<int32_t>(key_index(kr.key));
@@ -1152,47 +1190,65 @@ __global__ void __launch_bounds__(kThreads, 4) stream_sample_kernel(const Sample
           const uint32_t maxk16[2] = {key16_of<TIn>(ss.maxkey[0]), key16_of<TIn>(ss.maxkey[0])};
           stats_slow<TIn>(ss.fb, rows, 1, V, st[0].c2, topk, topp, maxk16, st, step, 1);
         }
-        const RngKey rk{P.seed_lo, P.seed_hi ^ 0x53414D50u, P.off_lo, P.off_hi};  // the sampler's own streams
-        const uint32_t rs = P.row_base + static_cast<uint32_t>(r);
-        const float *Erow = kTest ? P.exponentials + static_cast<int64_t>(r) * P.exp_stride : nullptr;
-        float bk = 0.0f;
-        int bx = -1;
-        uint32_t fl = 0;
-        if (fast)
-          cand_race<TIn, kTest, false>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl, Procs{nullptr, nullptr, 1.0f});
-        else
-          race_chunks<TIn, kTest, false>(row, row, st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl);
-        const KeyFlags kr = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, ss.red, step++, 1);
-        bits |= kr.flags;
-        if (kr.key == 0ull) {
-          bits |= SV_DATA_EMPTY_DISTRIBUTION;
-          token = 0;
-        } else {
-          token = static_cast<int32_t>(key_index(kr.key));
+        bool live = true;  // (false: the processors left no distribution; the status bit is set)
+        if (kProc) {
+          uint32_t ymark = 0u;
+          live = fast ? cand_process<TIn>(ss, 1, pr, st, &bits)
+                      : proc_correct<TIn>(ss.fb, inbox, rows, 1, V, words, pr, st, -1, ymark, &bits, step, 1, 0);
         }
-        if (P.probs) {  // the transformed row
-          float *prow = P.probs + static_cast<int64_t>(r) * P.probs_stride;
-          int xs = 0;
-          if (sizeof(TIn) == 2 && (reinterpret_cast<uintptr_t>(prow) & 15u) == 0) {
-            // eight bf16 logits in, two float4 probabilities out
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
-            float4 *p4 = reinterpret_cast<float4 *>(prow);
-            const int ng = V >> 3;
-            for (int v = tid; v < ng; v += kThreads) {
-              const uint4 d = ld_stream_u4(s4 + v);
-              const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-              float o[8];
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                o[2 * t] = prob_of<TIn>(w[t] & 0xFFFFu, st[0]);
-                o[2 * t + 1] = prob_of<TIn>(w[t] >> 16, st[0]);
-              }
-              p4[2 * v] = make_float4(o[0], o[1], o[2], o[3]);
-              p4[2 * v + 1] = make_float4(o[4], o[5], o[6], o[7]);
-            }
-            xs = ng << 3;
+        if (live) {
+          const RngKey rk{P.seed_lo, P.seed_hi ^ 0x53414D50u, P.off_lo, P.off_hi};  // the sampler's own streams
+          const uint32_t rs = P.row_base + static_cast<uint32_t>(r);
+          const float *Erow = kTest ? P.exponentials + static_cast<int64_t>(r) * P.exp_stride : nullptr;
+          float bk = 0.0f;
+          int bx = -1;
+          uint32_t fl = 0;
+          if (fast)
+            cand_race<TIn, kTest, false, kProc>(ss, st[0], st[0], Erow, rk, rs, bk, bx, fl, pr);
+          else
+            race_chunks<TIn, kTest, false, kProc>(row, row, st[0], st[0], 0, V, Erow, rk, rs, bk, bx, fl, pr);
+          const KeyFlags kr = cluster_reduce(KeyFlags{bx >= 0 ? pack_key(bk, bx) : 0ull, fl}, ss.red, step++, 1);
+          bits |= kr.flags;
+          if (kr.key == 0ull) {
+            bits |= SV_DATA_EMPTY_DISTRIBUTION;
+            token = 0;
+          } else {
+            token = static_cast<int32_t>(key_index(kr.key));
           }
-          for (int x = xs + tid; x < V; x += kThreads) prow[x] = prob_of<TIn>(bits_at(row, x), st[0]);
+          if (P.probs) {  // the transformed row
+            float *prow = P.probs + static_cast<int64_t>(r) * P.probs_stride;
+            int xs = 0;
+            if (sizeof(TIn) == 2 && (reinterpret_cast<uintptr_t>(prow) & 15u) == 0) {
+              // eight bf16 logits in, two float4 probabilities out
+              const uint4 *s4 = reinterpret_cast<const uint4 *>(row);
+              float4 *p4 = reinterpret_cast<float4 *>(prow);
+              const int ng = V >> 3;
+              for (int v = tid; v < ng; v += kThreads) {
+                const uint4 d = ld_stream_u4(s4 + v);
+                const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+                float o[8];
+  #pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  o[2 * t] = prob_of<TIn>(w[t] & 0xFFFFu, st[0]);
+                  o[2 * t + 1] = prob_of<TIn>(w[t] >> 16, st[0]);
+                }
+                if (kProc) {  // marked entries: their processed probabilities
+                  uint32_t mk = group_marks<8>(pr, 8 * v);
+                  while (mk) {
+                    const int t = __ffs(mk) - 1;
+                    mk &= mk - 1u;
+                    o[t] = prob_of_m<TIn>((w[t >> 1] >> (16 * (t & 1))) & 0xFFFFu, mark_at(pr, 8 * v + t), st[0], theta);
+                  }
+                }
+                p4[2 * v] = make_float4(o[0], o[1], o[2], o[3]);
+                p4[2 * v + 1] = make_float4(o[4], o[5], o[6], o[7]);
+              }
+              xs = ng << 3;
+            }
+            for (int x = xs + tid; x < V; x += kThreads)
+              prow[x] = kProc ? prob_of_m<TIn>(bits_at(row, x), mark_at(pr, x), st[0], theta)
+                              : prob_of<TIn>(bits_at(row, x), st[0]);
+          }
         }
       }
     }
@@ -1203,12 +1259,12 @@ __global__ void __launch_bounds__(kThreads, 4) stream_sample_kernel(const Sample
   }
 }
 
-template <typename TIn, bool kTest>
+template <typename TIn, bool kTest, bool kProc>
 cudaError_t launch_stream_sample_one(const SampleParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.R), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = sizeof(StreamSmem);
+  cfg.dynamicSmemBytes = stream_dyn_bytes(p.V, kProc);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (the exact statistics use cluster barriers)
@@ -1217,7 +1273,7 @@ cudaError_t launch_stream_sample_one(const SampleParams &p, cudaStream_t stream)
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stream_sample_kernel<TIn, kTest>, p);
+  return cudaLaunchKernelEx(&cfg, stream_sample_kernel<TIn, kTest, kProc>, p);
 }
 
 // max_dyn: the dynamic shared memory the processor form may request (its row bitmaps grow with V)
@@ -1231,11 +1287,11 @@ cudaError_t enable_type_stream(int max_dyn) {
   if ((e = cudaFuncSetAttribute(stream_kernel<TIn, false, kProc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 dyn)) != cudaSuccess)
     return e;
-  if (kProc) return cudaSuccess;
-  if ((e = cudaFuncSetAttribute(stream_sample_kernel<TIn, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((e = cudaFuncSetAttribute(stream_sample_kernel<TIn, true, kProc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 dyn)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(stream_sample_kernel<TIn, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  return cudaFuncSetAttribute(stream_sample_kernel<TIn, false, kProc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              dyn);
 }
 
 template <typename TIn, bool kProc>
@@ -1244,10 +1300,10 @@ cudaError_t launch_type_stream(const VerifyParams &p, cudaStream_t stream) {
                                    : launch_stream_one<TIn, false, kProc>(p, stream);
 }
 
-template <typename TIn>
+template <typename TIn, bool kProc>
 cudaError_t launch_type_stream_sample(const SampleParams &p, cudaStream_t stream) {
-  return p.exponentials != nullptr ? launch_stream_sample_one<TIn, true>(p, stream)
-                                   : launch_stream_sample_one<TIn, false>(p, stream);
+  return p.exponentials != nullptr ? launch_stream_sample_one<TIn, true, kProc>(p, stream)
+                                   : launch_stream_sample_one<TIn, false, kProc>(p, stream);
 }
 
 }  // namespace

@@ -12,7 +12,7 @@ cudaError_t launch_stream_bf16(const VerifyParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_stream_sample_bf16(const SampleParams &p, cudaStream_t stream) {
-  return launch_type_stream_sample<uint16_t>(p, stream);
+  return launch_type_stream_sample<uint16_t, false>(p, stream);
 }
 
 size_t stream_dyn_smem(int V, bool procs) { return stream_dyn_bytes(V, procs); }

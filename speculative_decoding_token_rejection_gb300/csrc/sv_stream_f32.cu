@@ -12,7 +12,7 @@ cudaError_t launch_stream_f32(const VerifyParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_stream_sample_f32(const SampleParams &p, cudaStream_t stream) {
-  return launch_type_stream_sample<float>(p, stream);
+  return launch_type_stream_sample<float, false>(p, stream);
 }
 
 }  // namespace sv

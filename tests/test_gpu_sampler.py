@@ -148,14 +148,14 @@ def _proc_lists(R, V, rng):
     return out
 
 
-@pytest.mark.parametrize("resident", [False, True])
+@pytest.mark.parametrize("form", ["in_place", "resident", "one_cta"])
 @pytest.mark.parametrize("bf16", [True, False])
 @pytest.mark.parametrize("temp", [0.0, 0.8])
-def test_sampler_with_processors(bf16, temp, resident):
+def test_sampler_with_processors(bf16, temp, form):
     """Banned tokens and the repetition penalty per row, against the oracle,
-    with the rows read in place or copied into shared memory: tokens exact
-    (outside the tolerance band of the race) and the written q rows within
-    1e-6."""
+    with the rows read in place or copied into shared memory by a cluster per
+    row, or by one CTA per row: tokens exact (outside the tolerance band of
+    the race) and the written q rows within 1e-6."""
     import torch
     import speculative_decoding_token_rejection_gb300 as sv
     rng = np.random.default_rng(int(bf16) + 2)
@@ -176,7 +176,8 @@ def test_sampler_with_processors(bf16, temp, resident):
     tok = torch.full((R,), -7, dtype=torch.int32, device=dev)
     probs = torch.zeros((R, V), dtype=torch.float32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    h = sv.spec_verify_create(R, 1, V, device=0, flags=sv.SV_FLAG_RESIDENT_ROWS if resident else 0)
+    flags = {"in_place": 0, "resident": sv.SV_FLAG_RESIDENT_ROWS, "one_cta": sv.SV_FLAG_ONE_CTA_PER_REQUEST}[form]
+    h = sv.spec_verify_create(R, 1, V, device=0, flags=flags)
     try:
         T = lambda x, dt: torch.as_tensor(x).to(dev)
         sv.spec_verify_sample(h, logits=t, tokens=tok, probs=probs, exponentials=torch.from_numpy(E).to(dev),
