@@ -75,7 +75,17 @@ def parse_args():
     ap.add_argument("--synthetic-steps", type=int, default=1000)
     ap.add_argument("--no-next", action="store_true",
                     help="skip the draft-side sampler, processors and synthetic-acceptance objects")
-    return ap.parse_args()
+    ap.add_argument("--serial-launch", action="store_true",
+                    help="create every handle with SV_FLAG_SERIAL_LAUNCH (plain stream order; comparison runs)")
+    args = ap.parse_args()
+    global LAUNCH_FLAGS
+    if args.serial_launch:
+        LAUNCH_FLAGS = 4  # SV_FLAG_SERIAL_LAUNCH (checked against the binding in main)
+    return args
+
+
+# flags OR-ed into every handle the bench creates (SV_FLAG_SERIAL_LAUNCH under --serial-launch)
+LAUNCH_FLAGS = 0
 
 
 def measured_peak():
@@ -225,7 +235,7 @@ def time_logits_entry(args, sv, lib, dev, world, rank, dist, stream, top_k=50, t
     w = dict(w, top_k=np.full(N, top_k, np.int32), top_p=np.full(N, top_p, np.float32))
     gam = workloads.gammas_of(w)
     t = workloads.as_torch(w, dev)
-    flags = sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0
+    flags = (sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0) | LAUNCH_FLAGS
     if args.logits_form == "stream":
         flags |= sv.SV_FLAG_ONE_CTA_PER_REQUEST
     ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster, flags=flags)
@@ -340,7 +350,7 @@ def time_sampler(args, sv, dev, world, rank, dist, stream, w, write_q):
     tokens = torch.empty((N,), dtype=torch.int32, device=dev)
     probs = torch.empty((N, V), dtype=torch.float32, device=dev) if write_q else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    h = sv.spec_verify_create(N, 1, V, device=dev.index, cluster_ctas=args.cluster)
+    h = sv.spec_verify_create(N, 1, V, device=dev.index, cluster_ctas=args.cluster, flags=LAUNCH_FLAGS)
     lib = sv.load_library()
     sptr = ctypes.c_void_p(stream.cuda_stream)
     # the caller knows its sampling parameters: top-k 50 is a small top-k (one CTA per row on a large batch)
@@ -348,7 +358,7 @@ def time_sampler(args, sv, dev, world, rank, dist, stream, w, write_q):
     flags_f = sv.SV_FLAG_ONE_CTA_PER_REQUEST if args.logits_form == "stream" else 0
     if flags_f:
         sv.spec_verify_destroy(h)
-        h = sv.spec_verify_create(N, 1, V, device=dev.index, cluster_ctas=args.cluster, flags=flags_f)
+        h = sv.spec_verify_create(N, 1, V, device=dev.index, cluster_ctas=args.cluster, flags=flags_f | LAUNCH_FLAGS)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     stream_form = bool(flags_f) or (bool(hints) and N >= 2 * sms)
     built = [sv.build_sample_args(logits=draft[:, j, :], tokens=tokens, probs=probs, temperature=temp,
@@ -416,7 +426,7 @@ def time_processors(args, sv, lib, dev, world, rank, dist, stream, w):
     gam = workloads.gammas_of(w)
     t = workloads.as_torch(w, dev)
     pl = {k: torch.from_numpy(v).to(dev) for k, v in processor_lists(N, V, seed=11 + 1000 * rank).items()}
-    flags = sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0
+    flags = (sv.SV_FLAG_RESIDENT_ROWS if args.logits_resident else 0) | LAUNCH_FLAGS
     if args.logits_form == "stream":
         flags |= sv.SV_FLAG_ONE_CTA_PER_REQUEST
     ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster, flags=flags)
@@ -476,7 +486,7 @@ def time_synthetic(args, sv, lib, dev, world, rank, dist, stream, t, gammas, N, 
     import torch
     rates = torch.tensor(SYNTHETIC_RATES[:G] + [0.0] * max(0, G - len(SYNTHETIC_RATES)), dtype=torch.float32,
                          device=dev)
-    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster)
+    ver = sv.Verifier(N, G, V, device=dev.index, cluster_ctas=args.cluster, flags=LAUNCH_FLAGS)
     K = max(3, min(args.steps, args.synthetic_steps))
     nacc = torch.empty((K + args.warmup, N), dtype=torch.int32, device=dev)
     out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
@@ -533,7 +543,7 @@ def time_ngram(args, sv, dev, world, rank, dist, stream):
     out = torch.empty((R, k), dtype=torch.int32, device=dev)
     num = torch.empty((R,), dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    h = sv.spec_verify_create(R, k, 1, device=dev.index)
+    h = sv.spec_verify_create(R, k, 1, device=dev.index, flags=LAUNCH_FLAGS)
     lib = sv.load_library()
     built = [sv.build_ngram_args(token_ids=t, cu_num_tokens=c, draft_token_ids=out, num_draft_tokens=num,
                                  min_ngram=n_min, max_ngram=n_max, max_model_len=1 << 20, status=status)
@@ -584,6 +594,7 @@ def run_ours(args, world, rank, local_rank):
     import speculative_decoding_token_rejection_gb300 as sv
     import workloads
 
+    assert sv.SV_FLAG_SERIAL_LAUNCH == 4
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     dist = None
@@ -605,7 +616,7 @@ def run_ours(args, world, rank, local_rank):
     N, G, V, T = w["N"], w["gamma"], w["V"], w["T"]
     gammas = workloads.gammas_of(w)
     t = workloads.as_torch(w, dev)
-    ver = sv.Verifier(N, G, V, device=local_rank, cluster_ctas=args.cluster)
+    ver = sv.Verifier(N, G, V, device=local_rank, cluster_ctas=args.cluster, flags=LAUNCH_FLAGS)
     lib = sv.load_library()
     out = torch.empty((N, G + 1), dtype=torch.int32, device=dev)
     K, W = args.steps, args.warmup
@@ -707,7 +718,9 @@ def run_ours(args, world, rank, local_rank):
         "config": {"workload": f"{WORKLOAD}: N={N} gamma={G} V={V} fp32 rows (T=0.8, top-k 50, top-p 0.9), "
                                "production Philox",
                    "entry": "probs", "l2": "no flush: ~0.6 GB of rows per step >> 126 MB L2",
-                   "cluster_ctas": args.cluster or "auto"},
+                   "cluster_ctas": args.cluster or "auto",
+                   "launch": "serial" if LAUNCH_FLAGS else "programmatic (back-to-back kernels may be scheduled "
+                                                           "early; each waits for the previous grid first)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg_mean, "launch_ms": launch_ms,

@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 7u
+#define SPEC_VERIFY_ABI_VERSION 8u
 #define SV_PLACEHOLDER_TOKEN_ID (-1)
 #define SV_PADDING_SLOT_ID (-1)
 #define SV_MAX_SPEC_LEN 256 /* largest max_spec_len a handle accepts */
@@ -99,6 +99,16 @@ enum sv_data_status {
  * (the one-CTA form sums the processed kept set afresh, the cluster form
  * corrects the raw sum). */
 #define SV_FLAG_ONE_CTA_PER_REQUEST 2u
+/* SV_FLAG_SERIAL_LAUNCH: launch the handle's kernels in plain stream order.
+ * By default every kernel is launched with programmatic stream serialization
+ * (CUDA's programmatic dependent launch): it may be scheduled onto the SMs
+ * while the previous kernel in the stream is still running, and its first
+ * instruction waits until that kernel has completed and all of its memory
+ * writes are visible.  Nothing is read or written earlier than in plain stream
+ * order, so results are identical; only the gap between back-to-back kernels
+ * shrinks.  Work that is not a kernel (copies, event records, host callbacks)
+ * orders the stream as usual. */
+#define SV_FLAG_SERIAL_LAUNCH 4u
 
 /* Call hints (the hints field of spec_verify_args and spec_verify_sample_args;
  * they never change a result).  SV_HINT_SMALL_TOP_K: the caller states that

@@ -36,6 +36,7 @@ _P = ctypes.c_void_p
 
 SV_FLAG_RESIDENT_ROWS = 1
 SV_FLAG_ONE_CTA_PER_REQUEST = 2
+SV_FLAG_SERIAL_LAUNCH = 4
 SV_HINT_SMALL_TOP_K = 1
 SV_SMALL_TOP_K_MAX = 256
 SV_TEST_EXPIRE_COPY_WAIT = 1

@@ -113,7 +113,7 @@ static sv_status check_config(const spec_verify_config *c) {
   const int cc = c->cluster_ctas;
   if (!(cc == 0 || cc == 1 || cc == 2 || cc == 4 || cc == 8 || cc == 16))
     return fail(SV_ERR_INVALID_ARG, "cluster_ctas must be 0, 1, 2, 4, 8 or 16");
-  if (c->flags & ~(SV_FLAG_RESIDENT_ROWS | SV_FLAG_ONE_CTA_PER_REQUEST))
+  if (c->flags & ~(SV_FLAG_RESIDENT_ROWS | SV_FLAG_ONE_CTA_PER_REQUEST | SV_FLAG_SERIAL_LAUNCH))
     return fail(SV_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   if (static_cast<long long>(c->max_num_reqs) * (cc ? cc : 16) > INT_MAX)
     return fail(SV_ERR_INVALID_ARG, "max_num_reqs too large for one grid");
@@ -282,6 +282,7 @@ sv_status spec_verify_run(spec_verify_t h, const spec_verify_args *a, void *stre
   p.stop_ids = a->stop_token_ids;
   p.stop_total = a->stop_total;
   p.first_wait = (a->test_flags & SV_TEST_EXPIRE_COPY_WAIT) ? 0u : sv::kCopyWaitPolls;
+  p.pdl = !(h->cfg.flags & SV_FLAG_SERIAL_LAUNCH);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (a->entry == SV_ENTRY_PROBS) {
@@ -383,6 +384,7 @@ sv_status spec_verify_sample(spec_verify_t h, const spec_verify_sample_args *a, 
   p.ban_ids = a->banned_token_ids;
   p.ban_total = a->banned_total;
   p.first_wait = (a->test_flags & SV_TEST_EXPIRE_COPY_WAIT) ? 0u : sv::kCopyWaitPolls;
+  p.pdl = !(h->cfg.flags & SV_FLAG_SERIAL_LAUNCH);
   const bool bf16 = a->dtype == SV_BF16;
   const int eb = bf16 ? 2 : 4;
   int cluster = 0, chunk = 0;
@@ -449,6 +451,7 @@ sv_status spec_verify_ngram_propose(spec_verify_t h, const spec_verify_ngram_arg
   p.out = a->draft_token_ids;
   p.num = a->num_draft_tokens;
   p.status = a->status;
+  p.pdl = !(h->cfg.flags & SV_FLAG_SERIAL_LAUNCH);
   const cudaError_t e = sv::launch_ngram(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "n-gram proposer launch: %s", cudaGetErrorString(e));
   return SV_OK;

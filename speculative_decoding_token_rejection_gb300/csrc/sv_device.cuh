@@ -31,6 +31,17 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Programmatic dependent launch (sm_90+): the kernels are launched so that
+// they may be scheduled while the previous kernel in the stream is still
+// running.  The first statement of every kernel waits until that grid has
+// completed and its memory operations are visible (at once when the launch
+// carried no such attribute), so nothing is read or written earlier than
+// under plain stream order; it then lets the next kernel in the stream be
+// scheduled in the same way.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 // Split form: arrive early (nothing to publish), wait later.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");

@@ -55,6 +55,7 @@ struct VerifyParams {
   const int32_t *stop_ids;
   int64_t stop_total;
   uint32_t first_wait;  // polls of the first wait for a bulk row copy (0 under SV_TEST_EXPIRE_COPY_WAIT)
+  bool pdl;             // launch with programmatic stream serialization (host side only)
 };
 
 // The draft-side sampler's parameters (device pointers, sizes).
@@ -81,6 +82,7 @@ struct SampleParams {
   const int32_t *ban_ids;
   int64_t ban_total;
   uint32_t first_wait;  // polls of the first wait for a bulk row copy (0 under SV_TEST_EXPIRE_COPY_WAIT)
+  bool pdl;             // launch with programmatic stream serialization (host side only)
 };
 
 // The n-gram proposer's parameters (device pointers, sizes).
@@ -92,7 +94,30 @@ struct NgramParams {
   int32_t *out;
   int32_t *num;
   int32_t *status;
+  bool pdl;  // launch with programmatic stream serialization (host side only)
 };
+
+// The attributes of every kernel launch: a cluster of `cluster` CTAs (none
+// for 0) and, with `pdl`, programmatic stream serialization, which lets the
+// kernel be scheduled while the previous kernel in the stream finishes (each
+// kernel first waits for that grid's completion: pdl_enter in sv_device.cuh).
+// Fills attr[0..] and returns the count.
+inline unsigned launch_attrs(cudaLaunchAttribute attr[2], unsigned cluster, bool pdl) {
+  unsigned n = 0;
+  if (cluster) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  return n;
+}
 cudaError_t launch_ngram(const NgramParams &p, cudaStream_t stream);
 
 // Polls of the ordinary wait for a bulk row copy (each poll may suspend for a while).

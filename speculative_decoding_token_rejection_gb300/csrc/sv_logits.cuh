@@ -1950,6 +1950,7 @@ __device__ __forceinline__ void argmax_logits(const TIn *g, int x0, int n, unsig
 // rows are never rewritten).
 template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const VerifyParams P, int chunk) {
+  pdl_enter();
   static_assert(kRes || kVec, "rows read in place must be 16-byte aligned");
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
@@ -2248,6 +2249,7 @@ __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) logits_kernel(const Ve
 // ---------------------------------------------------------------------------
 template <typename TIn, bool kTest, bool kVec, bool kRes, bool kProc>
 __global__ void __launch_bounds__(kThreads, kRes ? 2 : 4) sample_kernel(const SampleParams P, int chunk) {
+  pdl_enter();
   static_assert(kRes || kVec, "rows read in place must be 16-byte aligned");
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ LogitsSmem sm;
@@ -2415,13 +2417,9 @@ cudaError_t launch_sample_one(const SampleParams &p, int cluster, int chunk, siz
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_attrs(attr, static_cast<unsigned>(cluster), p.pdl);
   return cudaLaunchKernelEx(&cfg, sample_kernel<TIn, kTest, kVec, kRes, kProc>, p, chunk);
 }
 
@@ -2461,13 +2459,9 @@ cudaError_t launch_one(const VerifyParams &p, int cluster, int chunk, size_t dyn
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_attrs(attr, static_cast<unsigned>(cluster), p.pdl);
   return cudaLaunchKernelEx(&cfg, logits_kernel<TIn, kTest, kVec, kRes, kProc>, p, chunk);
 }
 

@@ -21,6 +21,7 @@ namespace {
 constexpr int kLoads = 8;  // 16-byte loads in flight per thread
 
 __global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
+  pdl_enter();
   __shared__ int32_t tail[SV_MAX_NGRAM];
   __shared__ unsigned long long warp_best[kWarps];
   const int q = blockIdx.x;
@@ -116,8 +117,14 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
 }  // namespace
 
 cudaError_t launch_ngram(const NgramParams &p, cudaStream_t stream) {
-  ngram_kernel<<<p.R, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.R), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_attrs(attr, 0, p.pdl);
+  return cudaLaunchKernelEx(&cfg, ngram_kernel, p);
 }
 
 }  // namespace sv

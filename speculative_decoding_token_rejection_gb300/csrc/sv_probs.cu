@@ -190,6 +190,7 @@ __device__ __forceinline__ void argmax_chunk(const float *row, int x0, int x1, u
 
 template <bool kTest, bool kVec>
 __global__ void __launch_bounds__(kThreads, 4) probs_kernel(const VerifyParams P) {
+  pdl_enter();
   __shared__ ProbsSmem sm;
   const uint32_t ncta = cluster_nctarank(), rank = cluster_ctarank();
   const int i = static_cast<int>(blockIdx.x / ncta);
@@ -362,13 +363,9 @@ cudaError_t launch_one(const VerifyParams &p, int cluster, cudaStream_t stream) 
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_attrs(attr, static_cast<unsigned>(cluster), p.pdl);
   return cudaLaunchKernelEx(&cfg, probs_kernel<kTest, kVec>, p);
 }
 

@@ -800,6 +800,7 @@ constexpr int kStreamCtasPerSm = 3;
 
 template <typename TIn, bool kTest, bool kProc>
 __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) stream_kernel(const VerifyParams P) {
+  pdl_enter();
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   StreamSmem &ss = *reinterpret_cast<StreamSmem *>(dyn_smem);
@@ -1078,13 +1079,9 @@ cudaError_t launch_stream_one(const VerifyParams &p, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = stream_dyn_bytes(p.V, kProc);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (the fallback paths use cluster barriers)
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];  // a cluster of one (the fallback paths use cluster barriers)
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_attrs(attr, 1, p.pdl);
   return cudaLaunchKernelEx(&cfg, stream_kernel<TIn, kTest, kProc>, p);
 }
 
@@ -1098,6 +1095,7 @@ cudaError_t launch_stream_one(const VerifyParams &p, cudaStream_t stream) {
 // and the race over the whole row.  The same results as sample_kernel.
 template <typename TIn, bool kTest, bool kProc>
 __global__ void __launch_bounds__(kThreads, 4) stream_sample_kernel(const SampleParams P) {
+  pdl_enter();
   using E = Elem<TIn>;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   StreamSmem &ss = *reinterpret_cast<StreamSmem *>(dyn_smem);
@@ -1266,13 +1264,9 @@ cudaError_t launch_stream_sample_one(const SampleParams &p, cudaStream_t stream)
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = stream_dyn_bytes(p.V, kProc);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;  // a cluster of one (the exact statistics use cluster barriers)
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];  // a cluster of one (the exact statistics use cluster barriers)
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_attrs(attr, 1, p.pdl);
   return cudaLaunchKernelEx(&cfg, stream_sample_kernel<TIn, kTest, kProc>, p);
 }
 

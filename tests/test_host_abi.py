@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_description(lib):
-    assert lib.spec_verify_abi_version() == 7
+    assert lib.spec_verify_abi_version() == 8
     assert lib.spec_verify_sizeof_args() == ctypes.sizeof(sv.SpecVerifyArgs)
     assert lib.spec_verify_sizeof_config() == ctypes.sizeof(sv.SpecVerifyConfig)
 
@@ -128,7 +128,9 @@ def test_check_args(lib, mutate, code):
     (dict(cluster_ctas=16), sv.SV_OK),
     (dict(flags=sv.SV_FLAG_RESIDENT_ROWS), sv.SV_OK),
     (dict(flags=sv.SV_FLAG_ONE_CTA_PER_REQUEST), sv.SV_OK),
-    (dict(flags=4), sv.SV_ERR_INVALID_ARG),
+    (dict(flags=sv.SV_FLAG_SERIAL_LAUNCH), sv.SV_OK),
+    (dict(flags=sv.SV_FLAG_SERIAL_LAUNCH | sv.SV_FLAG_ONE_CTA_PER_REQUEST), sv.SV_OK),
+    (dict(flags=8), sv.SV_ERR_INVALID_ARG),
 ])
 def test_check_config(lib, kw, code):
     assert sv.spec_verify_check_args(cfg(**kw), good_args()) == code
