@@ -8,7 +8,8 @@
 // prefetched into L2 in one bulk request), and compares each token
 // with the last one; only the rare equal tokens E (E <= L - 2, so a token
 // follows) start the backward comparison t[E - j] == t[L - 1 - j] against the
-// tail held in shared memory.  The CTA keeps the largest (length, E) -- the
+// tail held in shared memory, on the thread's own group and the previous
+// lane's (a warp shuffle) for the first four steps.  The CTA keeps the largest (length, E) -- the
 // longest match, then the most recent occurrence -- and copies the proposal.
 #include <cstdint>
 
@@ -74,22 +75,55 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
     for (int j = tid; j < span; j += kThreads) tail[j] = t[L - 1 - j];
     __syncthreads();
     const int32_t last = tail[0];
-    auto extend = [&](int64_t E) {  // t[E] == t[L - 1]: how far back does the match run?
-      const int cap = static_cast<int>(min(static_cast<int64_t>(P.max_n), E + 1));
-      int len = 1;
-      while (len < cap && __ldg(t + E - len) == tail[len]) ++len;
-      if (len >= P.min_n) best = umax64(best, (static_cast<unsigned long long>(len) << 32) | static_cast<uint64_t>(E));
-    };
     for (int64_t vb = 0; vb < ngroups; vb += static_cast<int64_t>(kLoads) * kThreads) {
       if (vb > 0) load_round(vb);
 #pragma unroll
       for (int u = 0; u < kLoads; ++u) {
-        if (d[u].x != last && d[u].y != last && d[u].z != last && d[u].w != last) continue;  // (almost every group)
-        const int64_t E0 = g0 + 4 * (vb + u * kThreads + tid) - s;
-        const int32_t w[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
+        const bool hit = d[u].x == last || d[u].y == last || d[u].z == last || d[u].w == last;
+        if (!__any_sync(0xFFFFFFFFu, hit)) continue;  // (almost every group of the warp)
+        // the group before this one is the previous lane's, so a match finds
+        // its preceding tokens in registers; lane 0 reads its neighbour's again
+        int4 pv;
+        pv.x = __shfl_up_sync(0xFFFFFFFFu, d[u].x, 1);
+        pv.y = __shfl_up_sync(0xFFFFFFFFu, d[u].y, 1);
+        pv.z = __shfl_up_sync(0xFFFFFFFFu, d[u].z, 1);
+        pv.w = __shfl_up_sync(0xFFFFFFFFu, d[u].w, 1);
+        if (!hit) continue;
+        const int64_t v = vb + u * kThreads + tid;
+        const int64_t E0 = g0 + 4 * v - s;  // history index of the group's first token
+        if (lane == 0) {
+          // (unused for the first group, whose matches never reach back, and
+          // for groups past the end, whose matches fail the range test)
+          pv = make_int4(0, 0, 0, 0);
+          if (v > 0 && v < ngroups) {
+            const int64_t gp = g0 + 4 * (v - 1);  // below the current group's start, so inside the buffer
+            if (vec) {
+              pv = __ldg(reinterpret_cast<const int4 *>(P.tokens + gp));
+            } else {
+              pv = make_int4(P.tokens[gp], P.tokens[gp + 1], P.tokens[gp + 2], P.tokens[gp + 3]);
+            }
+          }
+        }
+        const int32_t win[8] = {pv.x, pv.y, pv.z, pv.w, d[u].x, d[u].y, d[u].z, d[u].w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c)  // (groups past the end fail the range test)
-          if (w[c] == last && E0 + c >= 0 && E0 + c <= L - 2) extend(E0 + c);
+        for (int c = 0; c < 4; ++c) {  // a match at E = E0 + c: t[E - j] is win[4 + c - j]
+          const int64_t E = E0 + c;
+          if (win[4 + c] != last || E < 0 || E > L - 2) continue;  // (groups past the end fail the range test)
+          const int cap = static_cast<int>(min(static_cast<int64_t>(P.max_n), E + 1));
+          int len = 1;
+          bool run = true;
+#pragma unroll
+          for (int j = 1; j <= 4 + c; ++j) {  // (len == j while the run lasts)
+            if (run && len < cap && win[4 + c - j] == tail[j])
+              ++len;
+            else
+              run = false;
+          }
+          if (run)  // longer n-grams than the registers hold
+            while (len < cap && __ldg(t + E - len) == tail[len]) ++len;
+          if (len >= P.min_n)
+            best = umax64(best, (static_cast<unsigned long long>(len) << 32) | static_cast<uint64_t>(E));
+        }
       }
     }
   }
