@@ -102,6 +102,7 @@ def measured_peak():
 LOGITS_KERNEL_SOURCES = ["sv_logits.cuh", "sv_logits.cu", "sv_logits_bf16.cu", "sv_logits_f32.cu", "sv_sample_bf16.cu",
                          "sv_sample_f32.cu", "sv_device.cuh"]  # (the processor units instantiate the same templates)
 STREAM_KERNEL_SOURCES = ["sv_stream.cuh", "sv_stream_bf16.cu", "sv_logits.cuh", "sv_device.cuh"]
+NGRAM_KERNEL_SOURCES = ["sv_ngram.cu", "sv_device.cuh"]
 
 
 def kernel_source_hash(sources=None) -> str:
@@ -562,6 +563,7 @@ def time_ngram(args, sv, dev, world, rank, dist, stream):
     total = float(np.mean([n for _, _, n in batches]))
     alg = 4 * total + 8 * R + 4 * R * (k + 1)
     peak, src = measured_peak()
+    traffic, _ = stored_traffic("ngram_propose_histories", NGRAM_KERNEL_SOURCES)
     return {"value": world * R / (ms / 1e3), "unit": "requests/s", "ms_per_step": ms, "steps": K,
             "history_tokens_per_s": world * total / (ms / 1e3),
             "config": {"workload": f"ngram: R={R} histories of 1024..16384 tokens (mean {int(total) // R}), "
@@ -570,8 +572,9 @@ def time_ngram(args, sv, dev, world, rank, dist, stream):
                                                    f"({NGRAM_BATCHES} batches, {NGRAM_BATCHES * 4 * total / 1e6:.0f} MB "
                                                    "together, > 126 MB L2), launches back to back"},
             "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
-                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None, "peak_source": src,
-                         "algorithmic_bytes_per_launch": alg},
+                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": traffic, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg,
+                         "kernel_source_sha": kernel_source_hash(NGRAM_KERNEL_SOURCES)},
             "proposed_fraction_last_batch": float((proposed > 0).mean()), "gpu_launches": K}
 
 
