@@ -52,3 +52,24 @@ def test_source_hash_ignores_comments_and_whitespace(tmp_path, monkeypatch):
     assert bench.kernel_source_hash(["k.cu"]) == a
     (csrc / "k.cu").write_text("int f(int x) { return 3 * x; }\n")
     assert bench.kernel_source_hash(["k.cu"]) != a
+
+
+def test_stored_traffic_records_resolve():
+    """Every committed DRAM traffic record names the hash of the kernel
+    sources it was taken on; the bench reads its bytes while that hash matches
+    the sources and reports no traffic once it does not."""
+    import json
+    for name, sources in (("verify_probs_fused_probs", bench.KERNEL_SOURCES),
+                          ("verify_logits_fused", bench.LOGITS_KERNEL_SOURCES),
+                          ("verify_logits_fused_stream", bench.STREAM_KERNEL_SOURCES),
+                          ("draft_sampler_fused_rows", bench.LOGITS_KERNEL_SOURCES),
+                          ("draft_sampler_fused_rows_per_row", bench.STREAM_KERNEL_SOURCES),
+                          ("ngram_propose_histories", bench.NGRAM_KERNEL_SOURCES)):
+        rec = json.loads((bench.ROOT / "profiles" / f"{name}.traffic.json").read_text())
+        assert rec["dram_bytes_per_launch"] > 0 and len(rec["kernel_source_sha"]) == 16
+        traffic, sha = bench.stored_traffic(name, sources)
+        assert sha == rec["kernel_source_sha"]
+        if sha == bench.kernel_source_hash(sources):
+            assert traffic == rec["dram_bytes_per_launch"]
+        else:
+            assert traffic is None
