@@ -9,8 +9,9 @@
 // with the last one; only the rare equal tokens E (E <= L - 2, so a token
 // follows) start the backward comparison t[E - j] == t[L - 1 - j] against the
 // tail held in shared memory, on the thread's own group and the previous
-// lane's (a warp shuffle) for the first four steps.  The CTA keeps the largest (length, E) -- the
-// longest match, then the most recent occurrence -- and copies the proposal.
+// lane's (a warp shuffle) for the first four steps.  The CTA keeps the
+// largest (length, E) -- the longest match, then the most recent occurrence --
+// and copies the proposal.
 #include <cstdint>
 
 #include "sv_device.cuh"
